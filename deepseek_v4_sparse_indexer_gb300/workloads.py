@@ -1,0 +1,185 @@
+"""Seeded synthetic inputs shaped like the pages' workloads.
+
+This module only builds inputs: it holds none of the step's arithmetic (no
+scoring, selection or attention).  The tests feed the same tensors to the CUDA
+library and to the fp64 oracle, and the benchmark uses them for timing.
+
+Value recipe: every bf16/fp16 tensor is N(0,1)/sqrt(d) rounded to nearest
+even, with d = 512 for queries, compressed rows and raw rows and d = 128 for
+indexer queries and keys; indexer weights are U(0,1) fp32.  Compressed rows,
+queries and indexer tensors are bf16; raw-window rows are fp16 (the raw tier is
+kept rounded to f16: "DwarfStar(ds4.c) のアーキテクチャを読む" §3-1).
+
+Workload shapes (query-token x layer units, compressed rows per unit):
+  decode_1x1024          1 unit, 1,024 rows                  (small parity case)
+  decode_8x16384         8 units, 16,384 rows
+  decode_32x43x65536     32 sequences x 43 layers = 1,376 units, 65,536 rows
+  prefill_2048x65536     one 2,048-query chunk over 65,536 prior rows + 512 rows
+                         finalised inside the chunk (causal)
+  longctx_4x262144       4 units, 262,144 rows, 5 % of indexer keys scaled x4
+The shapes follow the pages: 43 layers, 64 heads x 512, indexer 64 x 128,
+top_k 512, 128-row raw window (§2 DS4_SHAPE_FLASH); prefill advances in
+2,048-token chunks and benchmarks reach depth 65,536 (the Qwen3.8-Flash-Next
+on DwarfStar article, 測定条件); a 1M-token context holds ~250k ratio-4
+compressed rows (§3-3).
+"""
+from dataclasses import dataclass, field
+import math
+
+import torch
+
+N_HEAD = 64
+HEAD_DIM = 512
+N_IDX_HEAD = 64
+IDX_DIM = 128
+N_SWA = 128
+COMPRESS_RATIO = 4
+
+
+@dataclass
+class Workload:
+    name: str
+    kind: str              # "decode" or "prefill"
+    units: int             # decode: sequences x layers; prefill: 1
+    n_rows: int            # compressed rows per unit (prefill: prior + in-chunk)
+    top_k: int = 512
+    queries: int = 1       # queries per unit (prefill chunk length T)
+    heavy_frac: float = 0.0
+    heavy_scale: float = 4.0
+    seed: int = 0
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def query_units(self) -> int:
+        """Query-token x layer units one pass of the step processes."""
+        return self.units * self.queries
+
+
+WORKLOADS = {
+    "decode_1x1024": Workload("decode_1x1024", "decode", 1, 1024),
+    "decode_8x16384": Workload("decode_8x16384", "decode", 8, 16384),
+    "decode_32x43x65536": Workload("decode_32x43x65536", "decode", 32 * 43, 65536),
+    "prefill_2048x65536": Workload("prefill_2048x65536", "prefill", 1, 65536 + 512,
+                                   queries=2048, extra=dict(prior_rows=65536)),
+    "longctx_4x262144": Workload("longctx_4x262144", "decode", 4, 262144,
+                                 heavy_frac=0.05),
+}
+
+
+def _gen(seed: int, stream: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    # Distinct, reproducible stream per tensor: mix (seed, stream) into one 63-bit seed.
+    g.manual_seed((seed * 0x9E3779B97F4A7C15 + stream * 0xBF58476D1CE4E5B9 + 1) & ((1 << 63) - 1))
+    return g
+
+
+def normal_fill_(dst: torch.Tensor, d: int, seed: int, stream: int, chunk_elems: int = 1 << 28):
+    """Fill dst (bf16 or fp16, any device) with N(0,1)/sqrt(d), rounded to nearest even.
+
+    Generates in fp32 chunks so multi-GB tensors need only a bounded temporary.
+    """
+    g = _gen(seed, stream, dst.device)
+    flat = dst.view(-1)
+    inv = 1.0 / math.sqrt(d)
+    for s in range(0, flat.numel(), chunk_elems):
+        n = min(chunk_elems, flat.numel() - s)
+        t = torch.randn(n, generator=g, device=dst.device, dtype=torch.float32)
+        t.mul_(inv)
+        flat[s:s + n].copy_(t)
+    return dst
+
+
+def uniform_fill_(dst: torch.Tensor, seed: int, stream: int):
+    g = _gen(seed, stream, dst.device)
+    dst.copy_(torch.rand(dst.shape, generator=g, device=dst.device, dtype=torch.float32))
+    return dst
+
+
+def apply_heavy_tail_(ik: torch.Tensor, frac: float, scale: float, seed: int, stream: int):
+    """Scale a seeded fraction `frac` of the indexer keys (rows of the last-but-one
+    dim) by `scale` (a power of two, so bf16 stays exact), giving the score
+    distribution a heavy tail and sharp top-k boundaries."""
+    g = _gen(seed, stream, ik.device)
+    rows = ik.view(-1, ik.shape[-1])
+    chunk = 1 << 22
+    for s in range(0, rows.shape[0], chunk):
+        n = min(chunk, rows.shape[0] - s)
+        heavy = torch.rand(n, generator=g, device=ik.device) < frac
+        seg = rows[s:s + n]
+        seg[heavy] = seg[heavy] * scale
+    return ik
+
+
+def make_decode_inputs(units, n_cap, device="cpu", seed=0, n_rows=None, n_raw=None,
+                       heavy_frac=0.0, heavy_scale=4.0, q_scale=1.0):
+    """Decode-step inputs for `units` independent (sequence x layer) caches.
+
+    n_rows / n_raw: per-unit valid compressed rows / raw-window slots (int or
+    list); default full.  q_scale multiplies the attention query (x32 gives a
+    peaked softmax for stress cases).
+    """
+    dev = torch.device(device)
+    bf, hf = torch.bfloat16, torch.float16
+    x = {}
+    x["q"] = normal_fill_(torch.empty(units, N_HEAD, HEAD_DIM, dtype=bf, device=dev), HEAD_DIM, seed, 1)
+    if q_scale != 1.0:
+        x["q"].mul_(q_scale)
+    x["iq"] = normal_fill_(torch.empty(units, N_IDX_HEAD, IDX_DIM, dtype=bf, device=dev), IDX_DIM, seed, 2)
+    x["w"] = uniform_fill_(torch.empty(units, N_IDX_HEAD, dtype=torch.float32, device=dev), seed, 3)
+    x["ik"] = normal_fill_(torch.empty(units, n_cap, IDX_DIM, dtype=bf, device=dev), IDX_DIM, seed, 4)
+    if heavy_frac > 0:
+        apply_heavy_tail_(x["ik"], heavy_frac, heavy_scale, seed, 5)
+    x["rows"] = normal_fill_(torch.empty(units, n_cap, HEAD_DIM, dtype=bf, device=dev), HEAD_DIM, seed, 6)
+    x["raw"] = normal_fill_(torch.empty(units, N_SWA, HEAD_DIM, dtype=hf, device=dev), HEAD_DIM, seed, 7)
+    nr = n_rows if n_rows is not None else n_cap
+    nw = n_raw if n_raw is not None else N_SWA
+    x["n_rows"] = torch.tensor([nr] * units if isinstance(nr, int) else list(nr), dtype=torch.int32, device=dev)
+    x["n_raw"] = torch.tensor([nw] * units if isinstance(nw, int) else list(nw), dtype=torch.int32, device=dev)
+    return x
+
+
+def prefill_positions(T, prior_rows, ratio=COMPRESS_RATIO):
+    """Positions of a prefill chunk that starts right after `prior_rows`
+    ratio-4 compressed rows (one row per 4 tokens, "DwarfStar(ds4.c) の
+    アーキテクチャを読む" §3-2).  Row i covers tokens ratio*i .. ratio*i+3 and
+    is finalised at its last token; the chunk's queries are tokens P0..P0+T-1.
+
+    Returns (q_pos [T], row_pos [prior_rows + T // ratio], P0).
+    """
+    P0 = ratio * prior_rows
+    n_new = T // ratio
+    i = torch.arange(prior_rows + n_new, dtype=torch.int64)
+    row_pos = (ratio * i + (ratio - 1)).to(torch.int32)
+    q_pos = (P0 + torch.arange(T, dtype=torch.int64)).to(torch.int32)
+    return q_pos, row_pos, P0
+
+
+def make_prefill_inputs(T, prior_rows, device="cpu", seed=0, q_scale=1.0):
+    """Prefill-chunk inputs: T queries over prior_rows + T/4 compressed rows, and
+    a contiguous fp16 raw buffer holding positions P0-128 .. P0+T-1."""
+    dev = torch.device(device)
+    bf, hf = torch.bfloat16, torch.float16
+    q_pos, row_pos, P0 = prefill_positions(T, prior_rows)
+    n_cap = row_pos.numel()
+    x = {}
+    x["q"] = normal_fill_(torch.empty(T, N_HEAD, HEAD_DIM, dtype=bf, device=dev), HEAD_DIM, seed, 11)
+    if q_scale != 1.0:
+        x["q"].mul_(q_scale)
+    x["iq"] = normal_fill_(torch.empty(T, N_IDX_HEAD, IDX_DIM, dtype=bf, device=dev), IDX_DIM, seed, 12)
+    x["w"] = uniform_fill_(torch.empty(T, N_IDX_HEAD, dtype=torch.float32, device=dev), seed, 13)
+    x["ik"] = normal_fill_(torch.empty(n_cap, IDX_DIM, dtype=bf, device=dev), IDX_DIM, seed, 14)
+    x["rows"] = normal_fill_(torch.empty(n_cap, HEAD_DIM, dtype=bf, device=dev), HEAD_DIM, seed, 16)
+    raw_pos0 = max(P0 - N_SWA, 0)
+    n_raw_rows = P0 + T - raw_pos0
+    x["raw"] = normal_fill_(torch.empty(n_raw_rows, HEAD_DIM, dtype=hf, device=dev), HEAD_DIM, seed, 17)
+    x["q_pos"] = q_pos.to(dev)
+    x["row_pos"] = row_pos.to(dev)
+    x["n_rows"] = torch.tensor([n_cap], dtype=torch.int32, device=dev)
+    x["raw_pos0"] = raw_pos0
+    x["P0"] = P0
+    return x
+
+
+def as_u16(t: torch.Tensor):
+    """The raw 16-bit storage of a bf16/fp16 tensor as a numpy uint16 array (CPU copy)."""
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view("uint16")

@@ -1,0 +1,311 @@
+/*
+ * ds4a oracle: a plain, slow, fp64 CPU statement of the three-tier
+ * compressed-attention step of the DeepSeek V4 Flash engine (DwarfStar, ds4).
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the checker, not the product: only
+ * the test suite, the smoke check and the benchmark's CPU-baseline leg may load
+ * it.  It shares no code, header, table or helper with the CUDA library, and
+ * the CUDA library never calls it.
+ *
+ * Sources (the pages this restates):
+ *   [ARCH]  "Redis 作者が DeepSeek V4 専用の推論エンジンを C で書いた ―
+ *            DwarfStar(ds4.c) のアーキテクチャを読む【第1回/全8回】" (Qiita):
+ *            §2 (DS4_SHAPE_FLASH: 64 heads, 1 KV head, head dim 512, n_swa 128,
+ *            indexer 64 heads x 128 dims, top_k 512), §3 (three tiers: raw
+ *            window + compressed rows + indexer), §3-1 (raw window rounded
+ *            through f16), §3-2 (compressor pooling), §3-3 (indexer picks the
+ *            top-k compressed rows for the main attention).
+ *   [NOTES] "antirez/ds4 深度阅读笔记", section 固定模型形状 (fixed shapes).
+ *
+ * The pages print no indexer scoring formula.  This library specifies it as
+ *     s_r = sum_h w_h * max(0, sum_d iq[h,d] * ik[r,d])
+ * and the attention as one joint softmax over (selected compressed rows) U
+ * (raw-window rows), each cached row serving as both key and value (one KV
+ * head, [ARCH] §2 n_head_kv = 1).
+ *
+ * Everything is computed in double precision, summed sequentially in the
+ * order the definition states (d inner, then h; rows in list order).  Inputs
+ * are decoded exactly from their storage formats (bf16, fp16, fp32).
+ *
+ * Every function here is pinned by tests that do not re-type its formula
+ * (hand-worked cases, closed forms, invariants, library special cases).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+int oracle_abi_version(void) { return 1; }
+
+/* ------------------------------------------------------------------------ */
+/* Storage-format decoding (IEEE 754 binary16; bfloat16 = the top half of   */
+/* an IEEE binary32).  Written from the format definitions.                 */
+/* ------------------------------------------------------------------------ */
+
+/* bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits. */
+double oracle_bf16_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 7) & 0xFF;
+    int m = h & 0x7F;
+    double v;
+    if (e == 0xFF)
+        v = m ? NAN : INFINITY;
+    else if (e == 0)
+        v = ldexp((double)m, 1 - 127 - 7);          /* subnormal */
+    else
+        v = ldexp((double)(m | 0x80), e - 127 - 7); /* normal: 1.m * 2^(e-127) */
+    return sign ? -v : v;
+}
+
+/* binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double oracle_f16_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1F;
+    int m = h & 0x3FF;
+    double v;
+    if (e == 0x1F)
+        v = m ? NAN : INFINITY;
+    else if (e == 0)
+        v = ldexp((double)m, 1 - 15 - 10);
+    else
+        v = ldexp((double)(m | 0x400), e - 15 - 10);
+    return sign ? -v : v;
+}
+
+/* Round a double to the nearest binary16 value (ties to even), returned as
+ * its bit pattern.  Overflow goes to infinity.  Used by the raw-window push,
+ * which stores every row "rounded to f16" ([ARCH] §3-1). */
+uint16_t oracle_double_to_f16(double x)
+{
+    uint16_t sign = 0;
+    if (isnan(x))
+        return 0x7E00;
+    if (signbit(x)) {
+        sign = 0x8000;
+        x = -x;
+    }
+    if (isinf(x))
+        return sign | 0x7C00;
+    /* Spacing of binary16 values around x: 2^(E-10) for normal exponent E,
+     * 2^-24 for subnormals.  Round x to a multiple of that spacing. */
+    int E;
+    if (x == 0.0)
+        return sign;
+    frexp(x, &E);      /* x = f * 2^E with f in [0.5, 1) -> unbiased exp E-1 */
+    int ue = E - 1;
+    if (ue < -14)
+        ue = -14;      /* subnormal range shares the spacing of 2^-14 */
+    double ulp = ldexp(1.0, ue - 10);
+    double q = x / ulp;               /* exact: scaling by a power of two */
+    double fl = floor(q);
+    double rem = q - fl;
+    double n;
+    if (rem > 0.5)
+        n = fl + 1.0;
+    else if (rem < 0.5)
+        n = fl;
+    else
+        n = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+    double r = n * ulp;
+    if (r > 65504.0)
+        return sign | 0x7C00;         /* beyond the largest finite half */
+    /* Encode r. */
+    if (r < ldexp(1.0, -14)) {
+        int mant = (int)(r / ldexp(1.0, -24));
+        return sign | (uint16_t)mant;
+    }
+    int e2;
+    double f = frexp(r, &e2);         /* r = f * 2^e2, f in [0.5,1) */
+    int be = e2 - 1 + 15;
+    int mant = (int)((f * 2.0 - 1.0) * 1024.0);
+    return sign | (uint16_t)(be << 10) | (uint16_t)mant;
+}
+
+/* ------------------------------------------------------------------------ */
+/* A1. Indexer score                                                        */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Scores every compressed row of one unit (one sequence x layer) for n_q
+ * queries.  [ARCH] §3-3: the indexer has its own light query system (64
+ * heads x 128 dims, [ARCH] §2) and one 128-d key per compressed row; its
+ * score ranks the rows.  Formula (this library's specification):
+ *     s[q,r] = sum_h w[q,h] * max(0, sum_d iq[q,h,d] * ik[r,d])
+ *
+ * Visibility: row r exists iff r < n_rows.  With positions given (a prefill
+ * chunk), query q also needs row_pos[r] <= q_pos[q] (it may not look at rows
+ * finalised after its own position).  Rows that are not visible get -inf.
+ *
+ * iq:  bf16 [n_q][n_head][dim]       w: fp32 [n_q][n_head]
+ * ik:  bf16 [n_cap][dim]             scores: double [n_q][n_cap]
+ */
+void oracle_indexer_score(const uint16_t *iq, const float *w, const uint16_t *ik,
+                          int64_t n_rows, int64_t n_cap, int n_q, int n_head, int dim,
+                          const int32_t *q_pos, const int32_t *row_pos, double *scores)
+{
+    double *qd = (double *)malloc(sizeof(double) * (size_t)n_head * (size_t)dim);
+    double *kd = (double *)malloc(sizeof(double) * (size_t)dim);
+    for (int q = 0; q < n_q; q++) {
+        for (int64_t i = 0; i < (int64_t)n_head * dim; i++)
+            qd[i] = oracle_bf16_to_double(iq[(int64_t)q * n_head * dim + i]);
+        for (int64_t r = 0; r < n_cap; r++) {
+            int visible = r < n_rows;
+            if (visible && q_pos != NULL && row_pos != NULL)
+                visible = row_pos[r] <= q_pos[q];
+            if (!visible) {
+                scores[(int64_t)q * n_cap + r] = -INFINITY;
+                continue;
+            }
+            for (int d = 0; d < dim; d++)
+                kd[d] = oracle_bf16_to_double(ik[r * dim + d]);
+            double s = 0.0;
+            for (int h = 0; h < n_head; h++) {
+                double dot = 0.0;
+                for (int d = 0; d < dim; d++)
+                    dot += qd[(int64_t)h * dim + d] * kd[d];
+                double relu = dot > 0.0 ? dot : 0.0;
+                s += (double)w[(int64_t)q * n_head + h] * relu;
+            }
+            scores[(int64_t)q * n_cap + r] = s;
+        }
+    }
+    free(qd);
+    free(kd);
+}
+
+/* ------------------------------------------------------------------------ */
+/* A2. Top-k selection                                                      */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    double s;
+    int32_t r;
+} oracle_scored_row;
+
+/* Highest score first; equal scores: lower row index first. */
+static int by_score_desc_then_row(const void *a, const void *b)
+{
+    const oracle_scored_row *x = (const oracle_scored_row *)a;
+    const oracle_scored_row *y = (const oracle_scored_row *)b;
+    if (x->s > y->s) return -1;
+    if (x->s < y->s) return 1;
+    return (x->r > y->r) - (x->r < y->r);
+}
+
+static int int32_ascending(const void *a, const void *b)
+{
+    int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
+    return (x > y) - (x < y);
+}
+
+/*
+ * [ARCH] §3-3: the indexer passes only the n_indexer_top_k (512 on Flash,
+ * 1024 on Pro) highest-scoring compressed rows to the main attention.
+ * Visible rows are those with a score that is not -inf and not NaN.
+ * Result: m = min(top_k, n_visible) row indices in ascending order in idx,
+ * the m-th highest score in *kth (-inf when m == 0).  Returns m.
+ */
+int oracle_topk_select(const double *scores, int64_t n, int top_k, int32_t *idx, double *kth)
+{
+    oracle_scored_row *v = (oracle_scored_row *)malloc(sizeof(oracle_scored_row) * (size_t)(n > 0 ? n : 1));
+    int64_t nv = 0;
+    for (int64_t r = 0; r < n; r++) {
+        double s = scores[r];
+        if (isnan(s) || s == -INFINITY)
+            continue;
+        v[nv].s = s;
+        v[nv].r = (int32_t)r;
+        nv++;
+    }
+    qsort(v, (size_t)nv, sizeof(oracle_scored_row), by_score_desc_then_row);
+    int m = (int)(nv < top_k ? nv : top_k);
+    for (int i = 0; i < m; i++)
+        idx[i] = v[i].r;
+    qsort(idx, (size_t)m, sizeof(int32_t), int32_ascending);
+    if (kth)
+        *kth = m > 0 ? v[m - 1].s : -INFINITY;
+    free(v);
+    return m;
+}
+
+/* ------------------------------------------------------------------------ */
+/* A4. Sparse attention over selected compressed rows U raw-window rows      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * One query (n_head heads of width dim) attends over one joint row set:
+ *   - n_sel compressed rows comp[sel[j]] (bf16), then
+ *   - n_raw raw-window rows raw[raw_sel[j]] (fp16: the raw tier is kept
+ *     "rounded to f16", [ARCH] §3-1).
+ * Each row is used as both key and value (one KV head, [ARCH] §2).  For each
+ * head h:
+ *     l_j = scale * sum_d q[h,d] * x_j[d]
+ *     a_j = exp(l_j - max l) / sum_i exp(l_i - max l)
+ *     out[h,:] = sum_j a_j * x_j[:]
+ *     lse[h] = max l + log(sum_j exp(l_j - max l))
+ * An empty row set gives out = 0 and lse = -inf.
+ * q: bf16 [n_head][dim]; out: double [n_head][dim]; lse: double [n_head] or NULL.
+ * Returns 0, or -1 when a row index is negative.
+ */
+int oracle_sparse_attention(const uint16_t *q, int n_head, int dim,
+                            const uint16_t *comp, const int32_t *sel, int n_sel,
+                            const uint16_t *raw, const int32_t *raw_sel, int n_raw,
+                            double scale, double *out, double *lse)
+{
+    int n = n_sel + n_raw;
+    for (int j = 0; j < n_sel; j++)
+        if (sel[j] < 0) return -1;
+    for (int j = 0; j < n_raw; j++)
+        if (raw_sel[j] < 0) return -1;
+    if (n == 0) {
+        for (int64_t i = 0; i < (int64_t)n_head * dim; i++)
+            out[i] = 0.0;
+        if (lse)
+            for (int h = 0; h < n_head; h++)
+                lse[h] = -INFINITY;
+        return 0;
+    }
+    double *x = (double *)malloc(sizeof(double) * (size_t)n * (size_t)dim);
+    double *qd = (double *)malloc(sizeof(double) * (size_t)dim);
+    double *l = (double *)malloc(sizeof(double) * (size_t)n);
+    double *a = (double *)malloc(sizeof(double) * (size_t)n);
+    for (int j = 0; j < n_sel; j++)
+        for (int d = 0; d < dim; d++)
+            x[(int64_t)j * dim + d] = oracle_bf16_to_double(comp[(int64_t)sel[j] * dim + d]);
+    for (int j = 0; j < n_raw; j++)
+        for (int d = 0; d < dim; d++)
+            x[(int64_t)(n_sel + j) * dim + d] = oracle_f16_to_double(raw[(int64_t)raw_sel[j] * dim + d]);
+
+    for (int h = 0; h < n_head; h++) {
+        for (int d = 0; d < dim; d++)
+            qd[d] = oracle_bf16_to_double(q[(int64_t)h * dim + d]);
+        double mx = -INFINITY;
+        for (int j = 0; j < n; j++) {
+            double dot = 0.0;
+            for (int d = 0; d < dim; d++)
+                dot += qd[d] * x[(int64_t)j * dim + d];
+            l[j] = scale * dot;
+            if (l[j] > mx) mx = l[j];
+        }
+        double z = 0.0;
+        for (int j = 0; j < n; j++)
+            z += exp(l[j] - mx);
+        for (int j = 0; j < n; j++)
+            a[j] = exp(l[j] - mx) / z;
+        for (int d = 0; d < dim; d++) {
+            double acc = 0.0;
+            for (int j = 0; j < n; j++)
+                acc += a[j] * x[(int64_t)j * dim + d];
+            out[(int64_t)h * dim + d] = acc;
+        }
+        if (lse)
+            lse[h] = mx + log(z);
+    }
+    free(x);
+    free(qd);
+    free(l);
+    free(a);
+    return 0;
+}
