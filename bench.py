@@ -1,0 +1,440 @@
+#!/usr/bin/env python3
+"""Benchmark: one step = indexer score -> top-k select -> sparse attention over
+every unit of a workload, through the C ABI of libds4a.so on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-cpu-baseline]
+
+Prints one JSON line (rank 0).  Default workload: decode of 32 sequences x 43
+layers (1,376 independent caches of 65,536 compressed rows), the decode batch
+the HBM roofline is judged on.  Inputs (115 GB) exceed the 126 MB L2 many times
+over, so no flush is needed between steps.  With --gpus N (torchrun, one rank
+per GPU) every rank runs the whole workload on its own GPU (weak scaling, no
+collective on the data path); the timing is the max over ranks.
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload (the slow, obviously-correct statement of the
+step), with the same metric and units.
+"""
+import argparse
+import concurrent.futures as cf
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-attn query-token·layers/s and achieved HBM GB/s (fraction of GB300 peak)"
+UNIT = "query-token·layers/s"
+SCALE = 1.0 / math.sqrt(512)
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--workload", default="decode_32x43x65536")
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU work budget of the oracle sample")
+    return p.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, src="fallback")
+
+
+# ----------------------------------------------------------------------------
+# Clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(self.NAMES, parts[3:]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id_for_smi(torch, dev):
+    try:
+        u = torch.cuda.get_device_properties(dev).uuid
+        return "GPU-" + str(u)
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        return vis.split(",")[dev] if vis else str(dev)
+
+
+# ----------------------------------------------------------------------------
+# Workload arithmetic (algorithmic bytes / flops)
+# ----------------------------------------------------------------------------
+def decode_bytes(wl):
+    """Algorithmic HBM bytes per unit: every indexer key, the selected rows, the
+    raw window, q, iq, w, the fp32 output and the selected indices."""
+    per_unit_fixed = wl.top_k * 1024 + 128 * 1024 + 64 * 512 * 2 + 64 * 128 * 2 + 64 * 4 + 64 * 512 * 4 + wl.top_k * 4
+    ik = wl.n_rows * 128 * 2
+    idx_kernel = wl.n_rows * 256 + 64 * 128 * 2 + 64 * 4
+    return wl.units * (ik + per_unit_fixed), wl.units * idx_kernel
+
+
+def prefill_flops(x, wl):
+    import torch
+    q_pos = x["q_pos"].cpu().to(torch.int64)
+    row_pos = x["row_pos"].cpu().to(torch.int64)
+    visible = torch.searchsorted(row_pos, q_pos, right=True)          # rows sorted by position
+    idx_flops = float(visible.sum().item()) * 64 * 128 * 2
+    # attention: (k selected + window rows) x 64 heads x 512 x 2 (QK) x 2 (PV)
+    raw0 = x["raw_pos0"]
+    win = torch.clamp(torch.minimum(q_pos - raw0, torch.tensor(x["raw"].shape[0] - 1)) -
+                      torch.clamp(q_pos - 127 - raw0, min=0) + 1, min=0)
+    rows = torch.clamp(visible, max=wl.top_k) + win
+    attn_flops = float(rows.sum().item()) * 64 * 512 * 4
+    return idx_flops, attn_flops
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle sample (cpu_baseline leg and the reference arm)
+# ----------------------------------------------------------------------------
+class OracleSample:
+    """A bounded sample of a workload prepared for the fp64 oracle: whole decode
+    units (all rows scored, top-k, attention) or prefill queries spread over the
+    chunk.  The sample size is calibrated so one timed pass costs about
+    `seconds_budget` of CPU work."""
+
+    def __init__(self, wl, seconds_budget, unit_source=None, max_distinct=16):
+        import numpy as np
+        import torch
+
+        import oracle
+        from deepseek_v4_sparse_indexer_gb300.workloads import make_decode_inputs, make_prefill_inputs
+
+        self.wl = wl
+        self.oracle = oracle
+
+        def u16(t):
+            return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+        if wl.kind == "decode":
+            def get_unit(i):
+                if unit_source is not None:
+                    return unit_source(i)
+                x = make_decode_inputs(1, wl.n_rows, device="cpu", seed=wl.seed + 1000 + i,
+                                       heavy_frac=wl.heavy_frac, heavy_scale=wl.heavy_scale)
+                return dict(q=u16(x["q"][0]), iq=u16(x["iq"][0]), w=x["w"][0].numpy(), ik=u16(x["ik"][0]),
+                            rows=u16(x["rows"][0]), raw=u16(x["raw"][0]), n=wl.n_rows, nraw=128)
+
+            first = get_unit(0)
+            t = time.perf_counter()
+            self._run(first)
+            t1 = time.perf_counter() - t
+            n = self._size(seconds_budget, t1, wl.query_units)
+            # At most `pool` distinct units are materialised; the sample cycles
+            # through them (the oracle's work per unit does not depend on values).
+            pool = [first] + [get_unit(i) for i in range(1, min(n, max_distinct))]
+            self.items = [pool[i % len(pool)] for i in range(n)]
+            self.text = f"{n} of {wl.query_units} units (each whole: {wl.n_rows} rows scored, top-{wl.top_k}, " \
+                        f"attention over the selected rows + 128-row window)"
+        else:
+            x = make_prefill_inputs(wl.queries, wl.extra["prior_rows"], device="cpu", seed=wl.seed)
+            self.np_in = (u16(x["q"]), u16(x["iq"]), x["w"].numpy(), u16(x["ik"]), u16(x["rows"]),
+                          x["row_pos"].numpy(), x["q_pos"].numpy(), u16(x["raw"]))
+            self.nr = int(x["n_rows"][0])
+            self.raw_pos0 = x["raw_pos0"]
+            t = time.perf_counter()
+            self._run(wl.queries - 1)
+            t1 = time.perf_counter() - t
+            n = self._size(seconds_budget, t1, wl.queries)
+            self.items = [int(v) for v in np.linspace(0, wl.queries - 1, n)]
+            self.text = f"{n} of {wl.queries} queries spread over the chunk (first and last included)"
+
+    @staticmethod
+    def _size(budget, t1, cap):
+        return max(1, min(cap, int(round(budget / max(t1, 1e-3)))))
+
+    def _run(self, item):
+        wl, o = self.wl, self.oracle
+        if wl.kind == "decode":
+            d = item
+            o.decode_unit(d["q"], d["iq"], d["w"], d["ik"], d["rows"], d["n"], d["raw"], d["nraw"], wl.top_k, SCALE)
+        else:
+            q, iq, w, ik, rows, row_pos, q_pos, raw = self.np_in
+            o.prefill_query(item, q, iq, w, ik, rows, self.nr, row_pos, q_pos, raw, self.raw_pos0, wl.top_k, SCALE)
+
+    def rate(self, cores):
+        """Query-token x layer units per second over the sample, on `cores` threads."""
+        t = time.perf_counter()
+        with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+            list(ex.map(self._run, self.items))
+        return len(self.items) / (time.perf_counter() - t)
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------
+# Reference arm: the oracle on host cores
+# ----------------------------------------------------------------------------
+def run_reference(args, wl):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    cores = host_cores()
+    # Size the sample so that warmup + steps stay within a few minutes of wall time.
+    wall_per_step = max(1.0, min(6.0, 90.0 / max(1, args.steps + args.warmup)))
+    sample = OracleSample(wl, wall_per_step * cores)
+    vals = []
+    for i in range(args.warmup + args.steps):
+        v = sample.rate(cores)
+        if i >= args.warmup:
+            vals.append(v)
+    value = statistics.median(vals)
+    sample_text = sample.text + f", threads={cores}, each step one pass over the sample"
+    units_per_step = wl.query_units
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": units_per_step / value * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic, seeded (CPU-generated with the same recipe)",
+            "config": {"workload": wl.name, "units": wl.units, "queries_per_unit": wl.queries,
+                       "rows_per_unit": wl.n_rows, "top_k": wl.top_k},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample_text},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------
+# Our arm
+# ----------------------------------------------------------------------------
+def main():
+    args = parse()
+    from deepseek_v4_sparse_indexer_gb300.workloads import WORKLOADS
+    if args.workload not in WORKLOADS:
+        raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(WORKLOADS)}")
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    import torch
+    import torch.distributed as dist
+
+    import deepseek_v4_sparse_indexer_gb300 as pkg
+    from deepseek_v4_sparse_indexer_gb300.workloads import make_decode_inputs, make_prefill_inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pkg.load()
+    pk = peaks()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    seed = wl.seed + rank
+    if wl.kind == "decode":
+        x = make_decode_inputs(wl.units, wl.n_rows, device=dev, seed=seed, heavy_frac=wl.heavy_frac,
+                               heavy_scale=wl.heavy_scale)
+        step = pkg.DecodeStep(wl.units, wl.n_rows, wl.top_k, device=dev)
+    else:
+        x = make_prefill_inputs(wl.queries, wl.extra["prior_rows"], device=dev, seed=seed)
+        step = pkg.PrefillStep(wl.queries, x["ik"].shape[0], wl.top_k, device=dev)
+    torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step(x, SCALE)
+    torch.cuda.synchronize()
+    st, flags = pkg.ds4a_get_device_status()
+    if st != 0:
+        raise SystemExit(f"device status flags {flags} after warm-up")
+
+    # ---------------- device-timed region
+    K = args.steps
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    t0, t1 = ev(), ev()
+    sc_s, sc_e = [ev() for _ in range(K)], [ev() for _ in range(K)]
+    sampler = ClockSampler(gpu_id_for_smi(torch, dev.index))
+    barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    t0.record()
+    for i in range(K):
+        sc_s[i].record()
+        step.score(x)
+        sc_e[i].record()
+        step.select(x)
+        step.attend(x, SCALE)
+    t1.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier()
+    ms = t0.elapsed_time(t1) / K
+    idx_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(sc_s, sc_e))
+    if world > 1:
+        t = torch.tensor([ms, idx_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, idx_ms = float(t[0]), float(t[1])
+    units = wl.query_units
+    value = world * units / (ms / 1e3)
+
+    # ---------------- end to end through the public API with host buffers
+    host_in = {k: x[k].cpu().pin_memory() for k in ("q", "iq", "w")}
+    host_out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    host_lse = torch.empty(step.lse.shape, dtype=step.lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * 4 + host_lse.numel() * 4
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = ev(), ev()
+    e0.record()
+    for i in range(K):
+        for k, t in host_in.items():
+            x[k].copy_(t, non_blocking=True)
+        step(x, SCALE)
+        host_out.copy_(step.out, non_blocking=True)
+        host_lse.copy_(step.lse, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / K
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+    e2e_value = world * units / (e2e_ms / 1e3)
+    st, flags = pkg.ds4a_get_device_status()
+    if st != 0:
+        raise SystemExit(f"device status flags {flags} after the timed region")
+
+    # ---------------- roofline of the dominant kernel (indexer score)
+    launches_per_step = 1 + 3 + 1 + (1 if pkg.ds4a_workspace_bytes(
+        2 if wl.kind == "decode" else 3, wl.units if wl.kind == "decode" else 1,
+        1 if wl.kind == "decode" else wl.queries, wl.n_rows, wl.top_k) else 0)
+    cfg = {"workload": wl.name, "units": wl.units, "queries_per_unit": wl.queries, "rows_per_unit": wl.n_rows,
+           "top_k": wl.top_k, "raw_window": 128, "heads": 64, "head_dim": 512, "indexer": "64x128",
+           "l2": "inputs exceed the L2 many times over; no flush", "parallelism": f"replicas x{world}",
+           "peak_source": pk["src"]}
+    if wl.kind == "decode":
+        step_bytes, idx_bytes = decode_bytes(wl)
+        achieved = idx_bytes / (idx_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
+                "frac": achieved / pk["hbm"], "traffic": None, "kernel": "indexer_score_kernel<1>",
+                "algorithmic_bytes_per_launch": idx_bytes, "launch_ms": idx_ms}
+        cfg["step_algorithmic_bytes"] = step_bytes
+        cfg["step_hbm_GBps"] = step_bytes / (ms / 1e3) / 1e9
+        cfg["step_hbm_frac"] = cfg["step_hbm_GBps"] / pk["hbm"]
+    else:
+        idx_flops, attn_flops = prefill_flops(x, wl)
+        achieved = idx_flops / (idx_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16"], "unit": "TFLOP/s",
+                "frac": achieved / pk["bf16"], "traffic": None, "kernel": "indexer_score_kernel<4>",
+                "algorithmic_flops_per_launch": idx_flops, "launch_ms": idx_ms}
+        cfg["step_algorithmic_flops"] = idx_flops + attn_flops
+        cfg["step_TFLOPs"] = (idx_flops + attn_flops) / (ms / 1e3) / 1e12
+        cfg["step_tensor_frac"] = cfg["step_TFLOPs"] / pk["bf16"]
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic: seeded N(0,1)/sqrt(d) bf16 rows/keys/queries, fp16 raw window, U(0,1) weights",
+            "config": cfg, "roofline": roof,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms, "note": "per step: H2D of the queries (q, iq, w) from pinned memory, "
+                                                  "the three C-ABI ops, D2H of out and lse; the KV caches stay "
+                                                  "resident in HBM"},
+            "gpu_launches": launches_per_step * K, "clocks": clocks}
+
+    # ---------------- CPU baseline: the oracle on the host cores (rank 0, N = 1)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import numpy as np
+        cores = host_cores()
+
+        def u16(t):
+            return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+        unit_source = None
+        if wl.kind == "decode":
+            def unit_source(i):
+                u = (i * 7919) % wl.units
+                return dict(q=u16(x["q"][u]), iq=u16(x["iq"][u]), w=x["w"][u].cpu().numpy(), ik=u16(x["ik"][u]),
+                            rows=u16(x["rows"][u]), raw=u16(x["raw"][u]), n=wl.n_rows, nraw=128)
+        sample = OracleSample(wl, args.cpu_seconds, unit_source)
+        v = sample.rate(cores)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": sample.text + f", threads={cores}"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,373 @@
+// Indexer score on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// Computes, for every (unit u, query q, compressed row r):
+//     scores[u,q,r] = sum_h w[u,q,h] * max(0, sum_d iq[u,q,h,d] * ik[u,r,d])
+// The pages name the indexer (64 heads x 128 dims scoring every compressed
+// row, "DwarfStar(ds4.c) のアーキテクチャを読む" §2 and §3-3) but print no
+// formula; this is the library's specification of it.
+//
+// Mapping: one UMMA tile is D[128 rows x N] = ik_tile[128 x 128] * iq^T with
+// rows on M and (query, head) pairs on N = 64*G (G queries share the rows of a
+// tile: G = 1 in decode, 4 in a prefill chunk).  With rows on M, TMEM lane i
+// holds all head sums of row i, so the ReLU-weighted head reduction is a
+// per-thread loop after one tcgen05.ld, with no cross-thread traffic.
+//
+// Roles (warp specialised, one CTA per SM, persistent over work items):
+//   warp 0      TMA producer: streams 32 KB key tiles through a K-stage ring
+//               (L2 evict-first: each key is read once) and the G queries'
+//               iq block per work item (L2 evict-last: shared by many CTAs);
+//   warp 1      TMEM owner and UMMA issuer (one thread): 8 x (M128,N,K16)
+//               per tile into a ring of TMEM accumulators;
+//   warps 2..   epilogue: tcgen05.ld of the row's N accumulators, ReLU,
+//               weight, sum over heads, masked store of one fp32 per (q,row).
+// A work item is (unit, query group, chunk of 128-row tiles).
+//
+// The decode scan is HBM-bound (256 B of keys per row for 16 kFLOP); the
+// prefill chunk (G = 4) is tensor-bound.  Every wait is bounded: on timeout
+// the kernel flags DS4A_DEV_TIMEOUT, waits (bounded) for its copies and
+// UMMAs in flight, frees TMEM and returns.
+#include "common.cuh"
+#include "internal.h"
+
+namespace ds4a {
+namespace {
+
+constexpr int kTileRows = 128;   // UMMA M
+
+template <int G>
+struct IdxCfg {
+    static constexpr int N = 64 * G;                      // UMMA N
+    static constexpr int kStages = (G == 1) ? 5 : 4;      // key-tile ring depth
+    static constexpr int kBBufs = (G == 1) ? 2 : 1;       // iq block buffers
+    static constexpr int kAccBufs = (G == 1) ? 4 : 2;     // TMEM accumulators
+    static constexpr int kEpiSplit = (G == 1) ? 1 : 2;    // epilogue warps per TMEM lane quarter
+    static constexpr int kEpiWarps = 4 * kEpiSplit;
+    static constexpr int kQPerEpiWarp = G / kEpiSplit;    // queries one epilogue thread reduces
+    static constexpr int kThreads = 64 + 32 * kEpiWarps;
+    static constexpr uint32_t kTmemCols = kAccBufs * N;   // 256 or 512
+    static constexpr int kASub = kTileRows * 128;         // one 64-element K half of a key tile
+    static constexpr int kABytes = 2 * kASub;             // 32 KB
+    static constexpr int kBSub = N * 128;
+    static constexpr int kBBytes = 2 * kBSub;
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kOffA + kStages * kABytes;
+    static constexpr int kWFloatsPerWarp = kQPerEpiWarp * 64;
+    static constexpr int kOffW = kOffB + kBBufs * kBBytes;
+    static constexpr int kOffBar = kOffW + kEpiWarps * kWFloatsPerWarp * 4;
+    static constexpr int kNumBars = 2 * kStages + 2 * kBBufs + 2 * kAccBufs + 1;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + slack to 1024-align the base
+    static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation must be a power of two");
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+struct Item {
+    int u, g, t0, t1;
+};
+
+DS4A_DEV Item decode_item(const IndexerArgs &a, long long it) {
+    Item m;
+    const int per_unit = a.n_groups * a.n_chunks;
+    m.u = static_cast<int>(it / per_unit);
+    const int rem = static_cast<int>(it - static_cast<long long>(m.u) * per_unit);
+    m.g = rem / a.n_chunks;
+    const int c = rem - m.g * a.n_chunks;
+    int nr = a.n_rows[m.u];
+    nr = nr < 0 ? 0 : (nr > a.N_cap ? a.N_cap : nr);
+    const int nt = (nr + kTileRows - 1) / kTileRows;
+    m.t0 = c * a.chunk_tiles;
+    m.t1 = min(m.t0 + a.chunk_tiles, nt);
+    return m;
+}
+
+// Bounded wait that ignores the abort flag (used to drain in-flight work).
+DS4A_DEV bool mbar_wait_drain(uint64_t *bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
+// tcgen05.ld of 32 columns whose wait is tied to the destination registers,
+// so no use of them can be scheduled before the load has completed.
+DS4A_DEV void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+DS4A_DEV void tmem_wait_ld(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
+                   "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
+                   "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+DS4A_DEV void tmem_wait_ld2(uint32_t (&r)[32], uint32_t (&s)[32]) {
+    tmem_wait_ld(r);
+    // The second array's wait is already satisfied; this ties its registers too.
+    tmem_wait_ld(s);
+}
+
+template <int G>
+__global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
+    indexer_score_kernel(const __grid_constant__ IndexerArgs a) {
+    using C = IdxCfg<G>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sA = smem + C::kOffA;
+    uint8_t *sB = smem + C::kOffB;
+    float *sW = reinterpret_cast<float *>(smem + C::kOffW);
+    uint64_t *a_full = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
+    uint64_t *a_empty = a_full + C::kStages;
+    uint64_t *b_full = a_empty + C::kStages;
+    uint64_t *b_empty = b_full + C::kBBufs;
+    uint64_t *acc_full = b_empty + C::kBBufs;
+    uint64_t *acc_empty = acc_full + C::kAccBufs;
+    uint64_t *drain_bar = acc_empty + C::kAccBufs;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&a_full[s], 1);
+            mbar_init(&a_empty[s], 1);
+        }
+        for (int b = 0; b < C::kBBufs; ++b) {
+            mbar_init(&b_full[b], 1);
+            mbar_init(&b_empty[b], 1);
+        }
+        for (int c = 0; c < C::kAccBufs; ++c) {
+            mbar_init(&acc_full[c], 1);
+            mbar_init(&acc_empty[c], C::kEpiWarps);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+        tma_prefetch_desc(&a.tm_ik);
+        tma_prefetch_desc(&a.tm_iq);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const long long items = a.total_items;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_stream = l2_policy_evict_first();
+            const uint64_t pol_keep = l2_policy_evict_last();
+            int s = 0, bb = 0;
+            uint32_t sph = 0, bph = 0;
+            bool used_s[C::kStages] = {}, used_b[C::kBBufs] = {};
+            uint32_t par_s[C::kStages] = {}, par_b[C::kBBufs] = {};
+            bool ok = true;
+            for (long long it = blockIdx.x; ok && it < items; it += gridDim.x) {
+                const Item m = decode_item(a, it);
+                if (m.t0 >= m.t1) continue;
+                if (!mbar_wait(&b_empty[bb], bph ^ 1, abort_flag)) { ok = false; break; }
+                mbar_arrive_expect_tx(&b_full[bb], C::kBBytes);
+                const int qrow = (m.u * a.Q + m.g * G) * kNIdxHead;
+                uint8_t *dstB = sB + bb * C::kBBytes;
+                tma_load_2d(dstB, &a.tm_iq, &b_full[bb], 0, qrow, pol_keep);
+                tma_load_2d(dstB + C::kBSub, &a.tm_iq, &b_full[bb], 64, qrow, pol_keep);
+                used_b[bb] = true;
+                par_b[bb] = bph;
+                if (++bb == C::kBBufs) { bb = 0; bph ^= 1; }
+                for (int t = m.t0; t < m.t1; ++t) {
+                    if (!mbar_wait(&a_empty[s], sph ^ 1, abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&a_full[s], C::kABytes);
+                    uint8_t *dstA = sA + s * C::kABytes;
+                    tma_load_3d(dstA, &a.tm_ik, &a_full[s], 0, t * kTileRows, m.u, pol_stream);
+                    tma_load_3d(dstA + C::kASub, &a.tm_ik, &a_full[s], 64, t * kTileRows, m.u, pol_stream);
+                    used_s[s] = true;
+                    par_s[s] = sph;
+                    if (++s == C::kStages) { s = 0; sph ^= 1; }
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                report(a.status, DS4A_DEV_TIMEOUT);
+                // Let every copy already issued land before the CTA exits.
+                for (int i = 0; i < C::kStages; ++i)
+                    if (used_s[i]) mbar_wait_drain(&a_full[i], par_s[i]);
+                for (int i = 0; i < C::kBBufs; ++i)
+                    if (used_b[i]) mbar_wait_drain(&b_full[i], par_b[i]);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ UMMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(kTileRows, C::N);
+            int s = 0, bb = 0, ab = 0;
+            uint32_t sph = 0, bph = 0, aph = 0;
+            bool ok = true;
+            for (long long it = blockIdx.x; ok && it < items; it += gridDim.x) {
+                const Item m = decode_item(a, it);
+                if (m.t0 >= m.t1) continue;
+                if (!mbar_wait(&b_full[bb], bph, abort_flag)) { ok = false; break; }
+                const uint32_t b_addr = smem_u32(sB + bb * C::kBBytes);
+                for (int t = m.t0; t < m.t1; ++t) {
+                    if (!mbar_wait(&acc_empty[ab], aph ^ 1, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(&a_full[s], sph, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(sA + s * C::kABytes);
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * C::N);
+#pragma unroll
+                    for (int k = 0; k < kIdxDim / 16; ++k) {
+                        const uint32_t ka = (k >> 2) * C::kASub + (k & 3) * 32;
+                        const uint32_t kb = (k >> 2) * C::kBSub + (k & 3) * 32;
+                        umma_bf16(d_tmem, sw128_kmajor_desc(a_addr + ka), sw128_kmajor_desc(b_addr + kb), idesc,
+                                  k > 0 ? 1u : 0u);
+                    }
+                    umma_commit(&a_empty[s]);       // key tile may be overwritten once read
+                    umma_commit(&acc_full[ab]);     // accumulator ready for the epilogue
+                    if (++s == C::kStages) { s = 0; sph ^= 1; }
+                    if (++ab == C::kAccBufs) { ab = 0; aph ^= 1; }
+                }
+                if (!ok) break;
+                umma_commit(&b_empty[bb]);          // iq block free after this item's UMMAs
+                if (++bb == C::kBBufs) { bb = 0; bph ^= 1; }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                report(a.status, DS4A_DEV_TIMEOUT);
+            }
+            // Every UMMA issued has completed once this commit arrives.
+            umma_commit(drain_bar);
+            mbar_wait_drain(drain_bar, 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int e = warp - 2;
+        const int quarter = warp & 3;             // TMEM lanes this warp may access
+        const int half = e / 4;                   // which queries of the group
+        const int row_in_tile = quarter * 32 + lane;
+        float *wsm = sW + e * C::kWFloatsPerWarp;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        int ab = 0;
+        uint32_t aph = 0;
+        bool ok = true;
+        for (long long it = blockIdx.x; ok && it < items; it += gridDim.x) {
+            const Item m = decode_item(a, it);
+            if (m.t0 >= m.t1) continue;
+            const int nr_raw = a.n_rows[m.u];
+            if ((nr_raw < 0 || nr_raw > a.N_cap) && e == 0 && lane == 0 && m.t0 == 0 && m.g == 0)
+                report(a.status, DS4A_DEV_BOUNDS);
+            const int nr = nr_raw < 0 ? 0 : (nr_raw > a.N_cap ? a.N_cap : nr_raw);
+            const int q0 = m.g * G + half * C::kQPerEpiWarp;
+            __syncwarp();
+            for (int i = lane; i < C::kWFloatsPerWarp; i += 32) {
+                const int qq = q0 + i / kNIdxHead;
+                wsm[i] = (qq < a.Q) ? a.w[(static_cast<long long>(m.u) * a.Q + qq) * kNIdxHead + (i % kNIdxHead)]
+                                    : 0.f;
+            }
+            __syncwarp();
+            int qpos[C::kQPerEpiWarp];
+#pragma unroll
+            for (int j = 0; j < C::kQPerEpiWarp; ++j)
+                qpos[j] = (a.q_pos && q0 + j < a.Q) ? a.q_pos[static_cast<long long>(m.u) * a.Q + q0 + j] : 0;
+
+            for (int t = m.t0; t < m.t1; ++t) {
+                // Warp-uniform outcome: the tcgen05.ld below is .sync.aligned.
+                if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[ab], aph, abort_flag))) { ok = false; break; }
+                tc_fence_after();
+                const int row = t * kTileRows + row_in_tile;
+                int rpos = 0;
+                if (a.row_pos && row < nr) rpos = a.row_pos[static_cast<long long>(m.u) * a.N_cap + row];
+                float sc[C::kQPerEpiWarp];
+#pragma unroll
+                for (int j = 0; j < C::kQPerEpiWarp; ++j) {
+                    const uint32_t col = static_cast<uint32_t>(ab * C::N + (half * C::kQPerEpiWarp + j) * 64);
+                    uint32_t v0[32], v1[32];
+                    tmem_ld32_sync(tmem_base + lane_off + col, v0);
+                    tmem_ld32_sync(tmem_base + lane_off + col + 32, v1);
+                    tmem_wait_ld2(v0, v1);
+                    const float *wj = wsm + j * 64;
+                    float s = 0.f;
+#pragma unroll
+                    for (int h = 0; h < 32; ++h) s = fmaf(wj[h], fmaxf(__uint_as_float(v0[h]), 0.f), s);
+#pragma unroll
+                    for (int h = 0; h < 32; ++h) s = fmaf(wj[32 + h], fmaxf(__uint_as_float(v1[h]), 0.f), s);
+                    sc[j] = s;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[ab]);
+                if (row < nr) {
+#pragma unroll
+                    for (int j = 0; j < C::kQPerEpiWarp; ++j) {
+                        const int qq = q0 + j;
+                        if (qq < a.Q) {
+                            float out = sc[j];
+                            if (a.q_pos && rpos > qpos[j]) out = -__int_as_float(0x7f800000);
+                            a.scores[(static_cast<long long>(m.u) * a.Q + qq) * a.N_cap + row] = out;
+                        }
+                    }
+                }
+                if (++ab == C::kAccBufs) { ab = 0; aph ^= 1; }
+            }
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            if (lane == 0) report(a.status, DS4A_DEV_TIMEOUT);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+template <int G>
+cudaError_t launch_g(const IndexerArgs &a, cudaStream_t s) {
+    using C = IdxCfg<G>;
+    cudaError_t e = cudaFuncSetAttribute(indexer_score_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    indexer_score_kernel<G><<<a.grid, C::kThreads, C::kSmemBytes, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int indexer_group_size(int Q) { return Q >= 4 ? 4 : 1; }
+
+void indexer_plan(IndexerArgs &a, int num_sms) {
+    a.G = indexer_group_size(a.Q);
+    a.n_groups = (a.Q + a.G - 1) / a.G;
+    const int tiles_per_unit = (a.N_cap + kTileRows - 1) / kTileRows;
+    const long long work = static_cast<long long>(a.U) * a.n_groups;
+    int chunk = a.G == 1 ? 32 : 64;
+    while (chunk > 1 && work * ((tiles_per_unit + chunk - 1) / chunk) < 8LL * num_sms) chunk >>= 1;
+    a.chunk_tiles = chunk;
+    a.n_chunks = (tiles_per_unit + chunk - 1) / chunk;
+    a.total_items = work * a.n_chunks;
+    a.grid = static_cast<int>(a.total_items < num_sms ? a.total_items : num_sms);
+}
+
+cudaError_t launch_indexer_score(const IndexerArgs &a, cudaStream_t s) {
+    if (a.G == 4) return launch_g<4>(a, s);
+    return launch_g<1>(a, s);
+}
+
+}  // namespace ds4a

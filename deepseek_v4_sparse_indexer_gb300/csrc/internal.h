@@ -1,0 +1,80 @@
+// Internal launcher interface between the C ABI (ds4a_api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ds4a {
+
+constexpr int kNHead = 64;       // attention heads
+constexpr int kHeadDim = 512;    // row width
+constexpr int kNIdxHead = 64;    // indexer heads
+constexpr int kIdxDim = 128;     // indexer width
+constexpr int kNSwa = 128;       // raw window
+constexpr int kMaxTopK = 2048;
+
+// ---- indexer score -------------------------------------------------------
+struct IndexerArgs {
+    CUtensorMap tm_ik;          // 3-D (128, N_cap, U) bf16, box (64, 128, 1), 128B swizzle
+    CUtensorMap tm_iq;          // 2-D (128, U*Q*64) bf16, box (64, 64*G), 128B swizzle
+    const float *w;             // [U*Q][64]
+    const int32_t *n_rows;      // [U]
+    const int32_t *q_pos;       // [U*Q] or null
+    const int32_t *row_pos;     // [U*N_cap] or null
+    float *scores;              // [U*Q][N_cap]
+    uint32_t *status;
+    int U, Q, N_cap;
+    int G;                      // queries per UMMA (1 or 4)
+    int n_groups;               // ceil(Q / G)
+    int chunk_tiles;            // 128-row tiles per work item
+    int n_chunks;               // work items per (unit, group)
+    long long total_items;
+    int grid;
+};
+cudaError_t launch_indexer_score(const IndexerArgs &a, cudaStream_t s);
+int indexer_group_size(int Q);                       // G for a given Q
+void indexer_plan(IndexerArgs &a, int num_sms);      // fills n_groups .. grid
+
+// ---- top-k ---------------------------------------------------------------
+constexpr int kTopkBins = 4096;        // first radix digit: key bits 31..20
+constexpr int kTopkCandCap = 8192;     // candidate list capacity per (u,q)
+struct TopkArgs {
+    const float *scores;
+    const int32_t *n_rows;
+    int U, Q, N_cap, top_k;
+    int32_t *idx;
+    int32_t *count;
+    void *ws;
+    uint32_t *status;
+};
+size_t topk_ws_bytes(long long R, int top_k);
+cudaError_t launch_topk(const TopkArgs &a, int num_sms, cudaStream_t s);
+
+// ---- sparse attention ----------------------------------------------------
+struct AttnArgs {
+    const uint16_t *q;           // [units][64][512] bf16
+    const uint16_t *rows;        // bf16 rows base
+    long long rows_unit_stride;  // elements (0 in prefill: one shared row store)
+    int N_cap;
+    const int32_t *idx;          // [units][top_k]
+    const int32_t *count;        // [units]
+    int top_k;
+    const uint16_t *raw;         // fp16
+    long long raw_unit_stride;   // decode: per-unit ring stride (elements)
+    const int32_t *n_raw;        // decode: [units]; null in prefill
+    const int32_t *q_pos;        // prefill: [units]; null in decode
+    int raw_pos0, n_raw_rows;    // prefill raw buffer
+    float scale;
+    float *out;                  // [units][64][512]
+    float *lse;                  // [units][64] or null
+    int units;
+    void *ws;
+    uint32_t *status;
+};
+int attn_num_splits(int units, int top_k);
+size_t attn_ws_bytes(int units, int top_k);
+cudaError_t launch_sparse_attn(const AttnArgs &a, cudaStream_t s);
+
+}  // namespace ds4a

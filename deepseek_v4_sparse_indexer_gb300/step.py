@@ -1,0 +1,84 @@
+"""One pass of the three-tier compressed-attention step through the C ABI.
+
+DecodeStep: U units (sequence x layer caches), one query each.
+PrefillStep: one chunk of T queries of one sequence over a causal row store.
+
+Both own their outputs and workspaces (allocated once, reused every call, so a
+call can be captured in a CUDA graph) and run indexer score -> top-k select ->
+sparse attention on one CUDA stream, each op a C-ABI call into libds4a.so.
+"""
+import math
+
+import torch
+
+from . import _binding as B
+
+DEFAULT_SCALE = 1.0 / math.sqrt(B.HEAD_DIM)
+
+
+def _ws(nbytes, device):
+    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device) if nbytes else None
+
+
+class DecodeStep:
+    def __init__(self, U, N_cap, top_k=512, device="cuda"):
+        self.U, self.N_cap, self.top_k = U, N_cap, top_k
+        dev = torch.device(device)
+        self.scores = torch.empty(U, 1, N_cap, dtype=torch.float32, device=dev)
+        self.idx = torch.empty(U, 1, top_k, dtype=torch.int32, device=dev)
+        self.count = torch.empty(U, 1, dtype=torch.int32, device=dev)
+        self.out = torch.empty(U, B.N_HEAD, B.HEAD_DIM, dtype=torch.float32, device=dev)
+        self.lse = torch.empty(U, B.N_HEAD, dtype=torch.float32, device=dev)
+        self.ws_topk = _ws(B.ds4a_workspace_bytes(B.DS4A_OP_TOPK_SELECT, U, 1, N_cap, top_k), dev)
+        self.ws_attn = _ws(B.ds4a_workspace_bytes(B.DS4A_OP_SPARSE_ATTN_DECODE, U, 1, N_cap, top_k), dev)
+
+    def score(self, x, stream=None):
+        B.ds4a_indexer_score(x["iq"].view(self.U, 1, B.N_IDX_HEAD, B.IDX_DIM),
+                             x["w"].view(self.U, 1, B.N_IDX_HEAD), x["ik"], x["n_rows"], self.scores,
+                             stream=stream)
+
+    def select(self, x, stream=None):
+        B.ds4a_topk_select(self.scores, x["n_rows"], self.top_k, self.idx, self.count, self.ws_topk, stream=stream)
+
+    def attend(self, x, scale=DEFAULT_SCALE, stream=None):
+        B.ds4a_sparse_attn_decode(x["q"], x["rows"], self.idx.view(self.U, self.top_k), self.count.view(self.U),
+                                  x["raw"], x["n_raw"], scale, self.out, self.lse, self.ws_attn, stream=stream)
+
+    def __call__(self, x, scale=DEFAULT_SCALE, stream=None):
+        self.score(x, stream)
+        self.select(x, stream)
+        self.attend(x, scale, stream)
+        return self.out
+
+
+class PrefillStep:
+    def __init__(self, T, N_cap, top_k=512, device="cuda"):
+        self.T, self.N_cap, self.top_k = T, N_cap, top_k
+        dev = torch.device(device)
+        self.scores = torch.empty(1, T, N_cap, dtype=torch.float32, device=dev)
+        self.idx = torch.empty(1, T, top_k, dtype=torch.int32, device=dev)
+        self.count = torch.empty(1, T, dtype=torch.int32, device=dev)
+        self.out = torch.empty(T, B.N_HEAD, B.HEAD_DIM, dtype=torch.float32, device=dev)
+        self.lse = torch.empty(T, B.N_HEAD, dtype=torch.float32, device=dev)
+        self.ws_topk = _ws(B.ds4a_workspace_bytes(B.DS4A_OP_TOPK_SELECT, 1, T, N_cap, top_k), dev)
+        self.ws_attn = _ws(B.ds4a_workspace_bytes(B.DS4A_OP_SPARSE_ATTN_PREFILL, 1, T, N_cap, top_k), dev)
+
+    def score(self, x, stream=None):
+        T, N = self.T, self.N_cap
+        B.ds4a_indexer_score(x["iq"].view(1, T, B.N_IDX_HEAD, B.IDX_DIM), x["w"].view(1, T, B.N_IDX_HEAD),
+                             x["ik"].view(1, N, B.IDX_DIM), x["n_rows"], self.scores,
+                             q_pos=x["q_pos"].view(1, T), row_pos=x["row_pos"].view(1, N), stream=stream)
+
+    def select(self, x, stream=None):
+        B.ds4a_topk_select(self.scores, x["n_rows"], self.top_k, self.idx, self.count, self.ws_topk, stream=stream)
+
+    def attend(self, x, scale=DEFAULT_SCALE, stream=None):
+        B.ds4a_sparse_attn_prefill(x["q"], x["q_pos"], x["rows"], self.idx.view(self.T, self.top_k),
+                                   self.count.view(self.T), x["raw"], x["raw_pos0"], scale, self.out, self.lse,
+                                   self.ws_attn, stream=stream)
+
+    def __call__(self, x, scale=DEFAULT_SCALE, stream=None):
+        self.score(x, stream)
+        self.select(x, stream)
+        self.attend(x, scale, stream)
+        return self.out

@@ -1,0 +1,219 @@
+/*
+ * ds4a.h — C ABI of the GB300 (sm_103a) three-tier compressed-attention step
+ * of the DeepSeek V4 Flash engine described for DwarfStar (ds4).
+ *
+ * The step, per query token and layer (a "unit"):
+ *   1. indexer score  — score every compressed KV row with the light indexer
+ *                       (64 heads x 128 dims);
+ *   2. top-k select   — keep the 512 highest-scoring rows;
+ *   3. sparse attention — 64 query heads (head dim 512, one shared KV head)
+ *                       attend over those rows plus the 128-row raw window,
+ *                       in one joint softmax.
+ * Sources: "Redis 作者が DeepSeek V4 専用の推論エンジンを C で書いた ―
+ * DwarfStar(ds4.c) のアーキテクチャを読む【第1回/全8回】" (Qiita), §2
+ * (DS4_SHAPE_FLASH), §3 (three-tier attention), §3-1 (raw sliding-window KV,
+ * rows rounded through f16), §3-2 (compressed rows, ratio 4 with an indexer),
+ * §3-3 (indexer keys, one per compressed row; top-k rows go to attention);
+ * "antirez/ds4 深度阅读笔记", 固定模型形状 (fixed shapes).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers named as device buffers are CUDA device pointers owned by the
+ *    caller; the library never frees, keeps or allocates memory.  Scratch
+ *    memory, where an op needs it, is a caller-provided workspace `ws` of at
+ *    least ds4a_workspace_bytes(...) bytes (NULL/0 when that returns 0).
+ *  - bf16 and fp16 tensors are passed as uint16_t storage words.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every op only enqueues kernels on it and returns; nothing
+ *    synchronises except ds4a_get_device_status().
+ *  - The shapes of the pages are fixed at compile time: 64 attention heads x
+ *    512, 64 indexer heads x 128, raw window 128.  top_k is a runtime value in
+ *    [1, DS4A_MAX_TOP_K] (512 on Flash, 1024 on Pro).
+ *  - Arguments are validated on the host before anything is launched; a
+ *    failure returns a negative status and launches nothing.  A CUDA launch
+ *    error returns DS4A_ECUDA.  Conditions only the device can see (a row
+ *    index out of range, an internal wait that gave up) set bits in a
+ *    per-process device status word, read by ds4a_get_device_status().
+ *  - Thread-safety: entry points keep no host state between calls (the only
+ *    host global is the test hook ds4a_debug_inject_error) and may be called
+ *    concurrently on different streams.
+ */
+#ifndef DS4A_H
+#define DS4A_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int ds4a_status;
+
+#define DS4A_OK 0
+#define DS4A_EINVAL (-1)        /* bad pointer, size, alignment or value      */
+#define DS4A_EUNSUPPORTED (-2)  /* no device of compute capability 10.3       */
+#define DS4A_ECUDA (-3)         /* a CUDA runtime call or launch failed        */
+#define DS4A_EWORKSPACE (-4)    /* ws missing or smaller than required         */
+#define DS4A_EDEVICE (-5)       /* device status word has bits set             */
+
+/* Fixed shapes ("DwarfStar(ds4.c) のアーキテクチャを読む" §2 DS4_SHAPE_FLASH). */
+#define DS4A_N_HEAD 64          /* attention query heads (n_head)              */
+#define DS4A_HEAD_DIM 512       /* row width = head dim (n_head_kv = 1)        */
+#define DS4A_N_INDEXER_HEAD 64  /* n_indexer_head                              */
+#define DS4A_INDEXER_DIM 128    /* n_indexer_head_dim                          */
+#define DS4A_N_SWA 128          /* raw sliding window (n_swa)                  */
+#define DS4A_MAX_TOP_K 2048
+
+/* Bits of the device status word. */
+#define DS4A_DEV_TIMEOUT 1u     /* a bounded device-side wait gave up          */
+#define DS4A_DEV_BOUNDS 2u      /* a row index or count was out of range; the
+                                   offending row was masked out               */
+
+/* Ops for ds4a_workspace_bytes. */
+#define DS4A_OP_INDEXER_SCORE 0
+#define DS4A_OP_TOPK_SELECT 1
+#define DS4A_OP_SPARSE_ATTN_DECODE 2
+#define DS4A_OP_SPARSE_ATTN_PREFILL 3
+
+/* Human-readable text of a status code (static storage). */
+const char *ds4a_strerror(ds4a_status status);
+
+/* Library version, (major << 16) | minor. */
+int ds4a_version(void);
+
+/*
+ * Workspace bytes an op needs for the given sizes (0: pass ws = NULL).
+ * U = units, Q = queries per unit (prefill: T with U = 1), N_cap = row
+ * capacity per unit.  Returns (size_t)-1 for out-of-range sizes.
+ */
+size_t ds4a_workspace_bytes(int op, int U, int Q, int N_cap, int top_k);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word.  *flags (if not NULL) receives the DS4A_DEV_* bits.  Returns DS4A_OK
+ * when no bit was set, DS4A_EDEVICE when some were, DS4A_ECUDA on a CUDA error.
+ */
+ds4a_status ds4a_get_device_status(void *stream, unsigned *flags);
+
+/*
+ * Test hook: the next call of any compute entry point returns `code` without
+ * launching (0 disarms).  For exercising callers' error paths on the host.
+ */
+void ds4a_debug_inject_error(ds4a_status code);
+
+/*
+ * 1. Indexer score ("DwarfStar(ds4.c) のアーキテクチャを読む" §3-3: the
+ *    indexer's light query system scores each compressed row through its
+ *    128-d key; the pages print no formula, this library specifies it):
+ *
+ *      scores[u,q,r] = sum_h w[u,q,h] * max(0, sum_d iq[u,q,h,d] * ik[u,r,d])
+ *
+ *    bf16 inputs, fp32 accumulation on the tensor cores, fp32 result.
+ *
+ *    iq      bf16 [U][Q][64][128], contiguous (device).
+ *    w       fp32 [U][Q][64], contiguous (device).
+ *    ik      bf16 [U][N_cap][128]; unit u starts at ik + u*ik_unit_stride
+ *            elements (device).  ik and ik_unit_stride*2 bytes must be
+ *            16-byte aligned (the keys are streamed by TMA).
+ *    n_rows  int32 [U]: rows 0..n_rows[u]-1 of unit u exist, 0 <= n_rows[u]
+ *            <= N_cap (device).
+ *    q_pos, row_pos   NULL for decode.  For a causal prefill chunk: q_pos
+ *            int32 [U][Q] query positions and row_pos int32 [U][N_cap] (unit
+ *            stride N_cap) row positions; row r is visible to query q only
+ *            if row_pos[u,r] <= q_pos[u,q].  Both NULL or both set.
+ *    scores  fp32 [U][Q][N_cap] (device), written for r < n_rows[u];
+ *            -inf marks a row the query may not see.  Entries r >= n_rows[u]
+ *            are left untouched.
+ *    Sizes: U >= 1, Q >= 1, N_cap >= 1, U*Q*N_cap < 2^40.
+ */
+ds4a_status ds4a_indexer_score(const uint16_t *iq, const float *w, const uint16_t *ik,
+                               int64_t ik_unit_stride, const int32_t *n_rows,
+                               const int32_t *q_pos, const int32_t *row_pos,
+                               float *scores, int U, int Q, int N_cap, void *stream);
+
+/*
+ * 2. Top-k select (§3-3: only the n_indexer_top_k highest-scoring compressed
+ *    rows reach the main attention).  For each (u,q): among rows r <
+ *    n_rows[u] whose score is neither -inf nor NaN, select the top_k highest
+ *    scores; equal scores prefer the lower row index.  -0.0 and +0.0 compare
+ *    equal.
+ *
+ *    scores  fp32 [U][Q][N_cap] (device), as written by ds4a_indexer_score.
+ *    n_rows  int32 [U] (device).
+ *    idx     int32 [U][Q][top_k] (device): the selected row indices in
+ *            ascending order, then -1 padding.
+ *    count   int32 [U][Q] (device): number selected = min(top_k, visible).
+ *    ws      workspace of ds4a_workspace_bytes(DS4A_OP_TOPK_SELECT, U, Q,
+ *            N_cap, top_k) bytes, 256-byte aligned (device).
+ */
+ds4a_status ds4a_topk_select(const float *scores, const int32_t *n_rows, int U, int Q,
+                             int N_cap, int top_k, int32_t *idx, int32_t *count,
+                             void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * 3a. Sparse attention, decode (one query per unit; §3 three tiers: the raw
+ *    window plus the indexer-selected compressed rows, one KV head whose
+ *    512-d rows serve as key and value).  Per unit u and head h, over the
+ *    joint row set X = {rows[u, idx[u,j]] : j < count[u]} U {raw[u, s] : s <
+ *    n_raw[u]}:
+ *
+ *      l_j = scale * q[u,h,:] . x_j ;  a = softmax(l) ;  out[u,h,:] = sum_j a_j x_j
+ *      lse[u,h] = log sum_j exp(l_j)            (natural log)
+ *
+ *    fp32 softmax and accumulation on the tensor cores.  Compressed rows
+ *    multiply in bf16; raw rows (kept rounded to f16, §3-1) multiply in fp16
+ *    with q rounded to fp16 and the probabilities in fp16.  An empty row set
+ *    gives out = 0, lse = -inf.
+ *
+ *    q       bf16 [U][64][512] (device).
+ *    rows    bf16 [U][N_cap][512]; unit u at rows + u*rows_unit_stride (device).
+ *    idx     int32 [U][top_k], count int32 [U] (device), as from
+ *            ds4a_topk_select with Q = 1.  An index outside [0, N_cap) or a
+ *            count outside [0, top_k] sets DS4A_DEV_BOUNDS and is masked.
+ *    raw     fp16 [U][128][512] raw-window ring; unit u at raw +
+ *            u*raw_unit_stride; slots 0..n_raw[u]-1 valid, in any order
+ *            (softmax does not depend on row order) (device).
+ *    n_raw   int32 [U], 0..128 (device).
+ *    out     fp32 [U][64][512] (device).   lse   fp32 [U][64] or NULL (device).
+ *    ws      workspace of ds4a_workspace_bytes(DS4A_OP_SPARSE_ATTN_DECODE, U, 1,
+ *            N_cap, top_k) bytes (used when units are few and each unit's row
+ *            set is split over several CTAs).
+ *    All row buffers and q must be 16-byte aligned; strides multiples of 8.
+ */
+ds4a_status ds4a_sparse_attn_decode(const uint16_t *q, const uint16_t *rows,
+                                    int64_t rows_unit_stride, int N_cap,
+                                    const int32_t *idx, const int32_t *count, int top_k,
+                                    const uint16_t *raw, int64_t raw_unit_stride,
+                                    const int32_t *n_raw, float scale, float *out, float *lse,
+                                    int U, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * 3b. Sparse attention, one prefill chunk of T queries of one sequence (the
+ *    engine prefills in 2,048-token chunks).  Query t (position q_pos[t])
+ *    attends over its own selected compressed rows {rows[idx[t,j]] : j <
+ *    count[t]} and the raw rows at positions q_pos[t]-127 .. q_pos[t] (the
+ *    128 tokens ending at the query, its own row included) that the raw
+ *    buffer holds.  Same arithmetic as 3a.
+ *
+ *    q       bf16 [T][64][512] (device).    q_pos  int32 [T] (device).
+ *    rows    bf16 [N_cap][512] (device).
+ *    idx     int32 [T][top_k], count int32 [T] (device), from the causal
+ *            scores (so every selected row is at or before its query).
+ *    raw     fp16 [n_raw_rows][512] (device): row i holds position raw_pos0 + i.
+ *    out     fp32 [T][64][512]; lse fp32 [T][64] or NULL (device).
+ *    ws      workspace of ds4a_workspace_bytes(DS4A_OP_SPARSE_ATTN_PREFILL, 1, T,
+ *            N_cap, top_k) bytes.
+ */
+ds4a_status ds4a_sparse_attn_prefill(const uint16_t *q, const int32_t *q_pos,
+                                     const uint16_t *rows, int N_cap,
+                                     const int32_t *idx, const int32_t *count, int top_k,
+                                     const uint16_t *raw, int32_t raw_pos0, int n_raw_rows,
+                                     float scale, float *out, float *lse, int T,
+                                     void *ws, size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DS4A_H */

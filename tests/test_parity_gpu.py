@@ -1,0 +1,352 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Small cases cover several tiles and ragged tails, every branch of the kernels
+(query groups, split rows, candidate-list overflow, empty sets, out-of-range
+indices), and stress inputs with a peaked softmax; the five workloads are
+checked in full where the oracle finishes in seconds, and on sampled units /
+queries at full size.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from deepseek_v4_sparse_indexer_gb300 import DecodeStep, PrefillStep, _binding as B
+from deepseek_v4_sparse_indexer_gb300.workloads import WORKLOADS, make_decode_inputs, make_prefill_inputs
+from tests.parity_util import (check_index_set, check_output, check_scores, pool, score_tolerance, u16)
+
+pytestmark = pytest.mark.gpu
+SCALE = 1.0 / math.sqrt(512)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_lib):
+    yield
+    torch.cuda.synchronize()
+
+
+def device_ok():
+    st, flags = B.ds4a_get_device_status()
+    assert st == B.DS4A_OK and flags == 0, f"device status flags {flags}"
+
+
+# ----------------------------------------------------------------------------
+# decode: unit-level check shared by the tests below
+# ----------------------------------------------------------------------------
+
+def check_decode_unit(x, st, u, top_k, scale, check_sc=True):
+    n = int(x["n_rows"][u])
+    nraw = int(x["n_raw"][u])
+    iq = u16(x["iq"][u])
+    w = x["w"][u].cpu().numpy()
+    ik = u16(x["ik"][u, :max(n, 1)])
+    ref = oracle.indexer_score(iq[None], w[None], ik, n)[0][:n]
+    gpu_s = st.scores[u, 0, :n].cpu().numpy()
+    if check_sc:
+        check_scores(gpu_s, ref, score_tolerance(iq, w, ik, n))
+    cnt = int(st.count[u, 0])
+    gidx = st.idx[u, 0].cpu().numpy()
+    swaps = check_index_set(gidx, cnt, ref, top_k)
+    rows = u16(x["rows"][u, :max(n, 1)])
+    raw = u16(x["raw"][u])
+    out, lse = oracle.sparse_attention(u16(x["q"][u]), rows, gidx[:cnt], raw, np.arange(nraw), scale)
+    stats = check_output(st.out[u].cpu().numpy(), out, st.lse[u].cpu().numpy(), lse)
+    stats["swaps"] = swaps
+    return stats
+
+
+def run_decode(x, top_k, scale=SCALE):
+    U, N_cap = x["ik"].shape[:2]
+    st = DecodeStep(U, N_cap, top_k)
+    st(x, scale)
+    torch.cuda.synchronize()
+    device_ok()
+    return st
+
+
+# ----------------------------------------------------------------------------
+# A1 indexer score
+# ----------------------------------------------------------------------------
+
+def test_indexer_scores_decode_ragged_and_untouched_tail():
+    x = make_decode_inputs(3, 300, device="cuda", seed=1, n_rows=[300, 129, 1])
+    scores = torch.full((3, 1, 300), 12345.0, device="cuda")
+    B.ds4a_indexer_score(x["iq"].view(3, 1, 64, 128), x["w"].view(3, 1, 64), x["ik"], x["n_rows"], scores)
+    torch.cuda.synchronize()
+    device_ok()
+    for u, n in enumerate([300, 129, 1]):
+        iq, w, ik = u16(x["iq"][u]), x["w"][u].cpu().numpy(), u16(x["ik"][u])
+        ref = oracle.indexer_score(iq[None], w[None], ik, n)[0]
+        check_scores(scores[u, 0, :n].cpu().numpy(), ref[:n], score_tolerance(iq, w, ik, n))
+        assert torch.all(scores[u, 0, n:] == 12345.0)
+
+
+@pytest.mark.parametrize("Q", [2, 4, 6, 9])
+def test_indexer_scores_query_groups_with_positions(Q):
+    U, N_cap = 2, 400
+    g = torch.Generator().manual_seed(Q)
+    iq = (torch.randn(U, Q, 64, 128, generator=g) / math.sqrt(128)).to(torch.bfloat16).cuda()
+    w = torch.rand(U, Q, 64, generator=g).cuda()
+    ik = (torch.randn(U, N_cap, 128, generator=g) / math.sqrt(128)).to(torch.bfloat16).cuda()
+    n_rows = torch.tensor([400, 333], dtype=torch.int32).cuda()
+    row_pos = torch.sort(torch.randint(0, 2000, (U, N_cap), generator=g), dim=1).values.to(torch.int32).cuda()
+    q_pos = torch.randint(0, 2100, (U, Q), generator=g).to(torch.int32).cuda()
+    scores = torch.empty(U, Q, N_cap, device="cuda")
+    B.ds4a_indexer_score(iq, w, ik, n_rows, scores, q_pos=q_pos, row_pos=row_pos)
+    torch.cuda.synchronize()
+    device_ok()
+    for u in range(U):
+        n = int(n_rows[u])
+        iqn, wn, ikn = u16(iq[u]), w[u].cpu().numpy(), u16(ik[u])
+        ref = oracle.indexer_score(iqn, wn, ikn, n, q_pos=q_pos[u].cpu().numpy(), row_pos=row_pos[u].cpu().numpy())
+        for q in range(Q):
+            tol = score_tolerance(iqn[q], wn[q], ikn, n)
+            check_scores(scores[u, q, :n].cpu().numpy(), ref[q, :n], tol)
+
+
+# ----------------------------------------------------------------------------
+# A2 top-k on given scores: bit-exact against the oracle
+# ----------------------------------------------------------------------------
+
+def topk_case(rows_f32, n_rows, top_k):
+    """rows_f32: float32 [R, N_cap] (one unit per row); checks every row exactly."""
+    R, N_cap = rows_f32.shape
+    s = torch.from_numpy(rows_f32).cuda().view(R, 1, N_cap)
+    nr = torch.tensor(n_rows, dtype=torch.int32).cuda()
+    idx = torch.full((R, 1, top_k), 777, dtype=torch.int32, device="cuda")
+    cnt = torch.full((R, 1), -5, dtype=torch.int32, device="cuda")
+    ws = torch.empty(B.ds4a_workspace_bytes(B.DS4A_OP_TOPK_SELECT, R, 1, N_cap, top_k), dtype=torch.uint8,
+                     device="cuda")
+    B.ds4a_topk_select(s, nr, top_k, idx, cnt, ws)
+    torch.cuda.synchronize()
+    device_ok()
+    for r in range(R):
+        n = n_rows[r]
+        ref_idx, _ = oracle.topk_select(rows_f32[r, :n].astype(np.float64), top_k)
+        c = int(cnt[r, 0])
+        got = idx[r, 0].cpu().numpy()
+        assert c == len(ref_idx), (r, c, len(ref_idx))
+        assert np.array_equal(got[:c], ref_idx), f"row {r}"
+        assert np.all(got[c:] == -1)
+
+
+def test_topk_random_and_ragged():
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal((5, 5000)).astype(np.float32)
+    topk_case(x, [5000, 4999, 513, 512, 77], 512)
+
+
+def test_topk_ties_neginf_nan_and_signed_zero():
+    rng = np.random.default_rng(1)
+    x = (np.round(rng.standard_normal((4, 3000)) * 2) / 2).astype(np.float32)   # heavy ties
+    x[0, rng.random(3000) < 0.3] = -np.inf
+    x[1, rng.random(3000) < 0.1] = np.nan
+    x[2] = 0.0
+    x[2, ::2] = -0.0                                                          # -0 == +0: lower rows win
+    x[2, 5:20] = 1.0
+    x[3] = -np.abs(x[3])                                                      # all negative
+    topk_case(x, [3000, 3000, 3000, 2999], 100)
+
+
+@pytest.mark.parametrize("k", [1, 7, 2048])
+def test_topk_k_extremes(k):
+    rng = np.random.default_rng(k)
+    x = rng.standard_normal((3, 4096)).astype(np.float32)
+    topk_case(x, [4096, 1000, 3], k)
+
+
+def test_topk_all_equal_small_and_overflowing_candidates():
+    # 3000 equal scores fit the candidate list; 20000 overflow it (fallback path).
+    topk_case(np.full((2, 3000), 0.5, np.float32), [3000, 2500], 512)
+    topk_case(np.full((2, 20000), 0.25, np.float32), [20000, 19999], 512)
+
+
+def test_topk_one_long_row_split_over_many_ctas():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((1, 262144)).astype(np.float32)
+    x[0, rng.random(262144) < 0.05] *= 4
+    topk_case(x, [262144], 512)
+
+
+# ----------------------------------------------------------------------------
+# A4 attention on given row sets
+# ----------------------------------------------------------------------------
+
+def attention_case(U, N_cap, top_k, seed, q_scale=1.0, n_raw=None):
+    rng = np.random.default_rng(seed)
+    x = make_decode_inputs(U, N_cap, device="cuda", seed=seed, q_scale=q_scale,
+                           n_raw=n_raw if n_raw is not None else list(rng.integers(0, 129, U)))
+    idx = np.full((U, top_k), -1, np.int32)
+    cnt = rng.integers(0, top_k + 1, U).astype(np.int32)
+    cnt[0] = top_k
+    for u in range(U):
+        idx[u, :cnt[u]] = np.sort(rng.choice(N_cap, size=cnt[u], replace=False))
+    idx_t, cnt_t = torch.from_numpy(idx).cuda(), torch.from_numpy(cnt).cuda()
+    out = torch.empty(U, 64, 512, device="cuda")
+    lse = torch.empty(U, 64, device="cuda")
+    nb = B.ds4a_workspace_bytes(B.DS4A_OP_SPARSE_ATTN_DECODE, U, 1, N_cap, top_k)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda") if nb else None
+    B.ds4a_sparse_attn_decode(x["q"], x["rows"], idx_t, cnt_t, x["raw"], x["n_raw"], SCALE, out, lse, ws)
+    torch.cuda.synchronize()
+    device_ok()
+
+    def one(u):
+        nraw = int(x["n_raw"][u])
+        ro, rl = oracle.sparse_attention(u16(x["q"][u]), u16(x["rows"][u]), idx[u, :cnt[u]], u16(x["raw"][u]),
+                                         np.arange(nraw), SCALE)
+        return check_output(out[u].cpu().numpy(), ro, lse[u].cpu().numpy(), rl)
+
+    with pool() as p:
+        return list(p.map(one, range(U)))
+
+
+@pytest.mark.parametrize("q_scale", [1.0, 32.0])
+def test_attention_split_rows_few_units(q_scale):
+    attention_case(3, 2000, 512, seed=11, q_scale=q_scale)
+
+
+@pytest.mark.parametrize("q_scale", [1.0, 32.0])
+def test_attention_one_cta_per_unit(q_scale):
+    attention_case(160, 700, 512, seed=12, q_scale=q_scale)
+
+
+def test_attention_raw_window_extremes_and_odd_k():
+    attention_case(4, 300, 100, seed=13, n_raw=[0, 1, 127, 128])
+
+
+def test_attention_empty_row_set():
+    x = make_decode_inputs(2, 64, device="cuda", seed=3, n_raw=[0, 0])
+    idx = torch.full((2, 512), -1, dtype=torch.int32, device="cuda")
+    cnt = torch.zeros(2, dtype=torch.int32, device="cuda")
+    out = torch.full((2, 64, 512), 7.0, device="cuda")
+    lse = torch.zeros(2, 64, device="cuda")
+    ws = torch.empty(B.ds4a_workspace_bytes(B.DS4A_OP_SPARSE_ATTN_DECODE, 2, 1, 64, 512), dtype=torch.uint8,
+                     device="cuda")
+    B.ds4a_sparse_attn_decode(x["q"], x["rows"], idx, cnt, x["raw"], x["n_raw"], SCALE, out, lse, ws)
+    torch.cuda.synchronize()
+    device_ok()
+    assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
+
+
+def test_attention_out_of_range_index_is_masked_and_flagged():
+    U, N_cap = 160, 256
+    x = make_decode_inputs(U, N_cap, device="cuda", seed=4, n_raw=[5] * U)
+    rng = np.random.default_rng(4)
+    idx = np.stack([np.sort(rng.choice(N_cap, 64, replace=False)) for _ in range(U)]).astype(np.int32)
+    bad = idx.copy()
+    bad[0, 3] = N_cap + 5
+    bad[1, 0] = -3
+    out = torch.empty(U, 64, 512, device="cuda")
+    cnt = torch.full((U,), 64, dtype=torch.int32, device="cuda")
+    B.ds4a_sparse_attn_decode(x["q"], x["rows"], torch.from_numpy(bad).cuda(), cnt, x["raw"], x["n_raw"], SCALE,
+                              out, None, None)
+    st, flags = B.ds4a_get_device_status()
+    assert st == B.DS4A_EDEVICE and flags & B.DS4A_DEV_BOUNDS
+    for u, keep in [(0, np.delete(idx[0], 3)), (1, idx[1, 1:]), (2, idx[2])]:
+        ro, _ = oracle.sparse_attention(u16(x["q"][u]), u16(x["rows"][u]), keep, u16(x["raw"][u]), np.arange(5),
+                                        SCALE)
+        check_output(out[u].cpu().numpy(), ro)
+    device_ok()
+
+
+# ----------------------------------------------------------------------------
+# Whole decode step
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("q_scale", [1.0, 32.0])
+def test_decode_step_small_ragged(q_scale):
+    x = make_decode_inputs(2, 1000, device="cuda", seed=21, n_rows=[1000, 555], n_raw=[128, 37], q_scale=q_scale)
+    st = run_decode(x, 512)
+    for u in range(2):
+        check_decode_unit(x, st, u, 512, SCALE)
+
+
+def test_decode_step_fewer_rows_than_k():
+    x = make_decode_inputs(2, 700, device="cuda", seed=22, n_rows=[300, 0], n_raw=[128, 10])
+    st = run_decode(x, 512)
+    for u in range(2):
+        check_decode_unit(x, st, u, 512, SCALE)
+    assert int(st.count[1, 0]) == 0
+
+
+@pytest.mark.parametrize("name", ["decode_1x1024", "decode_8x16384"])
+def test_workload_decode_full(name):
+    wl = WORKLOADS[name]
+    x = make_decode_inputs(wl.units, wl.n_rows, device="cuda", seed=wl.seed)
+    st = run_decode(x, wl.top_k)
+    with pool() as p:
+        list(p.map(lambda u: check_decode_unit(x, st, u, wl.top_k, SCALE), range(wl.units)))
+
+
+@pytest.mark.slow
+def test_workload_longctx_4x262144_full():
+    wl = WORKLOADS["longctx_4x262144"]
+    x = make_decode_inputs(wl.units, wl.n_rows, device="cuda", seed=wl.seed, heavy_frac=wl.heavy_frac,
+                           heavy_scale=wl.heavy_scale)
+    st = run_decode(x, wl.top_k)
+    with pool() as p:
+        list(p.map(lambda u: check_decode_unit(x, st, u, wl.top_k, SCALE), range(wl.units)))
+
+
+@pytest.mark.slow
+def test_workload_decode_32x43x65536_sampled():
+    wl = WORKLOADS["decode_32x43x65536"]
+    x = make_decode_inputs(wl.units, wl.n_rows, device="cuda", seed=wl.seed)
+    st = run_decode(x, wl.top_k)
+    units = [0, 1, 42, 687, 1000, wl.units - 1]
+    with pool() as p:
+        list(p.map(lambda u: check_decode_unit(x, st, u, wl.top_k, SCALE), units))
+    del x, st
+    torch.cuda.empty_cache()
+
+
+# ----------------------------------------------------------------------------
+# Prefill chunk
+# ----------------------------------------------------------------------------
+
+def check_prefill_query(x, st, t, top_k, scale, np_in):
+    q, iq, w, ik, rows, row_pos, q_pos, raw = np_in
+    n = int(x["n_rows"][0])
+    res = oracle.prefill_query(t, q, iq, w, ik, rows, n, row_pos, q_pos, raw, x["raw_pos0"], top_k, scale)
+    gpu_s = st.scores[0, t].cpu().numpy()
+    tol = score_tolerance(iq[t], w[t], ik, n)
+    check_scores(gpu_s[:n], res["scores"][:n], tol)
+    cnt = int(st.count[0, t])
+    gidx = st.idx[0, t].cpu().numpy()
+    check_index_set(gidx, cnt, res["scores"][:n], top_k)
+    assert np.all(row_pos[gidx[:cnt]] <= q_pos[t])
+    ro, rl = oracle.sparse_attention(q[t], rows, gidx[:cnt], raw, res["window"], scale)
+    return check_output(st.out[t].cpu().numpy(), ro, st.lse[t].cpu().numpy(), rl)
+
+
+def prefill_numpy(x):
+    return (u16(x["q"]), u16(x["iq"]), x["w"].cpu().numpy(), u16(x["ik"]), u16(x["rows"]),
+            x["row_pos"].cpu().numpy(), x["q_pos"].cpu().numpy(), u16(x["raw"]))
+
+
+@pytest.mark.parametrize("T,prior,top_k,q_scale", [(64, 100, 32, 1.0), (37, 300, 512, 1.0), (64, 600, 256, 32.0)])
+def test_prefill_small(T, prior, top_k, q_scale):
+    x = make_prefill_inputs(T, prior, device="cuda", seed=T + prior, q_scale=q_scale)
+    st = PrefillStep(T, x["ik"].shape[0], top_k)
+    st(x, SCALE)
+    torch.cuda.synchronize()
+    device_ok()
+    np_in = prefill_numpy(x)
+    with pool() as p:
+        list(p.map(lambda t: check_prefill_query(x, st, t, top_k, SCALE, np_in), range(T)))
+
+
+@pytest.mark.slow
+def test_workload_prefill_2048x65536_sampled():
+    wl = WORKLOADS["prefill_2048x65536"]
+    x = make_prefill_inputs(wl.queries, wl.extra["prior_rows"], device="cuda", seed=wl.seed)
+    st = PrefillStep(wl.queries, x["ik"].shape[0], wl.top_k)
+    st(x, SCALE)
+    torch.cuda.synchronize()
+    device_ok()
+    np_in = prefill_numpy(x)
+    ts = [0, 1, 2, 3, 4, 127, 128, 1000, 2043, 2044, 2046, 2047]
+    with pool() as p:
+        list(p.map(lambda t: check_prefill_query(x, st, t, wl.top_k, SCALE, np_in), ts))
