@@ -32,7 +32,8 @@ N_HEAD, HEAD_DIM, N_IDX_HEAD, IDX_DIM, N_SWA = 64, 512, 64, 128, 128
 # The C entry points this binding (and include/ds4a.h) exposes.
 EXPORTS = ("ds4a_strerror", "ds4a_version", "ds4a_workspace_bytes", "ds4a_get_device_status",
            "ds4a_debug_inject_error", "ds4a_indexer_score", "ds4a_topk_select",
-           "ds4a_sparse_attn_decode", "ds4a_sparse_attn_prefill")
+           "ds4a_topk_select_noalloc", "ds4a_sparse_attn_decode", "ds4a_sparse_attn_prefill")
+DS4A_TOPK_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class Ds4aError(RuntimeError):
@@ -73,6 +74,8 @@ def load(build_if_missing: bool = True):
     L.ds4a_indexer_score.restype = _i32
     L.ds4a_topk_select.argtypes = [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _sz, _vp]
     L.ds4a_topk_select.restype = _i32
+    L.ds4a_topk_select_noalloc.argtypes = [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp]
+    L.ds4a_topk_select_noalloc.restype = _i32
     L.ds4a_sparse_attn_decode.argtypes = [_vp, _vp, _i64, _i32, _vp, _vp, _i32, _vp, _i64, _vp, _f32, _vp, _vp,
                                           _i32, _vp, _sz, _vp]
     L.ds4a_sparse_attn_decode.restype = _i32
@@ -181,6 +184,22 @@ def ds4a_topk_select(scores, n_rows, top_k, idx, count, ws, stream=None):
     st = load().ds4a_topk_select(_ptr(scores), _ptr(n_rows), U, Q, N_cap, top_k, _ptr(idx), _ptr(count), _ptr(ws),
                                  ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream))
     _check(st, "ds4a_topk_select")
+
+
+def ds4a_topk_select_noalloc(scores, n_rows, top_k, idx, count, stream=None):
+    """Same result as ds4a_topk_select, with no workspace argument: the scratch
+    is the library's fixed 8 MiB device array.  For callers that cannot
+    allocate device memory; calls on one device must not overlap on the GPU."""
+    _req(scores, "scores", torch.float32)
+    _req(n_rows, "n_rows", torch.int32)
+    _req(idx, "idx", torch.int32)
+    _req(count, "count", torch.int32)
+    U, Q, N_cap = scores.shape
+    if idx.shape != (U, Q, top_k) or count.shape != (U, Q):
+        raise ValueError("idx / count shape")
+    st = load().ds4a_topk_select_noalloc(_ptr(scores), _ptr(n_rows), U, Q, N_cap, top_k, _ptr(idx), _ptr(count),
+                                         _stream(stream))
+    _check(st, "ds4a_topk_select_noalloc")
 
 
 def ds4a_sparse_attn_decode(q, rows, idx, count, raw, n_raw, scale, out, lse=None, ws=None, stream=None):

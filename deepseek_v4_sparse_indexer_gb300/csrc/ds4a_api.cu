@@ -89,6 +89,18 @@ ds4a_status take_injected() {
 
 }  // namespace
 
+namespace ds4a {
+int current_device_info(uint32_t **status, int *sms) {
+    DevInfo *di = nullptr;
+    const ds4a_status st = current_device(&di);
+    if (st) return st;
+    *status = di->status;
+    *sms = di->sms;
+    return DS4A_OK;
+}
+int take_injected_error() { return take_injected(); }
+}  // namespace ds4a
+
 extern "C" {
 
 const char *ds4a_strerror(ds4a_status s) {

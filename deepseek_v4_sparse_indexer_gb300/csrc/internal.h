@@ -77,4 +77,10 @@ int attn_num_splits(int units, int top_k);
 size_t attn_ws_bytes(int units, int top_k);
 cudaError_t launch_sparse_attn(const AttnArgs &a, cudaStream_t s);
 
+// ---- shared host helpers of the C ABI -------------------------------------
+// Status word address and SM count of the current device (set up on first use).
+int current_device_info(uint32_t **status, int *sms);
+// Returns (and disarms) the error code armed by ds4a_debug_inject_error, or 0.
+int take_injected_error();
+
 }  // namespace ds4a

@@ -151,6 +151,41 @@ ds4a_status ds4a_topk_select(const float *scores, const int32_t *n_rows, int U, 
                              int N_cap, int top_k, int32_t *idx, int32_t *count,
                              void *ws, size_t ws_bytes, void *stream);
 
+/* Capacity of the scratch array behind ds4a_topk_select_noalloc (bytes). */
+#define DS4A_TOPK_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * 2'. Top-k select with no workspace argument, for callers that cannot
+ *    allocate device memory.  The pages have no counterpart: this is a service
+ *    of the library, not a step of the method.
+ *
+ *    Some callers cannot call cudaMalloc or hand over a buffer: a plugin
+ *    running inside a serving engine that has reserved the device's memory for
+ *    its own pool, or a runtime with a fixed memory plan decided before it
+ *    starts.  This entry point computes exactly what ds4a_topk_select computes
+ *    (same kernels, same results), with its scratch in a fixed array of
+ *    DS4A_TOPK_NOALLOC_SCRATCH_BYTES (8 MiB) in the library's device memory;
+ *    every GPU that loads the library holds that array until the process exits.
+ *
+ *    Limits and rules:
+ *    - the request must fit: ds4a_workspace_bytes(DS4A_OP_TOPK_SELECT, U, Q,
+ *      N_cap, top_k) <= DS4A_TOPK_NOALLOC_SCRATCH_BYTES (up to 99 (u, q)
+ *      rows at top_k 512, 93 at top_k 2048, whatever N_cap); a larger request returns
+ *      DS4A_EWORKSPACE and launches nothing;
+ *    - the first call on a device looks up the array's device address (one
+ *      cudaGetSymbolAddress with that device current); make that first call
+ *      before any stream capture;
+ *    - all calls on a device share the one array, and it keeps what the last
+ *      call left (each call clears what must start at zero): calls whose
+ *      kernels overlap on the GPU (other streams, other threads) race and give
+ *      wrong results; serialise them on one stream;
+ *    - it calls no cudaMalloc, cudaFree or allocating routine.
+ *    Arguments as for ds4a_topk_select.
+ */
+ds4a_status ds4a_topk_select_noalloc(const float *scores, const int32_t *n_rows, int U, int Q,
+                                     int N_cap, int top_k, int32_t *idx, int32_t *count,
+                                     void *stream);
+
 /*
  * 3a. Sparse attention, decode (one query per unit; §3 three tiers: the raw
  *    window plus the indexer-selected compressed rows, one KV head whose
