@@ -44,6 +44,8 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU work budget of the oracle sample")
+    p.add_argument("--units", type=int, default=None,
+                   help="decode workloads: run only this many units (small cases for profiling)")
     return p.parse_args()
 
 
@@ -274,6 +276,9 @@ def main():
     if args.workload not in WORKLOADS:
         raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(WORKLOADS)}")
     wl = WORKLOADS[args.workload]
+    if args.units is not None and wl.kind == "decode":
+        import dataclasses
+        wl = dataclasses.replace(wl, name=f"{wl.name}[units={args.units}]", units=args.units)
     if args.impl == "reference":
         return run_reference(args, wl)
     if args.warmup < 3:

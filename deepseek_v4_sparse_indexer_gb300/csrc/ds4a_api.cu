@@ -99,6 +99,18 @@ int current_device_info(uint32_t **status, int *sms) {
     return DS4A_OK;
 }
 int take_injected_error() { return take_injected(); }
+bool encode_2d_sw128(CUtensorMap *m, bool f16, const void *base, unsigned long long cols, unsigned long long rows,
+                     unsigned box_cols, unsigned box_rows) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return f(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base),
+             dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 }  // namespace ds4a
 
 extern "C" {
@@ -228,9 +240,15 @@ ds4a_status ds4a_sparse_attn_decode(const uint16_t *q, const uint16_t *rows, int
     if (ds4a_status inj = take_injected()) return inj;
     if (ds4a_status st = check_attn_common(q, rows, N_cap, idx, count, top_k, out)) return st;
     if (!raw || !n_raw || U < 1) return DS4A_EINVAL;
-    if (!aligned(raw, 16) || (rows_unit_stride & 7) || (raw_unit_stride & 7)) return DS4A_EINVAL;
-    if (U > 1 && (rows_unit_stride < static_cast<int64_t>(N_cap) * kHeadDim ||
-                  raw_unit_stride < static_cast<int64_t>(kNSwa) * kHeadDim))
+    if (!aligned(raw, 16)) return DS4A_EINVAL;
+    if (U > 1 && (rows_unit_stride < static_cast<int64_t>(N_cap) * kHeadDim || rows_unit_stride % kHeadDim ||
+                  raw_unit_stride < static_cast<int64_t>(kNSwa) * kHeadDim || raw_unit_stride % kHeadDim))
+        return DS4A_EINVAL;
+    const long long rows_per_unit = U > 1 ? rows_unit_stride / kHeadDim : N_cap;
+    const long long raw_per_unit = U > 1 ? raw_unit_stride / kHeadDim : kNSwa;
+    const long long total_rows = (static_cast<long long>(U) - 1) * rows_per_unit + N_cap;
+    const long long total_raw = (static_cast<long long>(U) - 1) * raw_per_unit + kNSwa;
+    if (total_rows >= (1LL << 31) || total_raw >= (1LL << 31) || static_cast<long long>(U) * kNHead >= (1LL << 31))
         return DS4A_EINVAL;
     if (!(scale == scale)) return DS4A_EINVAL;
     const size_t need = attn_ws_bytes(U, top_k);
@@ -255,7 +273,13 @@ ds4a_status ds4a_sparse_attn_decode(const uint16_t *q, const uint16_t *rows, int
     a.units = U;
     a.ws = ws;
     a.status = di->status;
-    return launch_sparse_attn(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DS4A_OK : DS4A_ECUDA;
+    a.rows_per_unit = rows_per_unit;
+    a.raw_per_unit = raw_per_unit;
+    if (!encode_2d_sw128(&a.tm_q, false, q, kHeadDim, static_cast<unsigned long long>(U) * kNHead, 64, 64) ||
+        !encode_2d_sw128(&a.tm_rows, false, rows, kHeadDim, total_rows, 64, 1) ||
+        !encode_2d_sw128(&a.tm_raw, true, raw, kHeadDim, total_raw, 64, 1))
+        return DS4A_EINVAL;
+    return launch_sparse_attn(a, di->sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DS4A_OK : DS4A_ECUDA;
 }
 
 ds4a_status ds4a_sparse_attn_prefill(const uint16_t *q, const int32_t *q_pos, const uint16_t *rows, int N_cap,
@@ -291,7 +315,15 @@ ds4a_status ds4a_sparse_attn_prefill(const uint16_t *q, const int32_t *q_pos, co
     a.units = T;
     a.ws = ws;
     a.status = di->status;
-    return launch_sparse_attn(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DS4A_OK : DS4A_ECUDA;
+    a.rows_per_unit = 0;
+    a.raw_per_unit = 0;
+    if (static_cast<long long>(T) * kNHead >= (1LL << 31)) return DS4A_EINVAL;
+    if (!encode_2d_sw128(&a.tm_q, false, q, kHeadDim, static_cast<unsigned long long>(T) * kNHead, 64, 64) ||
+        !encode_2d_sw128(&a.tm_rows, false, rows, kHeadDim, static_cast<unsigned long long>(N_cap), 64, 1) ||
+        !encode_2d_sw128(&a.tm_raw, true, a.raw, kHeadDim,
+                         static_cast<unsigned long long>(n_raw_rows > 0 ? n_raw_rows : 1), 64, 1))
+        return DS4A_EINVAL;
+    return launch_sparse_attn(a, di->sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DS4A_OK : DS4A_ECUDA;
 }
 
 }  // extern "C"

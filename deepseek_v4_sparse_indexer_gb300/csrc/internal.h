@@ -54,6 +54,11 @@ cudaError_t launch_topk(const TopkArgs &a, int num_sms, cudaStream_t s);
 
 // ---- sparse attention ----------------------------------------------------
 struct AttnArgs {
+    CUtensorMap tm_q;            // 2-D (512, units*64) bf16, box (64, 64), 128B swizzle
+    CUtensorMap tm_rows;         // 2-D (512, all compressed rows) bf16, box (64, 1): gather4
+    CUtensorMap tm_raw;          // 2-D (512, all raw rows) fp16, box (64, 1): gather4
+    long long rows_per_unit;     // row-coordinate offset between units (0 in prefill)
+    long long raw_per_unit;      // decode: raw-row offset between units
     const uint16_t *q;           // [units][64][512] bf16
     const uint16_t *rows;        // bf16 rows base
     long long rows_unit_stride;  // elements (0 in prefill: one shared row store)
@@ -75,12 +80,16 @@ struct AttnArgs {
 };
 int attn_num_splits(int units, int top_k);
 size_t attn_ws_bytes(int units, int top_k);
-cudaError_t launch_sparse_attn(const AttnArgs &a, cudaStream_t s);
+cudaError_t launch_sparse_attn(const AttnArgs &a, int num_sms, cudaStream_t s);
 
 // ---- shared host helpers of the C ABI -------------------------------------
 // Status word address and SM count of the current device (set up on first use).
 int current_device_info(uint32_t **status, int *sms);
 // Returns (and disarms) the error code armed by ds4a_debug_inject_error, or 0.
 int take_injected_error();
+// 2-D tiled tensor map over a row-major [rows][cols] 16-bit matrix (row pitch
+// cols*2 bytes) with the 128-byte swizzle.  False if the driver rejects it.
+bool encode_2d_sw128(CUtensorMap *m, bool f16, const void *base, unsigned long long cols, unsigned long long rows,
+                     unsigned box_cols, unsigned box_rows);
 
 }  // namespace ds4a

@@ -12,7 +12,7 @@
 //   2. filter  (chunks x rows CTAs): every CTA finds the row's threshold bin
 //               b1 (the bin where the count from the top reaches k), then
 //               appends rows with a higher bin to the row's "sure" list and
-//               rows in bin b1 to its candidate list (warp-aggregated atomics).
+//               rows in bin b1 to its candidate list (staged in shared queues).
 //   3. final   (one CTA per row): resolves the exact k-th key inside the
 //               candidate list (digits 19..8 and 7..0), applies the tie rule
 //               (lower row index first), sorts the chosen indices ascending and
@@ -78,12 +78,31 @@ __global__ void __launch_bounds__(kHistThreads) topk_hist_kernel(const float *__
     const float *s = scores + row * N_cap;
     if ((N_cap & 3) == 0) {
         const int vend = start + ((end - start) & ~3);
-        for (int i = start + 4 * threadIdx.x; i < vend; i += 4 * blockDim.x) {
+        auto add = [&](float f) {
+            if (score_visible(f)) atomicAdd(&h[float_key(f) >> 20], 1u);
+        };
+        // Four 16-byte loads in flight per thread before any is consumed.
+        constexpr int B = 4;
+        const int stride = 4 * blockDim.x;
+        int i = start + 4 * threadIdx.x;
+        for (; i + (B - 1) * stride < vend; i += B * stride) {
+            float4 v[B];
+#pragma unroll
+            for (int j = 0; j < B; ++j) v[j] = __ldg(reinterpret_cast<const float4 *>(s + i + j * stride));
+#pragma unroll
+            for (int j = 0; j < B; ++j) {
+                add(v[j].x);
+                add(v[j].y);
+                add(v[j].z);
+                add(v[j].w);
+            }
+        }
+        for (; i < vend; i += stride) {
             const float4 v = __ldg(reinterpret_cast<const float4 *>(s + i));
-            if (score_visible(v.x)) atomicAdd(&h[float_key(v.x) >> 20], 1u);
-            if (score_visible(v.y)) atomicAdd(&h[float_key(v.y) >> 20], 1u);
-            if (score_visible(v.z)) atomicAdd(&h[float_key(v.z) >> 20], 1u);
-            if (score_visible(v.w)) atomicAdd(&h[float_key(v.w) >> 20], 1u);
+            add(v.x);
+            add(v.y);
+            add(v.z);
+            add(v.w);
         }
         for (int i = vend + threadIdx.x; i < end; i += blockDim.x) {
             const float f = s[i];
@@ -104,43 +123,62 @@ __global__ void __launch_bounds__(kHistThreads) topk_hist_kernel(const float *__
 // Block-wide: finds the largest bin b with sum_{b' >= b} hist[b'] >= k.
 // Returns b (-1 when the total is below k), the count strictly above b in
 // *above and the total in *total.  `hist` is in shared memory, nbins a
-// multiple of NT = blockDim.x.  Every thread gets the same result.
+// multiple of NT = blockDim.x, NT a multiple of 32 and at most 1024.  Every
+// thread gets the same result.
+//   1. every thread sums nbins/NT consecutive bins;
+//   2. warp 0: each lane sums NT/32 consecutive partials, an inclusive suffix
+//      scan over the lanes finds the lane whose range crosses k, and that lane
+//      walks its partials, then the bins of the crossing partial.
 template <int NT>
 DS4A_DEV int find_threshold_bin(const uint32_t *hist, int nbins, uint32_t k, uint32_t *above, uint32_t *total,
                                 uint32_t *scratch /* NT + 4 u32 in smem */) {
+    static_assert(NT % 32 == 0 && NT <= 1024, "block size");
+    constexpr int PPL = NT / 32;               // partials per lane
     const int per = nbins / NT;
     const int t = threadIdx.x;
     uint32_t mine = 0;
     for (int i = 0; i < per; ++i) mine += hist[t * per + i];
     scratch[t] = mine;
     __syncthreads();
-    if (t == 0) {
-        // Serial walk from the top over the NT partial sums, then inside the
-        // partial where the running count reaches k.
-        uint32_t run = 0;
-        int hit = -1;
-        uint32_t hit_above = 0;
-        for (int j = NT - 1; j >= 0; --j) {
-            const uint32_t v = scratch[j];
-            if (hit < 0 && run + v >= k) {
-                hit = j;
-                hit_above = run;
-            }
-            run += v;
+    if (t < 32) {
+        uint32_t lane_sum = 0;
+#pragma unroll
+        for (int i = 0; i < PPL; ++i) lane_sum += scratch[t * PPL + i];
+        // Inclusive suffix sum over lanes: suf = sum of lane_sum for lanes >= t.
+        uint32_t suf = lane_sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t v = __shfl_down_sync(0xffffffffu, suf, off);
+            if (t + off < 32) suf += v;
         }
-        int b = -1;
-        uint32_t ab = run;
-        if (hit >= 0) {
-            uint32_t r2 = hit_above;
-            for (b = hit * per + per - 1; b > hit * per; --b) {
-                if (r2 + hist[b] >= k) break;
-                r2 += hist[b];
+        const uint32_t tot = __shfl_sync(0xffffffffu, suf, 0);
+        // The crossing lane: the highest lane whose suffix reaches k.
+        const uint32_t hit_mask = __ballot_sync(0xffffffffu, suf >= k);
+        if (t == 0) {
+            scratch[NT + 2] = tot;
+            if (hit_mask == 0) {
+                scratch[NT] = static_cast<uint32_t>(-1);
+                scratch[NT + 1] = tot;
             }
-            ab = r2;
         }
-        scratch[NT] = static_cast<uint32_t>(b);
-        scratch[NT + 1] = ab;
-        scratch[NT + 2] = run;
+        if (hit_mask != 0) {
+            const int L = 31 - __clz(hit_mask);
+            if (t == L) {
+                uint32_t run = suf - lane_sum;     // count above this lane's range
+                int p = t * PPL + PPL - 1;
+                for (; p > t * PPL; --p) {
+                    if (run + scratch[p] >= k) break;
+                    run += scratch[p];
+                }
+                int b = p * per + per - 1;
+                for (; b > p * per; --b) {
+                    if (run + hist[b] >= k) break;
+                    run += hist[b];
+                }
+                scratch[NT] = static_cast<uint32_t>(b);
+                scratch[NT + 1] = run;
+            }
+        }
     }
     __syncthreads();
     const int b = static_cast<int>(scratch[NT]);
@@ -150,25 +188,22 @@ DS4A_DEV int find_threshold_bin(const uint32_t *hist, int nbins, uint32_t k, uin
     return b;
 }
 
-// Warp-aggregated append: returns the slot for this lane (valid if pred).
-DS4A_DEV uint32_t warp_append(uint32_t *counter, bool pred) {
-    const uint32_t mask = __ballot_sync(0xffffffffu, pred);
-    if (!mask) return 0;
-    const int lane = threadIdx.x & 31;
-    const int leader = __ffs(mask) - 1;
-    uint32_t base = 0;
-    if (lane == leader) base = atomicAdd(counter, static_cast<uint32_t>(__popc(mask)));
-    base = __shfl_sync(0xffffffffu, base, leader);
-    return base + __popc(mask & ((1u << lane) - 1u));
-}
-
 // ---------------------------------------------------------------- 2. filter
+// Qualifying rows (bin >= b1, about 2 % of a random row) are staged in shared
+// queues with one shared atomic each, then appended to the row's global lists
+// with one global atomic per list per CTA.  A full candidate queue spills
+// straight to the global list.
+constexpr int kQueueCap = 2048;
+
 __global__ void __launch_bounds__(kHistThreads) topk_filter_kernel(const float *__restrict__ scores,
                                                                    const int32_t *__restrict__ n_rows, int Q,
                                                                    int N_cap, int top_k, int chunk, int n_chunks,
                                                                    TopkWs ws) {
     __shared__ uint32_t h[kBins];
     __shared__ uint32_t scratch[kHistThreads + 4];
+    __shared__ int32_t q_sure[kMaxTopK];
+    __shared__ uint2 q_cand[kQueueCap];
+    __shared__ uint32_t n_qs, n_qc, base_s, base_c;
     const long long row = blockIdx.x / n_chunks;
     const int cidx = static_cast<int>(blockIdx.x - row * n_chunks);
     const int u = static_cast<int>(row / Q);
@@ -178,6 +213,7 @@ __global__ void __launch_bounds__(kHistThreads) topk_filter_kernel(const float *
     if (start >= end && cidx != 0) return;
     const uint32_t *gh = ws.hist + row * kBins;
     for (int i = threadIdx.x; i < kBins; i += blockDim.x) h[i] = gh[i];
+    if (threadIdx.x == 0) n_qs = n_qc = 0;
     __syncthreads();
     uint32_t above, total;
     int b1 = find_threshold_bin<kHistThreads>(h, kBins, static_cast<uint32_t>(top_k), &above, &total, scratch);
@@ -191,26 +227,65 @@ __global__ void __launch_bounds__(kHistThreads) topk_filter_kernel(const float *
     const float *s = scores + row * N_cap;
     int32_t *sure = ws.sure + row * top_k;
     uint2 *cand = ws.cand + row * kCandCap;
-    // Whole warps iterate together so the ballots see every lane.
-    const int span = end - start;
-    const int iters = (span + blockDim.x - 1) / blockDim.x;
-    for (int it = 0; it < iters; ++it) {
-        const int i = start + it * blockDim.x + threadIdx.x;
-        bool vis = false;
-        uint32_t key = 0;
-        if (i < end) {
-            const float f = s[i];
-            vis = score_visible(f);
-            key = float_key(f);
+    const uint32_t key_lo = b1 < 0 ? 0u : (static_cast<uint32_t>(b1) << 20);
+    auto consider = [&](int i, float f) {
+        if (!score_visible(f)) return;
+        const uint32_t key = float_key(f);
+        if (key < key_lo) return;
+        if (static_cast<int>(key >> 20) > b1) {
+            const uint32_t p = atomicAdd(&n_qs, 1u);
+            if (p < static_cast<uint32_t>(top_k)) q_sure[p] = i;      // never more than k in total
+        } else {
+            const uint32_t p = atomicAdd(&n_qc, 1u);
+            if (p < static_cast<uint32_t>(kQueueCap)) {
+                q_cand[p] = make_uint2(key, static_cast<uint32_t>(i));
+            } else {
+                const uint32_t g = atomicAdd(&meta[1], 1u);
+                if (g < static_cast<uint32_t>(kCandCap)) cand[g] = make_uint2(key, static_cast<uint32_t>(i));
+            }
         }
-        const int d = static_cast<int>(key >> 20);
-        const bool is_sure = vis && d > b1;
-        const bool is_cand = vis && b1 >= 0 && d == b1;
-        const uint32_t ps = warp_append(&meta[0], is_sure);
-        if (is_sure && ps < static_cast<uint32_t>(top_k)) sure[ps] = i;
-        const uint32_t pc = warp_append(&meta[1], is_cand);
-        if (is_cand && pc < static_cast<uint32_t>(kCandCap)) cand[pc] = make_uint2(key, static_cast<uint32_t>(i));
+    };
+    if ((N_cap & 3) == 0) {
+        const int vend = start + ((end - start) & ~3);
+        constexpr int B = 4;
+        const int stride = 4 * blockDim.x;
+        int i = start + 4 * threadIdx.x;
+        for (; i + (B - 1) * stride < vend; i += B * stride) {
+            float4 v[B];
+#pragma unroll
+            for (int j = 0; j < B; ++j) v[j] = __ldg(reinterpret_cast<const float4 *>(s + i + j * stride));
+#pragma unroll
+            for (int j = 0; j < B; ++j) {
+                const int b = i + j * stride;
+                consider(b, v[j].x);
+                consider(b + 1, v[j].y);
+                consider(b + 2, v[j].z);
+                consider(b + 3, v[j].w);
+            }
+        }
+        for (; i < vend; i += stride) {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(s + i));
+            consider(i, v.x);
+            consider(i + 1, v.y);
+            consider(i + 2, v.z);
+            consider(i + 3, v.w);
+        }
+        for (int i = vend + threadIdx.x; i < end; i += blockDim.x) consider(i, s[i]);
+    } else {
+        for (int i = start + threadIdx.x; i < end; i += blockDim.x) consider(i, s[i]);
     }
+    __syncthreads();
+    const uint32_t ns = min(n_qs, static_cast<uint32_t>(top_k));
+    const uint32_t nc = min(n_qc, static_cast<uint32_t>(kQueueCap));
+    if (threadIdx.x == 0) {
+        base_s = ns ? atomicAdd(&meta[0], ns) : 0u;
+        base_c = nc ? atomicAdd(&meta[1], nc) : 0u;
+    }
+    __syncthreads();
+    for (uint32_t j = threadIdx.x; j < ns; j += blockDim.x)
+        if (base_s + j < static_cast<uint32_t>(top_k)) sure[base_s + j] = q_sure[j];
+    for (uint32_t j = threadIdx.x; j < nc; j += blockDim.x)
+        if (base_c + j < static_cast<uint32_t>(kCandCap)) cand[base_c + j] = q_cand[j];
 }
 
 // ---------------------------------------------------------------- 3. final

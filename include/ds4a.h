@@ -214,7 +214,9 @@ ds4a_status ds4a_topk_select_noalloc(const float *scores, const int32_t *n_rows,
  *    ws      workspace of ds4a_workspace_bytes(DS4A_OP_SPARSE_ATTN_DECODE, U, 1,
  *            N_cap, top_k) bytes (used when units are few and each unit's row
  *            set is split over several CTAs).
- *    All row buffers and q must be 16-byte aligned; strides multiples of 8.
+ *    q, rows and raw must be 16-byte aligned; with U > 1 the unit strides must
+ *    be whole rows (multiples of 512 elements), at least N_cap resp. 128 rows
+ *    (rows are gathered by TMA from one row-indexed view of each buffer).
  */
 ds4a_status ds4a_sparse_attn_decode(const uint16_t *q, const uint16_t *rows,
                                     int64_t rows_unit_stride, int N_cap,
