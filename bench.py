@@ -46,6 +46,8 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU work budget of the oracle sample")
     p.add_argument("--units", type=int, default=None,
                    help="decode workloads: run only this many units (small cases for profiling)")
+    p.add_argument("--prior-rows", type=int, default=None,
+                   help="prefill workload: compressed rows before the chunk (small cases for profiling)")
     return p.parse_args()
 
 
@@ -276,9 +278,12 @@ def main():
     if args.workload not in WORKLOADS:
         raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(WORKLOADS)}")
     wl = WORKLOADS[args.workload]
+    import dataclasses
     if args.units is not None and wl.kind == "decode":
-        import dataclasses
         wl = dataclasses.replace(wl, name=f"{wl.name}[units={args.units}]", units=args.units)
+    if args.prior_rows is not None and wl.kind == "prefill":
+        wl = dataclasses.replace(wl, name=f"{wl.name}[prior_rows={args.prior_rows}]",
+                                 n_rows=args.prior_rows + wl.queries // 4, extra=dict(prior_rows=args.prior_rows))
     if args.impl == "reference":
         return run_reference(args, wl)
     if args.warmup < 3:

@@ -275,9 +275,7 @@ ds4a_status ds4a_sparse_attn_decode(const uint16_t *q, const uint16_t *rows, int
     a.status = di->status;
     a.rows_per_unit = rows_per_unit;
     a.raw_per_unit = raw_per_unit;
-    if (!encode_2d_sw128(&a.tm_q, false, q, kHeadDim, static_cast<unsigned long long>(U) * kNHead, 64, 64) ||
-        !encode_2d_sw128(&a.tm_rows, false, rows, kHeadDim, total_rows, 64, 1) ||
-        !encode_2d_sw128(&a.tm_raw, true, raw, kHeadDim, total_raw, 64, 1))
+    if (!encode_2d_sw128(&a.tm_q, false, q, kHeadDim, static_cast<unsigned long long>(U) * kNHead, 64, 64))
         return DS4A_EINVAL;
     return launch_sparse_attn(a, di->sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DS4A_OK : DS4A_ECUDA;
 }
@@ -318,10 +316,7 @@ ds4a_status ds4a_sparse_attn_prefill(const uint16_t *q, const int32_t *q_pos, co
     a.rows_per_unit = 0;
     a.raw_per_unit = 0;
     if (static_cast<long long>(T) * kNHead >= (1LL << 31)) return DS4A_EINVAL;
-    if (!encode_2d_sw128(&a.tm_q, false, q, kHeadDim, static_cast<unsigned long long>(T) * kNHead, 64, 64) ||
-        !encode_2d_sw128(&a.tm_rows, false, rows, kHeadDim, static_cast<unsigned long long>(N_cap), 64, 1) ||
-        !encode_2d_sw128(&a.tm_raw, true, a.raw, kHeadDim,
-                         static_cast<unsigned long long>(n_raw_rows > 0 ? n_raw_rows : 1), 64, 1))
+    if (!encode_2d_sw128(&a.tm_q, false, q, kHeadDim, static_cast<unsigned long long>(T) * kNHead, 64, 64))
         return DS4A_EINVAL;
     return launch_sparse_attn(a, di->sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DS4A_OK : DS4A_ECUDA;
 }

@@ -19,7 +19,8 @@
 //   warp 1      TMEM owner and UMMA issuer (one thread): 8 x (M128,N,K16)
 //               per tile into a ring of TMEM accumulators;
 //   warps 2..   epilogue: tcgen05.ld of the row's N accumulators, ReLU,
-//               weight, sum over heads, masked store of one fp32 per (q,row).
+//               weight, sum over heads (packed fp32x2 FMAs, eight partial
+//               sums), masked store of one fp32 per (q,row).
 // A work item is (unit, query group, chunk of 128-row tiles).
 //
 // The decode scan is HBM-bound (256 B of keys per row for 16 kFLOP); the
@@ -117,6 +118,42 @@ DS4A_DEV void tmem_wait_ld2(uint32_t (&r)[32], uint32_t (&s)[32]) {
     tmem_wait_ld(r);
     // The second array's wait is already satisfied; this ties its registers too.
     tmem_wait_ld(s);
+}
+
+// Two fp32 lanes as one 64-bit register pair, for the packed fp32x2 FMA.
+DS4A_DEV unsigned long long pack_f2(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+DS4A_DEV float2 unpack_f2(unsigned long long v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+
+// sum_h w[h] * max(0, acc[h]) over one query's 64 head sums (v0: heads 0..31,
+// v1: heads 32..63).  The ReLU is per element; the weighted sum runs as packed
+// fp32x2 FMAs into four independent pair accumulators (eight partial sums),
+// combined in a fixed order, which keeps the dependency chains short.
+DS4A_DEV float relu_weighted_sum(const float *w, const uint32_t (&v0)[32], const uint32_t (&v1)[32]) {
+    unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};
+    const float4 *w4 = reinterpret_cast<const float4 *>(w);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        const float4 ww = w4[q];
+        const uint32_t *v = q < 8 ? v0 : v1;
+        const int h = (q & 7) * 4;
+        const unsigned long long x01 = pack_f2(fmaxf(__uint_as_float(v[h]), 0.f), fmaxf(__uint_as_float(v[h + 1]), 0.f));
+        const unsigned long long x23 =
+            pack_f2(fmaxf(__uint_as_float(v[h + 2]), 0.f), fmaxf(__uint_as_float(v[h + 3]), 0.f));
+        unsigned long long &a0 = acc[(2 * q) & 3];
+        unsigned long long &a1 = acc[(2 * q + 1) & 3];
+        asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a0) : "l"(pack_f2(ww.x, ww.y)), "l"(x01));
+        asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a1) : "l"(pack_f2(ww.z, ww.w)), "l"(x23));
+    }
+    const float2 s0 = unpack_f2(acc[0]), s1 = unpack_f2(acc[1]), s2 = unpack_f2(acc[2]), s3 = unpack_f2(acc[3]);
+    return ((s0.x + s0.y) + (s1.x + s1.y)) + ((s2.x + s2.y) + (s3.x + s3.y));
 }
 
 template <int G>
@@ -299,13 +336,7 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
                     tmem_ld32_sync(tmem_base + lane_off + col, v0);
                     tmem_ld32_sync(tmem_base + lane_off + col + 32, v1);
                     tmem_wait_ld2(v0, v1);
-                    const float *wj = wsm + j * 64;
-                    float s = 0.f;
-#pragma unroll
-                    for (int h = 0; h < 32; ++h) s = fmaf(wj[h], fmaxf(__uint_as_float(v0[h]), 0.f), s);
-#pragma unroll
-                    for (int h = 0; h < 32; ++h) s = fmaf(wj[32 + h], fmaxf(__uint_as_float(v1[h]), 0.f), s);
-                    sc[j] = s;
+                    sc[j] = relu_weighted_sum(wsm + j * 64, v0, v1);
                 }
                 tc_fence_before();
                 __syncwarp();

@@ -55,10 +55,8 @@ cudaError_t launch_topk(const TopkArgs &a, int num_sms, cudaStream_t s);
 // ---- sparse attention ----------------------------------------------------
 struct AttnArgs {
     CUtensorMap tm_q;            // 2-D (512, units*64) bf16, box (64, 64), 128B swizzle
-    CUtensorMap tm_rows;         // 2-D (512, all compressed rows) bf16, box (64, 1): gather4
-    CUtensorMap tm_raw;          // 2-D (512, all raw rows) fp16, box (64, 1): gather4
-    long long rows_per_unit;     // row-coordinate offset between units (0 in prefill)
-    long long raw_per_unit;      // decode: raw-row offset between units
+    long long rows_per_unit;     // row offset between units' compressed rows (0 in prefill)
+    long long raw_per_unit;      // decode: row offset between units' raw rings
     const uint16_t *q;           // [units][64][512] bf16
     const uint16_t *rows;        // bf16 rows base
     long long rows_unit_stride;  // elements (0 in prefill: one shared row store)

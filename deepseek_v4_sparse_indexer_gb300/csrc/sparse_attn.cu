@@ -6,26 +6,31 @@
 //
 // One CTA (persistent, one per SM) walks work items = (unit, split), where a
 // unit is one decode query or one query of a prefill chunk.  The unit's row
-// list [selected compressed rows..., raw-window rows...] is cut into 128-row
-// tiles.  Per tile:
-//   gather   warp 0: TMA tile::gather4 loads (4 rows x 64 columns each, 128B
-//            swizzle) of the tile's rows into eight 16 KB column blocks;
-//            a masked row uses an out-of-range coordinate and lands as zeros;
-//   logits   warp 1 (one thread): S^T[128 rows x 64 heads] = X . q^T, 32
-//            UMMAs (M=128, N=64, K=16) from the K-major row blocks and the
-//            K-major q into TMEM;
-//   softmax  warps 2-5 (thread i = row i): tcgen05.ld the row's 64 logits,
-//            per-head tile max with redux.sync.max.f32 across the warp and a
-//            4-way max across warps, p = exp2(l - m) written as P^T (the
-//            16-bit MN-major operand) to shared memory, per-thread partial row
-//            sums kept in registers;
-//   values   warp 1: O^T[512 dims x 64 heads] += X^T . P^T as four M=128
-//            chunks (X read as the MN-major operand), accumulating in TMEM;
-//            each chunk's commit frees its two column blocks for the next tile.
+// list [selected compressed rows..., raw-window rows...] is cut into 64-row
+// tiles, double-buffered in shared memory so that the next tile's gather and
+// logits overlap this tile's softmax:
+//   gather   warps 0-1: 16-byte cp.async copies of the tile's rows into eight
+//            8 KB column blocks in the 128B-swizzled layout (a warp moves four
+//            whole 128-byte row segments per instruction; masked rows are
+//            zero-filled); each thread fences its copies into the async proxy
+//            before arriving on the buffer's barrier.  The two gather warps
+//            take alternate tiles;
+//   logits   warp 2 (one thread): S^T[64 rows x 64 heads] = X . q^T, 32 UMMAs
+//            (M=64, N=64, K=16) from the K-major row blocks and the K-major q,
+//            into one of two TMEM buffers (row m of an M=64 accumulator sits in
+//            TMEM lane 32*(m/16) + m%16);
+//   softmax  warps 3-10 (one thread = one row x 32 heads): tcgen05.ld of the
+//            row's 32 logits, per-head tile max with redux.sync.max.f32 across
+//            the warp and a 4-way max across lane quarters, p = exp2(l - m)
+//            written as P^T (the 16-bit MN-major operand) to one of two shared
+//            buffers, per-thread partial row sums kept in registers;
+//   values   warp 2: O^T[512 dims x 64 heads] += X^T . P^T as four M=128
+//            chunks (K = 64 rows, X read as the MN-major operand), accumulating
+//            in TMEM; its commit frees the row buffer.
 // The running max per head is only raised when a tile exceeds it by more than
 // 2^8 (then O^T and the partial sums are rescaled), so p <= 256 always and the
-// rescale is rare.  Compressed tiles multiply in bf16; the raw tile in fp16
-// with q converted in place to fp16 (exact for |q| in [2^-14, 65504]).
+// rescale is rare.  Compressed tiles multiply in bf16; raw tiles in fp16 with
+// q converted in place to fp16 (exact for |q| in [2^-14, 65504]).
 // Split items write unnormalised partials (O, m, l) that attn_merge_kernel
 // combines by log-sum-exp.
 //
@@ -37,34 +42,44 @@
 namespace ds4a {
 namespace {
 
-constexpr int TR = 128;                       // rows per tile (UMMA M of the logit GEMM)
-constexpr int kThreads = 192;                 // warp 0 gather, warp 1 UMMA/TMEM, warps 2-5 softmax
+constexpr int TR = 64;                        // rows per tile (UMMA M of the logit GEMM)
+constexpr int kProducerWarps = 2;             // warps 0-1: row gather (cp.async)
+constexpr int kProducerThreads = kProducerWarps * 32;
+constexpr int kMmaWarp = 2;                   // warp 2: TMEM owner + UMMA issuer
+constexpr int kFirstSoftmaxWarp = 3;          // warps 3-10: softmax + epilogue
+constexpr int kSoftmaxWarps = 8;
+constexpr int kThreads = (kFirstSoftmaxWarp + kSoftmaxWarps) * 32;
+constexpr int kRowsPerThread = TR / 8;        // rows one gather thread copies per block
 constexpr int kQBlk = kNHead * 128;           // 64 heads x 64 dims x 2 B = 8 KB
-constexpr int kXBlk = TR * 128;               // 128 rows x 64 dims x 2 B = 16 KB
+constexpr int kXBlk = TR * 128;               // 64 rows x 64 dims x 2 B = 8 KB
+constexpr int kXBuf = 8 * kXBlk;              // one row tile: 64 KB
+constexpr int kPBuf = TR * 128;               // P^T [64 rows][64 heads] 16-bit: 8 KB
 constexpr int kOffQ = 0;
-constexpr int kOffX = kOffQ + 8 * kQBlk;      // 64 KB
-constexpr int kOffP = kOffX + 8 * kXBlk;      // +128 KB
-constexpr int kOffSmax = kOffP + TR * 128;    // +16 KB: P^T [128 rows][64 heads]
+constexpr int kOffX = kOffQ + 8 * kQBlk;      // q: 64 KB
+constexpr int kOffP = kOffX + 2 * kXBuf;      // two row tiles: 128 KB
+constexpr int kOffSmax = kOffP + 2 * kPBuf;   // two P^T buffers: 16 KB
 constexpr int kOffMused = kOffSmax + 4 * kNHead * 4;
 constexpr int kOffAlpha = kOffMused + kNHead * 4;
 constexpr int kOffInvL = kOffAlpha + kNHead * 4;
 constexpr int kOffBar = kOffInvL + kNHead * 4;
-constexpr int kNumBars = 8 + 8 + 10;
+constexpr int kNumBars = 20;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 32 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-constexpr uint32_t kTmemCols = 512;           // S^T: 64 columns, O^T: 4 x 64 columns
+constexpr uint32_t kTmemCols = 512;           // S^T: 2 x 64 columns, O^T: 4 x 64 columns
 constexpr uint32_t kTmemS = 0;
-constexpr uint32_t kTmemO = 64;
+constexpr uint32_t kTmemO = 128;
 constexpr int kMaxSplit = 16;
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
 
-// UMMA instruction descriptors (see idesc_bf16_f32): logits with K-major A/B,
-// values with MN-major A (rows x dims read as dims x rows) and MN-major B.
-__host__ __device__ constexpr uint32_t idesc_f16(bool f16_inputs, bool mn_major) {
+// UMMA instruction descriptors (see idesc_bf16_f32): logits (M = 64 rows,
+// N = 64 heads) with K-major A/B; values (M = 128 dims, N = 64 heads) with
+// MN-major A (rows x dims read as dims x rows) and MN-major B.
+__host__ __device__ constexpr uint32_t idesc_f16(bool f16_inputs, bool values) {
     const uint32_t fmt = f16_inputs ? 0u : 1u;
-    return (1u << 4) | (fmt << 7) | (fmt << 10) | (mn_major ? (1u << 15) | (1u << 16) : 0u) |
-           (static_cast<uint32_t>(kNHead >> 3) << 17) | (static_cast<uint32_t>(TR >> 4) << 24);
+    const uint32_t m = values ? 128u : static_cast<uint32_t>(TR);
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | (values ? (1u << 15) | (1u << 16) : 0u) |
+           (static_cast<uint32_t>(kNHead >> 3) << 17) | ((m >> 4) << 24);
 }
 
 // Shared-memory descriptor with explicit leading / stride byte offsets (128B swizzle).
@@ -78,13 +93,6 @@ DS4A_DEV uint64_t sw128_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
     return d;
 }
 
-DS4A_DEV void gather4(void *dst, const void *map, uint64_t *bar, int col, int r0, int r1, int r2, int r3) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
-        : "memory");
-}
 DS4A_DEV void tma_load_2d_nohint(void *dst, const void *map, uint64_t *bar, int x, int y) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
@@ -148,8 +156,8 @@ struct Item {
     int nrw;             // raw rows
     int ct;              // compressed tiles
     int t0, t1;          // tile range of this split
-    long long raw_row0;  // row coordinate of raw row 0 in the raw map
-    long long comp_row0; // row coordinate of compressed row 0 of the unit in the rows map
+    long long raw_row0;  // row index of the unit's raw row 0 in the raw buffer
+    long long comp_row0; // row index of the unit's compressed row 0 in the rows buffer
 };
 
 DS4A_DEV Item make_item(const AttnArgs &a, int it, int n_split) {
@@ -181,6 +189,7 @@ DS4A_DEV Item make_item(const AttnArgs &a, int it, int n_split) {
 }
 
 // Row j of tile t: valid?  (compressed rows need an index inside [0, N_cap)).
+// *coord receives the row's index in the rows buffer (compressed) or the raw buffer.
 DS4A_DEV bool row_valid(const AttnArgs &a, const Item &m, int t, int j, int *coord) {
     if (t < m.ct) {
         const int jj = t * TR + j;
@@ -204,160 +213,256 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
     uint8_t *sX = smem + kOffX;
     uint8_t *sP = smem + kOffP;
     float *sSmax = reinterpret_cast<float *>(smem + kOffSmax);
-    float *sMused = reinterpret_cast<float *>(smem + kOffMused);
-    float *sAlpha = reinterpret_cast<float *>(smem + kOffAlpha);
+    float *sMused = reinterpret_cast<float *>(smem + kOffMused);   // running max per head (log2 units)
+    float *sAlpha = reinterpret_cast<float *>(smem + kOffAlpha);   // this tile's rescale factor per head
     float *sInvL = reinterpret_cast<float *>(smem + kOffInvL);
-    uint64_t *slot_full = reinterpret_cast<uint64_t *>(smem + kOffBar);
-    uint64_t *slot_empty = slot_full + 8;
-    uint64_t *q_full = slot_empty + 8;
+    uint64_t *x_full = reinterpret_cast<uint64_t *>(smem + kOffBar);   // [2] row tile landed
+    uint64_t *x_empty = x_full + 2;                                    // [2] row tile consumed
+    uint64_t *s_full = x_empty + 2;                                    // [2] logits in TMEM
+    uint64_t *s_empty = s_full + 2;                                    // [2] logits read
+    uint64_t *p_full = s_empty + 2;                                    // [2] P^T written
+    uint64_t *q_full = p_full + 2;
     uint64_t *q_free = q_full + 1;
     uint64_t *q16_ready = q_free + 1;
-    uint64_t *s_full = q16_ready + 1;
-    uint64_t *s_empty = s_full + 1;
-    uint64_t *p_full = s_empty + 1;
-    uint64_t *o_ready = p_full + 1;
-    uint64_t *o_free = o_ready + 1;
+    uint64_t *pv_done = q16_ready + 1;                                 // after every values GEMM
+    uint64_t *o_free = pv_done + 1;
     uint64_t *drain = o_free + 1;
-    uint64_t *grp = drain + 1;                   // softmax-group barrier (4 warps)
+    uint64_t *grp = drain + 1;                                         // softmax-group barrier
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
-    int *any_rescale = reinterpret_cast<int *>(smem + kOffMisc + 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int b = 0; b < 8; ++b) {
-            mbar_init(&slot_full[b], 1);
-            mbar_init(&slot_empty[b], 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&x_full[b], 32);                 // the one gather warp of that buffer
+            mbar_init(&x_empty[b], 1);
+            mbar_init(&s_full[b], 1);
+            mbar_init(&s_empty[b], kSoftmaxWarps);
+            mbar_init(&p_full[b], kSoftmaxWarps);
         }
         mbar_init(q_full, 1);
         mbar_init(q_free, 1);
-        mbar_init(q16_ready, 4);
-        mbar_init(s_full, 1);
-        mbar_init(s_empty, 4);
-        mbar_init(p_full, 4);
-        mbar_init(o_ready, 1);
-        mbar_init(o_free, 4);
+        mbar_init(q16_ready, kSoftmaxWarps);
+        mbar_init(pv_done, 1);
+        mbar_init(o_free, kSoftmaxWarps);
         mbar_init(drain, 1);
-        mbar_init(grp, 4);
+        mbar_init(grp, kSoftmaxWarps);
         *abort_flag = 0;
-        *any_rescale = 0;
         mbar_fence_init();
         tma_prefetch_desc(&a.tm_q);
-        tma_prefetch_desc(&a.tm_rows);
-        tma_prefetch_desc(&a.tm_raw);
     }
-    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+    if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const float NEG_INF = -__int_as_float(0x7f800000);
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ gather producer
-        uint32_t qph = 0, sph[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (warp < kProducerWarps) {
+        // ------------------------------------------------------------ row gather
+        // The two gather warps take alternate tiles (warp w: tiles with
+        // counter jt % 2 == w), so one tile's copies are in flight while the
+        // other warp still waits for its own.  Lane l copies 16-byte chunk
+        // (l & 7) of rows r_k = 4k + (l >> 3) of every 64-column block: a warp
+        // instruction moves four full 128-byte row segments.  Destinations
+        // follow the 128B swizzle.
+        const int chunk = lane & 7, rsub = lane >> 3;
+        uint32_t xeph = 0;
         bool ok = true;
-        for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-            const Item m = make_item(a, it, n_split);
-            if (m.t0 >= m.t1) continue;
-            ok = __all_sync(0xffffffffu, mbar_wait(q_free, qph ^ 1, abort_flag));
-            if (!ok) break;
-            qph ^= 1;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(q_full, 8 * kQBlk);
-                for (int b = 0; b < 8; ++b) tma_load_2d_nohint(sQ + b * kQBlk, &a.tm_q, q_full, b * 64, m.unit * kNHead);
+        auto first_tile = [&](int it, Item &m) -> int {
+            for (; it < n_items; it += gridDim.x) {
+                m = make_item(a, it, n_split);
+                if (m.t0 < m.t1) return it;
             }
-            for (int t = m.t0; ok && t < m.t1; ++t) {
-                int c[4];
-                bool bad_idx = false;
-                for (int i = 0; i < 4; ++i) {
-                    c[i] = -1;                                   // out of range: loads zeros
-                    int co = 0;
-                    if (row_valid(a, m, t, 4 * lane + i, &co)) {
-                        c[i] = co;
-                    } else if (t < m.ct && t * TR + 4 * lane + i < m.cnt) {
-                        bad_idx = true;                          // index outside [0, N_cap)
-                    }
-                }
-                if (__any_sync(0xffffffffu, bad_idx) && lane == 0) report(a.status, DS4A_DEV_BOUNDS);
-                const void *map = t < m.ct ? static_cast<const void *>(&a.tm_rows) : static_cast<const void *>(&a.tm_raw);
-                for (int b = 0; b < 8; ++b) {
-                    ok = __all_sync(0xffffffffu, mbar_wait(&slot_empty[b], sph[b] ^ 1, abort_flag));
-                    if (!ok) break;
-                    sph[b] ^= 1;
-                    if (lane == 0) mbar_arrive_expect_tx(&slot_full[b], kXBlk);
-                    __syncwarp();
-                    gather4(sX + b * kXBlk + lane * 512, map, &slot_full[b], b * 64, c[0], c[1], c[2], c[3]);
+            return n_items;
+        };
+        int ordinal = 0;                                   // item ordinal within this CTA's sequence
+        auto advance = [&](int &it, int &t, Item &m) {
+            if (++t >= m.t1) {
+                it = first_tile(it + gridDim.x, m);
+                t = it < n_items ? m.t0 : 0;
+                ++ordinal;
+            }
+        };
+        // Row list entries of tile t for this lane (< 0: masked).
+        auto fetch_rows = [&](const Item &m, int t, int (&rv)[16]) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const int r = 4 * k + rsub;
+                if (t < m.ct) {
+                    const int jj = t * TR + r;
+                    rv[k] = jj < m.cnt ? __ldg(a.idx + static_cast<long long>(m.unit) * a.top_k + jj) : -1;
+                } else {
+                    const int jj = (t - m.ct) * TR + r;
+                    rv[k] = jj < m.nrw ? jj : -1;
                 }
             }
+        };
+        auto row_index = [&](const Item &m, int t, int v) -> int {
+            if (t < m.ct) return (v < 0 || v >= a.N_cap) ? -1 : static_cast<int>(m.comp_row0 + v);
+            return v < 0 ? -1 : static_cast<int>(m.raw_row0 + v);
+        };
+        // Walk this CTA's (item, tile) sequence; this warp handles every second tile.
+        Item cm;
+        int cit = first_tile(blockIdx.x, cm);
+        int ct_ = cit < n_items ? cm.t0 : 0;
+        uint32_t jt = 0;
+        if (warp == 1 && cit < n_items) {
+            advance(cit, ct_, cm);
+            jt = 1;
         }
+        int rv[16];
+        if (cit < n_items) fetch_rows(cm, ct_, rv);
+        while (ok && cit < n_items) {
+            if (ct_ == cm.t0) {
+                // First tile of an item: q (bf16) by TMA once the previous item's
+                // logits are done (the warp owning the first tile loads it).
+                // q_free completes once per item, so item k waits for phase k-1.
+                if (ordinal > 0) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(q_free, (ordinal - 1) & 1, abort_flag));
+                    if (!ok) break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(q_full, 8 * kQBlk);
+                    for (int b = 0; b < 8; ++b)
+                        tma_load_2d_nohint(sQ + b * kQBlk, &a.tm_q, q_full, b * 64, cm.unit * kNHead);
+                }
+            }
+            int src[16];
+            bool bad_idx = false;
+            const uint16_t *base = (ct_ < cm.ct ? a.rows : a.raw) + chunk * 8;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                src[k] = row_index(cm, ct_, rv[k]);
+                // A listed row whose index lies outside [0, N_cap) is masked and flagged.
+                if (ct_ < cm.ct && ct_ * TR + 4 * k + rsub < cm.cnt && src[k] < 0) bad_idx = true;
+            }
+            if (__any_sync(0xffffffffu, bad_idx) && lane == 0) report(a.status, DS4A_DEV_BOUNDS);
+            const int xb = jt & 1;                        // == warp
+            ok = __all_sync(0xffffffffu, mbar_wait(&x_empty[xb], xeph ^ 1, abort_flag));
+            if (!ok) break;
+            xeph ^= 1;
+            const uint32_t buf = smem_u32(sX) + xb * kXBuf;
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int r = 4 * k + rsub;
+                    cp_async16(buf + b * kXBlk + r * 128 + ((chunk ^ (r & 7)) << 4),
+                               src[k] >= 0 ? base + static_cast<long long>(src[k]) * kHeadDim + b * 64 : a.q,
+                               src[k] >= 0 ? 16u : 0u);
+                }
+            }
+            cp_async_commit();
+            // While the copies land: the row list of this warp's next tile (two ahead).
+            advance(cit, ct_, cm);
+            if (cit < n_items) advance(cit, ct_, cm);
+            if (cit < n_items) fetch_rows(cm, ct_, rv);
+            cp_async_wait<0>();
+            fence_proxy_async();
+            mbar_arrive(&x_full[xb]);
+            jt += 2;
+        }
+        cp_async_wait<0>();
         if (!ok) {
             *abort_flag = 1;
             if (lane == 0) report(a.status, DS4A_DEV_TIMEOUT);
-            // Let issued copies land: the last armed phase of every slot and of q.
-            for (int b = 0; b < 8; ++b) wait_drain(&slot_full[b], sph[b] ^ 1);
-            wait_drain(q_full, qph ^ 1);
         }
-    } else if (warp == 1) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ UMMA issuer
+        // Per item, the logits GEMMs S(t) and the values GEMMs V(t) are issued
+        // in tile order, each stream as soon as its inputs are ready, V first:
+        // V(t-1) frees its row buffer for the gather as early as possible, and
+        // S(t) runs while the softmax works on tile t - 1.
         if (lane == 0) {
-            uint32_t qph = 0, q16ph = 0, sfph[8] = {0, 0, 0, 0, 0, 0, 0, 0}, seph = 0, pph = 0, ofph = 0;
+            uint32_t qph = 0, q16ph = 0, ofph = 0;
+            uint32_t xfph[2] = {0, 0}, seph[2] = {0, 0}, pfph[2] = {0, 0};
             bool ok = true, first_item = true;
             constexpr uint32_t id_s_bf = idesc_f16(false, false), id_s_f16 = idesc_f16(true, false);
             constexpr uint32_t id_v_bf = idesc_f16(false, true), id_v_f16 = idesc_f16(true, true);
             const uint32_t aQ = smem_u32(sQ), aX = smem_u32(sX), aP = smem_u32(sP);
+            uint32_t jt = 0;                                 // tile counter: buffers jt & 1
             for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
                 const Item m = make_item(a, it, n_split);
                 if (m.t0 >= m.t1) continue;
                 if (!mbar_wait(q_full, qph, abort_flag)) { ok = false; break; }
                 qph ^= 1;
-                bool q16 = false, first_pv = true;
-                for (int t = m.t0; ok && t < m.t1; ++t) {
-                    const bool raw = t >= m.ct;
-                    if (raw && !q16) {
-                        if (!mbar_wait(q16_ready, q16ph, abort_flag)) { ok = false; break; }
-                        q16ph ^= 1;
-                        q16 = true;
-                    }
-                    // logits S^T = X . q^T
-                    if (!mbar_wait(s_empty, seph ^ 1, abort_flag)) { ok = false; break; }
-                    seph ^= 1;
-                    for (int b = 0; b < 8 && ok; ++b) {
-                        if (!mbar_wait(&slot_full[b], sfph[b], abort_flag)) { ok = false; break; }
-                        sfph[b] ^= 1;
-                        tc_fence_after();
+                bool q16 = false;
+                int ns = m.t0, nv = m.t0;                    // next S / next V tile
+                uint32_t js = jt, jv = jt;                   // their tile counters
+                uint64_t idle_since = 0;
+                while (nv < m.t1) {
+                    bool progressed = false;
+                    if (nv < ns) {
+                        const int b = jv & 1;
+                        if (mbar_test(&p_full[b], pfph[b])) {
+                            pfph[b] ^= 1;
+                            if (nv == m.t0 && !first_item) {
+                                if (!mbar_wait(o_free, ofph, abort_flag)) { ok = false; break; }
+                                ofph ^= 1;
+                            }
+                            tc_fence_after();
+                            const bool raw = nv >= m.ct;
+                            const uint32_t xa = aX + b * kXBuf, pa = aP + b * kPBuf;
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            umma_bf16(tmem + kTmemS, sw128_desc(aX + b * kXBlk + kk * 32, 16, 1024),
-                                      sw128_desc(aQ + b * kQBlk + kk * 32, 16, 1024), raw ? id_s_f16 : id_s_bf,
-                                      (b | kk) ? 1u : 0u);
-                    }
-                    if (!ok) break;
-                    umma_commit(s_full);
-                    if (t == m.t1 - 1) umma_commit(q_free);
-                    // values O^T += X^T . P^T
-                    if (!mbar_wait(p_full, pph, abort_flag)) { ok = false; break; }
-                    pph ^= 1;
-                    if (first_pv && !first_item) {
-                        if (!mbar_wait(o_free, ofph, abort_flag)) { ok = false; break; }
-                        ofph ^= 1;
-                    }
-                    tc_fence_after();
+                            for (int c = 0; c < 4; ++c) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-#pragma unroll
-                        for (int ks = 0; ks < TR / 16; ++ks)
-                            umma_bf16(tmem + kTmemO + c * kNHead,
-                                      sw128_desc(aX + 2 * c * kXBlk + ks * 2048, kXBlk, 1024),
-                                      sw128_desc(aP + ks * 2048, 8192, 1024), raw ? id_v_f16 : id_v_bf,
-                                      (first_pv && ks == 0) ? 0u : 1u);
-                        umma_commit(&slot_empty[2 * c]);
-                        umma_commit(&slot_empty[2 * c + 1]);
+                                for (int ks = 0; ks < TR / 16; ++ks)
+                                    umma_bf16(tmem + kTmemO + c * kNHead,
+                                              sw128_desc(xa + 2 * c * kXBlk + ks * 2048, kXBlk, 1024),
+                                              sw128_desc(pa + ks * 2048, 8192, 1024), raw ? id_v_f16 : id_v_bf,
+                                              (nv == m.t0 && ks == 0) ? 0u : 1u);
+                            }
+                            umma_commit(&x_empty[b]);        // row tile free for the gather
+                            umma_commit(pv_done);
+                            ++nv;
+                            ++jv;
+                            progressed = true;
+                        }
                     }
-                    first_pv = false;
+                    if (!progressed && ns < m.t1) {
+                        const bool raw = ns >= m.ct;
+                        const int b = js & 1;
+                        bool ready = true;
+                        if (raw && !q16) {
+                            ready = mbar_test(q16_ready, q16ph);
+                            if (ready) {
+                                q16ph ^= 1;
+                                q16 = true;
+                            }
+                        }
+                        ready = ready && mbar_test(&s_empty[b], seph[b] ^ 1) && mbar_test(&x_full[b], xfph[b]);
+                        if (ready) {
+                            seph[b] ^= 1;
+                            xfph[b] ^= 1;
+                            tc_fence_after();
+                            const uint32_t xa = aX + b * kXBuf;
+                            for (int blk = 0; blk < 8; ++blk) {
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk)
+                                    umma_bf16(tmem + kTmemS + b * kNHead,
+                                              sw128_desc(xa + blk * kXBlk + kk * 32, 16, 1024),
+                                              sw128_desc(aQ + blk * kQBlk + kk * 32, 16, 1024),
+                                              raw ? id_s_f16 : id_s_bf, (blk | kk) ? 1u : 0u);
+                            }
+                            umma_commit(&s_full[b]);
+                            if (ns == m.t1 - 1) umma_commit(q_free);
+                            ++ns;
+                            ++js;
+                            progressed = true;
+                        }
+                    }
+                    if (progressed) {
+                        idle_since = 0;
+                    } else if (idle_since == 0) {
+                        idle_since = globaltimer_ns();
+                    } else if (*abort_flag || globaltimer_ns() - idle_since > kWaitLimitNs) {
+                        ok = false;
+                        break;
+                    }
                 }
                 if (!ok) break;
-                umma_commit(o_ready);
+                jt = jv;
                 first_item = false;
             }
             if (!ok) {
@@ -370,15 +475,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax + epilogue
-        const int q4 = warp & 3;                 // TMEM lane quarter
-        const int i = q4 * 32 + lane;            // tile row (logits) / dim within a chunk (values)
-        const int e = (warp - 2) * 32 + lane;    // 0..127 inside the softmax group
+        // Eight warps: TMEM lane quarter q4, head half hh.  Logits: lane < 16
+        // holds tile row 16*q4 + lane (M = 64 layout).  Values: lane = dim.
+        const int sw = warp - kFirstSoftmaxWarp;        // 0..7
+        const int q4 = warp & 3;
+        const int hh = sw >> 2;                         // heads 32*hh .. 32*hh+31
+        const int row = 16 * q4 + lane;                 // tile row (lane < 16)
+        const int e = sw * 32 + lane;                   // 0..255 inside the softmax group
         const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
         const float sl2 = a.scale * 1.4426950408889634f;
-        uint32_t qph = 0, sfph = 0, orph = 0, gph = 0;
+        uint32_t qph = 0, pvph = 0, gph = 0, sfph[2] = {0, 0};
+        uint32_t jt = 0;
         bool ok = true;
-        // Barrier of the four softmax warps on an mbarrier, so that a wait that
-        // gives up (abort) cannot leave the other warps stuck.
+        // Barrier of the softmax warps on an mbarrier, so that a wait that gives
+        // up (abort) cannot leave the other warps stuck.
         auto group_sync = [&]() -> bool {
             __syncwarp();
             if (lane == 0) mbar_arrive(grp);
@@ -386,13 +496,28 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
             gph ^= 1;
             return r;
         };
+        auto convert_q = [&]() {
+            // q -> fp16 in place for the fp16 raw tier (no logit GEMM reads q now).
+            uint4 *qv = reinterpret_cast<uint4 *>(sQ);
+            for (int k = e; k < 8 * kQBlk / 16; k += kSoftmaxWarps * 32) {
+                uint4 v = qv[k];
+                uint32_t *w = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    w[j] = pack2<true>(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xffff0000u));
+                qv[k] = v;
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q16_ready);
+        };
         for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
             const Item m = make_item(a, it, n_split);
             if (m.t0 >= m.t1) {
                 // Empty row set: out = 0, lse = -inf (or an empty partial).
                 if (n_split == 1) {
                     float *o = a.out + static_cast<long long>(m.unit) * kNHead * kHeadDim;
-                    for (int k = e; k < kNHead * kHeadDim; k += 128) o[k] = 0.f;
+                    for (int k = e; k < kNHead * kHeadDim; k += kSoftmaxWarps * 32) o[k] = 0.f;
                     if (a.lse && e < kNHead) a.lse[static_cast<long long>(m.unit) * kNHead + e] = NEG_INF;
                 } else if (e < kNHead) {
                     float *ml = static_cast<float *>(a.ws) + static_cast<long long>(a.units) * n_split * kNHead * kHeadDim;
@@ -406,127 +531,117 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
             if (!ok) break;
             qph ^= 1;
             if (e < kNHead) sMused[e] = NEG_INF;
-            float lacc[kNHead];
+            float lacc[32];
 #pragma unroll
-            for (int h = 0; h < kNHead; ++h) lacc[h] = 0.f;
-            bool q16 = false, first_pv = true;
+            for (int k = 0; k < 32; ++k) lacc[k] = 0.f;
+            bool q16 = false;
             if (!(ok = group_sync())) break;
-            for (int t = m.t0; ok && t < m.t1; ++t) {
+            if (m.t0 >= m.ct) {                          // the item starts with a raw tile
+                convert_q();
+                q16 = true;
+            }
+            for (int t = m.t0; ok && t < m.t1; ++t, ++jt) {
                 const bool raw = t >= m.ct;
-                if (raw && !q16) {
-                    // Previous logit GEMMs of this item have completed (their S
-                    // was consumed); q -> fp16 in place for the fp16 raw tier.
-                    uint4 *qv = reinterpret_cast<uint4 *>(sQ);
-                    for (int k = e; k < 8 * kQBlk / 16; k += 128) {
-                        uint4 v = qv[k];
-                        uint32_t *w = reinterpret_cast<uint32_t *>(&v);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            w[j] = pack2<true>(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xffff0000u));
-                        qv[k] = v;
-                    }
-                    fence_proxy_async();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(q16_ready);
+                const int b = jt & 1;
+                const bool valid = lane < 16 && row_valid(a, m, t, row, nullptr);
+                ok = __all_sync(0xffffffffu, mbar_wait(&s_full[b], sfph[b], abort_flag));
+                if (!ok) break;
+                sfph[b] ^= 1;
+                // The next tile is the first raw one: its logits need q in fp16,
+                // and every compressed logit GEMM has completed (this one too).
+                if (!q16 && t + 1 < m.t1 && t + 1 >= m.ct) {
+                    convert_q();
                     q16 = true;
                 }
-                const bool valid = row_valid(a, m, t, i, nullptr);
-                ok = __all_sync(0xffffffffu, mbar_wait(s_full, sfph, abort_flag));
-                if (!ok) break;
-                sfph ^= 1;
                 tc_fence_after();
-                uint32_t r0[32], r1[32];
-                tmem_ld32(tmem + lane_off + kTmemS, r0);
-                tmem_ld32(tmem + lane_off + kTmemS + 32, r1);
-                tmem_wait_ld(r0);
-                tmem_wait_ld(r1);
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_off + kTmemS + b * kNHead + hh * 32, r);
+                tmem_wait_ld(r);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(s_empty);
-                float x[kNHead];
+                if (lane == 0) mbar_arrive(&s_empty[b]);
+                float x[32];
 #pragma unroll
-                for (int h = 0; h < 32; ++h) {
-                    x[h] = valid ? __uint_as_float(r0[h]) * sl2 : NEG_INF;
-                    x[32 + h] = valid ? __uint_as_float(r1[h]) * sl2 : NEG_INF;
-                }
-                // per-head max over this warp's 32 rows, then over the 4 warps
+                for (int k = 0; k < 32; ++k) x[k] = valid ? __uint_as_float(r[k]) * sl2 : NEG_INF;
+                // per-head max over this warp's 16 rows, then over the 4 lane quarters
 #pragma unroll
-                for (int h = 0; h < kNHead; ++h) {
-                    const float mx = warp_max(x[h]);
-                    if (lane == (h & 31)) sSmax[q4 * kNHead + h] = mx;
+                for (int k = 0; k < 32; ++k) {
+                    const float mx = warp_max(x[k]);
+                    if (lane == k) sSmax[q4 * kNHead + hh * 32 + k] = mx;
                 }
-                if (e == 0) *any_rescale = 0;
                 if (!(ok = group_sync())) break;
+                // Threads 0..63 combine the quarters for head e and update its
+                // running max (raised only when exceeded by more than 2^8).
                 if (e < kNHead) {
                     const float mt = fmaxf(fmaxf(sSmax[e], sSmax[kNHead + e]),
                                            fmaxf(sSmax[2 * kNHead + e], sSmax[3 * kNHead + e]));
                     const float mo = sMused[e];
-                    float alpha = 1.f;
+                    float al = 1.f;
                     if (mo == NEG_INF) {
                         sMused[e] = mt;                 // first finite max (O and sums are still 0)
                     } else if (mt > mo + kRescaleThreshold) {
                         sMused[e] = mt;
-                        alpha = exp2f(mo - mt);
-                        *any_rescale = 1;
+                        al = exp2f(mo - mt);
                     }
-                    sAlpha[e] = alpha;
+                    sAlpha[e] = al;
                 }
                 if (!(ok = group_sync())) break;
-                const bool rescale = *any_rescale != 0;
-                uint32_t pk[32];
+                bool rescale = false;
+                uint32_t pk[16];
 #pragma unroll
-                for (int h = 0; h < kNHead; h += 2) {
-                    const float m0 = sMused[h], m1 = sMused[h + 1];
-                    const float p0 = exp2f(x[h] - (m0 == NEG_INF ? 0.f : m0));
-                    const float p1 = exp2f(x[h + 1] - (m1 == NEG_INF ? 0.f : m1));
-                    if (rescale) {
-                        lacc[h] *= sAlpha[h];
-                        lacc[h + 1] *= sAlpha[h + 1];
-                    }
-                    lacc[h] += p0;
-                    lacc[h + 1] += p1;
-                    pk[h >> 1] = raw ? pack2<true>(p0, p1) : pack2<false>(p0, p1);
+                for (int k = 0; k < 32; k += 2) {
+                    const float m0 = sMused[hh * 32 + k], m1 = sMused[hh * 32 + k + 1];
+                    const float a0 = sAlpha[hh * 32 + k], a1 = sAlpha[hh * 32 + k + 1];
+                    rescale |= (a0 != 1.f) | (a1 != 1.f);
+                    const float p0 = exp2f(x[k] - (m0 == NEG_INF ? 0.f : m0));
+                    const float p1 = exp2f(x[k + 1] - (m1 == NEG_INF ? 0.f : m1));
+                    lacc[k] = lacc[k] * a0 + p0;
+                    lacc[k + 1] = lacc[k + 1] * a1 + p1;
+                    pk[k >> 1] = raw ? pack2<true>(p0, p1) : pack2<false>(p0, p1);
                 }
-                // P^T row i: 64 heads = 8 chunks of 16 B, 128B swizzle.
-                uint4 *prow = reinterpret_cast<uint4 *>(sP + i * 128);
+                // The previous values GEMM of this item must be complete before
+                // O^T may be rescaled (its buffer was also the one before last).
+                if (t > m.t0) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(pv_done, pvph, abort_flag));
+                    if (!ok) break;
+                    pvph ^= 1;
+                }
+                if (lane < 16) {
+                    // P^T row `row`, heads 32*hh..: chunks 4*hh..4*hh+3 of the 128B-swizzled row.
+                    uint4 *prow = reinterpret_cast<uint4 *>(sP + b * kPBuf + row * 128);
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    prow[c ^ (i & 7)] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                    for (int c = 0; c < 4; ++c)
+                        prow[(4 * hh + c) ^ (row & 7)] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                }
                 fence_proxy_async();
-                if (rescale && !first_pv) {
-                    // The previous values GEMM is complete (this tile's logits needed
-                    // every column block it freed): scale O^T column h by alpha_h.
+                if (rescale && t > m.t0) {
                     tc_fence_after();
                     for (int c = 0; c < 4; ++c) {
-                        for (int half = 0; half < 2; ++half) {
-                            uint32_t v[32];
-                            const uint32_t ta = tmem + lane_off + kTmemO + c * kNHead + half * 32;
-                            tmem_ld32(ta, v);
-                            tmem_wait_ld(v);
+                        uint32_t v[32];
+                        const uint32_t ta = tmem + lane_off + kTmemO + c * kNHead + hh * 32;
+                        tmem_ld32(ta, v);
+                        tmem_wait_ld(v);
 #pragma unroll
-                            for (int k = 0; k < 32; ++k)
-                                v[k] = __float_as_uint(__uint_as_float(v[k]) * sAlpha[half * 32 + k]);
-                            tmem_st32(ta, v);
-                        }
+                        for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * sAlpha[hh * 32 + k]);
+                        tmem_st32(ta, v);
                     }
                     tmem_wait_st();
                     tc_fence_before();
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(p_full);
-                first_pv = false;
+                if (lane == 0) mbar_arrive(&p_full[b]);
             }
             if (!ok) break;
-            // ---- epilogue: row sums across the 128 rows, then O^T out
+            // ---- epilogue: row sums across the 64 rows, then O^T out
 #pragma unroll
-            for (int h = 0; h < kNHead; ++h) {
-                float v = lacc[h];
+            for (int k = 0; k < 32; ++k) {
+                float v = lacc[k];
                 v += __shfl_xor_sync(0xffffffffu, v, 1);
                 v += __shfl_xor_sync(0xffffffffu, v, 2);
                 v += __shfl_xor_sync(0xffffffffu, v, 4);
                 v += __shfl_xor_sync(0xffffffffu, v, 8);
                 v += __shfl_xor_sync(0xffffffffu, v, 16);
-                if (lane == (h & 31)) sSmax[q4 * kNHead + h] = v;
+                if (lane == k) sSmax[q4 * kNHead + hh * 32 + k] = v;
             }
             if (!(ok = group_sync())) break;
             const long long slot = static_cast<long long>(m.unit) * n_split + m.split;
@@ -546,22 +661,22 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                 }
             }
             if (!(ok = group_sync())) break;
-            ok = __all_sync(0xffffffffu, mbar_wait(o_ready, orph, abort_flag));
+            // the item's last values GEMM
+            ok = __all_sync(0xffffffffu, mbar_wait(pv_done, pvph, abort_flag));
             if (!ok) break;
-            orph ^= 1;
+            pvph ^= 1;
             tc_fence_after();
             float *obase = n_split == 1 ? a.out + static_cast<long long>(m.unit) * kNHead * kHeadDim
                                         : static_cast<float *>(a.ws) + slot * kNHead * kHeadDim;
             for (int c = 0; c < 4; ++c) {
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + lane_off + kTmemO + c * kNHead + half * 32, v);
-                    tmem_wait_ld(v);
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_off + kTmemO + c * kNHead + hh * 32, v);
+                tmem_wait_ld(v);
+                const int d = c * 128 + q4 * 32 + lane;
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const int h = half * 32 + k;
-                        obase[static_cast<long long>(h) * kHeadDim + c * TR + i] = __uint_as_float(v[k]) * sInvL[h];
-                    }
+                for (int k = 0; k < 32; ++k) {
+                    const int h = hh * 32 + k;
+                    obase[static_cast<long long>(h) * kHeadDim + d] = __uint_as_float(v[k]) * sInvL[h];
                 }
             }
             tc_fence_before();
@@ -576,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
