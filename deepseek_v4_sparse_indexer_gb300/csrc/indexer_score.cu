@@ -44,7 +44,14 @@ struct IdxCfg {
     static constexpr int kEpiSplit = (G == 1) ? 1 : 2;    // epilogue warps per TMEM lane quarter
     static constexpr int kEpiWarps = 4 * kEpiSplit;
     static constexpr int kQPerEpiWarp = G / kEpiSplit;    // queries one epilogue thread reduces
-    static constexpr int kThreads = 64 + 32 * kEpiWarps;
+    // G = 4 keeps two queries' 64 weights per epilogue thread in registers:
+    // warps 0-3 (producer, issuer, two idle) give registers up and the two
+    // epilogue warpgroups (warps 4-11) take them (setmaxnreg).
+    static constexpr bool kSplitRegs = (G != 1);
+    static constexpr int kFirstEpiWarp = kSplitRegs ? 4 : 2;
+    static constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
+    static constexpr int kLowRegs = 56, kHighRegs = 224;   // per thread after setmaxnreg
+    static constexpr int kRegsNeeded = 128 * kLowRegs + 32 * kEpiWarps * kHighRegs;
     static constexpr uint32_t kTmemCols = kAccBufs * N;   // 256 or 512
     static constexpr int kASub = kTileRows * 128;         // one 64-element K half of a key tile
     static constexpr int kABytes = 2 * kASub;             // 32 KB
@@ -132,26 +139,20 @@ DS4A_DEV float2 unpack_f2(unsigned long long v) {
     return r;
 }
 
-// sum_h w[h] * max(0, acc[h]) over one query's 64 head sums (v0: heads 0..31,
-// v1: heads 32..63).  The ReLU is per element; the weighted sum runs as packed
-// fp32x2 FMAs into four independent pair accumulators (eight partial sums),
-// combined in a fixed order, which keeps the dependency chains short.
-DS4A_DEV float relu_weighted_sum(const float *w, const uint32_t (&v0)[32], const uint32_t (&v1)[32]) {
-    unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};
-    const float4 *w4 = reinterpret_cast<const float4 *>(w);
+// Accumulates sum_h w[h] * max(0, acc[h]) over 32 head sums v (heads
+// 32*half .. 32*half + 31 of one query) into four packed fp32x2 partial sums.
+// w2 holds the query's 64 weights as 32 (even, odd) pairs in registers, so the
+// reduction reads no memory.  The ReLU is per element; the FMAs are packed.
+DS4A_DEV void relu_weighted_acc(unsigned long long (&acc)[4], const unsigned long long (&w2)[32], int half,
+                                const uint32_t (&v)[32]) {
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-        const float4 ww = w4[q];
-        const uint32_t *v = q < 8 ? v0 : v1;
-        const int h = (q & 7) * 4;
-        const unsigned long long x01 = pack_f2(fmaxf(__uint_as_float(v[h]), 0.f), fmaxf(__uint_as_float(v[h + 1]), 0.f));
-        const unsigned long long x23 =
-            pack_f2(fmaxf(__uint_as_float(v[h + 2]), 0.f), fmaxf(__uint_as_float(v[h + 3]), 0.f));
-        unsigned long long &a0 = acc[(2 * q) & 3];
-        unsigned long long &a1 = acc[(2 * q + 1) & 3];
-        asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a0) : "l"(pack_f2(ww.x, ww.y)), "l"(x01));
-        asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a1) : "l"(pack_f2(ww.z, ww.w)), "l"(x23));
+    for (int p = 0; p < 16; ++p) {
+        const unsigned long long x =
+            pack_f2(fmaxf(__uint_as_float(v[2 * p]), 0.f), fmaxf(__uint_as_float(v[2 * p + 1]), 0.f));
+        asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc[p & 3]) : "l"(w2[half * 16 + p]), "l"(x));
     }
+}
+DS4A_DEV float sum_pairs(const unsigned long long (&acc)[4]) {
     const float2 s0 = unpack_f2(acc[0]), s1 = unpack_f2(acc[1]), s2 = unpack_f2(acc[2]), s3 = unpack_f2(acc[3]);
     return ((s0.x + s0.y) + (s1.x + s1.y)) + ((s2.x + s2.y) + (s3.x + s3.y));
 }
@@ -204,6 +205,9 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
     const long long items = a.total_items;
 
+    if (warp < C::kFirstEpiWarp) {
+        if constexpr (C::kSplitRegs) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kLowRegs));
+    }
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -290,9 +294,10 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
             mbar_wait_drain(drain_bar, 0);
         }
         __syncwarp();
-    } else {
+    } else if (warp >= C::kFirstEpiWarp) {
         // ------------------------------------------------------------ epilogue
-        const int e = warp - 2;
+        if constexpr (C::kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kHighRegs));
+        const int e = warp - C::kFirstEpiWarp;
         const int quarter = warp & 3;             // TMEM lanes this warp may access
         const int half = e / 4;                   // which queries of the group
         const int row_in_tile = quarter * 32 + lane;
@@ -316,6 +321,18 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
                                     : 0.f;
             }
             __syncwarp();
+            // The item's weights stay in registers for all of its tiles.
+            unsigned long long w2[C::kQPerEpiWarp][32];
+#pragma unroll
+            for (int j = 0; j < C::kQPerEpiWarp; ++j) {
+                const float4 *w4 = reinterpret_cast<const float4 *>(wsm + j * 64);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float4 ww = w4[i];
+                    w2[j][2 * i] = pack_f2(ww.x, ww.y);
+                    w2[j][2 * i + 1] = pack_f2(ww.z, ww.w);
+                }
+            }
             int qpos[C::kQPerEpiWarp];
 #pragma unroll
             for (int j = 0; j < C::kQPerEpiWarp; ++j)
@@ -332,11 +349,15 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < C::kQPerEpiWarp; ++j) {
                     const uint32_t col = static_cast<uint32_t>(ab * C::N + (half * C::kQPerEpiWarp + j) * 64);
-                    uint32_t v0[32], v1[32];
-                    tmem_ld32_sync(tmem_base + lane_off + col, v0);
-                    tmem_ld32_sync(tmem_base + lane_off + col + 32, v1);
-                    tmem_wait_ld2(v0, v1);
-                    sc[j] = relu_weighted_sum(wsm + j * 64, v0, v1);
+                    unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t v[32];
+                        tmem_ld32_sync(tmem_base + lane_off + col + hh * 32, v);
+                        tmem_wait_ld(v);
+                        relu_weighted_acc(acc, w2[j], hh, v);
+                    }
+                    sc[j] = sum_pairs(acc);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -375,6 +396,14 @@ cudaError_t launch_g(const IndexerArgs &a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(indexer_score_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
+    if constexpr (C::kSplitRegs) {
+        // setmaxnreg.inc draws on the registers the block was launched with: the
+        // split must fit in them, or the raising warps would wait forever.
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, indexer_score_kernel<G>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs * C::kThreads < C::kRegsNeeded) return cudaErrorInvalidConfiguration;
+    }
     indexer_score_kernel<G><<<a.grid, C::kThreads, C::kSmemBytes, s>>>(a);
     return cudaGetLastError();
 }

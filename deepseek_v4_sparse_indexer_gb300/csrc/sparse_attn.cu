@@ -7,32 +7,35 @@
 // One CTA (persistent, one per SM) walks work items = (unit, split), where a
 // unit is one decode query or one query of a prefill chunk.  The unit's row
 // list [selected compressed rows..., raw-window rows...] is cut into 64-row
-// tiles, double-buffered in shared memory so that the next tile's gather and
-// logits overlap this tile's softmax:
-//   gather   warps 0-1: 16-byte cp.async copies of the tile's rows into eight
-//            8 KB column blocks in the 128B-swizzled layout (a warp moves four
-//            whole 128-byte row segments per instruction; masked rows are
-//            zero-filled); each thread fences its copies into the async proxy
-//            before arriving on the buffer's barrier.  The two gather warps
-//            take alternate tiles;
-//   logits   warp 2 (one thread): S^T[64 rows x 64 heads] = X . q^T, 32 UMMAs
-//            (M=64, N=64, K=16) from the K-major row blocks and the K-major q,
-//            into one of two TMEM buffers (row m of an M=64 accumulator sits in
-//            TMEM lane 32*(m/16) + m%16);
-//   softmax  warps 3-10 (one thread = one row x 32 heads): tcgen05.ld of the
-//            row's 32 logits, per-head tile max with redux.sync.max.f32 across
-//            the warp and a 4-way max across lane quarters, p = exp2(l - m)
-//            written as P^T (the 16-bit MN-major operand) to one of two shared
-//            buffers, per-thread partial row sums kept in registers;
-//   values   warp 2: O^T[512 dims x 64 heads] += X^T . P^T as four M=128
-//            chunks (K = 64 rows, X read as the MN-major operand), accumulating
-//            in TMEM; its commit frees the row buffer.
+// tiles, double-buffered in shared memory:
+//   gather   warps 5-11: the seven warps share every tile (4-row groups dealt
+//            round-robin) with 16-byte cp.async into eight 8 KB column
+//            blocks in the 128B-swizzled layout; masked rows are zero-filled
+//            and per-group row-validity bits go to shared memory; each
+//            thread fences its copies into the async proxy before its warp
+//            arrives on the buffer's barrier;
+//   logits   warp 4 (one thread): S[64 heads x 64 rows] = q . X^T, 32 UMMAs
+//            (M=64, N=64, K=16, both operands K-major) into one of two TMEM
+//            buffers (head h of the M=64 accumulator sits in TMEM lane
+//            32*(h/16) + h%16);
+//   softmax  warps 0-3 (warp w reads TMEM lanes 32w..32w+15 = heads
+//            16w..16w+15 with the 16x256b shape: thread t holds heads
+//            16w + t/4 and 16w + t/4 + 8 for the 16 rows 8j + 2(t%4) + {0,1}).
+//            The per-head tile max is a register max plus two shuffles;
+//            p = exp2(l - m) goes to P[head][row] (the K-major operand of the
+//            values GEMM), row sums stay in registers;
+//   values   warp 4: O^T[512 dims x 64 heads] += X^T . P^T as four M=128
+//            chunks (K = 64 rows; X read as the MN-major operand, P as the
+//            K-major one), accumulating in TMEM; its commit frees the row
+//            buffer and the P buffer.
 // The running max per head is only raised when a tile exceeds it by more than
-// 2^8 (then O^T and the partial sums are rescaled), so p <= 256 always and the
-// rescale is rare.  Compressed tiles multiply in bf16; raw tiles in fp16 with
-// q converted in place to fp16 (exact for |q| in [2^-14, 65504]).
-// Split items write unnormalised partials (O, m, l) that attn_merge_kernel
-// combines by log-sum-exp.
+// 2^8, so p <= 256 always.  A raise needs O^T (whose TMEM lanes are the 512
+// dims, spread over all four softmax warps) rescaled: the four warps exchange
+// a flag and the factors once per tile, and all of them rescale their lanes
+// when any head was raised (rare).  Compressed tiles multiply in bf16; raw
+// tiles in fp16 with q converted in place to fp16 (exact for |q| in
+// [2^-14, 65504]).  Split items write unnormalised partials (O, m, l) that
+// attn_merge_kernel combines by log-sum-exp.
 //
 // Every wait is bounded (DS4A_DEV_TIMEOUT); on timeout the CTA drains what it
 // issued (bounded), frees TMEM and returns.
@@ -42,44 +45,45 @@
 namespace ds4a {
 namespace {
 
-constexpr int TR = 64;                        // rows per tile (UMMA M of the logit GEMM)
-constexpr int kProducerWarps = 2;             // warps 0-1: row gather (cp.async)
-constexpr int kProducerThreads = kProducerWarps * 32;
-constexpr int kMmaWarp = 2;                   // warp 2: TMEM owner + UMMA issuer
-constexpr int kFirstSoftmaxWarp = 3;          // warps 3-10: softmax + epilogue
-constexpr int kSoftmaxWarps = 8;
-constexpr int kThreads = (kFirstSoftmaxWarp + kSoftmaxWarps) * 32;
-constexpr int kRowsPerThread = TR / 8;        // rows one gather thread copies per block
+constexpr int TR = 64;                        // rows per tile (UMMA N of the logit GEMM)
+constexpr int kSoftmaxWarps = 4;              // warps 0-3: softmax + epilogue (TMEM lane quarters)
+constexpr int kMmaWarp = 4;                   // warp 4: TMEM owner + UMMA issuer
+constexpr int kFirstGatherWarp = 5;           // warps 5-11: row gather (cp.async)
+constexpr int kGatherWarps = 7;
+constexpr int kRowGroups = TR / 4;            // 4-row groups of a tile, dealt round-robin to the gather warps
+constexpr int kGroupsPerWarp = (kRowGroups + kGatherWarps - 1) / kGatherWarps;
+constexpr int kThreads = (kFirstGatherWarp + kGatherWarps) * 32;
 constexpr int kQBlk = kNHead * 128;           // 64 heads x 64 dims x 2 B = 8 KB
 constexpr int kXBlk = TR * 128;               // 64 rows x 64 dims x 2 B = 8 KB
 constexpr int kXBuf = 8 * kXBlk;              // one row tile: 64 KB
-constexpr int kPBuf = TR * 128;               // P^T [64 rows][64 heads] 16-bit: 8 KB
+constexpr int kPBuf = kNHead * 128;           // P [64 heads][64 rows] 16-bit: 8 KB
 constexpr int kOffQ = 0;
 constexpr int kOffX = kOffQ + 8 * kQBlk;      // q: 64 KB
 constexpr int kOffP = kOffX + 2 * kXBuf;      // two row tiles: 128 KB
-constexpr int kOffSmax = kOffP + 2 * kPBuf;   // two P^T buffers: 16 KB
-constexpr int kOffMused = kOffSmax + 4 * kNHead * 4;
-constexpr int kOffAlpha = kOffMused + kNHead * 4;
-constexpr int kOffInvL = kOffAlpha + kNHead * 4;
+constexpr int kOffValid = kOffP + 2 * kPBuf;  // two P buffers: 16 KB
+constexpr int kOffAlpha = kOffValid + 2 * kRowGroups;  // [2][16] row-validity nibbles
+constexpr int kOffFlag = kOffAlpha + 2 * kNHead * 4;
+constexpr int kOffInvL = kOffFlag + 2 * kSoftmaxWarps * 4;
 constexpr int kOffBar = kOffInvL + kNHead * 4;
-constexpr int kNumBars = 20;
+constexpr int kNumBars = 16;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 32 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-constexpr uint32_t kTmemCols = 512;           // S^T: 2 x 64 columns, O^T: 4 x 64 columns
+static_assert(kOffBar % 8 == 0, "mbarrier alignment");
+constexpr uint32_t kTmemCols = 512;           // S: 2 x 64 columns, O^T: 4 x 64 columns
 constexpr uint32_t kTmemS = 0;
 constexpr uint32_t kTmemO = 128;
 constexpr int kMaxSplit = 16;
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
 
-// UMMA instruction descriptors (see idesc_bf16_f32): logits (M = 64 rows,
-// N = 64 heads) with K-major A/B; values (M = 128 dims, N = 64 heads) with
-// MN-major A (rows x dims read as dims x rows) and MN-major B.
+// UMMA instruction descriptors (see idesc_bf16_f32): logits (M = 64 heads,
+// N = 64 rows, both K-major); values (M = 128 dims, N = 64 heads) with the
+// MN-major A (row tile read as dims x rows) and the K-major B (P).
 __host__ __device__ constexpr uint32_t idesc_f16(bool f16_inputs, bool values) {
     const uint32_t fmt = f16_inputs ? 0u : 1u;
-    const uint32_t m = values ? 128u : static_cast<uint32_t>(TR);
-    return (1u << 4) | (fmt << 7) | (fmt << 10) | (values ? (1u << 15) | (1u << 16) : 0u) |
-           (static_cast<uint32_t>(kNHead >> 3) << 17) | ((m >> 4) << 24);
+    const uint32_t m = values ? 128u : static_cast<uint32_t>(kNHead);
+    const uint32_t n = values ? static_cast<uint32_t>(kNHead) : static_cast<uint32_t>(TR);
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | (values ? (1u << 15) : 0u) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
 // Shared-memory descriptor with explicit leading / stride byte offsets (128B swizzle).
@@ -101,11 +105,6 @@ DS4A_DEV void tma_load_2d_nohint(void *dst, const void *map, uint64_t *bar, int 
         : "memory");
 }
 DS4A_DEV void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-DS4A_DEV float warp_max(float v) {
-    float r;
-    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-    return r;
-}
 
 DS4A_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
@@ -188,21 +187,17 @@ DS4A_DEV Item make_item(const AttnArgs &a, int it, int n_split) {
     return m;
 }
 
-// Row j of tile t: valid?  (compressed rows need an index inside [0, N_cap)).
-// *coord receives the row's index in the rows buffer (compressed) or the raw buffer.
-DS4A_DEV bool row_valid(const AttnArgs &a, const Item &m, int t, int j, int *coord) {
-    if (t < m.ct) {
-        const int jj = t * TR + j;
-        if (jj >= m.cnt) return false;
-        const int iv = __ldg(a.idx + static_cast<long long>(m.unit) * a.top_k + jj);
-        if (iv < 0 || iv >= a.N_cap) return false;
-        if (coord) *coord = static_cast<int>(m.comp_row0 + iv);
-        return true;
-    }
-    const int jj = (t - m.ct) * TR + j;
-    if (jj >= m.nrw) return false;
-    if (coord) *coord = static_cast<int>(m.raw_row0 + jj);
-    return true;
+DS4A_DEV void tmem_ld16x256_x8(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
 }
 
 __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_constant__ AttnArgs a, int n_split,
@@ -212,20 +207,19 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
     uint8_t *sQ = smem + kOffQ;
     uint8_t *sX = smem + kOffX;
     uint8_t *sP = smem + kOffP;
-    float *sSmax = reinterpret_cast<float *>(smem + kOffSmax);
-    float *sMused = reinterpret_cast<float *>(smem + kOffMused);   // running max per head (log2 units)
-    float *sAlpha = reinterpret_cast<float *>(smem + kOffAlpha);   // this tile's rescale factor per head
+    uint8_t *sValid = smem + kOffValid;          // [2][16] bit i of byte g: tile row 4g + i is listed and in range
+    float *sAlpha = reinterpret_cast<float *>(smem + kOffAlpha);        // [2][64] this tile's rescale factor per head
+    uint32_t *sFlag = reinterpret_cast<uint32_t *>(smem + kOffFlag);    // [2][4] softmax warp raised a head's max
     float *sInvL = reinterpret_cast<float *>(smem + kOffInvL);
     uint64_t *x_full = reinterpret_cast<uint64_t *>(smem + kOffBar);   // [2] row tile landed
-    uint64_t *x_empty = x_full + 2;                                    // [2] row tile consumed
+    uint64_t *x_empty = x_full + 2;                                    // [2] values GEMM done: row tile + P free
     uint64_t *s_full = x_empty + 2;                                    // [2] logits in TMEM
     uint64_t *s_empty = s_full + 2;                                    // [2] logits read
-    uint64_t *p_full = s_empty + 2;                                    // [2] P^T written
+    uint64_t *p_full = s_empty + 2;                                    // [2] P written
     uint64_t *q_full = p_full + 2;
     uint64_t *q_free = q_full + 1;
     uint64_t *q16_ready = q_free + 1;
-    uint64_t *pv_done = q16_ready + 1;                                 // after every values GEMM
-    uint64_t *o_free = pv_done + 1;
+    uint64_t *o_free = q16_ready + 1;
     uint64_t *drain = o_free + 1;
     uint64_t *grp = drain + 1;                                         // softmax-group barrier
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
@@ -234,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&x_full[b], 32);                 // the one gather warp of that buffer
+            mbar_init(&x_full[b], kGatherWarps);
             mbar_init(&x_empty[b], 1);
             mbar_init(&s_full[b], 1);
             mbar_init(&s_empty[b], kSoftmaxWarps);
@@ -243,7 +237,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
         mbar_init(q_full, 1);
         mbar_init(q_free, 1);
         mbar_init(q16_ready, kSoftmaxWarps);
-        mbar_init(pv_done, 1);
         mbar_init(o_free, kSoftmaxWarps);
         mbar_init(drain, 1);
         mbar_init(grp, kSoftmaxWarps);
@@ -258,16 +251,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
     const uint32_t tmem = *tmem_slot;
     const float NEG_INF = -__int_as_float(0x7f800000);
 
-    if (warp < kProducerWarps) {
+    if (warp >= kFirstGatherWarp) {
         // ------------------------------------------------------------ row gather
-        // The two gather warps take alternate tiles (warp w: tiles with
-        // counter jt % 2 == w), so one tile's copies are in flight while the
-        // other warp still waits for its own.  Lane l copies 16-byte chunk
-        // (l & 7) of rows r_k = 4k + (l >> 3) of every 64-column block: a warp
-        // instruction moves four full 128-byte row segments.  Destinations
-        // follow the 128B swizzle.
+        // All seven warps walk the CTA's (item, tile) sequence; warp g copies
+        // the 4-row groups g, g + 7, g + 14 (< 16) of every tile.  Lane l
+        // copies 16-byte chunk (l & 7) of row 4k + (l >> 3) of group k in
+        // every 64-column block: a warp instruction moves four full 128-byte
+        // row segments.  Destinations follow the 128B swizzle.
+        const int gw = warp - kFirstGatherWarp;
         const int chunk = lane & 7, rsub = lane >> 3;
-        uint32_t xeph = 0;
+        uint32_t xeph[2] = {0, 0};
         bool ok = true;
         auto first_tile = [&](int it, Item &m) -> int {
             for (; it < n_items; it += gridDim.x) {
@@ -285,10 +278,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
             }
         };
         // Row list entries of tile t for this lane (< 0: masked).
-        auto fetch_rows = [&](const Item &m, int t, int (&rv)[16]) {
+        auto fetch_rows = [&](const Item &m, int t, int (&rv)[kGroupsPerWarp]) {
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const int r = 4 * k + rsub;
+            for (int k = 0; k < kGroupsPerWarp; ++k) {
+                const int g = gw + k * kGatherWarps;
+                const int r = 4 * g + rsub;
+                if (g >= kRowGroups) {
+                    rv[k] = -1;
+                    continue;
+                }
                 if (t < m.ct) {
                     const int jj = t * TR + r;
                     rv[k] = jj < m.cnt ? __ldg(a.idx + static_cast<long long>(m.unit) * a.top_k + jj) : -1;
@@ -302,22 +300,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
             if (t < m.ct) return (v < 0 || v >= a.N_cap) ? -1 : static_cast<int>(m.comp_row0 + v);
             return v < 0 ? -1 : static_cast<int>(m.raw_row0 + v);
         };
-        // Walk this CTA's (item, tile) sequence; this warp handles every second tile.
+        auto nibble = [](uint32_t bal) -> uint32_t {   // lanes 0, 8, 16, 24 -> bits 0..3
+            return (bal & 1u) | ((bal >> 7) & 2u) | ((bal >> 14) & 4u) | ((bal >> 21) & 8u);
+        };
         Item cm;
         int cit = first_tile(blockIdx.x, cm);
         int ct_ = cit < n_items ? cm.t0 : 0;
         uint32_t jt = 0;
-        if (warp == 1 && cit < n_items) {
-            advance(cit, ct_, cm);
-            jt = 1;
-        }
-        int rv[16];
+        int rv[kGroupsPerWarp];
         if (cit < n_items) fetch_rows(cm, ct_, rv);
         while (ok && cit < n_items) {
-            if (ct_ == cm.t0) {
+            if (ct_ == cm.t0 && gw == 0) {
                 // First tile of an item: q (bf16) by TMA once the previous item's
-                // logits are done (the warp owning the first tile loads it).
-                // q_free completes once per item, so item k waits for phase k-1.
+                // logits are done.  q_free completes once per item, so item k
+                // waits for phase k-1.
                 if (ordinal > 0) {
                     ok = __all_sync(0xffffffffu, mbar_wait(q_free, (ordinal - 1) & 1, abort_flag));
                     if (!ok) break;
@@ -328,40 +324,49 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                         tma_load_2d_nohint(sQ + b * kQBlk, &a.tm_q, q_full, b * 64, cm.unit * kNHead);
                 }
             }
-            int src[16];
+            int src[kGroupsPerWarp];
             bool bad_idx = false;
             const uint16_t *base = (ct_ < cm.ct ? a.rows : a.raw) + chunk * 8;
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                src[k] = row_index(cm, ct_, rv[k]);
+            for (int k = 0; k < kGroupsPerWarp; ++k) {
+                const int g = gw + k * kGatherWarps;
+                src[k] = g < kRowGroups ? row_index(cm, ct_, rv[k]) : -1;
                 // A listed row whose index lies outside [0, N_cap) is masked and flagged.
-                if (ct_ < cm.ct && ct_ * TR + 4 * k + rsub < cm.cnt && src[k] < 0) bad_idx = true;
+                if (g < kRowGroups && ct_ < cm.ct && ct_ * TR + 4 * g + rsub < cm.cnt && src[k] < 0) bad_idx = true;
             }
             if (__any_sync(0xffffffffu, bad_idx) && lane == 0) report(a.status, DS4A_DEV_BOUNDS);
-            const int xb = jt & 1;                        // == warp
-            ok = __all_sync(0xffffffffu, mbar_wait(&x_empty[xb], xeph ^ 1, abort_flag));
+            const int xb = jt & 1;
+            ok = __all_sync(0xffffffffu, mbar_wait(&x_empty[xb], xeph[xb] ^ 1, abort_flag));
             if (!ok) break;
-            xeph ^= 1;
+            xeph[xb] ^= 1;
             const uint32_t buf = smem_u32(sX) + xb * kXBuf;
 #pragma unroll
             for (int b = 0; b < 8; ++b) {
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const int r = 4 * k + rsub;
+                for (int k = 0; k < kGroupsPerWarp; ++k) {
+                    const int g = gw + k * kGatherWarps;
+                    if (g >= kRowGroups) continue;
+                    const int r = 4 * g + rsub;
                     cp_async16(buf + b * kXBlk + r * 128 + ((chunk ^ (r & 7)) << 4),
                                src[k] >= 0 ? base + static_cast<long long>(src[k]) * kHeadDim + b * 64 : a.q,
                                src[k] >= 0 ? 16u : 0u);
                 }
             }
             cp_async_commit();
-            // While the copies land: the row list of this warp's next tile (two ahead).
+#pragma unroll
+            for (int k = 0; k < kGroupsPerWarp; ++k) {
+                const int g = gw + k * kGatherWarps;
+                const uint32_t bal = __ballot_sync(0xffffffffu, src[k] >= 0);
+                if (lane == 0 && g < kRowGroups) sValid[xb * kRowGroups + g] = static_cast<uint8_t>(nibble(bal));
+            }
+            // While the copies land: the row list of the next tile.
             advance(cit, ct_, cm);
-            if (cit < n_items) advance(cit, ct_, cm);
             if (cit < n_items) fetch_rows(cm, ct_, rv);
             cp_async_wait<0>();
             fence_proxy_async();
-            mbar_arrive(&x_full[xb]);
-            jt += 2;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&x_full[xb]);
+            ++jt;
         }
         cp_async_wait<0>();
         if (!ok) {
@@ -410,11 +415,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                                 for (int ks = 0; ks < TR / 16; ++ks)
                                     umma_bf16(tmem + kTmemO + c * kNHead,
                                               sw128_desc(xa + 2 * c * kXBlk + ks * 2048, kXBlk, 1024),
-                                              sw128_desc(pa + ks * 2048, 8192, 1024), raw ? id_v_f16 : id_v_bf,
+                                              sw128_desc(pa + ks * 32, 16, 1024), raw ? id_v_f16 : id_v_bf,
                                               (nv == m.t0 && ks == 0) ? 0u : 1u);
                             }
-                            umma_commit(&x_empty[b]);        // row tile free for the gather
-                            umma_commit(pv_done);
+                            umma_commit(&x_empty[b]);        // row tile and P buffer free
                             ++nv;
                             ++jv;
                             progressed = true;
@@ -440,9 +444,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                             for (int blk = 0; blk < 8; ++blk) {
 #pragma unroll
                                 for (int kk = 0; kk < 4; ++kk)
-                                    umma_bf16(tmem + kTmemS + b * kNHead,
-                                              sw128_desc(xa + blk * kXBlk + kk * 32, 16, 1024),
+                                    umma_bf16(tmem + kTmemS + b * TR,
                                               sw128_desc(aQ + blk * kQBlk + kk * 32, 16, 1024),
+                                              sw128_desc(xa + blk * kXBlk + kk * 32, 16, 1024),
                                               raw ? id_s_f16 : id_s_bf, (blk | kk) ? 1u : 0u);
                             }
                             umma_commit(&s_full[b]);
@@ -475,16 +479,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax + epilogue
-        // Eight warps: TMEM lane quarter q4, head half hh.  Logits: lane < 16
-        // holds tile row 16*q4 + lane (M = 64 layout).  Values: lane = dim.
-        const int sw = warp - kFirstSoftmaxWarp;        // 0..7
-        const int q4 = warp & 3;
-        const int hh = sw >> 2;                         // heads 32*hh .. 32*hh+31
-        const int row = 16 * q4 + lane;                 // tile row (lane < 16)
-        const int e = sw * 32 + lane;                   // 0..255 inside the softmax group
+        // Warp w = TMEM lane quarter w.  Logits (16x256b loads): thread t holds
+        // heads h0 = 16w + t/4 and h1 = h0 + 8 for tile rows 8j + 2(t%4) + {0,1},
+        // j = 0..7 (registers 4j, 4j+1: h0; 4j+2, 4j+3: h1).  Values: lane = dim.
+        const int q4 = warp;
+        const int t4 = lane & 3;
+        const int h0 = 16 * q4 + (lane >> 2), h1 = h0 + 8;
+        const int e = threadIdx.x;                      // 0..127 inside the softmax group
         const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
         const float sl2 = a.scale * 1.4426950408889634f;
-        uint32_t qph = 0, pvph = 0, gph = 0, sfph[2] = {0, 0};
+        uint32_t qph = 0, gph = 0, sfph[2] = {0, 0};
         uint32_t jt = 0;
         bool ok = true;
         // Barrier of the softmax warps on an mbarrier, so that a wait that gives
@@ -530,12 +534,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
             ok = __all_sync(0xffffffffu, mbar_wait(q_full, qph, abort_flag));
             if (!ok) break;
             qph ^= 1;
-            if (e < kNHead) sMused[e] = NEG_INF;
-            float lacc[32];
-#pragma unroll
-            for (int k = 0; k < 32; ++k) lacc[k] = 0.f;
+            float M0 = NEG_INF, M1 = NEG_INF, l0 = 0.f, l1 = 0.f;   // running max (log2 units) and partial sums
             bool q16 = false;
-            if (!(ok = group_sync())) break;
             if (m.t0 >= m.ct) {                          // the item starts with a raw tile
                 convert_q();
                 q16 = true;
@@ -543,7 +543,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
             for (int t = m.t0; ok && t < m.t1; ++t, ++jt) {
                 const bool raw = t >= m.ct;
                 const int b = jt & 1;
-                const bool valid = lane < 16 && row_valid(a, m, t, row, nullptr);
                 ok = __all_sync(0xffffffffu, mbar_wait(&s_full[b], sfph[b], abort_flag));
                 if (!ok) break;
                 sfph[b] ^= 1;
@@ -555,74 +554,99 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                 }
                 tc_fence_after();
                 uint32_t r[32];
-                tmem_ld32(tmem + lane_off + kTmemS + b * kNHead + hh * 32, r);
+                tmem_ld16x256_x8(tmem + lane_off + kTmemS + b * TR, r);
                 tmem_wait_ld(r);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s_empty[b]);
+                // Row validity of this tile (written by the gather before x_full).
+                ok = __all_sync(0xffffffffu, mbar_wait(&x_full[b], (jt >> 1) & 1, abort_flag));
+                if (!ok) break;
+                // rows 8j + 2(t%4) + {0,1}: group 2j + (t%4)/2, bits 2(t%4 & 1) + {0,1}
+                const uint4 vw = *reinterpret_cast<const uint4 *>(sValid + b * kRowGroups);
+                const uint32_t vsh = 8 * (t4 >> 1) + 2 * (t4 & 1);
                 float x[32];
 #pragma unroll
-                for (int k = 0; k < 32; ++k) x[k] = valid ? __uint_as_float(r[k]) * sl2 : NEG_INF;
-                // per-head max over this warp's 16 rows, then over the 4 lane quarters
-#pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const float mx = warp_max(x[k]);
-                    if (lane == k) sSmax[q4 * kNHead + hh * 32 + k] = mx;
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t w = (j < 2 ? vw.x : j < 4 ? vw.y : j < 6 ? vw.z : vw.w) >> (16 * (j & 1) + vsh);
+                    const bool va = w & 1u, vb = (w >> 1) & 1u;
+                    x[4 * j] = va ? __uint_as_float(r[4 * j]) * sl2 : NEG_INF;
+                    x[4 * j + 1] = vb ? __uint_as_float(r[4 * j + 1]) * sl2 : NEG_INF;
+                    x[4 * j + 2] = va ? __uint_as_float(r[4 * j + 2]) * sl2 : NEG_INF;
+                    x[4 * j + 3] = vb ? __uint_as_float(r[4 * j + 3]) * sl2 : NEG_INF;
                 }
+                float mx0 = NEG_INF, mx1 = NEG_INF;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    mx0 = fmaxf(mx0, fmaxf(x[4 * j], x[4 * j + 1]));
+                    mx1 = fmaxf(mx1, fmaxf(x[4 * j + 2], x[4 * j + 3]));
+                }
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                // The running max is raised only when the tile exceeds it by more than 2^8.
+                float al0 = 1.f, al1 = 1.f;
+                if (M0 == NEG_INF) {
+                    M0 = mx0;                            // first finite max: O and sums are still 0
+                } else if (mx0 > M0 + kRescaleThreshold) {
+                    al0 = exp2f(M0 - mx0);
+                    M0 = mx0;
+                }
+                if (M1 == NEG_INF) {
+                    M1 = mx1;
+                } else if (mx1 > M1 + kRescaleThreshold) {
+                    al1 = exp2f(M1 - mx1);
+                    M1 = mx1;
+                }
+                // Any head raised in any warp: every warp rescales its O^T lanes.
+                const int tb = jt & 1;
+                const bool wresc = __any_sync(0xffffffffu, (al0 != 1.f) | (al1 != 1.f));
+                if (t4 == 0) {
+                    sAlpha[tb * kNHead + h0] = al0;
+                    sAlpha[tb * kNHead + h1] = al1;
+                }
+                if (lane == 0) sFlag[tb * kSoftmaxWarps + q4] = wresc ? 1u : 0u;
                 if (!(ok = group_sync())) break;
-                // Threads 0..63 combine the quarters for head e and update its
-                // running max (raised only when exceeded by more than 2^8).
-                if (e < kNHead) {
-                    const float mt = fmaxf(fmaxf(sSmax[e], sSmax[kNHead + e]),
-                                           fmaxf(sSmax[2 * kNHead + e], sSmax[3 * kNHead + e]));
-                    const float mo = sMused[e];
-                    float al = 1.f;
-                    if (mo == NEG_INF) {
-                        sMused[e] = mt;                 // first finite max (O and sums are still 0)
-                    } else if (mt > mo + kRescaleThreshold) {
-                        sMused[e] = mt;
-                        al = exp2f(mo - mt);
-                    }
-                    sAlpha[e] = al;
-                }
-                if (!(ok = group_sync())) break;
-                bool rescale = false;
-                uint32_t pk[16];
+                const uint4 fl = *reinterpret_cast<const uint4 *>(sFlag + tb * kSoftmaxWarps);
+                const bool any_resc = (fl.x | fl.y | fl.z | fl.w) != 0u;
+                const float mr0 = M0 == NEG_INF ? 0.f : M0, mr1 = M1 == NEG_INF ? 0.f : M1;
+                float s0 = 0.f, s1 = 0.f;
+                uint32_t pk0[8], pk1[8];
 #pragma unroll
-                for (int k = 0; k < 32; k += 2) {
-                    const float m0 = sMused[hh * 32 + k], m1 = sMused[hh * 32 + k + 1];
-                    const float a0 = sAlpha[hh * 32 + k], a1 = sAlpha[hh * 32 + k + 1];
-                    rescale |= (a0 != 1.f) | (a1 != 1.f);
-                    const float p0 = exp2f(x[k] - (m0 == NEG_INF ? 0.f : m0));
-                    const float p1 = exp2f(x[k + 1] - (m1 == NEG_INF ? 0.f : m1));
-                    lacc[k] = lacc[k] * a0 + p0;
-                    lacc[k + 1] = lacc[k + 1] * a1 + p1;
-                    pk[k >> 1] = raw ? pack2<true>(p0, p1) : pack2<false>(p0, p1);
+                for (int j = 0; j < 8; ++j) {
+                    const float pa = exp2f(x[4 * j] - mr0), pb = exp2f(x[4 * j + 1] - mr0);
+                    const float pc = exp2f(x[4 * j + 2] - mr1), pd = exp2f(x[4 * j + 3] - mr1);
+                    s0 += pa + pb;
+                    s1 += pc + pd;
+                    pk0[j] = raw ? pack2<true>(pa, pb) : pack2<false>(pa, pb);
+                    pk1[j] = raw ? pack2<true>(pc, pd) : pack2<false>(pc, pd);
                 }
-                // The previous values GEMM of this item must be complete before
-                // O^T may be rescaled (its buffer was also the one before last).
-                if (t > m.t0) {
-                    ok = __all_sync(0xffffffffu, mbar_wait(pv_done, pvph, abort_flag));
-                    if (!ok) break;
-                    pvph ^= 1;
-                }
-                if (lane < 16) {
-                    // P^T row `row`, heads 32*hh..: chunks 4*hh..4*hh+3 of the 128B-swizzled row.
-                    uint4 *prow = reinterpret_cast<uint4 *>(sP + b * kPBuf + row * 128);
+                l0 = l0 * al0 + s0;
+                l1 = l1 * al1 + s1;
+                // P[h][row]: rows 8j + 2(t%4) + {0,1} are bytes 16j + 4(t%4) of the
+                // 128-byte row of head h, 16-byte chunk j swizzled with h & 7.
+                uint8_t *pbuf = sP + b * kPBuf;
+                const int sw = h0 & 7;                   // == h1 & 7
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        prow[(4 * hh + c) ^ (row & 7)] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                for (int j = 0; j < 8; ++j) {
+                    *reinterpret_cast<uint32_t *>(pbuf + h0 * 128 + ((j ^ sw) << 4) + 4 * t4) = pk0[j];
+                    *reinterpret_cast<uint32_t *>(pbuf + h1 * 128 + ((j ^ sw) << 4) + 4 * t4) = pk1[j];
                 }
                 fence_proxy_async();
-                if (rescale && t > m.t0) {
+                if (any_resc && t > m.t0) {
+                    // O^T holds the sum up to the previous values GEMM (tile jt - 1): wait for it.
+                    ok = __all_sync(0xffffffffu, mbar_wait(&x_empty[(jt - 1) & 1], ((jt - 1) >> 1) & 1, abort_flag));
+                    if (!ok) break;
                     tc_fence_after();
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < 8; ++c) {
                         uint32_t v[32];
-                        const uint32_t ta = tmem + lane_off + kTmemO + c * kNHead + hh * 32;
+                        const uint32_t ta = tmem + lane_off + kTmemO + c * 32;
                         tmem_ld32(ta, v);
                         tmem_wait_ld(v);
+                        const float *al = sAlpha + tb * kNHead + (c & 1) * 32;
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * sAlpha[hh * 32 + k]);
+                        for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * al[k]);
                         tmem_st32(ta, v);
                     }
                     tmem_wait_st();
@@ -632,50 +656,45 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                 if (lane == 0) mbar_arrive(&p_full[b]);
             }
             if (!ok) break;
-            // ---- epilogue: row sums across the 64 rows, then O^T out
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                float v = lacc[k];
-                v += __shfl_xor_sync(0xffffffffu, v, 1);
-                v += __shfl_xor_sync(0xffffffffu, v, 2);
-                v += __shfl_xor_sync(0xffffffffu, v, 4);
-                v += __shfl_xor_sync(0xffffffffu, v, 8);
-                v += __shfl_xor_sync(0xffffffffu, v, 16);
-                if (lane == k) sSmax[q4 * kNHead + hh * 32 + k] = v;
-            }
-            if (!(ok = group_sync())) break;
+            // ---- epilogue: row sums over the four threads of a head, then O^T out
+            l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+            l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
             const long long slot = static_cast<long long>(m.unit) * n_split + m.split;
-            if (e < kNHead) {
-                const float L = sSmax[e] + sSmax[kNHead + e] + sSmax[2 * kNHead + e] + sSmax[3 * kNHead + e];
-                const float M = sMused[e];
-                if (n_split == 1) {
-                    sInvL[e] = L > 0.f ? 1.f / L : 0.f;
-                    if (a.lse)
-                        a.lse[static_cast<long long>(m.unit) * kNHead + e] =
-                            L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : NEG_INF;
-                } else {
-                    sInvL[e] = 1.f;
-                    float *ml = static_cast<float *>(a.ws) + static_cast<long long>(a.units) * n_split * kNHead * kHeadDim;
-                    ml[(slot * kNHead + e) * 2] = L > 0.f ? M : NEG_INF;
-                    ml[(slot * kNHead + e) * 2 + 1] = L;
+            if (t4 == 0) {
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int h = k ? h1 : h0;
+                    const float L = k ? l1 : l0, M = k ? M1 : M0;
+                    if (n_split == 1) {
+                        sInvL[h] = L > 0.f ? 1.f / L : 0.f;
+                        if (a.lse)
+                            a.lse[static_cast<long long>(m.unit) * kNHead + h] =
+                                L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : NEG_INF;
+                    } else {
+                        sInvL[h] = 1.f;
+                        float *ml = static_cast<float *>(a.ws) + static_cast<long long>(a.units) * n_split * kNHead * kHeadDim;
+                        ml[(slot * kNHead + h) * 2] = L > 0.f ? M : NEG_INF;
+                        ml[(slot * kNHead + h) * 2 + 1] = L;
+                    }
                 }
             }
             if (!(ok = group_sync())) break;
-            // the item's last values GEMM
-            ok = __all_sync(0xffffffffu, mbar_wait(pv_done, pvph, abort_flag));
+            // the item's last values GEMM (tile jt - 1)
+            ok = __all_sync(0xffffffffu, mbar_wait(&x_empty[(jt - 1) & 1], ((jt - 1) >> 1) & 1, abort_flag));
             if (!ok) break;
-            pvph ^= 1;
             tc_fence_after();
             float *obase = n_split == 1 ? a.out + static_cast<long long>(m.unit) * kNHead * kHeadDim
                                         : static_cast<float *>(a.ws) + slot * kNHead * kHeadDim;
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 8; ++c) {
                 uint32_t v[32];
-                tmem_ld32(tmem + lane_off + kTmemO + c * kNHead + hh * 32, v);
+                tmem_ld32(tmem + lane_off + kTmemO + c * 32, v);
                 tmem_wait_ld(v);
-                const int d = c * 128 + q4 * 32 + lane;
+                const int d = (c >> 1) * 128 + q4 * 32 + lane;
 #pragma unroll
                 for (int k = 0; k < 32; ++k) {
-                    const int h = hh * 32 + k;
+                    const int h = (c & 1) * 32 + k;
                     obase[static_cast<long long>(h) * kHeadDim + d] = __uint_as_float(v[k]) * sInvL[h];
                 }
             }
@@ -744,7 +763,7 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const __grid_constant__
 }  // namespace
 
 int attn_num_splits(int units, int top_k) {
-    // Enough work items to cover 152 SMs; a split holds at least one 128-row tile.
+    // Enough work items to cover 152 SMs; a split holds at least one 64-row tile.
     const int max_tiles = (top_k + TR - 1) / TR + (kNSwa + TR - 1) / TR;
     if (units >= 152) return 1;
     int s = (152 + units - 1) / units;
