@@ -478,6 +478,261 @@ __global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float *
     if (threadIdx.x == 0) count_out[row] = static_cast<int32_t>(ns);
 }
 
+
+// ---------------------------------------------------------------- one CTA per row
+// For batches with at least as many rows as SMs (decode batches, prefill
+// chunks): each CTA selects one row's top-k alone and reads the row's scores
+// once from HBM in the common case.
+//   1. A systematic sample of kSample scores (row positions i*n/kSample) sets
+//      a threshold key T0: the r-th largest visible sample key with
+//      r = 3k*kSample/n, resolved to 24 bits (two 4096-bin digits over the
+//      sample), so that about 3k rows of the row lie at or above it.
+//   2. One pass over the row counts the visible scores and appends every row
+//      with key >= T0 to a shared candidate list (warp-aggregated appends).
+//   3. If at least k candidates arrived and none was dropped, the exact k-th
+//      key T and the tie count come from three radix digits over the
+//      candidates; otherwise (a sample that missed, heavy ties) the same
+//      digits come from passes over the row itself, which the pass above left
+//      in L2.  Rows with at most k visible scores take all of them.
+//   4. Output: the chosen candidates sorted ascending (bitonic), -1 padded;
+//      the fallback compacts the row in order instead.
+constexpr int kRowThreads = 512;
+constexpr int kSample = 2048;
+constexpr int kSampleOver = 3;     // expected candidates / k
+constexpr int kRowCandCap = 8192;
+constexpr int kRowSmemBytes = kRowCandCap * 8 + kBins * 4 + kMaxTopK * 4;   // candidates, histogram, chosen
+
+__global__ void __launch_bounds__(kRowThreads, 2) topk_row_kernel(const float *__restrict__ scores,
+                                                                  const int32_t *__restrict__ n_rows, int Q,
+                                                                  int N_cap, int top_k,
+                                                                  int32_t *__restrict__ idx_out,
+                                                                  int32_t *__restrict__ count_out, uint32_t *status) {
+    extern __shared__ __align__(16) uint8_t row_smem[];
+    uint2 *cand = reinterpret_cast<uint2 *>(row_smem);                               // [kRowCandCap]
+    uint32_t *h = reinterpret_cast<uint32_t *>(row_smem + kRowCandCap * 8);           // [kBins]
+    int32_t *sel = reinterpret_cast<int32_t *>(row_smem + kRowCandCap * 8 + kBins * 4);   // [kMaxTopK]
+    __shared__ uint32_t scratch[kRowThreads + 4];
+    __shared__ uint32_t n_cand, n_sel;
+    __shared__ uint32_t warp_sums[32];
+    const long long row = blockIdx.x;
+    const int u = static_cast<int>(row / Q);
+    const int n = row_len(n_rows, u, N_cap);
+    if (threadIdx.x == 0 && row % Q == 0 && (n_rows[u] < 0 || n_rows[u] > N_cap)) report(status, DS4A_DEV_BOUNDS);
+    const float *s = scores + row * N_cap;
+    const uint32_t k = static_cast<uint32_t>(top_k);
+    int32_t *out = idx_out + row * top_k;
+    const int lane = threadIdx.x & 31;
+
+    auto clear_hist = [&]() {
+        for (int i = threadIdx.x; i < kBins; i += blockDim.x) h[i] = 0;
+        __syncthreads();
+    };
+    // ---- 1. threshold estimate
+    uint32_t T0 = 0;
+    if (n > kRowCandCap) {
+        uint32_t skey[kSample / kRowThreads];
+        bool svis[kSample / kRowThreads];
+        clear_hist();
+#pragma unroll
+        for (int j = 0; j < kSample / kRowThreads; ++j) {
+            const int i = static_cast<int>((static_cast<long long>(threadIdx.x + j * kRowThreads) * n) / kSample);
+            const float f = __ldg(s + i);
+            svis[j] = score_visible(f);
+            skey[j] = float_key(f);
+            if (svis[j]) atomicAdd(&h[skey[j] >> 20], 1u);
+        }
+        __syncthreads();
+        const long long r_want = (static_cast<long long>(kSampleOver) * k * kSample + n - 1) / n;
+        const uint32_t rank = static_cast<uint32_t>(r_want < kSample ? r_want : kSample);
+        uint32_t above, total;
+        const int sb1 = find_threshold_bin<kRowThreads>(h, kBins, rank, &above, &total, scratch);
+        if (sb1 >= 0) {
+            clear_hist();
+#pragma unroll
+            for (int j = 0; j < kSample / kRowThreads; ++j)
+                if (svis[j] && static_cast<int>(skey[j] >> 20) == sb1) atomicAdd(&h[(skey[j] >> 8) & 0xFFFu], 1u);
+            __syncthreads();
+            uint32_t above2, total2;
+            int sb2 = find_threshold_bin<kRowThreads>(h, kBins, rank - above, &above2, &total2, scratch);
+            if (sb2 < 0) sb2 = 0;
+            T0 = (static_cast<uint32_t>(sb1) << 20) | (static_cast<uint32_t>(sb2) << 8);
+        }
+    }
+    // ---- 2. one pass: visible count and candidates (key >= T0)
+    if (threadIdx.x == 0) n_cand = 0;
+    __syncthreads();
+    uint32_t my_vis = 0;
+    auto consider = [&](int i, float f, bool in_range) {
+        const bool vis = in_range && score_visible(f);
+        const uint32_t key = float_key(f);
+        my_vis += vis ? 1u : 0u;
+        const bool take = vis && key >= T0;
+        const uint32_t bal = __ballot_sync(0xffffffffu, take);
+        if (bal) {
+            uint32_t base = 0;
+            if (lane == 0) base = atomicAdd(&n_cand, static_cast<uint32_t>(__popc(bal)));
+            base = __shfl_sync(0xffffffffu, base, 0);
+            const uint32_t p = base + __popc(bal & ((1u << lane) - 1u));
+            if (take && p < static_cast<uint32_t>(kRowCandCap)) cand[p] = make_uint2(key, static_cast<uint32_t>(i));
+        }
+    };
+    if ((N_cap & 3) == 0) {
+        // Whole float4 groups; every thread runs the same number of iterations
+        // (the ballot above is warp-wide), out-of-range lanes pass in_range = false.
+        constexpr int B = 4;
+        const int ngroups = (n + 3) / 4;
+        for (int g0 = 0; g0 < ngroups; g0 += B * kRowThreads) {
+            float4 v[B];
+#pragma unroll
+            for (int j = 0; j < B; ++j) {
+                const int g = g0 + j * kRowThreads + static_cast<int>(threadIdx.x);
+                v[j] = g < ngroups ? __ldg(reinterpret_cast<const float4 *>(s) + g) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int j = 0; j < B; ++j) {
+                const int i = 4 * (g0 + j * kRowThreads + static_cast<int>(threadIdx.x));
+                consider(i, v[j].x, i < n);
+                consider(i + 1, v[j].y, i + 1 < n);
+                consider(i + 2, v[j].z, i + 2 < n);
+                consider(i + 3, v[j].w, i + 3 < n);
+            }
+        }
+    } else {
+        for (int b = 0; b < n; b += kRowThreads) {
+            const int i = b + static_cast<int>(threadIdx.x);
+            consider(i, i < n ? s[i] : 0.f, i < n);
+        }
+    }
+    uint32_t total;
+    {
+        // block sum of my_vis
+        uint32_t v = my_vis;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (lane == 0) warp_sums[threadIdx.x >> 5] = v;
+        __syncthreads();
+        total = 0;
+        for (int w = 0; w < kRowThreads / 32; ++w) total += warp_sums[w];
+        __syncthreads();
+    }
+    const uint32_t nc = n_cand;
+    const uint32_t m = total < k ? total : k;           // number selected
+
+    // ---- 3. the exact k-th key T and how many keys equal to T to take
+    uint32_t T = 0, need_eq = 0;
+    const bool all_visible = total <= k;
+    const bool from_cand = all_visible ? nc == total : (nc >= k && nc <= static_cast<uint32_t>(kRowCandCap));
+    if (!all_visible) {
+        // digit d: bits [lo, lo + w) of keys whose higher bits equal prefix
+        uint32_t need = k;
+        uint32_t prefix = 0;
+        const int shifts[3] = {20, 8, 0};
+        const uint32_t masks[3] = {0xFFFu, 0xFFFu, 0xFFu};
+        for (int d = 0; d < 3; ++d) {
+            clear_hist();
+            const int sh = shifts[d];
+            const int hs = d == 0 ? 32 : shifts[d - 1];        // bits above this digit: key >> hs == prefix
+            if (from_cand) {
+                for (uint32_t i = threadIdx.x; i < nc; i += blockDim.x) {
+                    const uint32_t key = cand[i].x;
+                    if (hs == 32 || (key >> hs) == prefix) atomicAdd(&h[(key >> sh) & masks[d]], 1u);
+                }
+            } else {
+                for (int i = threadIdx.x; i < n; i += blockDim.x) {
+                    const float f = s[i];
+                    if (!score_visible(f)) continue;
+                    const uint32_t key = float_key(f);
+                    if (hs == 32 || (key >> hs) == prefix) atomicAdd(&h[(key >> sh) & masks[d]], 1u);
+                }
+            }
+            __syncthreads();
+            uint32_t gt, tot;
+            int b = find_threshold_bin<kRowThreads>(h, kBins, need, &gt, &tot, scratch);
+            if (b < 0) { b = 0; gt = 0; }     // cannot happen: need <= count of keys with this prefix
+            prefix = (d == 0 ? 0u : prefix << (d == 1 ? 12 : 8)) | static_cast<uint32_t>(b);
+            need -= gt;
+        }
+        T = prefix;                                     // bits 31..20 | 19..8 | 7..0
+        need_eq = need;                                 // keys equal to T to take, lowest rows first
+    }
+    if (from_cand) {
+        // ---- 4a. the chosen candidates, sorted ascending
+        if (threadIdx.x == 0) n_sel = 0;
+        __syncthreads();
+        uint32_t n_eq = 0;
+        if (!all_visible) {
+            for (uint32_t i = threadIdx.x; i < nc; i += blockDim.x) n_eq += cand[i].x == T ? 1u : 0u;
+            uint32_t v = n_eq;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+            if (lane == 0) warp_sums[threadIdx.x >> 5] = v;
+            __syncthreads();
+            n_eq = 0;
+            for (int w = 0; w < kRowThreads / 32; ++w) n_eq += warp_sums[w];
+            __syncthreads();
+        }
+        for (uint32_t i = threadIdx.x; i < nc; i += blockDim.x) {
+            const uint2 c = cand[i];
+            bool take = all_visible || c.x > T;
+            if (!all_visible && c.x == T) {
+                if (n_eq == need_eq) {
+                    take = true;
+                } else {
+                    uint32_t lower = 0;
+                    for (uint32_t j = 0; j < nc; ++j) {
+                        const uint2 o = cand[j];
+                        lower += (o.x == T && static_cast<int>(o.y) < static_cast<int>(c.y)) ? 1u : 0u;
+                    }
+                    take = lower < need_eq;
+                }
+            }
+            if (take) {
+                const uint32_t p = atomicAdd(&n_sel, 1u);
+                if (p < k) sel[p] = static_cast<int32_t>(c.y);
+            }
+        }
+        __syncthreads();
+        const uint32_t ns = n_sel < k ? n_sel : k;
+        int p2 = 1;
+        while (p2 < static_cast<int>(ns)) p2 <<= 1;
+        for (int i = static_cast<int>(ns) + threadIdx.x; i < p2; i += blockDim.x) sel[i] = 0x7fffffff;
+        __syncthreads();
+        block_bitonic_sort_asc(sel, p2);
+        for (uint32_t i = threadIdx.x; i < k; i += blockDim.x) out[i] = i < ns ? sel[i] : -1;
+        if (threadIdx.x == 0) count_out[row] = static_cast<int32_t>(ns);
+        return;
+    }
+    // ---- 4b. order-preserving compaction over the row: ascending output
+    uint32_t written = 0, eq_seen = 0;
+    for (int base = 0; base < n; base += blockDim.x) {
+        const int i = base + static_cast<int>(threadIdx.x);
+        bool vis = false;
+        uint32_t key = 0;
+        if (i < n) {
+            const float f = s[i];
+            vis = score_visible(f);
+            key = float_key(f);
+        }
+        bool take;
+        if (all_visible) {
+            take = vis;
+        } else {
+            const bool is_eq = vis && key == T;
+            uint32_t eq_tot;
+            const uint32_t eq_rank = eq_seen + block_rank(is_eq, warp_sums, &eq_tot);
+            take = vis && (key > T || (is_eq && eq_rank < need_eq));
+            eq_seen += eq_tot;
+        }
+        uint32_t tk_tot;
+        const uint32_t pos = written + block_rank(take, warp_sums, &tk_tot);
+        if (take && pos < k) out[pos] = i;
+        written += tk_tot;
+        if (written >= m) break;                        // block-uniform
+    }
+    for (uint32_t i = m + threadIdx.x; i < k; i += blockDim.x) out[i] = -1;
+    if (threadIdx.x == 0) count_out[row] = static_cast<int32_t>(m);
+}
+
 }  // namespace
 
 size_t topk_ws_bytes(long long R, int top_k) {
@@ -489,6 +744,15 @@ size_t topk_ws_bytes(long long R, int top_k) {
 
 cudaError_t launch_topk(const TopkArgs &a, int num_sms, cudaStream_t s) {
     const long long R = static_cast<long long>(a.U) * a.Q;
+    if (R >= num_sms) {
+        // Enough rows to fill the GPU: one CTA per row, no workspace.
+        if (R > 0x7fffffffLL) return cudaErrorInvalidValue;
+        cudaError_t e = cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowSmemBytes);
+        if (e != cudaSuccess) return e;
+        topk_row_kernel<<<static_cast<unsigned>(R), kRowThreads, kRowSmemBytes, s>>>(a.scores, a.n_rows, a.Q, a.N_cap, a.top_k,
+                                                                          a.idx, a.count, a.status);
+        return cudaGetLastError();
+    }
     TopkWs ws = topk_ws(a.ws, R, a.top_k);
     // Zero the histograms and counters (contiguous at the front).
     cudaError_t e = cudaMemsetAsync(a.ws, 0, static_cast<size_t>(R) * (kBins * 4 + 16), s);

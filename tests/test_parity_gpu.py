@@ -170,6 +170,55 @@ def test_topk_one_long_row_split_over_many_ctas():
     topk_case(x, [262144], 512)
 
 
+# Batches with at least as many rows as SMs take the one-CTA-per-row kernel
+# (sampled threshold, candidate list, exact fallback over the row).
+
+ROWS_MANY = 160      # > 152 SMs
+
+
+def _many(rng, n_cap, lens):
+    return [lens[i % len(lens)] for i in range(ROWS_MANY)]
+
+
+def test_topk_rows_random_and_ragged():
+    rng = np.random.default_rng(10)
+    x = rng.standard_normal((ROWS_MANY, 20000)).astype(np.float32)
+    x[::7] *= 1e-3                                   # narrow value range on some rows
+    x[3::7][:, rng.random(20000) < 0.05] *= 4        # heavy tail on others
+    topk_case(x, _many(rng, 20000, [20000, 19999, 4097, 4096, 3000, 513, 512, 77, 1, 0]), 512)
+
+
+def test_topk_rows_ties_neginf_nan_signed_zero():
+    rng = np.random.default_rng(11)
+    x = (np.round(rng.standard_normal((ROWS_MANY, 12000)) * 2) / 2).astype(np.float32)   # heavy ties
+    x[0::4][:, rng.random(12000) < 0.3] = -np.inf
+    x[1::4][:, rng.random(12000) < 0.1] = np.nan
+    x[2::4] = 0.0
+    x[2::4, ::2] = -0.0
+    x[2::4, 5:20] = 1.0
+    x[3::4] = -np.abs(x[3::4])
+    topk_case(x, _many(rng, 12000, [12000, 11999, 6000]), 100)
+
+
+def test_topk_rows_all_equal_sorted_and_prefix_visible():
+    rng = np.random.default_rng(12)
+    x = np.empty((ROWS_MANY, 16384), np.float32)
+    x[0::4] = 0.25                                              # all equal: candidate overflow
+    x[1::4] = np.arange(16384, dtype=np.float32)                # ascending by row
+    x[2::4] = -np.arange(16384, dtype=np.float32)               # descending by row
+    x[3::4] = rng.standard_normal((ROWS_MANY // 4, 16384)).astype(np.float32)
+    for r in range(3, ROWS_MANY, 4):                            # visible prefix, -inf after (causal)
+        x[r, rng.integers(100, 16384):] = -np.inf
+    topk_case(x, _many(rng, 16384, [16384, 16383, 9000]), 512)
+
+
+@pytest.mark.parametrize("k", [1, 2048])
+def test_topk_rows_k_extremes_and_odd_stride(k):
+    rng = np.random.default_rng(13 + k)
+    x = rng.standard_normal((ROWS_MANY, 5001)).astype(np.float32)     # N_cap not a multiple of 4
+    topk_case(x, _many(rng, 5001, [5001, 5000, 2048, 2047, 10]), k)
+
+
 # ----------------------------------------------------------------------------
 # A4 attention on given row sets
 # ----------------------------------------------------------------------------
