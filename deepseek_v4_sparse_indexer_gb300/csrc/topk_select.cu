@@ -494,8 +494,19 @@ __global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float *
 //      candidates; otherwise (a sample that missed, heavy ties) the same
 //      digits come from passes over the row itself, which the pass above left
 //      in L2.  Rows with at most k visible scores take all of them.
-//   4. Output: the chosen candidates sorted ascending (bitonic), -1 padded;
-//      the fallback compacts the row in order instead.
+//   4. Output: the chosen candidates in ascending row order (a bitmap of the
+//      row and a prefix sum of its popcounts; a bitonic sort for rows longer
+//      than 131,072), -1 padded; the fallback compacts the row in order.
+// Adds 1 to h[bin] for every lane with pred, one shared atomic per distinct
+// bin in the warp (scores of one row often share a few bins).  All 32 lanes
+// must call it.
+DS4A_DEV void hist_add_warp(uint32_t *h, uint32_t bin, bool pred) {
+    const uint32_t active = __ballot_sync(0xffffffffu, pred);
+    if (!pred) return;
+    const uint32_t peers = __match_any_sync(active, bin);
+    if (static_cast<int>(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&h[bin], static_cast<uint32_t>(__popc(peers)));
+}
+
 constexpr int kRowThreads = 512;
 constexpr int kSample = 2048;
 constexpr int kSampleOver = 3;     // expected candidates / k
@@ -539,7 +550,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) topk_row_kernel(const float *_
             const float f = __ldg(s + i);
             svis[j] = score_visible(f);
             skey[j] = float_key(f);
-            if (svis[j]) atomicAdd(&h[skey[j] >> 20], 1u);
+            hist_add_warp(h, skey[j] >> 20, svis[j]);
         }
         __syncthreads();
         const long long r_want = (static_cast<long long>(kSampleOver) * k * kSample + n - 1) / n;
@@ -550,7 +561,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) topk_row_kernel(const float *_
             clear_hist();
 #pragma unroll
             for (int j = 0; j < kSample / kRowThreads; ++j)
-                if (svis[j] && static_cast<int>(skey[j] >> 20) == sb1) atomicAdd(&h[(skey[j] >> 8) & 0xFFFu], 1u);
+                hist_add_warp(h, (skey[j] >> 8) & 0xFFFu, svis[j] && static_cast<int>(skey[j] >> 20) == sb1);
             __syncthreads();
             uint32_t above2, total2;
             int sb2 = find_threshold_bin<kRowThreads>(h, kBins, rank - above, &above2, &total2, scratch);
@@ -562,11 +573,8 @@ __global__ void __launch_bounds__(kRowThreads, 2) topk_row_kernel(const float *_
     if (threadIdx.x == 0) n_cand = 0;
     __syncthreads();
     uint32_t my_vis = 0;
-    auto consider = [&](int i, float f, bool in_range) {
-        const bool vis = in_range && score_visible(f);
-        const uint32_t key = float_key(f);
-        my_vis += vis ? 1u : 0u;
-        const bool take = vis && key >= T0;
+    // Appends the lanes' rows with key >= T0 (warp-aggregated); all lanes call it.
+    auto append = [&](int i, uint32_t key, bool take) {
         const uint32_t bal = __ballot_sync(0xffffffffu, take);
         if (bal) {
             uint32_t base = 0;
@@ -577,30 +585,67 @@ __global__ void __launch_bounds__(kRowThreads, 2) topk_row_kernel(const float *_
         }
     };
     if ((N_cap & 3) == 0) {
-        // Whole float4 groups; every thread runs the same number of iterations
-        // (the ballot above is warp-wide), out-of-range lanes pass in_range = false.
+        // Whole float4 groups, B per thread in flight plus the next B prefetched;
+        // every thread runs the same iterations (the ballots are warp-wide).
         constexpr int B = 4;
         const int ngroups = (n + 3) / 4;
-        for (int g0 = 0; g0 < ngroups; g0 += B * kRowThreads) {
-            float4 v[B];
+        auto load = [&](float4 (&v)[B], int g0) {
 #pragma unroll
             for (int j = 0; j < B; ++j) {
                 const int g = g0 + j * kRowThreads + static_cast<int>(threadIdx.x);
                 v[j] = g < ngroups ? __ldg(reinterpret_cast<const float4 *>(s) + g) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
+        };
+        float4 cur[B], nxt[B];
+        load(cur, 0);
+        for (int g0 = 0; g0 < ngroups; g0 += B * kRowThreads) {
+            if (g0 + B * kRowThreads < ngroups) load(nxt, g0 + B * kRowThreads);
 #pragma unroll
             for (int j = 0; j < B; ++j) {
                 const int i = 4 * (g0 + j * kRowThreads + static_cast<int>(threadIdx.x));
-                consider(i, v[j].x, i < n);
-                consider(i + 1, v[j].y, i + 1 < n);
-                consider(i + 2, v[j].z, i + 2 < n);
-                consider(i + 3, v[j].w, i + 3 < n);
+                const float f[4] = {cur[j].x, cur[j].y, cur[j].z, cur[j].w};
+                uint32_t key[4];
+                bool take[4];
+                bool any = false;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const bool vis = i + c < n && score_visible(f[c]);
+                    key[c] = float_key(f[c]);
+                    my_vis += vis ? 1u : 0u;
+                    take[c] = vis && key[c] >= T0;
+                    any |= take[c];
+                }
+                if (__any_sync(0xffffffffu, any)) {
+                    // one shared atomic per warp and float4
+                    uint32_t bal[4], tot = 0;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        bal[c] = __ballot_sync(0xffffffffu, take[c]);
+                        tot += __popc(bal[c]);
+                    }
+                    uint32_t pos = 0;
+                    if (lane == 0) pos = atomicAdd(&n_cand, tot);
+                    pos = __shfl_sync(0xffffffffu, pos, 0);
+                    const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t p = pos + __popc(bal[c] & lt);
+                        if (take[c] && p < static_cast<uint32_t>(kRowCandCap)) cand[p] = make_uint2(key[c], static_cast<uint32_t>(i + c));
+                        pos += __popc(bal[c]);
+                    }
+                }
             }
+#pragma unroll
+            for (int j = 0; j < B; ++j) cur[j] = nxt[j];
         }
     } else {
         for (int b = 0; b < n; b += kRowThreads) {
             const int i = b + static_cast<int>(threadIdx.x);
-            consider(i, i < n ? s[i] : 0.f, i < n);
+            const float f = i < n ? s[i] : 0.f;
+            const bool vis = i < n && score_visible(f);
+            const uint32_t key = float_key(f);
+            my_vis += vis ? 1u : 0u;
+            append(i, key, vis && key >= T0);
         }
     }
     uint32_t total;
@@ -633,9 +678,10 @@ __global__ void __launch_bounds__(kRowThreads, 2) topk_row_kernel(const float *_
             const int sh = shifts[d];
             const int hs = d == 0 ? 32 : shifts[d - 1];        // bits above this digit: key >> hs == prefix
             if (from_cand) {
-                for (uint32_t i = threadIdx.x; i < nc; i += blockDim.x) {
-                    const uint32_t key = cand[i].x;
-                    if (hs == 32 || (key >> hs) == prefix) atomicAdd(&h[(key >> sh) & masks[d]], 1u);
+                for (uint32_t i0 = 0; i0 < nc; i0 += blockDim.x) {   // block-uniform trip count
+                    const uint32_t i = i0 + threadIdx.x;
+                    const uint32_t key = i < nc ? cand[i].x : 0u;
+                    hist_add_warp(h, (key >> sh) & masks[d], i < nc && (hs == 32 || (key >> hs) == prefix));
                 }
             } else {
                 for (int i = threadIdx.x; i < n; i += blockDim.x) {
@@ -656,9 +702,11 @@ __global__ void __launch_bounds__(kRowThreads, 2) topk_row_kernel(const float *_
         need_eq = need;                                 // keys equal to T to take, lowest rows first
     }
     if (from_cand) {
-        // ---- 4a. the chosen candidates, sorted ascending
+        // ---- 4a. the chosen candidates in ascending row order: a bitmap of
+        // the row (in the histogram's space) and a block prefix sum of its
+        // popcounts; rows longer than the bitmap take a bitonic sort instead.
+        const bool use_bitmap = n <= kBins * 32;
         if (threadIdx.x == 0) n_sel = 0;
-        __syncthreads();
         uint32_t n_eq = 0;
         if (!all_visible) {
             for (uint32_t i = threadIdx.x; i < nc; i += blockDim.x) n_eq += cand[i].x == T ? 1u : 0u;
@@ -669,29 +717,82 @@ __global__ void __launch_bounds__(kRowThreads, 2) topk_row_kernel(const float *_
             __syncthreads();
             n_eq = 0;
             for (int w = 0; w < kRowThreads / 32; ++w) n_eq += warp_sums[w];
-            __syncthreads();
         }
-        for (uint32_t i = threadIdx.x; i < nc; i += blockDim.x) {
-            const uint2 c = cand[i];
-            bool take = all_visible || c.x > T;
-            if (!all_visible && c.x == T) {
-                if (n_eq == need_eq) {
-                    take = true;
-                } else {
-                    uint32_t lower = 0;
-                    for (uint32_t j = 0; j < nc; ++j) {
-                        const uint2 o = cand[j];
-                        lower += (o.x == T && static_cast<int>(o.y) < static_cast<int>(c.y)) ? 1u : 0u;
+        if (use_bitmap)
+            for (int i = threadIdx.x; i < kBins; i += blockDim.x) h[i] = 0;
+        __syncthreads();
+        for (uint32_t i0 = 0; i0 < nc; i0 += blockDim.x) {            // block-uniform trip count
+            const uint32_t i = i0 + threadIdx.x;
+            bool take = false;
+            uint2 c = make_uint2(0u, 0u);
+            if (i < nc) {
+                c = cand[i];
+                take = all_visible || c.x > T;
+                if (!all_visible && c.x == T) {
+                    if (n_eq == need_eq) {
+                        take = true;
+                    } else {
+                        uint32_t lower = 0;
+                        for (uint32_t j = 0; j < nc; ++j) {
+                            const uint2 o = cand[j];
+                            lower += (o.x == T && static_cast<int>(o.y) < static_cast<int>(c.y)) ? 1u : 0u;
+                        }
+                        take = lower < need_eq;
                     }
-                    take = lower < need_eq;
                 }
             }
-            if (take) {
-                const uint32_t p = atomicAdd(&n_sel, 1u);
-                if (p < k) sel[p] = static_cast<int32_t>(c.y);
+            if (use_bitmap) {
+                if (take) atomicOr(&h[c.y >> 5], 1u << (c.y & 31));
+            } else {
+                const uint32_t bal = __ballot_sync(0xffffffffu, take);
+                uint32_t base = 0;
+                if (lane == 0 && bal) base = atomicAdd(&n_sel, static_cast<uint32_t>(__popc(bal)));
+                base = __shfl_sync(0xffffffffu, base, 0);
+                const uint32_t p = base + __popc(bal & ((1u << lane) - 1u));
+                if (take && p < k) sel[p] = static_cast<int32_t>(c.y);
             }
         }
         __syncthreads();
+        if (use_bitmap) {
+            // thread t owns words 8t..8t+7 (rows 256t..256t+255)
+            constexpr int kWords = kBins / kRowThreads;
+            uint32_t wv[kWords], cnt = 0;
+#pragma unroll
+            for (int j = 0; j < kWords; ++j) {
+                wv[j] = h[threadIdx.x * kWords + j];
+                cnt += __popc(wv[j]);
+            }
+            // block exclusive prefix sum of cnt
+            uint32_t incl = cnt;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const uint32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += v;
+            }
+            if (lane == 31) warp_sums[threadIdx.x >> 5] = incl;
+            __syncthreads();
+            uint32_t before = 0, ns = 0;
+            for (int w = 0; w < kRowThreads / 32; ++w) {
+                const uint32_t v = warp_sums[w];
+                if (w < static_cast<int>(threadIdx.x >> 5)) before += v;
+                ns += v;
+            }
+            uint32_t pos = before + incl - cnt;
+#pragma unroll
+            for (int j = 0; j < kWords; ++j) {
+                uint32_t bits = wv[j];
+                while (bits) {
+                    const int b = __ffs(bits) - 1;
+                    bits &= bits - 1;
+                    if (pos < k) out[pos] = static_cast<int32_t>((threadIdx.x * kWords + j) * 32 + b);
+                    ++pos;
+                }
+            }
+            ns = ns < k ? ns : k;
+            for (uint32_t i = ns + threadIdx.x; i < k; i += blockDim.x) out[i] = -1;
+            if (threadIdx.x == 0) count_out[row] = static_cast<int32_t>(ns);
+            return;
+        }
         const uint32_t ns = n_sel < k ? n_sel : k;
         int p2 = 1;
         while (p2 < static_cast<int>(ns)) p2 <<= 1;
@@ -733,6 +834,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) topk_row_kernel(const float *_
     if (threadIdx.x == 0) count_out[row] = static_cast<int32_t>(m);
 }
 
+
 }  // namespace
 
 size_t topk_ws_bytes(long long R, int top_k) {
@@ -749,8 +851,8 @@ cudaError_t launch_topk(const TopkArgs &a, int num_sms, cudaStream_t s) {
         if (R > 0x7fffffffLL) return cudaErrorInvalidValue;
         cudaError_t e = cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowSmemBytes);
         if (e != cudaSuccess) return e;
-        topk_row_kernel<<<static_cast<unsigned>(R), kRowThreads, kRowSmemBytes, s>>>(a.scores, a.n_rows, a.Q, a.N_cap, a.top_k,
-                                                                          a.idx, a.count, a.status);
+        topk_row_kernel<<<static_cast<unsigned>(R), kRowThreads, kRowSmemBytes, s>>>(a.scores, a.n_rows, a.Q, a.N_cap,
+                                                                                     a.top_k, a.idx, a.count, a.status);
         return cudaGetLastError();
     }
     TopkWs ws = topk_ws(a.ws, R, a.top_k);
