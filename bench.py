@@ -139,6 +139,12 @@ def decode_bytes(wl):
     return wl.units * (ik + per_unit_fixed), wl.units * idx_kernel
 
 
+def dense_bytes(wl):
+    """Algorithmic HBM bytes per unit of a ratio-128 layer: every compressed row,
+    the raw window, q, the fp32 output and lse."""
+    return wl.units * (wl.n_rows * 1024 + 128 * 1024 + 64 * 512 * 2 + 64 * 512 * 4 + 64 * 4)
+
+
 def prefill_flops(x, wl):
     import torch
     q_pos = x["q_pos"].cpu().to(torch.int64)
@@ -176,14 +182,18 @@ class OracleSample:
         def u16(t):
             return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
-        if wl.kind == "decode":
+        if wl.kind in ("decode", "dense"):
+            dense = wl.kind == "dense"
+
             def get_unit(i):
                 if unit_source is not None:
                     return unit_source(i)
                 x = make_decode_inputs(1, wl.n_rows, device="cpu", seed=wl.seed + 1000 + i,
-                                       heavy_frac=wl.heavy_frac, heavy_scale=wl.heavy_scale)
-                return dict(q=u16(x["q"][0]), iq=u16(x["iq"][0]), w=x["w"][0].numpy(), ik=u16(x["ik"][0]),
-                            rows=u16(x["rows"][0]), raw=u16(x["raw"][0]), n=wl.n_rows, nraw=128)
+                                       heavy_frac=wl.heavy_frac, heavy_scale=wl.heavy_scale, with_indexer=not dense)
+                d = dict(q=u16(x["q"][0]), rows=u16(x["rows"][0]), raw=u16(x["raw"][0]), n=wl.n_rows, nraw=128)
+                if not dense:
+                    d.update(iq=u16(x["iq"][0]), w=x["w"][0].numpy(), ik=u16(x["ik"][0]))
+                return d
 
             first = get_unit(0)
             t = time.perf_counter()
@@ -194,8 +204,10 @@ class OracleSample:
             # through them (the oracle's work per unit does not depend on values).
             pool = [first] + [get_unit(i) for i in range(1, min(n, max_distinct))]
             self.items = [pool[i % len(pool)] for i in range(n)]
-            self.text = f"{n} of {wl.query_units} units (each whole: {wl.n_rows} rows scored, top-{wl.top_k}, " \
-                        f"attention over the selected rows + 128-row window)"
+            self.text = (f"{n} of {wl.query_units} units (each whole: attention over all {wl.n_rows} rows + "
+                         f"128-row window)") if dense else \
+                (f"{n} of {wl.query_units} units (each whole: {wl.n_rows} rows scored, top-{wl.top_k}, "
+                 f"attention over the selected rows + 128-row window)")
         else:
             x = make_prefill_inputs(wl.queries, wl.extra["prior_rows"], device="cpu", seed=wl.seed)
             self.np_in = (u16(x["q"]), u16(x["iq"]), x["w"].numpy(), u16(x["ik"]), u16(x["rows"]),
@@ -218,6 +230,9 @@ class OracleSample:
         if wl.kind == "decode":
             d = item
             o.decode_unit(d["q"], d["iq"], d["w"], d["ik"], d["rows"], d["n"], d["raw"], d["nraw"], wl.top_k, SCALE)
+        elif wl.kind == "dense":
+            d = item
+            o.dense_attention(d["q"], d["rows"], d["n"], d["raw"], d["nraw"], SCALE)
         else:
             q, iq, w, ik, rows, row_pos, q_pos, raw = self.np_in
             o.prefill_query(item, q, iq, w, ik, rows, self.nr, row_pos, q_pos, raw, self.raw_pos0, wl.top_k, SCALE)
@@ -279,7 +294,7 @@ def main():
         raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(WORKLOADS)}")
     wl = WORKLOADS[args.workload]
     import dataclasses
-    if args.units is not None and wl.kind == "decode":
+    if args.units is not None and wl.kind in ("decode", "dense"):
         wl = dataclasses.replace(wl, name=f"{wl.name}[units={args.units}]", units=args.units)
     if args.prior_rows is not None and wl.kind == "prefill":
         wl = dataclasses.replace(wl, name=f"{wl.name}[prior_rows={args.prior_rows}]",
@@ -314,6 +329,9 @@ def main():
         x = make_decode_inputs(wl.units, wl.n_rows, device=dev, seed=seed, heavy_frac=wl.heavy_frac,
                                heavy_scale=wl.heavy_scale)
         step = pkg.DecodeStep(wl.units, wl.n_rows, wl.top_k, device=dev)
+    elif wl.kind == "dense":
+        x = make_decode_inputs(wl.units, wl.n_rows, device=dev, seed=seed, with_indexer=False)
+        step = pkg.DenseStep(wl.units, wl.n_rows, device=dev)
     else:
         x = make_prefill_inputs(wl.queries, wl.extra["prior_rows"], device=dev, seed=seed)
         step = pkg.PrefillStep(wl.queries, x["ik"].shape[0], wl.top_k, device=dev)
@@ -339,6 +357,10 @@ def main():
     t0.record()
     for i in range(K):
         sc_s[i].record()
+        if wl.kind == "dense":                 # one op: the attention is the dominant kernel
+            step.attend(x, SCALE)
+            sc_e[i].record()
+            continue
         step.score(x)
         sc_e[i].record()
         step.select(x)
@@ -357,7 +379,7 @@ def main():
     value = world * units / (ms / 1e3)
 
     # ---------------- end to end through the public API with host buffers
-    host_in = {k: x[k].cpu().pin_memory() for k in ("q", "iq", "w")}
+    host_in = {k: x[k].cpu().pin_memory() for k in (("q",) if wl.kind == "dense" else ("q", "iq", "w"))}
     host_out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
     host_lse = torch.empty(step.lse.shape, dtype=step.lse.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
@@ -384,15 +406,30 @@ def main():
     if st != 0:
         raise SystemExit(f"device status flags {flags} after the timed region")
 
-    # ---------------- roofline of the dominant kernel (indexer score)
-    launches_per_step = 1 + 3 + 1 + (1 if pkg.ds4a_workspace_bytes(
-        2 if wl.kind == "decode" else 3, wl.units if wl.kind == "decode" else 1,
-        1 if wl.kind == "decode" else wl.queries, wl.n_rows, wl.top_k) else 0)
+    # ---------------- roofline of the dominant kernel (indexer score; the attention for dense)
+    if wl.kind == "dense":
+        launches_per_step = 1 + (1 if pkg.ds4a_workspace_bytes(4, wl.units, 1, wl.n_rows, 0) else 0)
+    else:
+        launches_per_step = 1 + 1 + 1 + (1 if pkg.ds4a_workspace_bytes(
+            2 if wl.kind == "decode" else 3, wl.units if wl.kind == "decode" else 1,
+            1 if wl.kind == "decode" else wl.queries, wl.n_rows, wl.top_k) else 0)
+        if wl.units * wl.queries < 152:
+            launches_per_step += 2            # top-k: histogram and filter passes before the final one
     cfg = {"workload": wl.name, "units": wl.units, "queries_per_unit": wl.queries, "rows_per_unit": wl.n_rows,
-           "top_k": wl.top_k, "raw_window": 128, "heads": 64, "head_dim": 512, "indexer": "64x128",
+           "top_k": wl.top_k if wl.kind != "dense" else "all rows", "raw_window": 128, "heads": 64,
+           "head_dim": 512, "indexer": "64x128" if wl.kind != "dense" else "none (ratio-128 layer)",
            "l2": "inputs exceed the L2 many times over; no flush", "parallelism": f"replicas x{world}",
            "peak_source": pk["src"]}
-    if wl.kind == "decode":
+    if wl.kind == "dense":
+        step_bytes = dense_bytes(wl)
+        achieved = step_bytes / (idx_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
+                "frac": achieved / pk["hbm"], "traffic": None, "kernel": "sparse_attn_kernel",
+                "algorithmic_bytes_per_launch": step_bytes, "launch_ms": idx_ms}
+        cfg["step_algorithmic_bytes"] = step_bytes
+        cfg["step_hbm_GBps"] = step_bytes / (ms / 1e3) / 1e9
+        cfg["step_hbm_frac"] = cfg["step_hbm_GBps"] / pk["hbm"]
+    elif wl.kind == "decode":
         step_bytes, idx_bytes = decode_bytes(wl)
         achieved = idx_bytes / (idx_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
@@ -416,9 +453,11 @@ def main():
             "data": "synthetic: seeded N(0,1)/sqrt(d) bf16 rows/keys/queries, fp16 raw window, U(0,1) weights",
             "config": cfg, "roofline": roof,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_ms, "note": "per step: H2D of the queries (q, iq, w) from pinned memory, "
-                                                  "the three C-ABI ops, D2H of out and lse; the KV caches stay "
-                                                  "resident in HBM"},
+                    "ms_per_step": e2e_ms,
+                    "note": ("per step: H2D of q from pinned memory, the dense attention C-ABI op, D2H of out and "
+                             "lse; the KV caches stay resident in HBM") if wl.kind == "dense" else
+                            ("per step: H2D of the queries (q, iq, w) from pinned memory, the three C-ABI ops, D2H "
+                             "of out and lse; the KV caches stay resident in HBM")},
             "gpu_launches": launches_per_step * K, "clocks": clocks}
 
     # ---------------- CPU baseline: the oracle on the host cores (rank 0, N = 1)
@@ -435,6 +474,10 @@ def main():
                 u = (i * 7919) % wl.units
                 return dict(q=u16(x["q"][u]), iq=u16(x["iq"][u]), w=x["w"][u].cpu().numpy(), ik=u16(x["ik"][u]),
                             rows=u16(x["rows"][u]), raw=u16(x["raw"][u]), n=wl.n_rows, nraw=128)
+        elif wl.kind == "dense":
+            def unit_source(i):
+                u = (i * 7919) % wl.units
+                return dict(q=u16(x["q"][u]), rows=u16(x["rows"][u]), raw=u16(x["raw"][u]), n=wl.n_rows, nraw=128)
         sample = OracleSample(wl, args.cpu_seconds, unit_source)
         v = sample.rate(cores)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",

@@ -3,13 +3,15 @@ engine (DwarfStar, ds4): indexer score -> top-k select -> sparse attention,
 hand-written CUDA behind the C ABI of include/ds4a.h.
 
 The Python surface is the ctypes binding (same names as the C entry points)
-and DecodeStep / PrefillStep, which chain the three ops on one stream.
+and DecodeStep / PrefillStep, which chain the three ops on one stream, plus
+DenseStep for the ratio-128 layers (attention over all rows, no indexer).
 """
 from ._binding import (Ds4aError, load, ds4a_version, ds4a_workspace_bytes, ds4a_get_device_status,
                        ds4a_debug_inject_error, ds4a_indexer_score, ds4a_topk_select,
-                       ds4a_sparse_attn_decode, ds4a_sparse_attn_prefill)
-from .step import DecodeStep, PrefillStep, DEFAULT_SCALE
+                       ds4a_sparse_attn_decode, ds4a_sparse_attn_prefill, ds4a_dense_attn_decode)
+from .step import DecodeStep, PrefillStep, DenseStep, DEFAULT_SCALE
 
 __all__ = ["Ds4aError", "load", "ds4a_version", "ds4a_workspace_bytes", "ds4a_get_device_status",
            "ds4a_debug_inject_error", "ds4a_indexer_score", "ds4a_topk_select", "ds4a_sparse_attn_decode",
-           "ds4a_sparse_attn_prefill", "DecodeStep", "PrefillStep", "DEFAULT_SCALE"]
+           "ds4a_sparse_attn_prefill", "ds4a_dense_attn_decode", "DecodeStep", "PrefillStep", "DenseStep",
+           "DEFAULT_SCALE"]

@@ -26,13 +26,15 @@ DS4A_OP_INDEXER_SCORE = 0
 DS4A_OP_TOPK_SELECT = 1
 DS4A_OP_SPARSE_ATTN_DECODE = 2
 DS4A_OP_SPARSE_ATTN_PREFILL = 3
+DS4A_OP_DENSE_ATTN_DECODE = 4
 
 N_HEAD, HEAD_DIM, N_IDX_HEAD, IDX_DIM, N_SWA = 64, 512, 64, 128, 128
 
 # The C entry points this binding (and include/ds4a.h) exposes.
 EXPORTS = ("ds4a_strerror", "ds4a_version", "ds4a_workspace_bytes", "ds4a_get_device_status",
            "ds4a_debug_inject_error", "ds4a_indexer_score", "ds4a_topk_select",
-           "ds4a_topk_select_noalloc", "ds4a_sparse_attn_decode", "ds4a_sparse_attn_prefill")
+           "ds4a_topk_select_noalloc", "ds4a_sparse_attn_decode", "ds4a_sparse_attn_prefill",
+           "ds4a_dense_attn_decode")
 DS4A_TOPK_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -78,6 +80,9 @@ def load(build_if_missing: bool = True):
     L.ds4a_topk_select_noalloc.restype = _i32
     L.ds4a_sparse_attn_decode.argtypes = [_vp, _vp, _i64, _i32, _vp, _vp, _i32, _vp, _i64, _vp, _f32, _vp, _vp,
                                           _i32, _vp, _sz, _vp]
+    L.ds4a_dense_attn_decode.argtypes = [_vp, _vp, _i64, _i32, _vp, _vp, _i64, _vp, _f32, _vp, _vp, _i32, _vp, _sz,
+                                         _vp]
+    L.ds4a_dense_attn_decode.restype = _i32
     L.ds4a_sparse_attn_decode.restype = _i32
     L.ds4a_sparse_attn_prefill.argtypes = [_vp, _vp, _vp, _i32, _vp, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _vp,
                                            _i32, _vp, _sz, _vp]
@@ -229,6 +234,32 @@ def ds4a_sparse_attn_decode(q, rows, idx, count, raw, n_raw, scale, out, lse=Non
                                         _ptr(out), _ptr(lse), U, _ptr(ws),
                                         ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream))
     _check(st, "ds4a_sparse_attn_decode")
+
+
+def ds4a_dense_attn_decode(q, rows, n_rows, raw, n_raw, scale, out, lse=None, ws=None, stream=None):
+    """q bf16 [U,64,512]; rows bf16 [U,N_cap,512]; n_rows i32 [U]; raw fp16
+    [U,128,512]; n_raw i32 [U]; out f32 [U,64,512]; lse f32 [U,64] or None;
+    ws uint8 workspace or None."""
+    _req(q, "q", torch.bfloat16)
+    _req(n_rows, "n_rows", torch.int32)
+    _req(n_raw, "n_raw", torch.int32)
+    _req(out, "out", torch.float32)
+    if rows.dtype != torch.bfloat16 or not rows.is_cuda or rows.dim() != 3 or rows.stride(2) != 1 \
+            or rows.stride(1) != HEAD_DIM:
+        raise ValueError("rows: bf16 CUDA tensor [U, N_cap, 512] with contiguous rows")
+    if raw.dtype != torch.float16 or not raw.is_cuda or raw.dim() != 3 or raw.stride(2) != 1 \
+            or raw.stride(1) != HEAD_DIM or raw.shape[1] != N_SWA:
+        raise ValueError("raw: fp16 CUDA tensor [U, 128, 512] with contiguous rows")
+    U = q.shape[0]
+    if q.shape != (U, N_HEAD, HEAD_DIM) or rows.shape[0] != U or n_rows.shape != (U,) or raw.shape[0] != U \
+            or n_raw.shape != (U,) or out.shape != (U, N_HEAD, HEAD_DIM):
+        raise ValueError("shape mismatch")
+    if lse is not None:
+        _req(lse, "lse", torch.float32)
+    st = load().ds4a_dense_attn_decode(_ptr(q), _ptr(rows), rows.stride(0), rows.shape[1], _ptr(n_rows), _ptr(raw),
+                                       raw.stride(0), _ptr(n_raw), float(scale), _ptr(out), _ptr(lse), U, _ptr(ws),
+                                       ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream))
+    _check(st, "ds4a_dense_attn_decode")
 
 
 def ds4a_sparse_attn_prefill(q, q_pos, rows, idx, count, raw, raw_pos0, scale, out, lse=None, ws=None, stream=None):

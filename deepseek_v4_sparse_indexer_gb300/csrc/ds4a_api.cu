@@ -139,6 +139,7 @@ size_t ds4a_workspace_bytes(int op, int U, int Q, int N_cap, int top_k) {
     case DS4A_OP_SPARSE_ATTN_DECODE:
         if (top_k < 1 || top_k > DS4A_MAX_TOP_K) return static_cast<size_t>(-1);
         return attn_ws_bytes(U, top_k);
+    case DS4A_OP_DENSE_ATTN_DECODE: return attn_ws_bytes(U, N_cap);
     case DS4A_OP_SPARSE_ATTN_PREFILL: {
         if (top_k < 1 || top_k > DS4A_MAX_TOP_K) return static_cast<size_t>(-1);
         const long long units = static_cast<long long>(U) * Q;
@@ -233,12 +234,13 @@ ds4a_status check_attn_common(const uint16_t *q, const uint16_t *rows, int N_cap
 }
 }  // namespace
 
-ds4a_status ds4a_sparse_attn_decode(const uint16_t *q, const uint16_t *rows, int64_t rows_unit_stride, int N_cap,
-                                    const int32_t *idx, const int32_t *count, int top_k, const uint16_t *raw,
-                                    int64_t raw_unit_stride, const int32_t *n_raw, float scale, float *out,
-                                    float *lse, int U, void *ws, size_t ws_bytes, void *stream) {
-    if (ds4a_status inj = take_injected()) return inj;
-    if (ds4a_status st = check_attn_common(q, rows, N_cap, idx, count, top_k, out)) return st;
+namespace {
+// Decode attention over an explicit row list (idx, count, top_k) or, with
+// idx == nullptr, over rows 0 .. count[u]-1 (count = n_rows, top_k = N_cap).
+ds4a_status attn_decode(const uint16_t *q, const uint16_t *rows, int64_t rows_unit_stride, int N_cap,
+                        const int32_t *idx, const int32_t *count, int top_k, const uint16_t *raw,
+                        int64_t raw_unit_stride, const int32_t *n_raw, float scale, float *out, float *lse, int U,
+                        void *ws, size_t ws_bytes, void *stream) {
     if (!raw || !n_raw || U < 1) return DS4A_EINVAL;
     if (!aligned(raw, 16)) return DS4A_EINVAL;
     if (U > 1 && (rows_unit_stride < static_cast<int64_t>(N_cap) * kHeadDim || rows_unit_stride % kHeadDim ||
@@ -277,7 +279,31 @@ ds4a_status ds4a_sparse_attn_decode(const uint16_t *q, const uint16_t *rows, int
     a.raw_per_unit = raw_per_unit;
     if (!encode_2d_sw128(&a.tm_q, false, q, kHeadDim, static_cast<unsigned long long>(U) * kNHead, 64, 64))
         return DS4A_EINVAL;
+    a.tma_rows = encode_2d_sw128(&a.tm_rows, false, rows, kHeadDim, static_cast<unsigned long long>(total_rows), 64, 64);
+    a.tma_raw = encode_2d_sw128(&a.tm_raw, true, raw, kHeadDim, static_cast<unsigned long long>(total_raw), 64, 64);
     return launch_sparse_attn(a, di->sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DS4A_OK : DS4A_ECUDA;
+}
+}  // namespace
+
+ds4a_status ds4a_sparse_attn_decode(const uint16_t *q, const uint16_t *rows, int64_t rows_unit_stride, int N_cap,
+                                    const int32_t *idx, const int32_t *count, int top_k, const uint16_t *raw,
+                                    int64_t raw_unit_stride, const int32_t *n_raw, float scale, float *out,
+                                    float *lse, int U, void *ws, size_t ws_bytes, void *stream) {
+    if (ds4a_status inj = take_injected()) return inj;
+    if (ds4a_status st = check_attn_common(q, rows, N_cap, idx, count, top_k, out)) return st;
+    return attn_decode(q, rows, rows_unit_stride, N_cap, idx, count, top_k, raw, raw_unit_stride, n_raw, scale, out,
+                       lse, U, ws, ws_bytes, stream);
+}
+
+ds4a_status ds4a_dense_attn_decode(const uint16_t *q, const uint16_t *rows, int64_t rows_unit_stride, int N_cap,
+                                   const int32_t *n_rows, const uint16_t *raw, int64_t raw_unit_stride,
+                                   const int32_t *n_raw, float scale, float *out, float *lse, int U, void *ws,
+                                   size_t ws_bytes, void *stream) {
+    if (ds4a_status inj = take_injected()) return inj;
+    if (!q || !rows || !n_rows || !out || N_cap < 1) return DS4A_EINVAL;
+    if (!aligned(q, 16) || !aligned(rows, 16) || !aligned(out, 16)) return DS4A_EINVAL;
+    return attn_decode(q, rows, rows_unit_stride, N_cap, nullptr, n_rows, N_cap, raw, raw_unit_stride, n_raw, scale,
+                       out, lse, U, ws, ws_bytes, stream);
 }
 
 ds4a_status ds4a_sparse_attn_prefill(const uint16_t *q, const int32_t *q_pos, const uint16_t *rows, int N_cap,
@@ -318,6 +344,9 @@ ds4a_status ds4a_sparse_attn_prefill(const uint16_t *q, const int32_t *q_pos, co
     if (static_cast<long long>(T) * kNHead >= (1LL << 31)) return DS4A_EINVAL;
     if (!encode_2d_sw128(&a.tm_q, false, q, kHeadDim, static_cast<unsigned long long>(T) * kNHead, 64, 64))
         return DS4A_EINVAL;
+    a.tma_rows = encode_2d_sw128(&a.tm_rows, false, rows, kHeadDim, static_cast<unsigned long long>(N_cap), 64, 64);
+    a.tma_raw = n_raw_rows > 0 &&
+                encode_2d_sw128(&a.tm_raw, true, raw, kHeadDim, static_cast<unsigned long long>(n_raw_rows), 64, 64);
     return launch_sparse_attn(a, di->sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DS4A_OK : DS4A_ECUDA;
 }
 

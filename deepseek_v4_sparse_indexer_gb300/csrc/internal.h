@@ -55,6 +55,9 @@ cudaError_t launch_topk(const TopkArgs &a, int num_sms, cudaStream_t s);
 // ---- sparse attention ----------------------------------------------------
 struct AttnArgs {
     CUtensorMap tm_q;            // 2-D (512, units*64) bf16, box (64, 64), 128B swizzle
+    CUtensorMap tm_rows;         // 2-D (512, all rows) bf16, box (64, 64): whole contiguous row tiles
+    CUtensorMap tm_raw;          // 2-D (512, all raw rows) fp16, box (64, 64)
+    int tma_rows, tma_raw;       // the maps above are valid
     long long rows_per_unit;     // row offset between units' compressed rows (0 in prefill)
     long long raw_per_unit;      // decode: row offset between units' raw rings
     const uint16_t *q;           // [units][64][512] bf16

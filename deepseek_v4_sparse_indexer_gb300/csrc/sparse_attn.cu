@@ -13,7 +13,9 @@
 //            blocks in the 128B-swizzled layout; masked rows are zero-filled
 //            and per-group row-validity bits go to shared memory; each
 //            thread fences its copies into the async proxy before its warp
-//            arrives on the buffer's barrier;
+//            arrives on the buffer's barrier.  A whole tile of contiguous
+//            rows (the raw window, or a dense row list) is instead eight TMA
+//            tile loads (64 columns x 64 rows each) issued by one thread;
 //   logits   warp 4 (one thread): S[64 heads x 64 rows] = q . X^T, 32 UMMAs
 //            (M=64, N=64, K=16, both operands K-major) into one of two TMEM
 //            buffers (head h of the M=64 accumulator sits in TMEM lane
@@ -164,6 +166,7 @@ DS4A_DEV Item make_item(const AttnArgs &a, int it, int n_split) {
     m.unit = it / n_split;
     m.split = it - m.unit * n_split;
     int cnt = a.count[m.unit];
+    if (m.split == 0 && (cnt < 0 || cnt > a.top_k) && threadIdx.x == 0) report(a.status, DS4A_DEV_BOUNDS);
     cnt = cnt < 0 ? 0 : (cnt > a.top_k ? a.top_k : cnt);
     m.cnt = cnt;
     m.comp_row0 = static_cast<long long>(m.unit) * a.rows_per_unit;
@@ -243,6 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
         *abort_flag = 0;
         mbar_fence_init();
         tma_prefetch_desc(&a.tm_q);
+        if (a.tma_rows) tma_prefetch_desc(&a.tm_rows);
+        if (a.tma_raw) tma_prefetch_desc(&a.tm_raw);
     }
     if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
     tc_fence_before();
@@ -288,8 +293,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                     continue;
                 }
                 if (t < m.ct) {
+                    // no idx: the row list is 0 .. count-1 (dense attention)
                     const int jj = t * TR + r;
-                    rv[k] = jj < m.cnt ? __ldg(a.idx + static_cast<long long>(m.unit) * a.top_k + jj) : -1;
+                    rv[k] = jj < m.cnt ? (a.idx ? __ldg(a.idx + static_cast<long long>(m.unit) * a.top_k + jj) : jj) : -1;
                 } else {
                     const int jj = (t - m.ct) * TR + r;
                     rv[k] = jj < m.nrw ? jj : -1;
@@ -339,33 +345,51 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
             ok = __all_sync(0xffffffffu, mbar_wait(&x_empty[xb], xeph[xb] ^ 1, abort_flag));
             if (!ok) break;
             xeph[xb] ^= 1;
-            const uint32_t buf = smem_u32(sX) + xb * kXBuf;
-#pragma unroll
-            for (int b = 0; b < 8; ++b) {
-#pragma unroll
-                for (int k = 0; k < kGroupsPerWarp; ++k) {
-                    const int g = gw + k * kGatherWarps;
-                    if (g >= kRowGroups) continue;
-                    const int r = 4 * g + rsub;
-                    cp_async16(buf + b * kXBlk + r * 128 + ((chunk ^ (r & 7)) << 4),
-                               src[k] >= 0 ? base + static_cast<long long>(src[k]) * kHeadDim + b * 64 : a.q,
-                               src[k] >= 0 ? 16u : 0u);
-                }
-            }
-            cp_async_commit();
+            // validity bits first: a warp's barrier arrival publishes them
 #pragma unroll
             for (int k = 0; k < kGroupsPerWarp; ++k) {
                 const int g = gw + k * kGatherWarps;
                 const uint32_t bal = __ballot_sync(0xffffffffu, src[k] >= 0);
                 if (lane == 0 && g < kRowGroups) sValid[xb * kRowGroups + g] = static_cast<uint8_t>(nibble(bal));
             }
+            // A whole tile of contiguous rows comes by TMA: raw-window tiles and
+            // the tiles of a dense row list (rows past the valid count must be
+            // zeros, so a partial tile takes the cp.async path).
+            const bool raw_tile = ct_ >= cm.ct;
+            const int first = raw_tile ? (ct_ - cm.ct) * TR : ct_ * TR;
+            const bool tma_tile = raw_tile ? (a.tma_raw && first + TR <= cm.nrw)
+                                           : (a.tma_rows && !a.idx && first + TR <= cm.cnt);
+            const uint32_t buf = smem_u32(sX) + xb * kXBuf;
+            if (tma_tile) {
+                if (gw == 0 && lane == 0) {
+                    const int y = static_cast<int>((raw_tile ? cm.raw_row0 : cm.comp_row0) + first);
+                    mbar_arrive_expect_tx(&x_full[xb], kXBuf);      // also this warp's arrival
+                    for (int b = 0; b < 8; ++b)
+                        tma_load_2d_nohint(sX + xb * kXBuf + b * kXBlk, raw_tile ? &a.tm_raw : &a.tm_rows,
+                                           &x_full[xb], b * 64, y);
+                }
+            } else {
+#pragma unroll
+                for (int b = 0; b < 8; ++b) {
+#pragma unroll
+                    for (int k = 0; k < kGroupsPerWarp; ++k) {
+                        const int g = gw + k * kGatherWarps;
+                        if (g >= kRowGroups) continue;
+                        const int r = 4 * g + rsub;
+                        cp_async16(buf + b * kXBlk + r * 128 + ((chunk ^ (r & 7)) << 4),
+                                   src[k] >= 0 ? base + static_cast<long long>(src[k]) * kHeadDim + b * 64 : a.q,
+                                   src[k] >= 0 ? 16u : 0u);
+                    }
+                }
+            }
+            cp_async_commit();
             // While the copies land: the row list of the next tile.
             advance(cit, ct_, cm);
             if (cit < n_items) fetch_rows(cm, ct_, rv);
             cp_async_wait<0>();
             fence_proxy_async();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&x_full[xb]);
+            if (lane == 0 && !(tma_tile && gw == 0)) mbar_arrive(&x_full[xb]);
             ++jt;
         }
         cp_async_wait<0>();

@@ -2,6 +2,8 @@
 
 DecodeStep: U units (sequence x layer caches), one query each.
 PrefillStep: one chunk of T queries of one sequence over a causal row store.
+DenseStep: the ratio-128 layers' attention over all compressed rows (no
+indexer, so no score or select).
 
 Both own their outputs and workspaces (allocated once, reused every call, so a
 call can be captured in a CUDA graph) and run indexer score -> top-k select ->
@@ -80,5 +82,22 @@ class PrefillStep:
     def __call__(self, x, scale=DEFAULT_SCALE, stream=None):
         self.score(x, stream)
         self.select(x, stream)
+        self.attend(x, scale, stream)
+        return self.out
+
+
+class DenseStep:
+    def __init__(self, U, N_cap, device="cuda"):
+        self.U, self.N_cap = U, N_cap
+        dev = torch.device(device)
+        self.out = torch.empty(U, B.N_HEAD, B.HEAD_DIM, dtype=torch.float32, device=dev)
+        self.lse = torch.empty(U, B.N_HEAD, dtype=torch.float32, device=dev)
+        self.ws_attn = _ws(B.ds4a_workspace_bytes(B.DS4A_OP_DENSE_ATTN_DECODE, U, 1, N_cap, 0), dev)
+
+    def attend(self, x, scale=DEFAULT_SCALE, stream=None):
+        B.ds4a_dense_attn_decode(x["q"], x["rows"], x["n_rows"], x["raw"], x["n_raw"], scale, self.out, self.lse,
+                                 self.ws_attn, stream=stream)
+
+    def __call__(self, x, scale=DEFAULT_SCALE, stream=None):
         self.attend(x, scale, stream)
         return self.out

@@ -39,7 +39,7 @@ COMPRESS_RATIO = 4
 @dataclass
 class Workload:
     name: str
-    kind: str              # "decode" or "prefill"
+    kind: str              # "decode", "prefill" or "dense" (ratio-128 layers: all rows, no indexer)
     units: int             # decode: sequences x layers; prefill: 1
     n_rows: int            # compressed rows per unit (prefill: prior + in-chunk)
     top_k: int = 512
@@ -63,6 +63,10 @@ WORKLOADS = {
                                    queries=2048, extra=dict(prior_rows=65536)),
     "longctx_4x262144": Workload("longctx_4x262144", "decode", 4, 262144,
                                  heavy_frac=0.05),
+    # Ratio-128 layers ("DwarfStar(ds4.c) のアーキテクチャを読む" §3-2: the odd
+    # layers 3..41 of the Flash shape fold 128 tokens into one row and attend to
+    # all rows): 32 sequences x 20 layers at 1M tokens of context = 8,192 rows.
+    "dense_32x20x8192": Workload("dense_32x20x8192", "dense", 32 * 20, 8192, top_k=0),
 }
 
 
@@ -111,12 +115,13 @@ def apply_heavy_tail_(ik: torch.Tensor, frac: float, scale: float, seed: int, st
 
 
 def make_decode_inputs(units, n_cap, device="cpu", seed=0, n_rows=None, n_raw=None,
-                       heavy_frac=0.0, heavy_scale=4.0, q_scale=1.0):
+                       heavy_frac=0.0, heavy_scale=4.0, q_scale=1.0, with_indexer=True):
     """Decode-step inputs for `units` independent (sequence x layer) caches.
 
     n_rows / n_raw: per-unit valid compressed rows / raw-window slots (int or
     list); default full.  q_scale multiplies the attention query (x32 gives a
-    peaked softmax for stress cases).
+    peaked softmax for stress cases).  with_indexer=False leaves out iq, w and
+    ik (the ratio-128 layers have no indexer).
     """
     dev = torch.device(device)
     bf, hf = torch.bfloat16, torch.float16
@@ -124,11 +129,12 @@ def make_decode_inputs(units, n_cap, device="cpu", seed=0, n_rows=None, n_raw=No
     x["q"] = normal_fill_(torch.empty(units, N_HEAD, HEAD_DIM, dtype=bf, device=dev), HEAD_DIM, seed, 1)
     if q_scale != 1.0:
         x["q"].mul_(q_scale)
-    x["iq"] = normal_fill_(torch.empty(units, N_IDX_HEAD, IDX_DIM, dtype=bf, device=dev), IDX_DIM, seed, 2)
-    x["w"] = uniform_fill_(torch.empty(units, N_IDX_HEAD, dtype=torch.float32, device=dev), seed, 3)
-    x["ik"] = normal_fill_(torch.empty(units, n_cap, IDX_DIM, dtype=bf, device=dev), IDX_DIM, seed, 4)
-    if heavy_frac > 0:
-        apply_heavy_tail_(x["ik"], heavy_frac, heavy_scale, seed, 5)
+    if with_indexer:
+        x["iq"] = normal_fill_(torch.empty(units, N_IDX_HEAD, IDX_DIM, dtype=bf, device=dev), IDX_DIM, seed, 2)
+        x["w"] = uniform_fill_(torch.empty(units, N_IDX_HEAD, dtype=torch.float32, device=dev), seed, 3)
+        x["ik"] = normal_fill_(torch.empty(units, n_cap, IDX_DIM, dtype=bf, device=dev), IDX_DIM, seed, 4)
+        if heavy_frac > 0:
+            apply_heavy_tail_(x["ik"], heavy_frac, heavy_scale, seed, 5)
     x["rows"] = normal_fill_(torch.empty(units, n_cap, HEAD_DIM, dtype=bf, device=dev), HEAD_DIM, seed, 6)
     x["raw"] = normal_fill_(torch.empty(units, N_SWA, HEAD_DIM, dtype=hf, device=dev), HEAD_DIM, seed, 7)
     nr = n_rows if n_rows is not None else n_cap

@@ -75,6 +75,7 @@ typedef int ds4a_status;
 #define DS4A_OP_TOPK_SELECT 1
 #define DS4A_OP_SPARSE_ATTN_DECODE 2
 #define DS4A_OP_SPARSE_ATTN_PREFILL 3
+#define DS4A_OP_DENSE_ATTN_DECODE 4
 
 /* Human-readable text of a status code (static storage). */
 const char *ds4a_strerror(ds4a_status status);
@@ -216,7 +217,7 @@ ds4a_status ds4a_topk_select_noalloc(const float *scores, const int32_t *n_rows,
  *            set is split over several CTAs).
  *    q, rows and raw must be 16-byte aligned; with U > 1 the unit strides must
  *    be whole rows (multiples of 512 elements), at least N_cap resp. 128 rows
- *    (rows are gathered by TMA from one row-indexed view of each buffer).
+ *    (each buffer is addressed as one array of 512-element rows).
  */
 ds4a_status ds4a_sparse_attn_decode(const uint16_t *q, const uint16_t *rows,
                                     int64_t rows_unit_stride, int N_cap,
@@ -224,6 +225,27 @@ ds4a_status ds4a_sparse_attn_decode(const uint16_t *q, const uint16_t *rows,
                                     const uint16_t *raw, int64_t raw_unit_stride,
                                     const int32_t *n_raw, float scale, float *out, float *lse,
                                     int U, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * 3c. Dense attention of the ratio-128 layers (§3-2: the 128:1 layers keep so
+ *    few compressed rows that they attend to all of them; they have no
+ *    indexer).  Per unit u and head h, over the joint row set
+ *    X = {rows[u, r] : r < n_rows[u]} U {raw[u, s] : s < n_raw[u]}, the same
+ *    arithmetic as 3a (it is 3a with the row list 0 .. n_rows[u]-1).
+ *
+ *    q       bf16 [U][64][512] (device).
+ *    rows    bf16 [U][N_cap][512]; unit u at rows + u*rows_unit_stride (device).
+ *    n_rows  int32 [U] (device): compressed rows of unit u; a value outside
+ *            [0, N_cap] sets DS4A_DEV_BOUNDS and is clamped.
+ *    raw, n_raw, out, lse, strides and alignment as in 3a.
+ *    ws      workspace of ds4a_workspace_bytes(DS4A_OP_DENSE_ATTN_DECODE, U, 1,
+ *            N_cap, 0) bytes.
+ */
+ds4a_status ds4a_dense_attn_decode(const uint16_t *q, const uint16_t *rows,
+                                   int64_t rows_unit_stride, int N_cap, const int32_t *n_rows,
+                                   const uint16_t *raw, int64_t raw_unit_stride,
+                                   const int32_t *n_raw, float scale, float *out, float *lse,
+                                   int U, void *ws, size_t ws_bytes, void *stream);
 
 /*
  * 3b. Sparse attention, one prefill chunk of T queries of one sequence (the

@@ -208,6 +208,14 @@ def prefill_query(t, q, iq, w, ik, rows, n_rows, row_pos, q_pos, raw, raw_pos0, 
     return dict(scores=s, idx=idx, kth=kth, out=out, lse=lse, window=win)
 
 
+def dense_attention(q, rows, n_rows, raw, n_raw, scale):
+    """Attention of a ratio-128 layer ([ARCH] §3-2: the 128:1 layers have no
+    indexer and attend to every compressed row): the joint softmax over rows
+    0 .. n_rows-1 and raw slots 0 .. n_raw-1, i.e. the attention definition
+    with every row selected."""
+    return sparse_attention(q, rows, np.arange(n_rows, dtype=np.int32), raw, np.arange(n_raw, dtype=np.int32), scale)
+
+
 def attention_with_given_set(q, rows, idx, raw, raw_sel, scale):
     """The attention step alone on a row set chosen elsewhere (used to check the
     device's output on the device's own selected set)."""

@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import oracle
-from deepseek_v4_sparse_indexer_gb300 import DecodeStep, PrefillStep, _binding as B
+from deepseek_v4_sparse_indexer_gb300 import DecodeStep, DenseStep, PrefillStep, _binding as B
 from deepseek_v4_sparse_indexer_gb300.workloads import WORKLOADS, make_decode_inputs, make_prefill_inputs
 from tests.parity_util import (check_index_set, check_output, check_scores, pool, score_tolerance, u16)
 
@@ -399,3 +399,94 @@ def test_workload_prefill_2048x65536_sampled():
     ts = [0, 1, 2, 3, 4, 127, 128, 1000, 2043, 2044, 2046, 2047]
     with pool() as p:
         list(p.map(lambda t: check_prefill_query(x, st, t, wl.top_k, SCALE, np_in), ts))
+
+
+# ----------------------------------------------------------------------------
+# Ratio-128 layers: dense attention over all compressed rows (no indexer)
+# ----------------------------------------------------------------------------
+
+def dense_case(U, N_cap, n_rows, n_raw, seed, q_scale=1.0):
+    x = make_decode_inputs(U, N_cap, device="cuda", seed=seed, n_rows=n_rows, n_raw=n_raw, q_scale=q_scale,
+                           with_indexer=False)
+    out = torch.full((U, 64, 512), float("nan"), device="cuda")
+    lse = torch.full((U, 64), float("nan"), device="cuda")
+    nb = B.ds4a_workspace_bytes(B.DS4A_OP_DENSE_ATTN_DECODE, U, 1, N_cap, 0)
+    ws = torch.empty(max(nb, 1), dtype=torch.uint8, device="cuda") if nb else None
+    B.ds4a_dense_attn_decode(x["q"], x["rows"], x["n_rows"], x["raw"], x["n_raw"], SCALE, out, lse, ws)
+    torch.cuda.synchronize()
+    return x, out, lse
+
+
+def check_dense_unit(x, out, lse, u):
+    n, nw = int(x["n_rows"][u]), int(x["n_raw"][u])
+    ro, rl = oracle.dense_attention(u16(x["q"][u]), u16(x["rows"][u]), n, u16(x["raw"][u]), nw, SCALE)
+    if n + nw == 0:
+        assert torch.all(out[u] == 0) and torch.all(torch.isneginf(lse[u]))
+        return
+    check_output(out[u].cpu().numpy(), ro)
+    assert np.allclose(lse[u].cpu().numpy(), rl, atol=1e-4, rtol=1e-5), u
+
+
+@pytest.mark.parametrize("q_scale", [1.0, 32.0])
+def test_dense_attention_small_ragged(q_scale):
+    # 160 units: one item per unit (no split); ragged row counts cover partial tiles
+    n_rows = [1000, 513, 0, 64, 65, 1] + [777] * 154
+    n_raw = [128, 7, 0, 0, 128, 1] + [33] * 154
+    x, out, lse = dense_case(160, 1000, n_rows, n_raw, seed=31, q_scale=q_scale)
+    device_ok()
+    for u in range(8):
+        check_dense_unit(x, out, lse, u)
+
+
+def test_dense_attention_few_units_split_rows():
+    # fewer units than SMs: each unit's rows are split over several CTAs and merged
+    x, out, lse = dense_case(3, 6000, [6000, 4500, 129], [128, 0, 5], seed=32)
+    device_ok()
+    for u in range(3):
+        check_dense_unit(x, out, lse, u)
+
+
+def test_dense_attention_row_count_out_of_range_is_clamped_and_flagged():
+    U, N_cap = 2, 300
+    x = make_decode_inputs(U, N_cap, device="cuda", seed=33, n_raw=[10, 10], with_indexer=False)
+    nr = torch.tensor([N_cap + 7, 120], dtype=torch.int32, device="cuda")
+    out = torch.empty(U, 64, 512, device="cuda")
+    nb = B.ds4a_workspace_bytes(B.DS4A_OP_DENSE_ATTN_DECODE, U, 1, N_cap, 0)
+    ws = torch.empty(max(nb, 1), dtype=torch.uint8, device="cuda")
+    B.ds4a_dense_attn_decode(x["q"], x["rows"], nr, x["raw"], x["n_raw"], SCALE, out, None, ws)
+    st, flags = B.ds4a_get_device_status()
+    assert st == B.DS4A_EDEVICE and flags & B.DS4A_DEV_BOUNDS
+    for u, n in [(0, N_cap), (1, 120)]:
+        ro, _ = oracle.dense_attention(u16(x["q"][u]), u16(x["rows"][u]), n, u16(x["raw"][u]), 10, SCALE)
+        check_output(out[u].cpu().numpy(), ro)
+    device_ok()
+
+
+def test_sparse_count_out_of_range_is_clamped_and_flagged():
+    U, N_cap, k = 160, 256, 64
+    x = make_decode_inputs(U, N_cap, device="cuda", seed=34, n_raw=[3] * U)
+    rng = np.random.default_rng(34)
+    idx = np.stack([np.sort(rng.choice(N_cap, k, replace=False)) for _ in range(U)]).astype(np.int32)
+    cnt = torch.full((U,), k, dtype=torch.int32, device="cuda")
+    cnt[0] = k + 9
+    out = torch.empty(U, 64, 512, device="cuda")
+    B.ds4a_sparse_attn_decode(x["q"], x["rows"], torch.from_numpy(idx).cuda(), cnt, x["raw"], x["n_raw"], SCALE,
+                              out, None, None)
+    st, flags = B.ds4a_get_device_status()
+    assert st == B.DS4A_EDEVICE and flags & B.DS4A_DEV_BOUNDS
+    ro, _ = oracle.sparse_attention(u16(x["q"][0]), u16(x["rows"][0]), idx[0], u16(x["raw"][0]), np.arange(3), SCALE)
+    check_output(out[0].cpu().numpy(), ro)
+    device_ok()
+
+
+@pytest.mark.slow
+def test_workload_dense_sampled():
+    wl = WORKLOADS["dense_32x20x8192"]
+    x = make_decode_inputs(wl.units, wl.n_rows, device="cuda", seed=wl.seed, with_indexer=False)
+    step = DenseStep(wl.units, wl.n_rows)
+    step(x)
+    torch.cuda.synchronize()
+    device_ok()
+    units = [0, 1, wl.units // 2, wl.units - 1]
+    with pool() as p:
+        list(p.map(lambda u: check_dense_unit(x, step.out, step.lse, u), units))
