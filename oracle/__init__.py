@@ -60,6 +60,10 @@ def lib():
                                               u16p, i32p, ctypes.c_int,
                                               ctypes.c_double, f64p, f64p]
         L.oracle_sparse_attention.restype = ctypes.c_int
+        L.oracle_compressor_pool.argtypes = [f32p, f32p, ctypes.c_int, ctypes.c_int, f64p]
+        L.oracle_compressor_pool.restype = None
+        L.oracle_push_raw.argtypes = [u16p, ctypes.POINTER(ctypes.c_int), ctypes.c_int, ctypes.c_int, f32p]
+        L.oracle_push_raw.restype = None
         _lib = L
     return _lib
 
@@ -220,3 +224,33 @@ def attention_with_given_set(q, rows, idx, raw, raw_sel, scale):
     """The attention step alone on a row set chosen elsewhere (used to check the
     device's output on the device's own selected set)."""
     return sparse_attention(q, rows, np.asarray(idx, np.int32), raw, raw_sel, scale)
+
+
+# ----------------------------------------------------------------------------
+# Cache producer: raw-window push and compressor pooling ([ARCH] §3-1, §3-2)
+# ----------------------------------------------------------------------------
+
+def compressor_pool(kv, score):
+    """One compressed row (float64 [width]) from a frontier of `ratio` rows:
+    per column, a softmax of the scores over the rows weights the kv values.
+    kv, score: float32 [ratio, width]."""
+    kv = np.ascontiguousarray(kv, dtype=np.float32)
+    score = np.ascontiguousarray(score, dtype=np.float32)
+    assert kv.shape == score.shape and kv.ndim == 2
+    ratio, width = kv.shape
+    out = np.empty(width, dtype=np.float64)
+    lib().oracle_compressor_pool(_ptr(kv, ctypes.c_float), _ptr(score, ctypes.c_float), ratio, width,
+                                 _ptr(out, ctypes.c_double))
+    return out
+
+
+def push_raw(ring, n_raw, kv, cap=N_SWA):
+    """Push one fp32 row into a raw window kept oldest first (f16 bits
+    [cap, dim]); returns (ring, n_raw) after the push (the ring is a copy)."""
+    ring = np.array(ring, dtype=np.uint16, copy=True)
+    kv = np.ascontiguousarray(kv, dtype=np.float32)
+    assert ring.ndim == 2 and ring.shape[0] == cap and ring.shape[1] == kv.shape[0]
+    n = ctypes.c_int(int(n_raw))
+    lib().oracle_push_raw(_ptr(ring, ctypes.c_uint16), ctypes.byref(n), cap, ring.shape[1],
+                          _ptr(kv, ctypes.c_float))
+    return ring, n.value

@@ -309,3 +309,53 @@ int oracle_sparse_attention(const uint16_t *q, int n_head, int dim,
     free(a);
     return 0;
 }
+
+/*
+ * Compressor pooling ([ARCH] §3-2, the pooling inside the compressor's
+ * decode step): `ratio` frontier rows of (kv, score) become one compressed
+ * row.  Each column j is pooled on its own: the scores of that column over
+ * the frontier rows are logits of a softmax whose weights average the kv
+ * values of the column,
+ *     m_j = max_r score[r][j]
+ *     out[j] = sum_r exp(score[r][j] - m_j) * kv[r][j] / sum_r exp(score[r][j] - m_j)
+ * and a column whose weights sum to zero (every score -inf) gives 0, as the
+ * pages' guard on the denominator does.  kv and score: fp32 [ratio][width],
+ * out: [width].
+ */
+void oracle_compressor_pool(const float *kv, const float *score, int ratio, int width, double *out)
+{
+    for (int j = 0; j < width; j++) {
+        double m = -INFINITY;
+        for (int r = 0; r < ratio; r++) {
+            const double s = (double)score[(int64_t)r * width + j];
+            if (s > m) m = s;
+        }
+        double num = 0.0, den = 0.0;
+        if (m > -INFINITY) {
+            for (int r = 0; r < ratio; r++) {
+                const double e = exp((double)score[(int64_t)r * width + j] - m);
+                den += e;
+                num += e * (double)kv[(int64_t)r * width + j];
+            }
+        }
+        out[j] = den > 0.0 ? num / den : 0.0;
+    }
+}
+
+/*
+ * Raw-window push ([ARCH] §3-1): the raw tier keeps the last `cap` (128)
+ * tokens' rows, each rounded through f16.  The window is kept oldest first:
+ * while it holds fewer than cap rows the new row is appended; a full window
+ * first drops its oldest row (the others move down one slot).  ring: f16 bits
+ * [cap][dim]; *n_raw: rows held (updated); kv: the new fp32 row.
+ */
+void oracle_push_raw(uint16_t *ring, int *n_raw, int cap, int dim, const float *kv)
+{
+    if (*n_raw >= cap) {
+        for (int s = 1; s < cap; s++)
+            for (int d = 0; d < dim; d++) ring[(int64_t)(s - 1) * dim + d] = ring[(int64_t)s * dim + d];
+        *n_raw = cap - 1;
+    }
+    for (int d = 0; d < dim; d++) ring[(int64_t)(*n_raw) * dim + d] = oracle_double_to_f16((double)kv[d]);
+    *n_raw += 1;
+}

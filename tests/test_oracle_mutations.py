@@ -27,6 +27,14 @@ MUTATIONS = {
                                       "*kth = m > 0 ? v[0].s : -INFINITY;"),
     "raw row decoded as bf16": ("x[(int64_t)(n_sel + j) * dim + d] = oracle_f16_to_double(",
                                 "x[(int64_t)(n_sel + j) * dim + d] = oracle_bf16_to_double("),
+    "pooling not normalised": ("out[j] = den > 0.0 ? num / den : 0.0;", "out[j] = den > 0.0 ? num : 0.0;"),
+    "pooling max taken as a min": ("if (s > m) m = s;", "if (s < m) m = s;"),
+    "pooling reads the next column's score": (
+        "const double e = exp((double)score[(int64_t)r * width + j] - m);",
+        "const double e = exp((double)score[(int64_t)r * width + (j + 1) % width] - m);"),
+    "push slides by two rows": ("ring[(int64_t)(s - 1) * dim + d] = ring[(int64_t)s * dim + d];",
+                                "ring[(int64_t)(s - 1) * dim + d] = ring[(int64_t)(s < cap - 1 ? s + 1 : s) * dim + d];"),
+    "push keeps the full window one row short": ("        *n_raw = cap - 1;\n", "        *n_raw = cap - 2;\n"),
 }
 
 

@@ -392,3 +392,76 @@ def test_prefill_query_equals_restricted_decode():
         assert np.array_equal(dec["idx"], res["idx"])
         assert np.array_equal(res["window"], win)
         np.testing.assert_allclose(dec["out"], res["out"], rtol=1e-13, atol=1e-16)
+
+
+# ----------------------------------------------------------------------------
+# Cache producer: compressor pooling and the raw-window push
+# ----------------------------------------------------------------------------
+
+def test_compressor_pool_two_rows_golden():
+    vals = {}
+    for line in open(os.path.join(GOLDEN, "compressor_pool_two_rows.txt")):
+        line = line.split("#")[0].split()
+        if line:
+            vals[line[0]] = [float(v) for v in line[1:]]
+    kv = np.array([vals["kv0"], vals["kv1"]], np.float32)
+    sc = np.array([vals["s0"], vals["s1"]], np.float32)
+    np.testing.assert_allclose(oracle.compressor_pool(kv, sc), vals["out"], rtol=0, atol=1e-7)
+
+
+@pytest.mark.parametrize("ratio", [1, 4, 128])
+def test_compressor_pool_equal_scores_give_the_mean_and_ratio_one_the_row(ratio):
+    r = rng(60 + ratio)
+    kv = r.standard_normal((ratio, 24)).astype(np.float32)
+    sc = np.broadcast_to(r.standard_normal(24).astype(np.float32), (ratio, 24))
+    out = oracle.compressor_pool(kv, sc)
+    np.testing.assert_allclose(out, kv.astype(np.float64).mean(axis=0), rtol=1e-13, atol=1e-14)
+    if ratio == 1:
+        assert np.array_equal(out, kv[0].astype(np.float64))
+
+
+def test_compressor_pool_matches_scipy_softmax_and_is_shift_invariant():
+    special = pytest.importorskip("scipy.special")
+    r = rng(70)
+    for ratio in (4, 128):
+        kv = r.standard_normal((ratio, 40)).astype(np.float32)
+        # scores on a 2^-10 grid, |s| < 16: adding 64 below is exact in fp32
+        sc = (np.round(np.clip(3 * r.standard_normal((ratio, 40)), -15, 15) * 1024) / 1024).astype(np.float32)
+        ref = (special.softmax(sc.astype(np.float64), axis=0) * kv.astype(np.float64)).sum(axis=0)
+        out = oracle.compressor_pool(kv, sc)
+        np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-13)
+        # adding one constant to a column's scores leaves it unchanged
+        shifted = oracle.compressor_pool(kv, sc + np.float32(64.0))
+        np.testing.assert_allclose(shifted, out, rtol=1e-12, atol=1e-13)
+
+
+def test_compressor_pool_dominant_score_and_masked_column():
+    r = rng(71)
+    kv = r.standard_normal((4, 8)).astype(np.float32)
+    sc = r.standard_normal((4, 8)).astype(np.float32)
+    sc[2, :] += 200.0                                   # row 2 dominates every column
+    out = oracle.compressor_pool(kv, sc)
+    np.testing.assert_allclose(out, kv[2].astype(np.float64), rtol=0, atol=1e-60)
+    sc[:, 5] = -np.inf                                  # no finite score: the column is 0
+    out = oracle.compressor_pool(kv, sc)
+    assert out[5] == 0.0
+    # the pooled value lies within the column's range (a convex combination)
+    sc = r.standard_normal((4, 8)).astype(np.float32)
+    out = oracle.compressor_pool(kv, sc)
+    assert np.all(out >= kv.min(axis=0) - 1e-12) and np.all(out <= kv.max(axis=0) + 1e-12)
+
+
+def test_push_raw_keeps_the_last_128_rows_rounded_through_f16():
+    r = rng(72)
+    dim, cap = 16, oracle.N_SWA
+    ring, n = np.zeros((cap, dim), np.uint16), 0
+    pushed = []
+    for t in range(300):
+        kv = (r.standard_normal(dim) * 1e3).astype(np.float32)
+        if t == 7:
+            kv[:4] = [65520.0, -65520.0, 1e-8, 2.0 ** -24 * 1.5]   # overflow, underflow, subnormal tie
+        ring, n = oracle.push_raw(ring, n, kv)
+        pushed.append(kv.astype(np.float16).view(np.uint16))      # numpy's f32 -> f16 cast (round to nearest even)
+        want = pushed[-cap:]
+        assert n == len(want)
+        assert np.array_equal(ring[:n], np.array(want)), t
