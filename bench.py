@@ -32,6 +32,15 @@ sys.path.insert(0, ROOT)
 
 METRIC = "sparse-attn query-token·layers/s and achieved HBM GB/s (fraction of GB300 peak)"
 UNIT = "query-token·layers/s"
+
+
+def metric_unit(wl):
+    """The bench line's metric and unit: the headline's for the attention
+    workloads, pooled units per second for the cache-producer workload."""
+    if wl.kind == "pool":
+        return ("cache-producer units/s (raw push + compressor pooling of the frontier) and achieved HBM GB/s",
+                "units/s")
+    return METRIC, UNIT
 SCALE = 1.0 / math.sqrt(512)
 
 
@@ -139,6 +148,12 @@ def decode_bytes(wl):
     return wl.units * (ik + per_unit_fixed), wl.units * idx_kernel
 
 
+def pool_bytes(wl, width=512):
+    """Algorithmic HBM bytes per launch of the pooling kernel: the fp32 (kv,
+    score) frontier and the fp32 pooled row of every unit."""
+    return wl.units * (2 * wl.n_rows * width * 4 + width * 4)
+
+
 def dense_bytes(wl):
     """Algorithmic HBM bytes per unit of a ratio-128 layer: every compressed row,
     the raw window, q, the fp32 output and lse."""
@@ -174,7 +189,8 @@ class OracleSample:
         import torch
 
         import oracle
-        from deepseek_v4_sparse_indexer_gb300.workloads import make_decode_inputs, make_prefill_inputs
+        from deepseek_v4_sparse_indexer_gb300.workloads import (make_decode_inputs, make_pool_inputs,
+                                                                make_prefill_inputs)
 
         self.wl = wl
         self.oracle = oracle
@@ -182,6 +198,17 @@ class OracleSample:
         def u16(t):
             return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
+        if wl.kind == "pool":
+            x = make_pool_inputs(min(4, wl.units), wl.n_rows, device="cpu", seed=wl.seed)
+            pool = [dict(kv=x["kv"][i].numpy(), score=x["score"][i].numpy(), row=x["row"][i].numpy())
+                    for i in range(x["kv"].shape[0])]
+            t = time.perf_counter()
+            self._run(pool[0])
+            t1 = time.perf_counter() - t
+            n = self._size(seconds_budget, t1, wl.units)
+            self.items = [pool[i % len(pool)] for i in range(n)]
+            self.text = f"{n} of {wl.units} units (each: raw push of one row + pooling of a {wl.n_rows}-row frontier)"
+            return
         if wl.kind in ("decode", "dense"):
             dense = wl.kind == "dense"
 
@@ -226,6 +253,7 @@ class OracleSample:
         return max(1, min(cap, int(round(budget / max(t1, 1e-3)))))
 
     def _run(self, item):
+        import numpy as np
         wl, o = self.wl, self.oracle
         if wl.kind == "decode":
             d = item
@@ -233,6 +261,10 @@ class OracleSample:
         elif wl.kind == "dense":
             d = item
             o.dense_attention(d["q"], d["rows"], d["n"], d["raw"], d["nraw"], SCALE)
+        elif wl.kind == "pool":
+            d = item
+            o.push_raw(np.zeros((128, 512), np.uint16), 128, d["row"])
+            o.compressor_pool(d["kv"], d["score"])
         else:
             q, iq, w, ik, rows, row_pos, q_pos, raw = self.np_in
             o.prefill_query(item, q, iq, w, ik, rows, self.nr, row_pos, q_pos, raw, self.raw_pos0, wl.top_k, SCALE)
@@ -259,6 +291,7 @@ def run_reference(args, wl):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
+    metric, unit = metric_unit(wl)
     cores = host_cores()
     # Size the sample so that warmup + steps stay within a few minutes of wall time.
     wall_per_step = max(1.0, min(6.0, 90.0 / max(1, args.steps + args.warmup)))
@@ -271,14 +304,14 @@ def run_reference(args, wl):
     value = statistics.median(vals)
     sample_text = sample.text + f", threads={cores}, each step one pass over the sample"
     units_per_step = wl.query_units
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+    line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": units_per_step / value * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic, seeded (CPU-generated with the same recipe)",
             "config": {"workload": wl.name, "units": wl.units, "queries_per_unit": wl.queries,
                        "rows_per_unit": wl.n_rows, "top_k": wl.top_k},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample_text},
-            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample_text},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
     print(json.dumps(line), flush=True)
     return 0
@@ -294,13 +327,14 @@ def main():
         raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(WORKLOADS)}")
     wl = WORKLOADS[args.workload]
     import dataclasses
-    if args.units is not None and wl.kind in ("decode", "dense"):
+    if args.units is not None and wl.kind in ("decode", "dense", "pool"):
         wl = dataclasses.replace(wl, name=f"{wl.name}[units={args.units}]", units=args.units)
     if args.prior_rows is not None and wl.kind == "prefill":
         wl = dataclasses.replace(wl, name=f"{wl.name}[prior_rows={args.prior_rows}]",
                                  n_rows=args.prior_rows + wl.queries // 4, extra=dict(prior_rows=args.prior_rows))
     if args.impl == "reference":
         return run_reference(args, wl)
+    metric, unit = metric_unit(wl)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
 
@@ -308,7 +342,7 @@ def main():
     import torch.distributed as dist
 
     import deepseek_v4_sparse_indexer_gb300 as pkg
-    from deepseek_v4_sparse_indexer_gb300.workloads import make_decode_inputs, make_prefill_inputs
+    from deepseek_v4_sparse_indexer_gb300.workloads import make_decode_inputs, make_pool_inputs, make_prefill_inputs
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -332,13 +366,16 @@ def main():
     elif wl.kind == "dense":
         x = make_decode_inputs(wl.units, wl.n_rows, device=dev, seed=seed, with_indexer=False)
         step = pkg.DenseStep(wl.units, wl.n_rows, device=dev)
+    elif wl.kind == "pool":
+        x = make_pool_inputs(wl.units, wl.n_rows, device=dev, seed=seed)
+        step = pkg.ProducerStep(wl.units, device=dev)
     else:
         x = make_prefill_inputs(wl.queries, wl.extra["prior_rows"], device=dev, seed=seed)
         step = pkg.PrefillStep(wl.queries, x["ik"].shape[0], wl.top_k, device=dev)
     torch.cuda.synchronize()
 
     for _ in range(args.warmup):
-        step(x, SCALE)
+        step(x) if wl.kind == "pool" else step(x, SCALE)
     torch.cuda.synchronize()
     st, flags = pkg.ds4a_get_device_status()
     if st != 0:
@@ -361,6 +398,11 @@ def main():
             step.attend(x, SCALE)
             sc_e[i].record()
             continue
+        if wl.kind == "pool":                  # the pooling is the dominant kernel
+            step.pool(x)
+            sc_e[i].record()
+            step.push(x)
+            continue
         step.score(x)
         sc_e[i].record()
         step.select(x)
@@ -379,11 +421,13 @@ def main():
     value = world * units / (ms / 1e3)
 
     # ---------------- end to end through the public API with host buffers
-    host_in = {k: x[k].cpu().pin_memory() for k in (("q",) if wl.kind == "dense" else ("q", "iq", "w"))}
+    in_keys = {"dense": ("q",), "pool": ("row", "kv", "score")}.get(wl.kind, ("q", "iq", "w"))
+    host_in = {k: x[k].cpu().pin_memory() for k in in_keys}
     host_out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
-    host_lse = torch.empty(step.lse.shape, dtype=step.lse.dtype).pin_memory()
+    has_lse = hasattr(step, "lse")
+    host_lse = torch.empty(step.lse.shape, dtype=step.lse.dtype).pin_memory() if has_lse else None
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = host_out.numel() * 4 + host_lse.numel() * 4
+    d2h = host_out.numel() * 4 + (host_lse.numel() * 4 if has_lse else 0)
     torch.cuda.synchronize()
     barrier()
     e0, e1 = ev(), ev()
@@ -391,9 +435,10 @@ def main():
     for i in range(K):
         for k, t in host_in.items():
             x[k].copy_(t, non_blocking=True)
-        step(x, SCALE)
+        step(x) if wl.kind == "pool" else step(x, SCALE)
         host_out.copy_(step.out, non_blocking=True)
-        host_lse.copy_(step.lse, non_blocking=True)
+        if has_lse:
+            host_lse.copy_(step.lse, non_blocking=True)
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / K
@@ -407,7 +452,9 @@ def main():
         raise SystemExit(f"device status flags {flags} after the timed region")
 
     # ---------------- roofline of the dominant kernel (indexer score; the attention for dense)
-    if wl.kind == "dense":
+    if wl.kind == "pool":
+        launches_per_step = 2
+    elif wl.kind == "dense":
         launches_per_step = 1 + (1 if pkg.ds4a_workspace_bytes(4, wl.units, 1, wl.n_rows, 0) else 0)
     else:
         launches_per_step = 1 + 1 + 1 + (1 if pkg.ds4a_workspace_bytes(
@@ -420,7 +467,19 @@ def main():
            "head_dim": 512, "indexer": "64x128" if wl.kind != "dense" else "none (ratio-128 layer)",
            "l2": "inputs exceed the L2 many times over; no flush", "parallelism": f"replicas x{world}",
            "peak_source": pk["src"]}
-    if wl.kind == "dense":
+    if wl.kind == "pool":
+        pb = pool_bytes(wl)
+        achieved = pb / (idx_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
+                "frac": achieved / pk["hbm"], "traffic": None, "kernel": "compressor_pool_kernel",
+                "algorithmic_bytes_per_launch": pb, "launch_ms": idx_ms}
+        step_bytes = pb + wl.units * (512 * 4 + 512 * 2 + 8)
+        cfg.update({"top_k": None, "rows_per_unit": None, "frontier_rows": wl.n_rows, "width": 512,
+                    "indexer": None, "heads": None, "head_dim": None})
+        cfg["step_algorithmic_bytes"] = step_bytes
+        cfg["step_hbm_GBps"] = step_bytes / (ms / 1e3) / 1e9
+        cfg["step_hbm_frac"] = cfg["step_hbm_GBps"] / pk["hbm"]
+    elif wl.kind == "dense":
         step_bytes = dense_bytes(wl)
         achieved = step_bytes / (idx_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
@@ -448,13 +507,16 @@ def main():
         cfg["step_TFLOPs"] = (idx_flops + attn_flops) / (ms / 1e3) / 1e12
         cfg["step_tensor_frac"] = cfg["step_TFLOPs"] / pk["bf16"]
 
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+    line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic: seeded N(0,1)/sqrt(d) bf16 rows/keys/queries, fp16 raw window, U(0,1) weights",
+            "data": ("synthetic: seeded fp32 frontiers, kv N(0,1)/sqrt(512), scores N(0,1)" if wl.kind == "pool" else
+                     "synthetic: seeded N(0,1)/sqrt(d) bf16 rows/keys/queries, fp16 raw window, U(0,1) weights"),
             "config": cfg, "roofline": roof,
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms,
-                    "note": ("per step: H2D of q from pinned memory, the dense attention C-ABI op, D2H of out and "
+                    "note": ("per step: H2D of the new rows and the (kv, score) frontiers from pinned memory, the "
+                             "push and pooling C-ABI ops, D2H of the pooled rows") if wl.kind == "pool" else
+                            ("per step: H2D of q from pinned memory, the dense attention C-ABI op, D2H of out and "
                              "lse; the KV caches stay resident in HBM") if wl.kind == "dense" else
                             ("per step: H2D of the queries (q, iq, w) from pinned memory, the three C-ABI ops, D2H "
                              "of out and lse; the KV caches stay resident in HBM")},
@@ -474,13 +536,15 @@ def main():
                 u = (i * 7919) % wl.units
                 return dict(q=u16(x["q"][u]), iq=u16(x["iq"][u]), w=x["w"][u].cpu().numpy(), ik=u16(x["ik"][u]),
                             rows=u16(x["rows"][u]), raw=u16(x["raw"][u]), n=wl.n_rows, nraw=128)
+        elif wl.kind == "pool":
+            unit_source = None
         elif wl.kind == "dense":
             def unit_source(i):
                 u = (i * 7919) % wl.units
                 return dict(q=u16(x["q"][u]), rows=u16(x["rows"][u]), raw=u16(x["raw"][u]), n=wl.n_rows, nraw=128)
         sample = OracleSample(wl, args.cpu_seconds, unit_source)
         v = sample.rate(cores)
-        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+        line["cpu_baseline"] = {"value": v, "unit": unit, "cores": cores, "kind": "oracle",
                                 "sample": sample.text + f", threads={cores}"}
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -8,10 +8,12 @@ DenseStep for the ratio-128 layers (attention over all rows, no indexer).
 """
 from ._binding import (Ds4aError, load, ds4a_version, ds4a_workspace_bytes, ds4a_get_device_status,
                        ds4a_debug_inject_error, ds4a_indexer_score, ds4a_topk_select,
-                       ds4a_sparse_attn_decode, ds4a_sparse_attn_prefill, ds4a_dense_attn_decode)
-from .step import DecodeStep, PrefillStep, DenseStep, DEFAULT_SCALE
+                       ds4a_sparse_attn_decode, ds4a_sparse_attn_prefill, ds4a_dense_attn_decode,
+                       ds4a_kv_push_raw, ds4a_compressor_pool)
+from .step import DecodeStep, PrefillStep, DenseStep, ProducerStep, DEFAULT_SCALE
 
 __all__ = ["Ds4aError", "load", "ds4a_version", "ds4a_workspace_bytes", "ds4a_get_device_status",
            "ds4a_debug_inject_error", "ds4a_indexer_score", "ds4a_topk_select", "ds4a_sparse_attn_decode",
-           "ds4a_sparse_attn_prefill", "ds4a_dense_attn_decode", "DecodeStep", "PrefillStep", "DenseStep",
+           "ds4a_sparse_attn_prefill", "ds4a_dense_attn_decode", "ds4a_kv_push_raw", "ds4a_compressor_pool",
+           "DecodeStep", "PrefillStep", "DenseStep", "ProducerStep",
            "DEFAULT_SCALE"]

@@ -34,7 +34,7 @@ N_HEAD, HEAD_DIM, N_IDX_HEAD, IDX_DIM, N_SWA = 64, 512, 64, 128, 128
 EXPORTS = ("ds4a_strerror", "ds4a_version", "ds4a_workspace_bytes", "ds4a_get_device_status",
            "ds4a_debug_inject_error", "ds4a_indexer_score", "ds4a_topk_select",
            "ds4a_topk_select_noalloc", "ds4a_sparse_attn_decode", "ds4a_sparse_attn_prefill",
-           "ds4a_dense_attn_decode")
+           "ds4a_dense_attn_decode", "ds4a_kv_push_raw", "ds4a_compressor_pool")
 DS4A_TOPK_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -83,6 +83,10 @@ def load(build_if_missing: bool = True):
     L.ds4a_dense_attn_decode.argtypes = [_vp, _vp, _i64, _i32, _vp, _vp, _i64, _vp, _f32, _vp, _vp, _i32, _vp, _sz,
                                          _vp]
     L.ds4a_dense_attn_decode.restype = _i32
+    L.ds4a_kv_push_raw.argtypes = [_vp, _vp, _i64, _vp, _vp, _i32, _vp]
+    L.ds4a_kv_push_raw.restype = _i32
+    L.ds4a_compressor_pool.argtypes = [_vp, _vp, _i32, _i32, _vp, _i32, _vp]
+    L.ds4a_compressor_pool.restype = _i32
     L.ds4a_sparse_attn_decode.restype = _i32
     L.ds4a_sparse_attn_prefill.argtypes = [_vp, _vp, _vp, _i32, _vp, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _vp,
                                            _i32, _vp, _sz, _vp]
@@ -286,3 +290,31 @@ def ds4a_sparse_attn_prefill(q, q_pos, rows, idx, count, raw, raw_pos0, scale, o
                                          _ptr(lse), T, _ptr(ws),
                                          ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream))
     _check(st, "ds4a_sparse_attn_prefill")
+
+
+def ds4a_kv_push_raw(kv, raw, pos, n_raw, stream=None):
+    """kv f32 [U,512]; raw fp16 [U,128,512] ring (written); pos i32 [U]; n_raw
+    i32 [U] (written)."""
+    _req(kv, "kv", torch.float32)
+    _req(pos, "pos", torch.int32)
+    _req(n_raw, "n_raw", torch.int32)
+    if raw.dtype != torch.float16 or not raw.is_cuda or raw.dim() != 3 or raw.stride(2) != 1 \
+            or raw.stride(1) != HEAD_DIM or raw.shape[1] != N_SWA:
+        raise ValueError("raw: fp16 CUDA tensor [U, 128, 512] with contiguous rows")
+    U = kv.shape[0]
+    if kv.shape != (U, HEAD_DIM) or raw.shape[0] != U or pos.shape != (U,) or n_raw.shape != (U,):
+        raise ValueError("shape mismatch")
+    st = load().ds4a_kv_push_raw(_ptr(kv), _ptr(raw), raw.stride(0), _ptr(pos), _ptr(n_raw), U, _stream(stream))
+    _check(st, "ds4a_kv_push_raw")
+
+
+def ds4a_compressor_pool(kv, score, out, stream=None):
+    """kv, score f32 [U,ratio,width]; out f32 [U,width] (written)."""
+    _req(kv, "kv", torch.float32)
+    _req(score, "score", torch.float32)
+    _req(out, "out", torch.float32)
+    if kv.dim() != 3 or score.shape != kv.shape or out.shape != (kv.shape[0], kv.shape[2]):
+        raise ValueError("shape mismatch")
+    U, ratio, width = kv.shape
+    st = load().ds4a_compressor_pool(_ptr(kv), _ptr(score), ratio, width, _ptr(out), U, _stream(stream))
+    _check(st, "ds4a_compressor_pool")

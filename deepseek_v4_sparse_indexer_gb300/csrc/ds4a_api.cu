@@ -350,4 +350,32 @@ ds4a_status ds4a_sparse_attn_prefill(const uint16_t *q, const int32_t *q_pos, co
     return launch_sparse_attn(a, di->sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DS4A_OK : DS4A_ECUDA;
 }
 
+ds4a_status ds4a_kv_push_raw(const float *kv, uint16_t *raw, int64_t raw_unit_stride, const int32_t *pos,
+                             int32_t *n_raw, int U, void *stream) {
+    if (ds4a_status inj = take_injected()) return inj;
+    if (!kv || !raw || !pos || !n_raw || U < 1) return DS4A_EINVAL;
+    if (!aligned(kv, 16) || !aligned(raw, 16)) return DS4A_EINVAL;
+    if (U > 1 && (raw_unit_stride < static_cast<int64_t>(kNSwa) * kHeadDim || raw_unit_stride % kHeadDim))
+        return DS4A_EINVAL;
+    DevInfo *di = nullptr;
+    if (ds4a_status st = current_device(&di)) return st;
+    return launch_kv_push_raw(kv, raw, U > 1 ? raw_unit_stride : 0, pos, n_raw, U, di->status,
+                              static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? DS4A_OK
+               : DS4A_ECUDA;
+}
+
+ds4a_status ds4a_compressor_pool(const float *kv, const float *score, int ratio, int width, float *out, int U,
+                                 void *stream) {
+    if (ds4a_status inj = take_injected()) return inj;
+    if (!kv || !score || !out || U < 1 || ratio < 1 || width < 4 || width % 4) return DS4A_EINVAL;
+    if (!aligned(kv, 16) || !aligned(score, 16) || !aligned(out, 16)) return DS4A_EINVAL;
+    if (static_cast<long long>(U) * ratio * width >= (1LL << 40)) return DS4A_EINVAL;
+    DevInfo *di = nullptr;
+    if (ds4a_status st = current_device(&di)) return st;
+    return launch_compressor_pool(kv, score, ratio, width, out, U, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? DS4A_OK
+               : DS4A_ECUDA;
+}
+
 }  // extern "C"

@@ -121,11 +121,6 @@ DS4A_DEV void tmem_wait_ld(uint32_t (&r)[32]) {
                  :
                  : "memory");
 }
-DS4A_DEV void tmem_wait_ld2(uint32_t (&r)[32], uint32_t (&s)[32]) {
-    tmem_wait_ld(r);
-    // The second array's wait is already satisfied; this ties its registers too.
-    tmem_wait_ld(s);
-}
 
 // Two fp32 lanes as one 64-bit register pair, for the packed fp32x2 FMA.
 DS4A_DEV unsigned long long pack_f2(float lo, float hi) {

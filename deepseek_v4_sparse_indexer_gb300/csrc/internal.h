@@ -83,6 +83,12 @@ int attn_num_splits(int units, int top_k);
 size_t attn_ws_bytes(int units, int top_k);
 cudaError_t launch_sparse_attn(const AttnArgs &a, int num_sms, cudaStream_t s);
 
+// ---- cache producer --------------------------------------------------------
+cudaError_t launch_kv_push_raw(const float *kv, uint16_t *raw, long long raw_unit_stride, const int32_t *pos,
+                               int32_t *n_raw, int U, uint32_t *status, cudaStream_t s);
+cudaError_t launch_compressor_pool(const float *kv, const float *score, int ratio, int width, float *out, int U,
+                                   cudaStream_t s);
+
 // ---- shared host helpers of the C ABI -------------------------------------
 // Status word address and SM count of the current device (set up on first use).
 int current_device_info(uint32_t **status, int *sms);

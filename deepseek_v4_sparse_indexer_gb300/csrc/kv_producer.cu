@@ -1,0 +1,107 @@
+// Producer side of the caches ("DwarfStar(ds4.c) のアーキテクチャを読む"):
+//   §3-1  the raw window keeps the last 128 tokens' rows rounded through f16;
+//   §3-2  the compressor pools a frontier of `ratio` rows (4 or 128) into one
+//         compressed row with a per-column softmax of learned scores.
+// The projections that produce kv and scores, the positional bias and the
+// normalisation / RoPE / FP8 steps after pooling need trained weights and are
+// not part of this library; these kernels take the frontier as given.
+//
+// The raw window here is a ring: the row of position p goes to slot p % 128,
+// so the window holds the same rows as the pages' oldest-first window (which
+// slides its rows down one slot when full), in rotated order; the attention
+// does not depend on slot order.
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace ds4a {
+namespace {
+
+constexpr int kPushThreads = kHeadDim / 4;   // one thread per 4 elements of the row
+
+__global__ void __launch_bounds__(kPushThreads) kv_push_raw_kernel(const float *__restrict__ kv, uint16_t *raw,
+                                                                   long long raw_unit_stride,
+                                                                   const int32_t *__restrict__ pos, int32_t *n_raw,
+                                                                   uint32_t *status) {
+    const int u = blockIdx.x;
+    const int p = pos[u];
+    if (p < 0) {                                  // no position: nothing is written
+        if (threadIdx.x == 0) report(status, DS4A_DEV_BOUNDS);
+        return;
+    }
+    const int slot = p % kNSwa;
+    const float4 v = reinterpret_cast<const float4 *>(kv + static_cast<long long>(u) * kHeadDim)[threadIdx.x];
+    const __half2 lo = __floats2half2_rn(v.x, v.y), hi = __floats2half2_rn(v.z, v.w);   // round to nearest even
+    uint2 o;
+    o.x = *reinterpret_cast<const uint32_t *>(&lo);
+    o.y = *reinterpret_cast<const uint32_t *>(&hi);
+    reinterpret_cast<uint2 *>(raw + static_cast<long long>(u) * raw_unit_stride +
+                              static_cast<long long>(slot) * kHeadDim)[threadIdx.x] = o;
+    if (threadIdx.x == 0) n_raw[u] = p + 1 < kNSwa ? p + 1 : kNSwa;
+}
+
+// One thread pools 4 consecutive columns of one unit: the column max over the
+// frontier rows, then the exp-weighted sums (the second pass mostly reads the
+// scores back from cache).  A column with no finite score gives 0.
+constexpr int kPoolThreads = 256;
+
+__global__ void __launch_bounds__(kPoolThreads) compressor_pool_kernel(const float *__restrict__ kv,
+                                                                       const float *__restrict__ score, int ratio,
+                                                                       int width, float *__restrict__ out, int U) {
+    const int w4 = width >> 2;
+    const long long t = static_cast<long long>(blockIdx.x) * kPoolThreads + threadIdx.x;
+    if (t >= static_cast<long long>(U) * w4) return;
+    const long long u = t / w4;
+    const int c = static_cast<int>(t - u * w4);
+    const float4 *s4 = reinterpret_cast<const float4 *>(score + u * ratio * width) + c;
+    const float4 *k4 = reinterpret_cast<const float4 *>(kv + u * ratio * width) + c;
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    float m[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
+    for (int r = 0; r < ratio; ++r) {
+        const float4 s = __ldg(s4 + static_cast<long long>(r) * w4);
+        m[0] = fmaxf(m[0], s.x);
+        m[1] = fmaxf(m[1], s.y);
+        m[2] = fmaxf(m[2], s.z);
+        m[3] = fmaxf(m[3], s.w);
+    }
+    float num[4] = {0.f, 0.f, 0.f, 0.f}, den[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int r = 0; r < ratio; ++r) {
+        const float4 s = __ldg(s4 + static_cast<long long>(r) * w4);
+        const float4 k = __ldg(k4 + static_cast<long long>(r) * w4);
+        const float sv[4] = {s.x, s.y, s.z, s.w}, kvv[4] = {k.x, k.y, k.z, k.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (m[i] > NEG_INF) {
+                const float e = expf(sv[i] - m[i]);
+                den[i] += e;
+                num[i] += e * kvv[i];
+            }
+        }
+    }
+    float4 o;
+    o.x = den[0] > 0.f ? num[0] / den[0] : 0.f;
+    o.y = den[1] > 0.f ? num[1] / den[1] : 0.f;
+    o.z = den[2] > 0.f ? num[2] / den[2] : 0.f;
+    o.w = den[3] > 0.f ? num[3] / den[3] : 0.f;
+    reinterpret_cast<float4 *>(out + u * width)[c] = o;
+}
+
+}  // namespace
+
+cudaError_t launch_kv_push_raw(const float *kv, uint16_t *raw, long long raw_unit_stride, const int32_t *pos,
+                               int32_t *n_raw, int U, uint32_t *status, cudaStream_t s) {
+    kv_push_raw_kernel<<<U, kPushThreads, 0, s>>>(kv, raw, raw_unit_stride, pos, n_raw, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_compressor_pool(const float *kv, const float *score, int ratio, int width, float *out, int U,
+                                   cudaStream_t s) {
+    const long long threads = static_cast<long long>(U) * (width >> 2);
+    const long long blocks = (threads + kPoolThreads - 1) / kPoolThreads;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    compressor_pool_kernel<<<static_cast<unsigned>(blocks), kPoolThreads, 0, s>>>(kv, score, ratio, width, out, U);
+    return cudaGetLastError();
+}
+
+}  // namespace ds4a

@@ -4,6 +4,8 @@ DecodeStep: U units (sequence x layer caches), one query each.
 PrefillStep: one chunk of T queries of one sequence over a causal row store.
 DenseStep: the ratio-128 layers' attention over all compressed rows (no
 indexer, so no score or select).
+ProducerStep: the cache producer at a ratio boundary: the raw-window push of
+the new token and the compressor pooling of the frontier.
 
 Both own their outputs and workspaces (allocated once, reused every call, so a
 call can be captured in a CUDA graph) and run indexer score -> top-k select ->
@@ -100,4 +102,21 @@ class DenseStep:
 
     def __call__(self, x, scale=DEFAULT_SCALE, stream=None):
         self.attend(x, scale, stream)
+        return self.out
+
+
+class ProducerStep:
+    def __init__(self, U, width=B.HEAD_DIM, device="cuda"):
+        self.U, self.width = U, width
+        self.out = torch.empty(U, width, dtype=torch.float32, device=torch.device(device))
+
+    def push(self, x, stream=None):
+        B.ds4a_kv_push_raw(x["row"], x["raw"], x["pos"], x["n_raw"], stream=stream)
+
+    def pool(self, x, stream=None):
+        B.ds4a_compressor_pool(x["kv"], x["score"], self.out, stream=stream)
+
+    def __call__(self, x, stream=None):
+        self.push(x, stream)
+        self.pool(x, stream)
         return self.out

@@ -39,7 +39,8 @@ COMPRESS_RATIO = 4
 @dataclass
 class Workload:
     name: str
-    kind: str              # "decode", "prefill" or "dense" (ratio-128 layers: all rows, no indexer)
+    kind: str              # "decode", "prefill", "dense" (ratio-128 layers: all rows, no indexer)
+                           # or "pool" (cache producer: raw push + compressor pooling; n_rows = ratio)
     units: int             # decode: sequences x layers; prefill: 1
     n_rows: int            # compressed rows per unit (prefill: prior + in-chunk)
     top_k: int = 512
@@ -67,6 +68,10 @@ WORKLOADS = {
     # layers 3..41 of the Flash shape fold 128 tokens into one row and attend to
     # all rows): 32 sequences x 20 layers at 1M tokens of context = 8,192 rows.
     "dense_32x20x8192": Workload("dense_32x20x8192", "dense", 32 * 20, 8192, top_k=0),
+    # Cache producer at a ratio-128 boundary (§3-1, §3-2): for each of 32
+    # sequences x 20 ratio-128 layers, push the new token's raw row and pool
+    # the 128-row (kv, score) frontier of width 512 into one compressed row.
+    "pool_32x20x128": Workload("pool_32x20x128", "pool", 32 * 20, 128, top_k=0),
 }
 
 
@@ -189,3 +194,22 @@ def make_prefill_inputs(T, prior_rows, device="cpu", seed=0, q_scale=1.0):
 def as_u16(t: torch.Tensor):
     """The raw 16-bit storage of a bf16/fp16 tensor as a numpy uint16 array (CPU copy)."""
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view("uint16")
+
+
+def make_pool_inputs(units, ratio, width=HEAD_DIM, device="cpu", seed=0):
+    """Cache-producer inputs: a frontier of `ratio` (kv, score) rows per unit
+    (fp32; kv ~ N(0,1)/sqrt(width), score ~ N(0,1)), the new token's row, a
+    raw ring per unit and the position of the new token (a ratio boundary
+    far into the context)."""
+    dev = torch.device(device)
+    x = {}
+    x["kv"] = torch.empty(units, ratio, width, dtype=torch.float32, device=dev)
+    normal_fill_(x["kv"], width, seed, 11)
+    x["score"] = torch.empty(units, ratio, width, dtype=torch.float32, device=dev)
+    normal_fill_(x["score"], 1, seed, 12)
+    x["row"] = torch.empty(units, width, dtype=torch.float32, device=dev)
+    normal_fill_(x["row"], width, seed, 13)
+    x["raw"] = torch.zeros(units, N_SWA, HEAD_DIM, dtype=torch.float16, device=dev)
+    x["n_raw"] = torch.full((units,), N_SWA, dtype=torch.int32, device=dev)
+    x["pos"] = torch.full((units,), 128 * 8191 - 1, dtype=torch.int32, device=dev)
+    return x

@@ -271,6 +271,48 @@ ds4a_status ds4a_sparse_attn_prefill(const uint16_t *q, const int32_t *q_pos,
                                      float scale, float *out, float *lse, int T,
                                      void *ws, size_t ws_bytes, void *stream);
 
+/*
+ * 4a. Raw-window push (§3-1: the raw tier keeps the K/V rows of the last 128
+ *    tokens at high precision, each rounded through f16).  For each unit u,
+ *    the row kv[u] of the token at position pos[u] is rounded to f16 (round
+ *    to nearest even; overflow gives +-inf) and written to ring slot
+ *    pos[u] % 128, and n_raw[u] = min(pos[u] + 1, 128).  Pushing positions
+ *    0, 1, 2, ... leaves the ring holding the last min(P, 128) rows, the same
+ *    rows as the pages' oldest-first window (which slides its rows down one
+ *    slot when full), in rotated order; 3a attends to the valid slots in any
+ *    order.
+ *
+ *    kv      fp32 [U][512] (device).
+ *    raw     fp16 [U][128][512] ring; unit u at raw + u*raw_unit_stride (device).
+ *    pos     int32 [U] (device): position of each unit's new row; a negative
+ *            position sets DS4A_DEV_BOUNDS and writes nothing for that unit.
+ *    n_raw   int32 [U] (device, written).
+ *    kv and raw must be 16-byte aligned; with U > 1, raw_unit_stride is a
+ *    multiple of 512 elements and at least 128 rows.
+ */
+ds4a_status ds4a_kv_push_raw(const float *kv, uint16_t *raw, int64_t raw_unit_stride,
+                             const int32_t *pos, int32_t *n_raw, int U, void *stream);
+
+/*
+ * 4b. Compressor pooling (§3-2: the compressor folds a frontier of `ratio`
+ *    token rows, 4 in the ratio-4 layers and 128 in the ratio-128 layers,
+ *    into one compressed row by a softmax of learned scores).  For each unit
+ *    u and column j, over the frontier rows r < ratio:
+ *
+ *      m = max_r score[u,r,j]
+ *      out[u,j] = sum_r e^(score[u,r,j] - m) kv[u,r,j] / sum_r e^(score[u,r,j] - m)
+ *
+ *    and out[u,j] = 0 when no score of the column is finite.  fp32 throughout.
+ *    The projections that produce kv and score, the positional bias added to
+ *    the scores and the steps after pooling (normalisation, RoPE, FP8 round
+ *    trip) need trained weights and are not part of this library.
+ *
+ *    kv, score  fp32 [U][ratio][width] (device).    out  fp32 [U][width] (device).
+ *    ratio >= 1; width a positive multiple of 4; pointers 16-byte aligned.
+ */
+ds4a_status ds4a_compressor_pool(const float *kv, const float *score, int ratio, int width,
+                                 float *out, int U, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
