@@ -41,10 +41,13 @@ __global__ void __launch_bounds__(kPushThreads) kv_push_raw_kernel(const float *
     if (threadIdx.x == 0) n_raw[u] = p + 1 < kNSwa ? p + 1 : kNSwa;
 }
 
-// One thread pools 4 consecutive columns of one unit: the column max over the
-// frontier rows, then the exp-weighted sums (the second pass mostly reads the
-// scores back from cache).  A column with no finite score gives 0.
-constexpr int kPoolThreads = 256;
+// One thread pools 4 consecutive columns of one unit in a single pass over
+// the frontier, eight rows of loads in flight at a time: the running column
+// max is raised per group of eight rows (the sums so far are rescaled by
+// e^(old max - new max)), then the group's weights e^(s - max) are added.  A
+// column with no finite score gives 0.
+constexpr int kPoolThreads = 64;
+constexpr int kPoolGroup = 8;
 
 __global__ void __launch_bounds__(kPoolThreads) compressor_pool_kernel(const float *__restrict__ kv,
                                                                        const float *__restrict__ score, int ratio,
@@ -58,24 +61,44 @@ __global__ void __launch_bounds__(kPoolThreads) compressor_pool_kernel(const flo
     const float4 *k4 = reinterpret_cast<const float4 *>(kv + u * ratio * width) + c;
     const float NEG_INF = -__int_as_float(0x7f800000);
     float m[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
-    for (int r = 0; r < ratio; ++r) {
-        const float4 s = __ldg(s4 + static_cast<long long>(r) * w4);
-        m[0] = fmaxf(m[0], s.x);
-        m[1] = fmaxf(m[1], s.y);
-        m[2] = fmaxf(m[2], s.z);
-        m[3] = fmaxf(m[3], s.w);
-    }
     float num[4] = {0.f, 0.f, 0.f, 0.f}, den[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int r = 0; r < ratio; ++r) {
-        const float4 s = __ldg(s4 + static_cast<long long>(r) * w4);
-        const float4 k = __ldg(k4 + static_cast<long long>(r) * w4);
-        const float sv[4] = {s.x, s.y, s.z, s.w}, kvv[4] = {k.x, k.y, k.z, k.w};
+    for (int r0 = 0; r0 < ratio; r0 += kPoolGroup) {
+        const int n = ratio - r0 < kPoolGroup ? ratio - r0 : kPoolGroup;
+        float4 s[kPoolGroup], k[kPoolGroup];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if (m[i] > NEG_INF) {
-                const float e = expf(sv[i] - m[i]);
-                den[i] += e;
-                num[i] += e * kvv[i];
+        for (int i = 0; i < kPoolGroup; ++i) {
+            if (i < n) {
+                s[i] = __ldg(s4 + static_cast<long long>(r0 + i) * w4);
+                k[i] = __ldg(k4 + static_cast<long long>(r0 + i) * w4);
+            } else {
+                s[i] = make_float4(NEG_INF, NEG_INF, NEG_INF, NEG_INF);
+                k[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+#pragma unroll
+        for (int col = 0; col < 4; ++col) {
+            float sv[kPoolGroup], kvv[kPoolGroup];
+#pragma unroll
+            for (int i = 0; i < kPoolGroup; ++i) {
+                sv[i] = col == 0 ? s[i].x : col == 1 ? s[i].y : col == 2 ? s[i].z : s[i].w;
+                kvv[i] = col == 0 ? k[i].x : col == 1 ? k[i].y : col == 2 ? k[i].z : k[i].w;
+            }
+            float gm = sv[0];
+#pragma unroll
+            for (int i = 1; i < kPoolGroup; ++i) gm = fmaxf(gm, sv[i]);
+            if (gm > m[col]) {
+                const float a = m[col] > NEG_INF ? expf(m[col] - gm) : 0.f;
+                num[col] *= a;
+                den[col] *= a;
+                m[col] = gm;
+            }
+            if (m[col] > NEG_INF) {
+#pragma unroll
+                for (int i = 0; i < kPoolGroup; ++i) {
+                    const float e = expf(sv[i] - m[col]);
+                    den[col] += e;
+                    num[col] += e * kvv[i];
+                }
             }
         }
     }
