@@ -142,7 +142,8 @@ def gpu_id_for_smi(torch, dev):
 def decode_bytes(wl):
     """Algorithmic HBM bytes per unit: every indexer key, the selected rows, the
     raw window, q, iq, w, the fp32 output and the selected indices."""
-    per_unit_fixed = wl.top_k * 1024 + 128 * 1024 + 64 * 512 * 2 + 64 * 128 * 2 + 64 * 4 + 64 * 512 * 4 + wl.top_k * 4
+    H = wl.heads
+    per_unit_fixed = wl.top_k * 1024 + 128 * 1024 + H * 512 * 2 + 64 * 128 * 2 + 64 * 4 + H * 512 * 4 + wl.top_k * 4
     ik = wl.n_rows * 128 * 2
     idx_kernel = wl.n_rows * 256 + 64 * 128 * 2 + 64 * 4
     return wl.units * (ik + per_unit_fixed), wl.units * idx_kernel
@@ -216,7 +217,8 @@ class OracleSample:
                 if unit_source is not None:
                     return unit_source(i)
                 x = make_decode_inputs(1, wl.n_rows, device="cpu", seed=wl.seed + 1000 + i,
-                                       heavy_frac=wl.heavy_frac, heavy_scale=wl.heavy_scale, with_indexer=not dense)
+                                       heavy_frac=wl.heavy_frac, heavy_scale=wl.heavy_scale, with_indexer=not dense,
+                                       n_head=wl.heads)
                 d = dict(q=u16(x["q"][0]), rows=u16(x["rows"][0]), raw=u16(x["raw"][0]), n=wl.n_rows, nraw=128)
                 if not dense:
                     d.update(iq=u16(x["iq"][0]), w=x["w"][0].numpy(), ik=u16(x["ik"][0]))
@@ -361,8 +363,8 @@ def main():
     seed = wl.seed + rank
     if wl.kind == "decode":
         x = make_decode_inputs(wl.units, wl.n_rows, device=dev, seed=seed, heavy_frac=wl.heavy_frac,
-                               heavy_scale=wl.heavy_scale)
-        step = pkg.DecodeStep(wl.units, wl.n_rows, wl.top_k, device=dev)
+                               heavy_scale=wl.heavy_scale, n_head=wl.heads)
+        step = pkg.DecodeStep(wl.units, wl.n_rows, wl.top_k, device=dev, n_head=wl.heads)
     elif wl.kind == "dense":
         x = make_decode_inputs(wl.units, wl.n_rows, device=dev, seed=seed, with_indexer=False)
         step = pkg.DenseStep(wl.units, wl.n_rows, device=dev)
@@ -458,12 +460,12 @@ def main():
         launches_per_step = 1 + (1 if pkg.ds4a_workspace_bytes(4, wl.units, 1, wl.n_rows, 0) else 0)
     else:
         launches_per_step = 1 + 1 + 1 + (1 if pkg.ds4a_workspace_bytes(
-            2 if wl.kind == "decode" else 3, wl.units if wl.kind == "decode" else 1,
+            (2 if wl.kind == "decode" else 3) | (0x100 if wl.heads == 128 else 0), wl.units if wl.kind == "decode" else 1,
             1 if wl.kind == "decode" else wl.queries, wl.n_rows, wl.top_k) else 0)
         if wl.units * wl.queries < 152:
             launches_per_step += 2            # top-k: histogram and filter passes before the final one
     cfg = {"workload": wl.name, "units": wl.units, "queries_per_unit": wl.queries, "rows_per_unit": wl.n_rows,
-           "top_k": wl.top_k if wl.kind != "dense" else "all rows", "raw_window": 128, "heads": 64,
+           "top_k": wl.top_k if wl.kind != "dense" else "all rows", "raw_window": 128, "heads": wl.heads,
            "head_dim": 512, "indexer": "64x128" if wl.kind != "dense" else "none (ratio-128 layer)",
            "l2": "inputs exceed the L2 many times over; no flush", "parallelism": f"replicas x{world}",
            "peak_source": pk["src"]}

@@ -27,6 +27,7 @@ DS4A_OP_TOPK_SELECT = 1
 DS4A_OP_SPARSE_ATTN_DECODE = 2
 DS4A_OP_SPARSE_ATTN_PREFILL = 3
 DS4A_OP_DENSE_ATTN_DECODE = 4
+DS4A_OP_FLAG_128_HEADS = 0x100
 
 N_HEAD, HEAD_DIM, N_IDX_HEAD, IDX_DIM, N_SWA = 64, 512, 64, 128, 128
 
@@ -34,7 +35,8 @@ N_HEAD, HEAD_DIM, N_IDX_HEAD, IDX_DIM, N_SWA = 64, 512, 64, 128, 128
 EXPORTS = ("ds4a_strerror", "ds4a_version", "ds4a_workspace_bytes", "ds4a_get_device_status",
            "ds4a_debug_inject_error", "ds4a_indexer_score", "ds4a_topk_select",
            "ds4a_topk_select_noalloc", "ds4a_sparse_attn_decode", "ds4a_sparse_attn_prefill",
-           "ds4a_dense_attn_decode", "ds4a_kv_push_raw", "ds4a_compressor_pool")
+           "ds4a_dense_attn_decode", "ds4a_kv_push_raw", "ds4a_compressor_pool",
+           "ds4a_sparse_attn_decode_heads", "ds4a_sparse_attn_prefill_heads", "ds4a_dense_attn_decode_heads")
 DS4A_TOPK_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -91,6 +93,12 @@ def load(build_if_missing: bool = True):
     L.ds4a_sparse_attn_prefill.argtypes = [_vp, _vp, _vp, _i32, _vp, _vp, _i32, _vp, _i32, _i32, _f32, _vp, _vp,
                                            _i32, _vp, _sz, _vp]
     L.ds4a_sparse_attn_prefill.restype = _i32
+    L.ds4a_sparse_attn_decode_heads.argtypes = [_i32] + L.ds4a_sparse_attn_decode.argtypes
+    L.ds4a_sparse_attn_decode_heads.restype = _i32
+    L.ds4a_sparse_attn_prefill_heads.argtypes = [_i32] + L.ds4a_sparse_attn_prefill.argtypes
+    L.ds4a_sparse_attn_prefill_heads.restype = _i32
+    L.ds4a_dense_attn_decode_heads.argtypes = [_i32] + L.ds4a_dense_attn_decode.argtypes
+    L.ds4a_dense_attn_decode_heads.restype = _i32
     _lib = L
     return L
 
@@ -212,9 +220,18 @@ def ds4a_topk_select_noalloc(scores, n_rows, top_k, idx, count, stream=None):
 
 
 def ds4a_sparse_attn_decode(q, rows, idx, count, raw, n_raw, scale, out, lse=None, ws=None, stream=None):
-    """q bf16 [U,64,512]; rows bf16 [U,N_cap,512]; idx i32 [U,top_k]; count i32
-    [U]; raw fp16 [U,128,512]; n_raw i32 [U]; out f32 [U,64,512]; lse f32
-    [U,64] or None; ws uint8 workspace or None."""
+    """The 64-head call (see ds4a_sparse_attn_decode_heads)."""
+    if q.dim() == 3 and q.shape[1] != N_HEAD:
+        raise ValueError("q: 64 heads (use ds4a_sparse_attn_decode_heads for 128)")
+    ds4a_sparse_attn_decode_heads(N_HEAD, q, rows, idx, count, raw, n_raw, scale, out, lse, ws, stream)
+
+
+def ds4a_sparse_attn_decode_heads(n_head, q, rows, idx, count, raw, n_raw, scale, out, lse=None, ws=None,
+                                  stream=None):
+    """q bf16 [U,H,512] (H = 64, or 128 through ds4a_sparse_attn_decode_heads);
+    rows bf16 [U,N_cap,512]; idx i32 [U,top_k]; count i32 [U]; raw fp16
+    [U,128,512]; n_raw i32 [U]; out f32 [U,H,512]; lse f32 [U,H] or None; ws
+    uint8 workspace or None."""
     _req(q, "q", torch.bfloat16)
     _req(idx, "idx", torch.int32)
     _req(count, "count", torch.int32)
@@ -228,19 +245,28 @@ def ds4a_sparse_attn_decode(q, rows, idx, count, raw, n_raw, scale, out, lse=Non
         raise ValueError("raw: fp16 CUDA tensor [U, 128, 512] with contiguous rows")
     U = q.shape[0]
     top_k = idx.shape[1]
-    if q.shape != (U, N_HEAD, HEAD_DIM) or rows.shape[0] != U or idx.shape[0] != U or count.shape != (U,) \
-            or raw.shape[0] != U or n_raw.shape != (U,) or out.shape != (U, N_HEAD, HEAD_DIM):
+    if q.shape != (U, n_head, HEAD_DIM) or rows.shape[0] != U or idx.shape[0] != U or count.shape != (U,) \
+            or raw.shape[0] != U or n_raw.shape != (U,) or out.shape != (U, n_head, HEAD_DIM):
         raise ValueError("shape mismatch")
     if lse is not None:
         _req(lse, "lse", torch.float32)
-    st = load().ds4a_sparse_attn_decode(_ptr(q), _ptr(rows), rows.stride(0), rows.shape[1], _ptr(idx),
+        if lse.shape != (U, n_head):
+            raise ValueError("lse: [U, n_head]")
+    st = load().ds4a_sparse_attn_decode_heads(int(n_head), _ptr(q), _ptr(rows), rows.stride(0), rows.shape[1], _ptr(idx),
                                         _ptr(count), top_k, _ptr(raw), raw.stride(0), _ptr(n_raw), float(scale),
                                         _ptr(out), _ptr(lse), U, _ptr(ws),
                                         ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream))
-    _check(st, "ds4a_sparse_attn_decode")
+    _check(st, "ds4a_sparse_attn_decode_heads")
 
 
 def ds4a_dense_attn_decode(q, rows, n_rows, raw, n_raw, scale, out, lse=None, ws=None, stream=None):
+    """The 64-head call (see ds4a_dense_attn_decode_heads)."""
+    if q.dim() == 3 and q.shape[1] != N_HEAD:
+        raise ValueError("q: 64 heads (use ds4a_dense_attn_decode_heads for 128)")
+    ds4a_dense_attn_decode_heads(N_HEAD, q, rows, n_rows, raw, n_raw, scale, out, lse, ws, stream)
+
+
+def ds4a_dense_attn_decode_heads(n_head, q, rows, n_rows, raw, n_raw, scale, out, lse=None, ws=None, stream=None):
     """q bf16 [U,64,512]; rows bf16 [U,N_cap,512]; n_rows i32 [U]; raw fp16
     [U,128,512]; n_raw i32 [U]; out f32 [U,64,512]; lse f32 [U,64] or None;
     ws uint8 workspace or None."""
@@ -255,18 +281,28 @@ def ds4a_dense_attn_decode(q, rows, n_rows, raw, n_raw, scale, out, lse=None, ws
             or raw.stride(1) != HEAD_DIM or raw.shape[1] != N_SWA:
         raise ValueError("raw: fp16 CUDA tensor [U, 128, 512] with contiguous rows")
     U = q.shape[0]
-    if q.shape != (U, N_HEAD, HEAD_DIM) or rows.shape[0] != U or n_rows.shape != (U,) or raw.shape[0] != U \
-            or n_raw.shape != (U,) or out.shape != (U, N_HEAD, HEAD_DIM):
+    if q.shape != (U, n_head, HEAD_DIM) or rows.shape[0] != U or n_rows.shape != (U,) or raw.shape[0] != U \
+            or n_raw.shape != (U,) or out.shape != (U, n_head, HEAD_DIM):
         raise ValueError("shape mismatch")
     if lse is not None:
         _req(lse, "lse", torch.float32)
-    st = load().ds4a_dense_attn_decode(_ptr(q), _ptr(rows), rows.stride(0), rows.shape[1], _ptr(n_rows), _ptr(raw),
+        if lse.shape != (U, n_head):
+            raise ValueError("lse: [U, n_head]")
+    st = load().ds4a_dense_attn_decode_heads(int(n_head), _ptr(q), _ptr(rows), rows.stride(0), rows.shape[1], _ptr(n_rows), _ptr(raw),
                                        raw.stride(0), _ptr(n_raw), float(scale), _ptr(out), _ptr(lse), U, _ptr(ws),
                                        ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream))
-    _check(st, "ds4a_dense_attn_decode")
+    _check(st, "ds4a_dense_attn_decode_heads")
 
 
 def ds4a_sparse_attn_prefill(q, q_pos, rows, idx, count, raw, raw_pos0, scale, out, lse=None, ws=None, stream=None):
+    """The 64-head call (see ds4a_sparse_attn_prefill_heads)."""
+    if q.dim() == 3 and q.shape[1] != N_HEAD:
+        raise ValueError("q: 64 heads (use ds4a_sparse_attn_prefill_heads for 128)")
+    ds4a_sparse_attn_prefill_heads(N_HEAD, q, q_pos, rows, idx, count, raw, raw_pos0, scale, out, lse, ws, stream)
+
+
+def ds4a_sparse_attn_prefill_heads(n_head, q, q_pos, rows, idx, count, raw, raw_pos0, scale, out, lse=None, ws=None,
+                                   stream=None):
     """q bf16 [T,64,512]; q_pos i32 [T]; rows bf16 [N_cap,512]; idx i32
     [T,top_k]; count i32 [T]; raw fp16 [n_raw_rows,512] (row i = position
     raw_pos0 + i); out f32 [T,64,512]; lse f32 [T,64] or None."""
@@ -279,17 +315,19 @@ def ds4a_sparse_attn_prefill(q, q_pos, rows, idx, count, raw, raw_pos0, scale, o
     _req(out, "out", torch.float32)
     T = q.shape[0]
     top_k = idx.shape[1]
-    if q.shape != (T, N_HEAD, HEAD_DIM) or q_pos.shape != (T,) or rows.dim() != 2 or rows.shape[1] != HEAD_DIM \
+    if q.shape != (T, n_head, HEAD_DIM) or q_pos.shape != (T,) or rows.dim() != 2 or rows.shape[1] != HEAD_DIM \
             or idx.shape[0] != T or count.shape != (T,) or raw.dim() != 2 or raw.shape[1] != HEAD_DIM \
-            or out.shape != (T, N_HEAD, HEAD_DIM):
+            or out.shape != (T, n_head, HEAD_DIM):
         raise ValueError("shape mismatch")
     if lse is not None:
         _req(lse, "lse", torch.float32)
-    st = load().ds4a_sparse_attn_prefill(_ptr(q), _ptr(q_pos), _ptr(rows), rows.shape[0], _ptr(idx), _ptr(count),
+        if lse.shape != (T, n_head):
+            raise ValueError("lse: [T, n_head]")
+    st = load().ds4a_sparse_attn_prefill_heads(int(n_head), _ptr(q), _ptr(q_pos), _ptr(rows), rows.shape[0], _ptr(idx), _ptr(count),
                                          top_k, _ptr(raw), int(raw_pos0), raw.shape[0], float(scale), _ptr(out),
                                          _ptr(lse), T, _ptr(ws),
                                          ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream))
-    _check(st, "ds4a_sparse_attn_prefill")
+    _check(st, "ds4a_sparse_attn_prefill_heads")
 
 
 def ds4a_kv_push_raw(kv, raw, pos, n_raw, stream=None):

@@ -131,6 +131,14 @@ int ds4a_version(void) { return (1 << 16) | 0; }
 
 size_t ds4a_workspace_bytes(int op, int U, int Q, int N_cap, int top_k) {
     if (U < 1 || Q < 1 || N_cap < 1) return static_cast<size_t>(-1);
+    // 128 heads run as two 64-head sub-units per unit (the attention ops only)
+    const int h = (op & DS4A_OP_FLAG_128_HEADS) ? 2 : 1;
+    op &= ~DS4A_OP_FLAG_128_HEADS;
+    if (h == 2 && op != DS4A_OP_SPARSE_ATTN_DECODE && op != DS4A_OP_SPARSE_ATTN_PREFILL &&
+        op != DS4A_OP_DENSE_ATTN_DECODE)
+        return static_cast<size_t>(-1);
+    if (static_cast<long long>(U) * h > 0x7fffffffLL) return static_cast<size_t>(-1);
+    U *= h;
     switch (op) {
     case DS4A_OP_INDEXER_SCORE: return 0;
     case DS4A_OP_TOPK_SELECT:
@@ -237,11 +245,12 @@ ds4a_status check_attn_common(const uint16_t *q, const uint16_t *rows, int N_cap
 namespace {
 // Decode attention over an explicit row list (idx, count, top_k) or, with
 // idx == nullptr, over rows 0 .. count[u]-1 (count = n_rows, top_k = N_cap).
-ds4a_status attn_decode(const uint16_t *q, const uint16_t *rows, int64_t rows_unit_stride, int N_cap,
+ds4a_status attn_decode(int hsplit, const uint16_t *q, const uint16_t *rows, int64_t rows_unit_stride, int N_cap,
                         const int32_t *idx, const int32_t *count, int top_k, const uint16_t *raw,
                         int64_t raw_unit_stride, const int32_t *n_raw, float scale, float *out, float *lse, int U,
                         void *ws, size_t ws_bytes, void *stream) {
     if (!raw || !n_raw || U < 1) return DS4A_EINVAL;
+    if (static_cast<long long>(U) * hsplit * kNHead >= (1LL << 31)) return DS4A_EINVAL;
     if (!aligned(raw, 16)) return DS4A_EINVAL;
     if (U > 1 && (rows_unit_stride < static_cast<int64_t>(N_cap) * kHeadDim || rows_unit_stride % kHeadDim ||
                   raw_unit_stride < static_cast<int64_t>(kNSwa) * kHeadDim || raw_unit_stride % kHeadDim))
@@ -253,7 +262,7 @@ ds4a_status attn_decode(const uint16_t *q, const uint16_t *rows, int64_t rows_un
     if (total_rows >= (1LL << 31) || total_raw >= (1LL << 31) || static_cast<long long>(U) * kNHead >= (1LL << 31))
         return DS4A_EINVAL;
     if (!(scale == scale)) return DS4A_EINVAL;
-    const size_t need = attn_ws_bytes(U, top_k);
+    const size_t need = attn_ws_bytes(U * hsplit, top_k);
     if (need && (!ws || ws_bytes < need || !aligned(ws, 256))) return DS4A_EWORKSPACE;
     DevInfo *di = nullptr;
     if (ds4a_status st = current_device(&di)) return st;
@@ -272,12 +281,13 @@ ds4a_status attn_decode(const uint16_t *q, const uint16_t *rows, int64_t rows_un
     a.scale = scale;
     a.out = out;
     a.lse = lse;
-    a.units = U;
+    a.units = U * hsplit;
+    a.hsplit = hsplit;
     a.ws = ws;
     a.status = di->status;
     a.rows_per_unit = rows_per_unit;
     a.raw_per_unit = raw_per_unit;
-    if (!encode_2d_sw128(&a.tm_q, false, q, kHeadDim, static_cast<unsigned long long>(U) * kNHead, 64, 64))
+    if (!encode_2d_sw128(&a.tm_q, false, q, kHeadDim, static_cast<unsigned long long>(U) * hsplit * kNHead, 64, 64))
         return DS4A_EINVAL;
     a.tma_rows = encode_2d_sw128(&a.tm_rows, false, rows, kHeadDim, static_cast<unsigned long long>(total_rows), 64, 64);
     a.tma_raw = encode_2d_sw128(&a.tm_raw, true, raw, kHeadDim, static_cast<unsigned long long>(total_raw), 64, 64);
@@ -285,37 +295,61 @@ ds4a_status attn_decode(const uint16_t *q, const uint16_t *rows, int64_t rows_un
 }
 }  // namespace
 
+ds4a_status ds4a_sparse_attn_decode_heads(int n_head, const uint16_t *q, const uint16_t *rows,
+                                          int64_t rows_unit_stride, int N_cap, const int32_t *idx,
+                                          const int32_t *count, int top_k, const uint16_t *raw,
+                                          int64_t raw_unit_stride, const int32_t *n_raw, float scale, float *out,
+                                          float *lse, int U, void *ws, size_t ws_bytes, void *stream) {
+    if (ds4a_status inj = take_injected()) return inj;
+    if (n_head != 64 && n_head != 128) return DS4A_EUNSUPPORTED;
+    if (ds4a_status st = check_attn_common(q, rows, N_cap, idx, count, top_k, out)) return st;
+    return attn_decode(n_head / kNHead, q, rows, rows_unit_stride, N_cap, idx, count, top_k, raw, raw_unit_stride,
+                       n_raw, scale, out, lse, U, ws, ws_bytes, stream);
+}
+
 ds4a_status ds4a_sparse_attn_decode(const uint16_t *q, const uint16_t *rows, int64_t rows_unit_stride, int N_cap,
                                     const int32_t *idx, const int32_t *count, int top_k, const uint16_t *raw,
                                     int64_t raw_unit_stride, const int32_t *n_raw, float scale, float *out,
                                     float *lse, int U, void *ws, size_t ws_bytes, void *stream) {
+    return ds4a_sparse_attn_decode_heads(64, q, rows, rows_unit_stride, N_cap, idx, count, top_k, raw,
+                                         raw_unit_stride, n_raw, scale, out, lse, U, ws, ws_bytes, stream);
+}
+
+ds4a_status ds4a_dense_attn_decode_heads(int n_head, const uint16_t *q, const uint16_t *rows,
+                                         int64_t rows_unit_stride, int N_cap, const int32_t *n_rows,
+                                         const uint16_t *raw, int64_t raw_unit_stride, const int32_t *n_raw,
+                                         float scale, float *out, float *lse, int U, void *ws, size_t ws_bytes,
+                                         void *stream) {
     if (ds4a_status inj = take_injected()) return inj;
-    if (ds4a_status st = check_attn_common(q, rows, N_cap, idx, count, top_k, out)) return st;
-    return attn_decode(q, rows, rows_unit_stride, N_cap, idx, count, top_k, raw, raw_unit_stride, n_raw, scale, out,
-                       lse, U, ws, ws_bytes, stream);
+    if (n_head != 64 && n_head != 128) return DS4A_EUNSUPPORTED;
+    if (!q || !rows || !n_rows || !out || N_cap < 1) return DS4A_EINVAL;
+    if (!aligned(q, 16) || !aligned(rows, 16) || !aligned(out, 16)) return DS4A_EINVAL;
+    return attn_decode(n_head / kNHead, q, rows, rows_unit_stride, N_cap, nullptr, n_rows, N_cap, raw,
+                       raw_unit_stride, n_raw, scale, out, lse, U, ws, ws_bytes, stream);
 }
 
 ds4a_status ds4a_dense_attn_decode(const uint16_t *q, const uint16_t *rows, int64_t rows_unit_stride, int N_cap,
                                    const int32_t *n_rows, const uint16_t *raw, int64_t raw_unit_stride,
                                    const int32_t *n_raw, float scale, float *out, float *lse, int U, void *ws,
                                    size_t ws_bytes, void *stream) {
-    if (ds4a_status inj = take_injected()) return inj;
-    if (!q || !rows || !n_rows || !out || N_cap < 1) return DS4A_EINVAL;
-    if (!aligned(q, 16) || !aligned(rows, 16) || !aligned(out, 16)) return DS4A_EINVAL;
-    return attn_decode(q, rows, rows_unit_stride, N_cap, nullptr, n_rows, N_cap, raw, raw_unit_stride, n_raw, scale,
-                       out, lse, U, ws, ws_bytes, stream);
+    return ds4a_dense_attn_decode_heads(64, q, rows, rows_unit_stride, N_cap, n_rows, raw, raw_unit_stride, n_raw,
+                                        scale, out, lse, U, ws, ws_bytes, stream);
 }
 
-ds4a_status ds4a_sparse_attn_prefill(const uint16_t *q, const int32_t *q_pos, const uint16_t *rows, int N_cap,
-                                     const int32_t *idx, const int32_t *count, int top_k, const uint16_t *raw,
-                                     int32_t raw_pos0, int n_raw_rows, float scale, float *out, float *lse, int T,
-                                     void *ws, size_t ws_bytes, void *stream) {
+ds4a_status ds4a_sparse_attn_prefill_heads(int n_head, const uint16_t *q, const int32_t *q_pos,
+                                           const uint16_t *rows, int N_cap, const int32_t *idx,
+                                           const int32_t *count, int top_k, const uint16_t *raw, int32_t raw_pos0,
+                                           int n_raw_rows, float scale, float *out, float *lse, int T, void *ws,
+                                           size_t ws_bytes, void *stream) {
     if (ds4a_status inj = take_injected()) return inj;
+    if (n_head != 64 && n_head != 128) return DS4A_EUNSUPPORTED;
+    const int hsplit = n_head / kNHead;
     if (ds4a_status st = check_attn_common(q, rows, N_cap, idx, count, top_k, out)) return st;
     if (!q_pos || T < 1 || n_raw_rows < 0) return DS4A_EINVAL;
     if (n_raw_rows > 0 && (!raw || !aligned(raw, 16))) return DS4A_EINVAL;
     if (!(scale == scale)) return DS4A_EINVAL;
-    const size_t need = attn_ws_bytes(T, top_k);
+    if (static_cast<long long>(T) * n_head >= (1LL << 31)) return DS4A_EINVAL;
+    const size_t need = attn_ws_bytes(T * hsplit, top_k);
     if (need && (!ws || ws_bytes < need || !aligned(ws, 256))) return DS4A_EWORKSPACE;
     DevInfo *di = nullptr;
     if (ds4a_status st = current_device(&di)) return st;
@@ -336,18 +370,26 @@ ds4a_status ds4a_sparse_attn_prefill(const uint16_t *q, const int32_t *q_pos, co
     a.scale = scale;
     a.out = out;
     a.lse = lse;
-    a.units = T;
+    a.units = T * hsplit;
+    a.hsplit = hsplit;
     a.ws = ws;
     a.status = di->status;
     a.rows_per_unit = 0;
     a.raw_per_unit = 0;
-    if (static_cast<long long>(T) * kNHead >= (1LL << 31)) return DS4A_EINVAL;
-    if (!encode_2d_sw128(&a.tm_q, false, q, kHeadDim, static_cast<unsigned long long>(T) * kNHead, 64, 64))
+    if (!encode_2d_sw128(&a.tm_q, false, q, kHeadDim, static_cast<unsigned long long>(T) * n_head, 64, 64))
         return DS4A_EINVAL;
     a.tma_rows = encode_2d_sw128(&a.tm_rows, false, rows, kHeadDim, static_cast<unsigned long long>(N_cap), 64, 64);
     a.tma_raw = n_raw_rows > 0 &&
                 encode_2d_sw128(&a.tm_raw, true, raw, kHeadDim, static_cast<unsigned long long>(n_raw_rows), 64, 64);
     return launch_sparse_attn(a, di->sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DS4A_OK : DS4A_ECUDA;
+}
+
+ds4a_status ds4a_sparse_attn_prefill(const uint16_t *q, const int32_t *q_pos, const uint16_t *rows, int N_cap,
+                                     const int32_t *idx, const int32_t *count, int top_k, const uint16_t *raw,
+                                     int32_t raw_pos0, int n_raw_rows, float scale, float *out, float *lse, int T,
+                                     void *ws, size_t ws_bytes, void *stream) {
+    return ds4a_sparse_attn_prefill_heads(64, q, q_pos, rows, N_cap, idx, count, top_k, raw, raw_pos0, n_raw_rows,
+                                          scale, out, lse, T, ws, ws_bytes, stream);
 }
 
 ds4a_status ds4a_kv_push_raw(const float *kv, uint16_t *raw, int64_t raw_unit_stride, const int32_t *pos,

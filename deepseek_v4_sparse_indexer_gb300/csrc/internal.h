@@ -75,7 +75,8 @@ struct AttnArgs {
     float scale;
     float *out;                  // [units][64][512]
     float *lse;                  // [units][64] or null
-    int units;
+    int units;                   // 64-head sub-units: row-side units x hsplit
+    int hsplit;                  // 1 (64 heads) or 2 (128 heads: two sub-units per row-side unit)
     void *ws;
     uint32_t *status;
 };

@@ -152,7 +152,8 @@ DS4A_DEV bool wait_drain(uint64_t *bar, uint32_t parity) {
 
 // What one work item covers.
 struct Item {
-    int unit, split;
+    int unit, split;     // unit: 64-head sub-unit (q, out, lse); ru: its row-side unit
+    int ru;
     int cnt;             // selected compressed rows (clamped to [0, top_k])
     int nrw;             // raw rows
     int ct;              // compressed tiles
@@ -165,22 +166,23 @@ DS4A_DEV Item make_item(const AttnArgs &a, int it, int n_split) {
     Item m;
     m.unit = it / n_split;
     m.split = it - m.unit * n_split;
-    int cnt = a.count[m.unit];
+    m.ru = a.hsplit == 2 ? m.unit >> 1 : m.unit;     // 128 heads: two sub-units share the rows
+    int cnt = a.count[m.ru];
     if (m.split == 0 && (cnt < 0 || cnt > a.top_k) && threadIdx.x == 0) report(a.status, DS4A_DEV_BOUNDS);
     cnt = cnt < 0 ? 0 : (cnt > a.top_k ? a.top_k : cnt);
     m.cnt = cnt;
-    m.comp_row0 = static_cast<long long>(m.unit) * a.rows_per_unit;
+    m.comp_row0 = static_cast<long long>(m.ru) * a.rows_per_unit;
     if (a.q_pos) {
-        const long long p = a.q_pos[m.unit];
+        const long long p = a.q_pos[m.ru];
         const long long lo = max(p - (kNSwa - 1) - a.raw_pos0, 0LL);
         const long long hi = min(p - a.raw_pos0, static_cast<long long>(a.n_raw_rows) - 1);
         m.nrw = hi >= lo ? static_cast<int>(hi - lo + 1) : 0;
         m.raw_row0 = m.nrw ? lo : 0;
     } else {
-        int n = a.n_raw[m.unit];
+        int n = a.n_raw[m.ru];
         n = n < 0 ? 0 : (n > kNSwa ? kNSwa : n);
         m.nrw = n;
-        m.raw_row0 = static_cast<long long>(m.unit) * a.raw_per_unit;
+        m.raw_row0 = static_cast<long long>(m.ru) * a.raw_per_unit;
     }
     m.ct = (m.cnt + TR - 1) / TR;
     const int nt = m.ct + (m.nrw + TR - 1) / TR;
@@ -295,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                 if (t < m.ct) {
                     // no idx: the row list is 0 .. count-1 (dense attention)
                     const int jj = t * TR + r;
-                    rv[k] = jj < m.cnt ? (a.idx ? __ldg(a.idx + static_cast<long long>(m.unit) * a.top_k + jj) : jj) : -1;
+                    rv[k] = jj < m.cnt ? (a.idx ? __ldg(a.idx + static_cast<long long>(m.ru) * a.top_k + jj) : jj) : -1;
                 } else {
                     const int jj = (t - m.ct) * TR + r;
                     rv[k] = jj < m.nrw ? jj : -1;

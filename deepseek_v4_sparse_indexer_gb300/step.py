@@ -25,16 +25,17 @@ def _ws(nbytes, device):
 
 
 class DecodeStep:
-    def __init__(self, U, N_cap, top_k=512, device="cuda"):
-        self.U, self.N_cap, self.top_k = U, N_cap, top_k
+    def __init__(self, U, N_cap, top_k=512, device="cuda", n_head=B.N_HEAD):
+        self.U, self.N_cap, self.top_k, self.n_head = U, N_cap, top_k, n_head
         dev = torch.device(device)
+        flag = B.DS4A_OP_FLAG_128_HEADS if n_head == 128 else 0
         self.scores = torch.empty(U, 1, N_cap, dtype=torch.float32, device=dev)
         self.idx = torch.empty(U, 1, top_k, dtype=torch.int32, device=dev)
         self.count = torch.empty(U, 1, dtype=torch.int32, device=dev)
-        self.out = torch.empty(U, B.N_HEAD, B.HEAD_DIM, dtype=torch.float32, device=dev)
-        self.lse = torch.empty(U, B.N_HEAD, dtype=torch.float32, device=dev)
+        self.out = torch.empty(U, n_head, B.HEAD_DIM, dtype=torch.float32, device=dev)
+        self.lse = torch.empty(U, n_head, dtype=torch.float32, device=dev)
         self.ws_topk = _ws(B.ds4a_workspace_bytes(B.DS4A_OP_TOPK_SELECT, U, 1, N_cap, top_k), dev)
-        self.ws_attn = _ws(B.ds4a_workspace_bytes(B.DS4A_OP_SPARSE_ATTN_DECODE, U, 1, N_cap, top_k), dev)
+        self.ws_attn = _ws(B.ds4a_workspace_bytes(B.DS4A_OP_SPARSE_ATTN_DECODE | flag, U, 1, N_cap, top_k), dev)
 
     def score(self, x, stream=None):
         B.ds4a_indexer_score(x["iq"].view(self.U, 1, B.N_IDX_HEAD, B.IDX_DIM),
@@ -45,8 +46,9 @@ class DecodeStep:
         B.ds4a_topk_select(self.scores, x["n_rows"], self.top_k, self.idx, self.count, self.ws_topk, stream=stream)
 
     def attend(self, x, scale=DEFAULT_SCALE, stream=None):
-        B.ds4a_sparse_attn_decode(x["q"], x["rows"], self.idx.view(self.U, self.top_k), self.count.view(self.U),
-                                  x["raw"], x["n_raw"], scale, self.out, self.lse, self.ws_attn, stream=stream)
+        B.ds4a_sparse_attn_decode_heads(self.n_head, x["q"], x["rows"], self.idx.view(self.U, self.top_k),
+                                        self.count.view(self.U), x["raw"], x["n_raw"], scale, self.out, self.lse,
+                                        self.ws_attn, stream=stream)
 
     def __call__(self, x, scale=DEFAULT_SCALE, stream=None):
         self.score(x, stream)
@@ -56,16 +58,17 @@ class DecodeStep:
 
 
 class PrefillStep:
-    def __init__(self, T, N_cap, top_k=512, device="cuda"):
-        self.T, self.N_cap, self.top_k = T, N_cap, top_k
+    def __init__(self, T, N_cap, top_k=512, device="cuda", n_head=B.N_HEAD):
+        self.T, self.N_cap, self.top_k, self.n_head = T, N_cap, top_k, n_head
         dev = torch.device(device)
+        flag = B.DS4A_OP_FLAG_128_HEADS if n_head == 128 else 0
         self.scores = torch.empty(1, T, N_cap, dtype=torch.float32, device=dev)
         self.idx = torch.empty(1, T, top_k, dtype=torch.int32, device=dev)
         self.count = torch.empty(1, T, dtype=torch.int32, device=dev)
-        self.out = torch.empty(T, B.N_HEAD, B.HEAD_DIM, dtype=torch.float32, device=dev)
-        self.lse = torch.empty(T, B.N_HEAD, dtype=torch.float32, device=dev)
+        self.out = torch.empty(T, n_head, B.HEAD_DIM, dtype=torch.float32, device=dev)
+        self.lse = torch.empty(T, n_head, dtype=torch.float32, device=dev)
         self.ws_topk = _ws(B.ds4a_workspace_bytes(B.DS4A_OP_TOPK_SELECT, 1, T, N_cap, top_k), dev)
-        self.ws_attn = _ws(B.ds4a_workspace_bytes(B.DS4A_OP_SPARSE_ATTN_PREFILL, 1, T, N_cap, top_k), dev)
+        self.ws_attn = _ws(B.ds4a_workspace_bytes(B.DS4A_OP_SPARSE_ATTN_PREFILL | flag, 1, T, N_cap, top_k), dev)
 
     def score(self, x, stream=None):
         T, N = self.T, self.N_cap
@@ -77,9 +80,9 @@ class PrefillStep:
         B.ds4a_topk_select(self.scores, x["n_rows"], self.top_k, self.idx, self.count, self.ws_topk, stream=stream)
 
     def attend(self, x, scale=DEFAULT_SCALE, stream=None):
-        B.ds4a_sparse_attn_prefill(x["q"], x["q_pos"], x["rows"], self.idx.view(self.T, self.top_k),
-                                   self.count.view(self.T), x["raw"], x["raw_pos0"], scale, self.out, self.lse,
-                                   self.ws_attn, stream=stream)
+        B.ds4a_sparse_attn_prefill_heads(self.n_head, x["q"], x["q_pos"], x["rows"], self.idx.view(self.T, self.top_k),
+                                         self.count.view(self.T), x["raw"], x["raw_pos0"], scale, self.out,
+                                         self.lse, self.ws_attn, stream=stream)
 
     def __call__(self, x, scale=DEFAULT_SCALE, stream=None):
         self.score(x, stream)
@@ -89,16 +92,17 @@ class PrefillStep:
 
 
 class DenseStep:
-    def __init__(self, U, N_cap, device="cuda"):
-        self.U, self.N_cap = U, N_cap
+    def __init__(self, U, N_cap, device="cuda", n_head=B.N_HEAD):
+        self.U, self.N_cap, self.n_head = U, N_cap, n_head
         dev = torch.device(device)
-        self.out = torch.empty(U, B.N_HEAD, B.HEAD_DIM, dtype=torch.float32, device=dev)
-        self.lse = torch.empty(U, B.N_HEAD, dtype=torch.float32, device=dev)
-        self.ws_attn = _ws(B.ds4a_workspace_bytes(B.DS4A_OP_DENSE_ATTN_DECODE, U, 1, N_cap, 0), dev)
+        flag = B.DS4A_OP_FLAG_128_HEADS if n_head == 128 else 0
+        self.out = torch.empty(U, n_head, B.HEAD_DIM, dtype=torch.float32, device=dev)
+        self.lse = torch.empty(U, n_head, dtype=torch.float32, device=dev)
+        self.ws_attn = _ws(B.ds4a_workspace_bytes(B.DS4A_OP_DENSE_ATTN_DECODE | flag, U, 1, N_cap, 0), dev)
 
     def attend(self, x, scale=DEFAULT_SCALE, stream=None):
-        B.ds4a_dense_attn_decode(x["q"], x["rows"], x["n_rows"], x["raw"], x["n_raw"], scale, self.out, self.lse,
-                                 self.ws_attn, stream=stream)
+        B.ds4a_dense_attn_decode_heads(self.n_head, x["q"], x["rows"], x["n_rows"], x["raw"], x["n_raw"], scale,
+                                       self.out, self.lse, self.ws_attn, stream=stream)
 
     def __call__(self, x, scale=DEFAULT_SCALE, stream=None):
         self.attend(x, scale, stream)

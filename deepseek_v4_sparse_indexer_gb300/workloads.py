@@ -48,6 +48,7 @@ class Workload:
     heavy_frac: float = 0.0
     heavy_scale: float = 4.0
     seed: int = 0
+    heads: int = 64        # query heads (64 Flash, 128 Pro)
     extra: dict = field(default_factory=dict)
 
     @property
@@ -68,6 +69,11 @@ WORKLOADS = {
     # layers 3..41 of the Flash shape fold 128 tokens into one row and attend to
     # all rows): 32 sequences x 20 layers at 1M tokens of context = 8,192 rows.
     "dense_32x20x8192": Workload("dense_32x20x8192", "dense", 32 * 20, 8192, top_k=0),
+    # Pro shape ("DwarfStar(ds4.c) のアーキテクチャを読む" §2: 128 heads, indexer
+    # top_k 1,024; 61 layers, of which the even layers 2..60 are ratio-4
+    # indexer layers): 16 sequences x 30 layers at depth 65,536 rows.
+    "pro_decode_16x30x65536": Workload("pro_decode_16x30x65536", "decode", 16 * 30, 65536, top_k=1024,
+                                       heads=128),
     # Cache producer at a ratio-128 boundary (§3-1, §3-2): for each of 32
     # sequences x 20 ratio-128 layers, push the new token's raw row and pool
     # the 128-row (kv, score) frontier of width 512 into one compressed row.
@@ -120,7 +126,7 @@ def apply_heavy_tail_(ik: torch.Tensor, frac: float, scale: float, seed: int, st
 
 
 def make_decode_inputs(units, n_cap, device="cpu", seed=0, n_rows=None, n_raw=None,
-                       heavy_frac=0.0, heavy_scale=4.0, q_scale=1.0, with_indexer=True):
+                       heavy_frac=0.0, heavy_scale=4.0, q_scale=1.0, with_indexer=True, n_head=N_HEAD):
     """Decode-step inputs for `units` independent (sequence x layer) caches.
 
     n_rows / n_raw: per-unit valid compressed rows / raw-window slots (int or
@@ -131,7 +137,7 @@ def make_decode_inputs(units, n_cap, device="cpu", seed=0, n_rows=None, n_raw=No
     dev = torch.device(device)
     bf, hf = torch.bfloat16, torch.float16
     x = {}
-    x["q"] = normal_fill_(torch.empty(units, N_HEAD, HEAD_DIM, dtype=bf, device=dev), HEAD_DIM, seed, 1)
+    x["q"] = normal_fill_(torch.empty(units, n_head, HEAD_DIM, dtype=bf, device=dev), HEAD_DIM, seed, 1)
     if q_scale != 1.0:
         x["q"].mul_(q_scale)
     if with_indexer:
@@ -165,7 +171,7 @@ def prefill_positions(T, prior_rows, ratio=COMPRESS_RATIO):
     return q_pos, row_pos, P0
 
 
-def make_prefill_inputs(T, prior_rows, device="cpu", seed=0, q_scale=1.0):
+def make_prefill_inputs(T, prior_rows, device="cpu", seed=0, q_scale=1.0, n_head=N_HEAD):
     """Prefill-chunk inputs: T queries over prior_rows + T/4 compressed rows, and
     a contiguous fp16 raw buffer holding positions P0-128 .. P0+T-1."""
     dev = torch.device(device)
@@ -173,7 +179,7 @@ def make_prefill_inputs(T, prior_rows, device="cpu", seed=0, q_scale=1.0):
     q_pos, row_pos, P0 = prefill_positions(T, prior_rows)
     n_cap = row_pos.numel()
     x = {}
-    x["q"] = normal_fill_(torch.empty(T, N_HEAD, HEAD_DIM, dtype=bf, device=dev), HEAD_DIM, seed, 11)
+    x["q"] = normal_fill_(torch.empty(T, n_head, HEAD_DIM, dtype=bf, device=dev), HEAD_DIM, seed, 11)
     if q_scale != 1.0:
         x["q"].mul_(q_scale)
     x["iq"] = normal_fill_(torch.empty(T, N_IDX_HEAD, IDX_DIM, dtype=bf, device=dev), IDX_DIM, seed, 12)

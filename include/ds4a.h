@@ -76,6 +76,8 @@ typedef int ds4a_status;
 #define DS4A_OP_SPARSE_ATTN_DECODE 2
 #define DS4A_OP_SPARSE_ATTN_PREFILL 3
 #define DS4A_OP_DENSE_ATTN_DECODE 4
+/* OR-ed into an attention op: the workspace of the 128-head (Pro shape) call. */
+#define DS4A_OP_FLAG_128_HEADS 0x100
 
 /* Human-readable text of a status code (static storage). */
 const char *ds4a_strerror(ds4a_status status);
@@ -270,6 +272,36 @@ ds4a_status ds4a_sparse_attn_prefill(const uint16_t *q, const int32_t *q_pos,
                                      const uint16_t *raw, int32_t raw_pos0, int n_raw_rows,
                                      float scale, float *out, float *lse, int T,
                                      void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * 3d. The attention calls for the Pro shape's 128 query heads (§2: the Pro
+ *    variant has 128 heads and an indexer top_k of 1,024; its other attention
+ *    shapes are those of Flash: one KV head of 512-d rows, a 128-row raw
+ *    window).  n_head is 64 or 128 (another value returns DS4A_EUNSUPPORTED);
+ *    q is [..][n_head][512], out [..][n_head][512] and lse [..][n_head]; every
+ *    other argument is that of the call without the suffix, and the result of
+ *    each head is what that call computes for it.  The workspace is
+ *    ds4a_workspace_bytes(op | DS4A_OP_FLAG_128_HEADS, ...) for 128 heads.
+ */
+ds4a_status ds4a_sparse_attn_decode_heads(int n_head, const uint16_t *q, const uint16_t *rows,
+                                          int64_t rows_unit_stride, int N_cap,
+                                          const int32_t *idx, const int32_t *count, int top_k,
+                                          const uint16_t *raw, int64_t raw_unit_stride,
+                                          const int32_t *n_raw, float scale, float *out,
+                                          float *lse, int U, void *ws, size_t ws_bytes,
+                                          void *stream);
+ds4a_status ds4a_sparse_attn_prefill_heads(int n_head, const uint16_t *q, const int32_t *q_pos,
+                                           const uint16_t *rows, int N_cap, const int32_t *idx,
+                                           const int32_t *count, int top_k, const uint16_t *raw,
+                                           int32_t raw_pos0, int n_raw_rows, float scale,
+                                           float *out, float *lse, int T, void *ws,
+                                           size_t ws_bytes, void *stream);
+ds4a_status ds4a_dense_attn_decode_heads(int n_head, const uint16_t *q, const uint16_t *rows,
+                                         int64_t rows_unit_stride, int N_cap,
+                                         const int32_t *n_rows, const uint16_t *raw,
+                                         int64_t raw_unit_stride, const int32_t *n_raw,
+                                         float scale, float *out, float *lse, int U, void *ws,
+                                         size_t ws_bytes, void *stream);
 
 /*
  * 4a. Raw-window push (§3-1: the raw tier keeps the K/V rows of the last 128
