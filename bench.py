@@ -149,6 +149,24 @@ def decode_bytes(wl):
     return wl.units * (ik + per_unit_fixed), wl.units * idx_kernel
 
 
+def dram_traffic(kernel, units, rows):
+    """DRAM bytes (read + write) of one launch of `kernel` on units x rows,
+    scaled from the ncu capture recorded in profiles/dram_traffic.json (the
+    traffic of these kernels grows in proportion to units x rows).  None when
+    there is no capture or the kernel's sources changed since it was taken."""
+    import hashlib
+    try:
+        rec = json.load(open(os.path.join(ROOT, "profiles", "dram_traffic.json")))[kernel]
+        m = hashlib.sha256()
+        for f in rec["sources"]:
+            m.update(open(os.path.join(ROOT, "deepseek_v4_sparse_indexer_gb300", "csrc", f), "rb").read())
+        if m.hexdigest() != rec["sources_sha256"]:
+            return None
+        return rec["dram_bytes"] * (units * rows) / (rec["units"] * rec["rows"])
+    except Exception:
+        return None
+
+
 def pool_bytes(wl, width=512):
     """Algorithmic HBM bytes per launch of the pooling kernel: the fp32 (kv,
     score) frontier and the fp32 pooled row of every unit."""
@@ -494,7 +512,8 @@ def main():
         step_bytes, idx_bytes = decode_bytes(wl)
         achieved = idx_bytes / (idx_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
-                "frac": achieved / pk["hbm"], "traffic": None, "kernel": "indexer_score_kernel<1>",
+                "frac": achieved / pk["hbm"], "traffic": dram_traffic("indexer_score_kernel<1>", wl.units, wl.n_rows),
+                "kernel": "indexer_score_kernel<1>",
                 "algorithmic_bytes_per_launch": idx_bytes, "launch_ms": idx_ms}
         cfg["step_algorithmic_bytes"] = step_bytes
         cfg["step_hbm_GBps"] = step_bytes / (ms / 1e3) / 1e9
@@ -503,7 +522,9 @@ def main():
         idx_flops, attn_flops = prefill_flops(x, wl)
         achieved = idx_flops / (idx_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16"], "unit": "TFLOP/s",
-                "frac": achieved / pk["bf16"], "traffic": None, "kernel": "indexer_score_kernel<4>",
+                "frac": achieved / pk["bf16"],
+                "traffic": dram_traffic("indexer_score_kernel<4>", wl.queries, wl.n_rows),
+                "kernel": "indexer_score_kernel<4>",
                 "algorithmic_flops_per_launch": idx_flops, "launch_ms": idx_ms}
         cfg["step_algorithmic_flops"] = idx_flops + attn_flops
         cfg["step_TFLOPs"] = (idx_flops + attn_flops) / (ms / 1e3) / 1e12
