@@ -87,6 +87,33 @@ DS4A_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
     }
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// sleeps until it completes (or the hint runs out) instead of returning at
+// once, so a waiting single-thread role takes no issue slots from the warps
+// that share its SM sub-partition.
+constexpr uint32_t kSuspendHintNs = 20000;
+DS4A_DEV bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+    return ok != 0;
+}
+// mbar_wait through the hinted try_wait; same limits.
+DS4A_DEV bool mbar_wait_hint(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    if (mbar_try_wait_hint(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait_hint(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor), no multicast
 // ---------------------------------------------------------------------------

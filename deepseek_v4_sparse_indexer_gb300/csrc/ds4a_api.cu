@@ -213,7 +213,7 @@ ds4a_status ds4a_indexer_score(const uint16_t *iq, const float *w, const uint16_
         cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kNIdxHead * a.G)};
         if (!encode_bf16(&a.tm_iq, iq, 2, dims, strides, box)) return DS4A_EINVAL;
     }
-    if (a.total_items == 0) return DS4A_OK;
+    if (a.total_tiles == 0) return DS4A_OK;
     return launch_indexer_score(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DS4A_OK : DS4A_ECUDA;
 }
 

@@ -21,7 +21,10 @@
 //   warps 2..   epilogue: tcgen05.ld of the row's N accumulators, ReLU,
 //               weight, sum over heads (packed fp32x2 FMAs, eight partial
 //               sums), masked store of one fp32 per (q,row).
-// A work item is (unit, query group, chunk of 128-row tiles).
+// The work is the list of (unit, query group, 128-row tile) triples, tile
+// fastest; each CTA takes one contiguous, equal share of it, so the CTAs end
+// together and a CTA reloads its iq block only where its share crosses into
+// the next (unit, group).
 //
 // The decode scan is HBM-bound (256 B of keys per row for 16 kFLOP); the
 // prefill chunk (G = 4) is tensor-bound.  Every wait is bounded: on timeout
@@ -69,22 +72,36 @@ struct IdxCfg {
     static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
+// One work item: tiles t0 .. t1-1 of (unit u, query group g).  first is the
+// tile the item starts at before clamping to the unit's row count.
 struct Item {
-    int u, g, t0, t1;
+    int u, g, t0, t1, first;
 };
 
-DS4A_DEV Item decode_item(const IndexerArgs &a, long long it) {
+// This CTA's share [lo, hi) of the U * n_groups * nt_cap tiles.
+DS4A_DEV void cta_share(const IndexerArgs &a, long long &lo, long long &hi) {
+    lo = a.total_tiles * blockIdx.x / gridDim.x;
+    hi = a.total_tiles * (blockIdx.x + 1) / gridDim.x;
+}
+
+// The item starting at tile index lin (lin < hi), which runs to the end of its
+// (unit, group) or of the share; advances lin past it.  Tiles beyond the
+// unit's n_rows are clamped away (t0 >= t1: nothing to do).
+DS4A_DEV Item next_item(const IndexerArgs &a, long long &lin, long long hi) {
     Item m;
-    const int per_unit = a.n_groups * a.n_chunks;
-    m.u = static_cast<int>(it / per_unit);
-    const int rem = static_cast<int>(it - static_cast<long long>(m.u) * per_unit);
-    m.g = rem / a.n_chunks;
-    const int c = rem - m.g * a.n_chunks;
+    const long long per_unit = static_cast<long long>(a.n_groups) * a.nt_cap;
+    m.u = static_cast<int>(lin / per_unit);
+    const int rem = static_cast<int>(lin - static_cast<long long>(m.u) * per_unit);
+    m.g = rem / a.nt_cap;
+    m.first = rem - m.g * a.nt_cap;
+    const long long left = hi - lin;
+    const int end = left < a.nt_cap - m.first ? m.first + static_cast<int>(left) : a.nt_cap;
+    lin += end - m.first;
     int nr = a.n_rows[m.u];
     nr = nr < 0 ? 0 : (nr > a.N_cap ? a.N_cap : nr);
     const int nt = (nr + kTileRows - 1) / kTileRows;
-    m.t0 = c * a.chunk_tiles;
-    m.t1 = min(m.t0 + a.chunk_tiles, nt);
+    m.t0 = m.first;
+    m.t1 = min(end, nt);
     return m;
 }
 
@@ -198,7 +215,8 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const long long items = a.total_items;
+    long long share_lo, share_hi;
+    cta_share(a, share_lo, share_hi);
 
     if (warp < C::kFirstEpiWarp) {
         if constexpr (C::kSplitRegs) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kLowRegs));
@@ -213,10 +231,10 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
             bool used_s[C::kStages] = {}, used_b[C::kBBufs] = {};
             uint32_t par_s[C::kStages] = {}, par_b[C::kBBufs] = {};
             bool ok = true;
-            for (long long it = blockIdx.x; ok && it < items; it += gridDim.x) {
-                const Item m = decode_item(a, it);
+            for (long long lin = share_lo; ok && lin < share_hi;) {
+                const Item m = next_item(a, lin, share_hi);
                 if (m.t0 >= m.t1) continue;
-                if (!mbar_wait(&b_empty[bb], bph ^ 1, abort_flag)) { ok = false; break; }
+                if (!mbar_wait_hint(&b_empty[bb], bph ^ 1, abort_flag)) { ok = false; break; }
                 mbar_arrive_expect_tx(&b_full[bb], C::kBBytes);
                 const int qrow = (m.u * a.Q + m.g * G) * kNIdxHead;
                 uint8_t *dstB = sB + bb * C::kBBytes;
@@ -226,7 +244,7 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
                 par_b[bb] = bph;
                 if (++bb == C::kBBufs) { bb = 0; bph ^= 1; }
                 for (int t = m.t0; t < m.t1; ++t) {
-                    if (!mbar_wait(&a_empty[s], sph ^ 1, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait_hint(&a_empty[s], sph ^ 1, abort_flag)) { ok = false; break; }
                     mbar_arrive_expect_tx(&a_full[s], C::kABytes);
                     uint8_t *dstA = sA + s * C::kABytes;
                     tma_load_3d(dstA, &a.tm_ik, &a_full[s], 0, t * kTileRows, m.u, pol_stream);
@@ -253,14 +271,14 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
             int s = 0, bb = 0, ab = 0;
             uint32_t sph = 0, bph = 0, aph = 0;
             bool ok = true;
-            for (long long it = blockIdx.x; ok && it < items; it += gridDim.x) {
-                const Item m = decode_item(a, it);
+            for (long long lin = share_lo; ok && lin < share_hi;) {
+                const Item m = next_item(a, lin, share_hi);
                 if (m.t0 >= m.t1) continue;
-                if (!mbar_wait(&b_full[bb], bph, abort_flag)) { ok = false; break; }
+                if (!mbar_wait_hint(&b_full[bb], bph, abort_flag)) { ok = false; break; }
                 const uint32_t b_addr = smem_u32(sB + bb * C::kBBytes);
                 for (int t = m.t0; t < m.t1; ++t) {
-                    if (!mbar_wait(&acc_empty[ab], aph ^ 1, abort_flag)) { ok = false; break; }
-                    if (!mbar_wait(&a_full[s], sph, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait_hint(&acc_empty[ab], aph ^ 1, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait_hint(&a_full[s], sph, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(sA + s * C::kABytes);
                     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * C::N);
@@ -301,12 +319,13 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
         int ab = 0;
         uint32_t aph = 0;
         bool ok = true;
-        for (long long it = blockIdx.x; ok && it < items; it += gridDim.x) {
-            const Item m = decode_item(a, it);
-            if (m.t0 >= m.t1) continue;
+        for (long long lin = share_lo; ok && lin < share_hi;) {
+            const Item m = next_item(a, lin, share_hi);
             const int nr_raw = a.n_rows[m.u];
-            if ((nr_raw < 0 || nr_raw > a.N_cap) && e == 0 && lane == 0 && m.t0 == 0 && m.g == 0)
+            // Reported once per unit: by the item holding its first tile.
+            if ((nr_raw < 0 || nr_raw > a.N_cap) && e == 0 && lane == 0 && m.first == 0 && m.g == 0)
                 report(a.status, DS4A_DEV_BOUNDS);
+            if (m.t0 >= m.t1) continue;
             const int nr = nr_raw < 0 ? 0 : (nr_raw > a.N_cap ? a.N_cap : nr_raw);
             const int q0 = m.g * G + half * C::kQPerEpiWarp;
             __syncwarp();
@@ -335,7 +354,7 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
 
             for (int t = m.t0; t < m.t1; ++t) {
                 // Warp-uniform outcome: the tcgen05.ld below is .sync.aligned.
-                if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[ab], aph, abort_flag))) { ok = false; break; }
+                if (!__all_sync(0xffffffffu, mbar_wait_hint(&acc_full[ab], aph, abort_flag))) { ok = false; break; }
                 tc_fence_after();
                 const int row = t * kTileRows + row_in_tile;
                 int rpos = 0;
@@ -410,14 +429,9 @@ int indexer_group_size(int Q) { return Q >= 4 ? 4 : 1; }
 void indexer_plan(IndexerArgs &a, int num_sms) {
     a.G = indexer_group_size(a.Q);
     a.n_groups = (a.Q + a.G - 1) / a.G;
-    const int tiles_per_unit = (a.N_cap + kTileRows - 1) / kTileRows;
-    const long long work = static_cast<long long>(a.U) * a.n_groups;
-    int chunk = a.G == 1 ? 32 : 64;
-    while (chunk > 1 && work * ((tiles_per_unit + chunk - 1) / chunk) < 8LL * num_sms) chunk >>= 1;
-    a.chunk_tiles = chunk;
-    a.n_chunks = (tiles_per_unit + chunk - 1) / chunk;
-    a.total_items = work * a.n_chunks;
-    a.grid = static_cast<int>(a.total_items < num_sms ? a.total_items : num_sms);
+    a.nt_cap = (a.N_cap + kTileRows - 1) / kTileRows;
+    a.total_tiles = static_cast<long long>(a.U) * a.n_groups * a.nt_cap;
+    a.grid = static_cast<int>(a.total_tiles < num_sms ? a.total_tiles : num_sms);
 }
 
 cudaError_t launch_indexer_score(const IndexerArgs &a, cudaStream_t s) {

@@ -28,9 +28,8 @@ struct IndexerArgs {
     int U, Q, N_cap;
     int G;                      // queries per UMMA (1 or 4)
     int n_groups;               // ceil(Q / G)
-    int chunk_tiles;            // 128-row tiles per work item
-    int n_chunks;               // work items per (unit, group)
-    long long total_items;
+    int nt_cap;                 // 128-row tiles per (unit, group): ceil(N_cap / 128)
+    long long total_tiles;      // U * n_groups * nt_cap, split evenly over the CTAs
     int grid;
 };
 cudaError_t launch_indexer_score(const IndexerArgs &a, cudaStream_t s);

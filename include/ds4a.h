@@ -120,7 +120,8 @@ void ds4a_debug_inject_error(ds4a_status code);
  *            elements (device).  ik and ik_unit_stride*2 bytes must be
  *            16-byte aligned (the keys are streamed by TMA).
  *    n_rows  int32 [U]: rows 0..n_rows[u]-1 of unit u exist, 0 <= n_rows[u]
- *            <= N_cap (device).
+ *            <= N_cap (device).  A count outside [0, N_cap] sets
+ *            DS4A_DEV_BOUNDS and is clamped into it.
  *    q_pos, row_pos   NULL for decode.  For a causal prefill chunk: q_pos
  *            int32 [U][Q] query positions and row_pos int32 [U][N_cap] (unit
  *            stride N_cap) row positions; row r is visible to query q only

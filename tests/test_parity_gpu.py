@@ -106,6 +106,59 @@ def test_indexer_scores_query_groups_with_positions(Q):
             check_scores(scores[u, q, :n].cpu().numpy(), ref[q, :n], tol)
 
 
+def _indexer_case(U, Q, N_cap, n_rows, seed, positions=False):
+    g = torch.Generator().manual_seed(seed)
+    iq = (torch.randn(U, Q, 64, 128, generator=g) / math.sqrt(128)).to(torch.bfloat16).cuda()
+    w = (torch.rand(U, Q, 64, generator=g) * 2 - 0.5).cuda()
+    ik = (torch.randn(U, N_cap, 128, generator=g) / math.sqrt(128)).to(torch.bfloat16).cuda()
+    nr = torch.tensor(n_rows, dtype=torch.int32).cuda()
+    q_pos = row_pos = None
+    if positions:
+        row_pos = torch.sort(torch.randint(0, 4 * N_cap, (U, N_cap), generator=g), dim=1).values.to(torch.int32).cuda()
+        q_pos = torch.randint(0, 4 * N_cap + 8, (U, Q), generator=g).to(torch.int32).cuda()
+    scores = torch.full((U, Q, N_cap), 12345.0, device="cuda")
+    B.ds4a_indexer_score(iq, w, ik, nr, scores, q_pos=q_pos, row_pos=row_pos)
+    torch.cuda.synchronize()
+    return iq, w, ik, q_pos, row_pos, scores
+
+
+def _check_indexer_unit(iq, w, ik, q_pos, row_pos, scores, u, n):
+    iqn, wn, ikn = u16(iq[u]), w[u].cpu().numpy(), u16(ik[u])
+    kw = {}
+    if q_pos is not None:
+        kw = dict(q_pos=q_pos[u].cpu().numpy(), row_pos=row_pos[u].cpu().numpy())
+    ref = oracle.indexer_score(iqn, wn, ikn, n, **kw)
+    for q in range(iq.shape[1]):
+        check_scores(scores[u, q, :n].cpu().numpy(), ref[q, :n], score_tolerance(iqn[q], wn[q], ikn, n))
+    assert torch.all(scores[u, :, n:] == 12345.0)
+
+
+@pytest.mark.parametrize("U,Q,N_cap,n_rows,positions", [
+    # one query (decode): 200 units x 3 tiles, so CTA shares end inside units
+    (200, 1, 260, [260 - (u % 7) * 37 for u in range(200)], False),
+    # query groups of 4 with a partial last group; shares cross groups and units,
+    # and units with no rows or one row sit between full ones
+    (5, 9, 3000, [3000, 1, 0, 2999, 1500], True),
+])
+def test_indexer_work_shares_cross_unit_and_group_boundaries(U, Q, N_cap, n_rows, positions):
+    case = _indexer_case(U, Q, N_cap, n_rows, seed=U + Q, positions=positions)
+    device_ok()
+    units = range(U) if U <= 8 else [0, 1, 2, 3, 50, 99, 150, 198, 199]
+    for u in units:
+        _check_indexer_unit(*case, u, n_rows[u])
+
+
+def test_indexer_row_count_out_of_range_is_clamped_and_flagged():
+    U, Q, N_cap = 3, 5, 300
+    iq, w, ik, q_pos, row_pos, scores = _indexer_case(U, Q, N_cap, [-4, N_cap + 7, 200], seed=35)
+    st, flags = B.ds4a_get_device_status()
+    assert st == B.DS4A_EDEVICE and flags & B.DS4A_DEV_BOUNDS
+    _check_indexer_unit(iq, w, ik, q_pos, row_pos, scores, 0, 0)
+    _check_indexer_unit(iq, w, ik, q_pos, row_pos, scores, 1, N_cap)
+    _check_indexer_unit(iq, w, ik, q_pos, row_pos, scores, 2, 200)
+    device_ok()
+
+
 # ----------------------------------------------------------------------------
 # A2 top-k on given scores: bit-exact against the oracle
 # ----------------------------------------------------------------------------
