@@ -352,13 +352,19 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
             for (int j = 0; j < C::kQPerEpiWarp; ++j)
                 qpos[j] = (a.q_pos && q0 + j < a.Q) ? a.q_pos[static_cast<long long>(m.u) * a.Q + q0 + j] : 0;
 
+            // The row's position is loaded one tile ahead: its global-load
+            // latency then hides behind a whole tile instead of stalling the
+            // store at the end of each tile.
+            const int32_t *rp = a.row_pos ? a.row_pos + static_cast<long long>(m.u) * a.N_cap : nullptr;
+            int rpos_next = 0;
+            if (rp && m.t0 * kTileRows + row_in_tile < nr) rpos_next = __ldg(rp + m.t0 * kTileRows + row_in_tile);
             for (int t = m.t0; t < m.t1; ++t) {
+                const int row = t * kTileRows + row_in_tile;
+                const int rpos = rpos_next;
+                if (rp && t + 1 < m.t1 && row + kTileRows < nr) rpos_next = __ldg(rp + row + kTileRows);
                 // Warp-uniform outcome: the tcgen05.ld below is .sync.aligned.
                 if (!__all_sync(0xffffffffu, mbar_wait_hint(&acc_full[ab], aph, abort_flag))) { ok = false; break; }
                 tc_fence_after();
-                const int row = t * kTileRows + row_in_tile;
-                int rpos = 0;
-                if (a.row_pos && row < nr) rpos = a.row_pos[static_cast<long long>(m.u) * a.N_cap + row];
                 float sc[C::kQPerEpiWarp];
 #pragma unroll
                 for (int j = 0; j < C::kQPerEpiWarp; ++j) {
