@@ -53,7 +53,7 @@ struct IdxCfg {
     static constexpr bool kSplitRegs = (G != 1);
     static constexpr int kFirstEpiWarp = kSplitRegs ? 4 : 2;
     static constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
-    static constexpr int kLowRegs = 56, kHighRegs = 224;   // per thread after setmaxnreg
+    static constexpr int kLowRegs = 72, kHighRegs = 216;   // per thread after setmaxnreg
     static constexpr int kRegsNeeded = 128 * kLowRegs + 32 * kEpiWarps * kHighRegs;
     static constexpr uint32_t kTmemCols = kAccBufs * N;   // 256 or 512
     static constexpr int kASub = kTileRows * 128;         // one 64-element K half of a key tile
