@@ -64,6 +64,20 @@ def lib():
         L.oracle_compressor_pool.restype = None
         L.oracle_push_raw.argtypes = [u16p, ctypes.POINTER(ctypes.c_int), ctypes.c_int, ctypes.c_int, f32p]
         L.oracle_push_raw.restype = None
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        L.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_to_double.restype = ctypes.c_double
+        L.oracle_double_to_e4m3.argtypes = [ctypes.c_double]
+        L.oracle_double_to_e4m3.restype = ctypes.c_uint8
+        L.oracle_fp8_row_exponent.argtypes = [ctypes.c_double]
+        L.oracle_fp8_row_exponent.restype = ctypes.c_int
+        L.oracle_quantize_rows_fp8.argtypes = [f32p, ctypes.c_int64, ctypes.c_int, u8p, f32p]
+        L.oracle_quantize_rows_fp8.restype = None
+        L.oracle_sparse_attention_fp8.argtypes = [u16p, ctypes.c_int, ctypes.c_int,
+                                                  u8p, f32p, i32p, ctypes.c_int,
+                                                  u16p, i32p, ctypes.c_int,
+                                                  ctypes.c_double, f64p, f64p]
+        L.oracle_sparse_attention_fp8.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -254,3 +268,70 @@ def push_raw(ring, n_raw, kv, cap=N_SWA):
     lib().oracle_push_raw(_ptr(ring, ctypes.c_uint16), ctypes.byref(n), cap, ring.shape[1],
                           _ptr(kv, ctypes.c_float))
     return ring, n.value
+
+
+# ----------------------------------------------------------------------------
+# FP8 row store ([ARCH] §3-2: the FP8 quantisation round trip of a new
+# compressed row).  Read as E4M3 codes with one power-of-two scale per row.
+# ----------------------------------------------------------------------------
+
+def e4m3_to_double(code: int) -> float:
+    return lib().oracle_e4m3_to_double(int(code) & 0xFF)
+
+
+def double_to_e4m3(x: float) -> int:
+    """Nearest E4M3 code (ties to even), saturating at +-448; NaN -> 0x7F."""
+    return lib().oracle_double_to_e4m3(float(x))
+
+
+def fp8_row_exponent(amax: float) -> int:
+    """Smallest e with amax <= 448 * 2^e, within [-126, 127]; 0 for amax 0 or not finite."""
+    return lib().oracle_fp8_row_exponent(float(amax))
+
+
+def quantize_rows_fp8(x):
+    """(codes uint8 [n, dim], row_scale float32 [n]) of fp32 rows x [n, dim]."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    assert x.ndim == 2
+    n, dim = x.shape
+    codes = np.empty((n, dim), dtype=np.uint8)
+    scale = np.empty(n, dtype=np.float32)
+    if n:
+        lib().oracle_quantize_rows_fp8(_ptr(x, ctypes.c_float), n, dim, _ptr(codes, ctypes.c_uint8),
+                                       _ptr(scale, ctypes.c_float))
+    return codes, scale
+
+
+def fp8_rows_to_double(codes, row_scale):
+    """Stored values (float64 [n, dim]) of FP8 rows: e4m3(code) * row scale."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    table = np.array([e4m3_to_double(c) for c in range(256)], dtype=np.float64)
+    return table[codes] * np.asarray(row_scale, dtype=np.float64)[:, None]
+
+
+def sparse_attention_fp8(q, codes, row_scale, sel, raw_rows, raw_sel, scale):
+    """sparse_attention with the compressed rows in the FP8 store (codes uint8
+    [N, D], row_scale float32 [N]); raw rows stay fp16 bits."""
+    q = _u16(q)
+    H, D = q.shape
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    row_scale = np.ascontiguousarray(row_scale, dtype=np.float32)
+    assert codes.shape[1] == D and row_scale.shape == (codes.shape[0],)
+    raw_rows = _u16(raw_rows) if raw_rows is not None else np.zeros((1, D), np.uint16)
+    sel = np.ascontiguousarray(sel if sel is not None else [], dtype=np.int32)
+    raw_sel = np.ascontiguousarray(raw_sel if raw_sel is not None else [], dtype=np.int32)
+    if sel.size:
+        assert sel.max() < codes.shape[0]
+    if raw_sel.size:
+        assert raw_sel.max() < raw_rows.shape[0]
+    out = np.empty((H, D), dtype=np.float64)
+    lse = np.empty(H, dtype=np.float64)
+    sel_p = sel if sel.size else np.zeros(1, np.int32)
+    raw_p = raw_sel if raw_sel.size else np.zeros(1, np.int32)
+    rc = lib().oracle_sparse_attention_fp8(_ptr(q, ctypes.c_uint16), H, D, _ptr(codes, ctypes.c_uint8),
+                                           _ptr(row_scale, ctypes.c_float), _ptr(sel_p, ctypes.c_int32), sel.size,
+                                           _ptr(raw_rows, ctypes.c_uint16), _ptr(raw_p, ctypes.c_int32), raw_sel.size,
+                                           float(scale), _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("negative row index")
+    return out, lse

@@ -249,35 +249,22 @@ int oracle_topk_select(const double *scores, int64_t n, int top_k, int32_t *idx,
  * q: bf16 [n_head][dim]; out: double [n_head][dim]; lse: double [n_head] or NULL.
  * Returns 0, or -1 when a row index is negative.
  */
-int oracle_sparse_attention(const uint16_t *q, int n_head, int dim,
-                            const uint16_t *comp, const int32_t *sel, int n_sel,
-                            const uint16_t *raw, const int32_t *raw_sel, int n_raw,
-                            double scale, double *out, double *lse)
+/* The definition above on rows already decoded to double: x [n][dim] holds
+ * the selected compressed rows followed by the raw rows.  Frees nothing. */
+static void attention_on_rows(const uint16_t *q, int n_head, int dim, const double *x, int n, double scale,
+                              double *out, double *lse)
 {
-    int n = n_sel + n_raw;
-    for (int j = 0; j < n_sel; j++)
-        if (sel[j] < 0) return -1;
-    for (int j = 0; j < n_raw; j++)
-        if (raw_sel[j] < 0) return -1;
     if (n == 0) {
         for (int64_t i = 0; i < (int64_t)n_head * dim; i++)
             out[i] = 0.0;
         if (lse)
             for (int h = 0; h < n_head; h++)
                 lse[h] = -INFINITY;
-        return 0;
+        return;
     }
-    double *x = (double *)malloc(sizeof(double) * (size_t)n * (size_t)dim);
     double *qd = (double *)malloc(sizeof(double) * (size_t)dim);
     double *l = (double *)malloc(sizeof(double) * (size_t)n);
     double *a = (double *)malloc(sizeof(double) * (size_t)n);
-    for (int j = 0; j < n_sel; j++)
-        for (int d = 0; d < dim; d++)
-            x[(int64_t)j * dim + d] = oracle_bf16_to_double(comp[(int64_t)sel[j] * dim + d]);
-    for (int j = 0; j < n_raw; j++)
-        for (int d = 0; d < dim; d++)
-            x[(int64_t)(n_sel + j) * dim + d] = oracle_f16_to_double(raw[(int64_t)raw_sel[j] * dim + d]);
-
     for (int h = 0; h < n_head; h++) {
         for (int d = 0; d < dim; d++)
             qd[d] = oracle_bf16_to_double(q[(int64_t)h * dim + d]);
@@ -303,10 +290,36 @@ int oracle_sparse_attention(const uint16_t *q, int n_head, int dim,
         if (lse)
             lse[h] = mx + log(z);
     }
-    free(x);
     free(qd);
     free(l);
     free(a);
+}
+
+/* Decodes the raw rows raw_sel[0..n_raw) (fp16) into x after n_sel rows. */
+static void decode_raw_rows(const uint16_t *raw, const int32_t *raw_sel, int n_raw, int n_sel, int dim, double *x)
+{
+    for (int j = 0; j < n_raw; j++)
+        for (int d = 0; d < dim; d++)
+            x[(int64_t)(n_sel + j) * dim + d] = oracle_f16_to_double(raw[(int64_t)raw_sel[j] * dim + d]);
+}
+
+int oracle_sparse_attention(const uint16_t *q, int n_head, int dim,
+                            const uint16_t *comp, const int32_t *sel, int n_sel,
+                            const uint16_t *raw, const int32_t *raw_sel, int n_raw,
+                            double scale, double *out, double *lse)
+{
+    int n = n_sel + n_raw;
+    for (int j = 0; j < n_sel; j++)
+        if (sel[j] < 0) return -1;
+    for (int j = 0; j < n_raw; j++)
+        if (raw_sel[j] < 0) return -1;
+    double *x = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * (size_t)dim);
+    for (int j = 0; j < n_sel; j++)
+        for (int d = 0; d < dim; d++)
+            x[(int64_t)j * dim + d] = oracle_bf16_to_double(comp[(int64_t)sel[j] * dim + d]);
+    decode_raw_rows(raw, raw_sel, n_raw, n_sel, dim, x);
+    attention_on_rows(q, n_head, dim, x, n, scale, out, lse);
+    free(x);
     return 0;
 }
 
@@ -358,4 +371,135 @@ void oracle_push_raw(uint16_t *ring, int *n_raw, int cap, int dim, const float *
     }
     for (int d = 0; d < dim; d++) ring[(int64_t)(*n_raw) * dim + d] = oracle_double_to_f16((double)kv[d]);
     *n_raw += 1;
+}
+
+/* ------------------------------------------------------------------------ */
+/* FP8 row store.  [ARCH] §3-2: a new compressed row is RMS-normalised, its */
+/* tail rotated, and then put through an FP8 quantisation round trip before */
+/* it is stored.  The pages name neither the FP8 format nor its scaling.    */
+/* This library reads the round trip as: E4M3 codes with one power-of-two   */
+/* scale per row, so that storing the codes and the scale keeps exactly the */
+/* values the round trip produces.                                          */
+/* ------------------------------------------------------------------------ */
+
+/* E4M3 ("FN" variant of the 8-bit floating-point formats): 1 sign bit, 4
+ * exponent bits (bias 7), 3 fraction bits.  Exponent field 15 with fraction 7
+ * is NaN; there are no infinities.  Normal values 2^(e-7) * (1 + m/8), largest
+ * 448; subnormals (exponent field 0) m * 2^-9. */
+double oracle_e4m3_to_double(uint8_t c)
+{
+    int sign = (c >> 7) & 1;
+    int e = (c >> 3) & 0xF;
+    int m = c & 7;
+    double v;
+    if (e == 15 && m == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)m, -9);
+    else
+        v = ldexp((double)(8 + m), e - 7 - 3);
+    return sign ? -v : v;
+}
+
+/* The E4M3 value nearest to x (ties to the even code), saturating: |x| >= 448
+ * (infinities included) gives +-448.  NaN gives the NaN code 0x7F. */
+uint8_t oracle_double_to_e4m3(double x)
+{
+    if (isnan(x))
+        return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    x = fabs(x);
+    if (x >= 448.0)
+        return sign | 0x7E;
+    if (x == 0.0)
+        return sign;
+    /* Grid spacing at x: 2^(E-3) in the binade [2^E, 2^(E+1)), E >= -6; the
+     * subnormal range below 2^-6 shares the spacing 2^-9. */
+    int E;
+    frexp(x, &E);
+    int ue = E - 1;
+    if (ue < -6)
+        ue = -6;
+    double ulp = ldexp(1.0, ue - 3);
+    double q = x / ulp;
+    double fl = floor(q);
+    double rem = q - fl;
+    double n;
+    if (rem > 0.5)
+        n = fl + 1.0;
+    else if (rem < 0.5)
+        n = fl;
+    else
+        n = fmod(fl, 2.0) == 0.0 ? fl : fl + 1.0;   /* tie: the even multiple */
+    double r = n * ulp;                 /* <= 448: x < 448 and 448 is on the grid */
+    if (r == 0.0)
+        return sign;
+    if (r < ldexp(1.0, -6))
+        return sign | (uint8_t)(r / ldexp(1.0, -9));
+    int e2;
+    double f = frexp(r, &e2);           /* r = f * 2^e2, f in [0.5, 1) */
+    int be = e2 - 1 + 7;
+    int mant = (int)((f * 2.0 - 1.0) * 8.0);
+    return sign | (uint8_t)(be << 3) | (uint8_t)mant;
+}
+
+/* The row's scale exponent: the smallest integer e with amax <= 448 * 2^e,
+ * kept within [-126, 127] (the scale 2^e is then a normal fp32).  amax 0, or
+ * not finite, gives 0. */
+int oracle_fp8_row_exponent(double amax)
+{
+    if (!(amax > 0.0) || isinf(amax))
+        return 0;
+    int e = 0;
+    while (amax > 448.0 * ldexp(1.0, e) && e < 127)
+        e++;
+    while (e > -126 && amax <= 448.0 * ldexp(1.0, e - 1))
+        e--;
+    return e;
+}
+
+/* The FP8 round trip's stored form for n_rows rows of dim fp32 values: per
+ * row, amax = max |x| over its elements (NaN elements do not count), scale =
+ * 2^oracle_fp8_row_exponent(amax), code[d] = nearest E4M3 of x[d] / scale.
+ * The stored value of element d is e4m3(code[d]) * scale. */
+void oracle_quantize_rows_fp8(const float *x, int64_t n_rows, int dim, uint8_t *codes, float *row_scale)
+{
+    for (int64_t r = 0; r < n_rows; r++) {
+        const float *xr = x + r * dim;
+        double amax = 0.0;
+        for (int d = 0; d < dim; d++) {
+            double v = fabs((double)xr[d]);
+            if (v > amax)
+                amax = v;              /* NaN compares false: skipped */
+        }
+        double s = ldexp(1.0, oracle_fp8_row_exponent(amax));
+        row_scale[r] = (float)s;
+        for (int d = 0; d < dim; d++)
+            codes[r * dim + d] = oracle_double_to_e4m3((double)xr[d] / s);
+    }
+}
+
+/* oracle_sparse_attention with the compressed rows in the FP8 store: row i
+ * holds codes[i][0..dim) and row_scale[i]; element d of row i is
+ * e4m3(codes[i][d]) * row_scale[i].  Raw rows stay fp16. */
+int oracle_sparse_attention_fp8(const uint16_t *q, int n_head, int dim,
+                                const uint8_t *codes, const float *row_scale, const int32_t *sel, int n_sel,
+                                const uint16_t *raw, const int32_t *raw_sel, int n_raw,
+                                double scale, double *out, double *lse)
+{
+    int n = n_sel + n_raw;
+    for (int j = 0; j < n_sel; j++)
+        if (sel[j] < 0) return -1;
+    for (int j = 0; j < n_raw; j++)
+        if (raw_sel[j] < 0) return -1;
+    double *x = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * (size_t)dim);
+    for (int j = 0; j < n_sel; j++) {
+        const double s = (double)row_scale[sel[j]];
+        for (int d = 0; d < dim; d++)
+            x[(int64_t)j * dim + d] = oracle_e4m3_to_double(codes[(int64_t)sel[j] * dim + d]) * s;
+    }
+    decode_raw_rows(raw, raw_sel, n_raw, n_sel, dim, x);
+    attention_on_rows(q, n_head, dim, x, n, scale, out, lse);
+    free(x);
+    return 0;
 }

@@ -35,6 +35,16 @@ MUTATIONS = {
     "push slides by two rows": ("ring[(int64_t)(s - 1) * dim + d] = ring[(int64_t)s * dim + d];",
                                 "ring[(int64_t)(s - 1) * dim + d] = ring[(int64_t)(s < cap - 1 ? s + 1 : s) * dim + d];"),
     "push keeps the full window one row short": ("        *n_raw = cap - 1;\n", "        *n_raw = cap - 2;\n"),
+    "e4m3 exponent bias": ("v = ldexp((double)(8 + m), e - 7 - 3);", "v = ldexp((double)(8 + m), e - 8 - 3);"),
+    "e4m3 subnormal step": ("v = ldexp((double)m, -9);", "v = ldexp((double)m, -10);"),
+    "e4m3 ties rounded up": ("n = fmod(fl, 2.0) == 0.0 ? fl : fl + 1.0;", "n = fl + 1.0;"),
+    "e4m3 saturates one step low": ("        return sign | 0x7E;\n    if (x == 0.0)", "        return sign | 0x7D;\n    if (x == 0.0)"),
+    "fp8 row scale one power too small": ("while (e > -126 && amax <= 448.0 * ldexp(1.0, e - 1))",
+                                          "while (e > -126 && amax <= 448.0 * ldexp(1.0, e))"),
+    "fp8 codes not divided by the row scale": ("oracle_double_to_e4m3((double)xr[d] / s);",
+                                               "oracle_double_to_e4m3((double)xr[d]);"),
+    "fp8 attention ignores the row scale": ("x[(int64_t)j * dim + d] = oracle_e4m3_to_double(codes[(int64_t)sel[j] * dim + d]) * s;",
+                                            "x[(int64_t)j * dim + d] = oracle_e4m3_to_double(codes[(int64_t)sel[j] * dim + d]);"),
 }
 
 

@@ -465,3 +465,141 @@ def test_push_raw_keeps_the_last_128_rows_rounded_through_f16():
         want = pushed[-cap:]
         assert n == len(want)
         assert np.array_equal(ring[:n], np.array(want)), t
+
+
+# ----------------------------------------------------------------------------
+# FP8 row store (E4M3 codes + one power-of-two scale per row)
+# ----------------------------------------------------------------------------
+
+def _torch_e4m3_decode(codes):
+    """torch's own float8_e4m3fn decoding, an implementation independent of the oracle."""
+    t = torch.from_numpy(np.asarray(codes, dtype=np.uint8).copy()).view(torch.float8_e4m3fn)
+    return t.to(torch.float64).numpy()
+
+
+def test_e4m3_decode_named_values():
+    assert oracle.e4m3_to_double(0x38) == 1.0
+    assert oracle.e4m3_to_double(0xB8) == -1.0
+    assert oracle.e4m3_to_double(0x40) == 2.0
+    assert oracle.e4m3_to_double(0x3F) == 1.875
+    assert oracle.e4m3_to_double(0x7E) == 448.0               # largest finite
+    assert oracle.e4m3_to_double(0x08) == 2.0 ** -6           # smallest normal
+    assert oracle.e4m3_to_double(0x01) == 2.0 ** -9           # smallest subnormal
+    assert oracle.e4m3_to_double(0x07) == 7 * 2.0 ** -9
+    assert oracle.e4m3_to_double(0x00) == 0.0
+    assert math.copysign(1.0, oracle.e4m3_to_double(0x80)) == -1.0
+    assert math.isnan(oracle.e4m3_to_double(0x7F)) and math.isnan(oracle.e4m3_to_double(0xFF))
+
+
+def test_e4m3_decode_all_codes_match_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = _torch_e4m3_decode(codes)
+    got = np.array([oracle.e4m3_to_double(int(c)) for c in codes])
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got))
+    assert np.array_equal(ref[~nan], got[~nan])
+    assert not np.isinf(got).any()                               # the format has no infinities
+    pos = got[:0x7F]
+    assert np.all(np.diff(pos) > 0)                              # codes 0x00..0x7E increase strictly
+
+
+def _e4m3_grid():
+    vals = np.array([oracle.e4m3_to_double(c) for c in range(0x7F)])
+    return vals                                                   # 0, 2^-9, ..., 448
+
+
+def test_e4m3_encode_matches_torch_in_range():
+    """Round to nearest, ties to even, against torch's float32 -> float8_e4m3fn
+    cast on values it converts with one rounding: float32 values below 448,
+    including every exact grid value and every midpoint between neighbours."""
+    r = rng(40)
+    grid = _e4m3_grid()
+    mids = (grid[:-1] + grid[1:]) / 2
+    rand = np.exp2(r.uniform(-13, np.log2(448), 4000)) * r.choice([-1, 1], 4000)
+    xs = np.concatenate([grid, -grid, mids, -mids, rand]).astype(np.float32)
+    xs = xs[np.abs(xs) < 448]
+    ref = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.double_to_e4m3(float(x)) for x in xs], dtype=np.uint8)
+    bad = np.nonzero(ref != got)[0]
+    assert bad.size == 0, [(float(xs[i]), int(ref[i]), int(got[i])) for i in bad[:5]]
+
+
+def test_e4m3_encode_saturates_rounds_ties_to_even_and_keeps_nan():
+    assert oracle.double_to_e4m3(448.0) == 0x7E
+    for big in (449.0, 464.0, 480.0, 1e6, math.inf):
+        assert oracle.double_to_e4m3(big) == 0x7E
+        assert oracle.double_to_e4m3(-big) == 0xFE
+    assert oracle.double_to_e4m3(math.nan) == 0x7F
+    assert oracle.double_to_e4m3(2.0 ** -10) == 0x00               # half the smallest subnormal: tie to 0
+    assert oracle.double_to_e4m3(2.0 ** -10 * 1.001) == 0x01
+    assert oracle.double_to_e4m3(3 * 2.0 ** -10) == 0x02           # tie between codes 1 and 2 -> even
+    assert oracle.double_to_e4m3(1.0625) == 0x38                   # tie between 1 and 1.125 -> 1
+    assert oracle.double_to_e4m3(1.1875) == 0x3A                   # tie between 1.125 and 1.25 -> 1.25
+    assert oracle.double_to_e4m3(-0.0) == 0x80
+
+
+def test_fp8_row_exponent_is_the_smallest_fitting_power_of_two():
+    assert oracle.fp8_row_exponent(448.0) == 0
+    assert oracle.fp8_row_exponent(448.0 * (1 + 2.0 ** -30)) == 1
+    assert oracle.fp8_row_exponent(1.0) == -8
+    assert oracle.fp8_row_exponent(0.0) == 0
+    assert oracle.fp8_row_exponent(math.inf) == 0
+    assert oracle.fp8_row_exponent(1e-40) == -126                 # clamped: the scale stays a normal fp32
+    r = rng(41)
+    for amax in np.exp2(r.uniform(-100, 100, 500)):
+        e = oracle.fp8_row_exponent(float(amax))
+        assert amax <= 448.0 * 2.0 ** e and not amax <= 448.0 * 2.0 ** (e - 1)
+
+
+def test_quantize_rows_fp8_picks_the_nearest_scaled_code_by_brute_force():
+    r = rng(42)
+    rows = []
+    for mag in (1e-3, 0.05, 1.0, 300.0, 7e4):
+        rows.append(r.standard_normal(64) * mag)
+    rows.append(np.zeros(64))
+    special = r.standard_normal(64)
+    special[3] = np.nan                                            # NaN does not set the scale
+    special[5] = -0.0
+    rows.append(special)
+    x = np.array(rows, dtype=np.float32)
+    codes, scale = oracle.quantize_rows_fp8(x)
+    grid = _e4m3_grid()
+    cand = np.concatenate([grid, -grid[1:]])
+    cand_codes = np.concatenate([np.arange(0x7F), 0x80 | np.arange(1, 0x7F)])
+    for i, row in enumerate(x.astype(np.float64)):
+        amax = np.nanmax(np.abs(row))
+        e = oracle.fp8_row_exponent(amax)
+        assert scale[i] == 2.0 ** e
+        for d, v in enumerate(row):
+            c = int(codes[i, d])
+            if np.isnan(v):
+                assert c == 0x7F
+                continue
+            dist = np.abs(cand * scale[i] - v)
+            best = cand_codes[dist == dist.min()]
+            if v == 0:
+                assert c in (0x00, 0x80)
+                continue
+            # nearest; a tie goes to the code with an even last bit
+            assert c in best and (best.size == 1 or c % 2 == 0), (i, d, v, c, best)
+
+
+def test_fp8_attention_equals_attention_on_the_stored_values():
+    """Attention over the FP8 store equals the already pinned attention over
+    bf16 rows holding the same values (every E4M3 value times a power of two in
+    range is a bf16 value)."""
+    r = rng(43)
+    N, D = 40, 512
+    x = (r.standard_normal((N, D)) / math.sqrt(D)).astype(np.float32)
+    x[7] *= 300.0
+    codes, scale = oracle.quantize_rows_fp8(x)
+    vals = oracle.fp8_rows_to_double(codes, scale)
+    bits = bf16_bits(vals)
+    assert np.array_equal(bits_bf16_to_f64(bits), vals)              # exact in bf16
+    q = rand_bf16(r, (64, D), 1.0)
+    raw = f16_bits(r.standard_normal((9, D)) / math.sqrt(D))
+    sel = np.array([3, 7, 0, 39, 12], dtype=np.int32)
+    raw_sel = np.arange(9, dtype=np.int32)
+    o8, l8 = oracle.sparse_attention_fp8(q, codes, scale, sel, raw, raw_sel, 1 / math.sqrt(D))
+    ob, lb = oracle.sparse_attention(q, bits, sel, raw, raw_sel, 1 / math.sqrt(D))
+    assert np.array_equal(o8, ob) and np.array_equal(l8, lb)
