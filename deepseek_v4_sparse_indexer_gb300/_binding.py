@@ -36,7 +36,8 @@ EXPORTS = ("ds4a_strerror", "ds4a_version", "ds4a_workspace_bytes", "ds4a_get_de
            "ds4a_debug_inject_error", "ds4a_indexer_score", "ds4a_topk_select",
            "ds4a_topk_select_noalloc", "ds4a_sparse_attn_decode", "ds4a_sparse_attn_prefill",
            "ds4a_dense_attn_decode", "ds4a_kv_push_raw", "ds4a_compressor_pool",
-           "ds4a_sparse_attn_decode_heads", "ds4a_sparse_attn_prefill_heads", "ds4a_dense_attn_decode_heads")
+           "ds4a_sparse_attn_decode_heads", "ds4a_sparse_attn_prefill_heads", "ds4a_dense_attn_decode_heads",
+           "ds4a_rows_to_fp8", "ds4a_sparse_attn_decode_fp8", "ds4a_sparse_attn_prefill_fp8")
 DS4A_TOPK_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -99,6 +100,14 @@ def load(build_if_missing: bool = True):
     L.ds4a_sparse_attn_prefill_heads.restype = _i32
     L.ds4a_dense_attn_decode_heads.argtypes = [_i32] + L.ds4a_dense_attn_decode.argtypes
     L.ds4a_dense_attn_decode_heads.restype = _i32
+    L.ds4a_rows_to_fp8.argtypes = [_vp, _i64, _vp, _vp, _vp]
+    L.ds4a_rows_to_fp8.restype = _i32
+    L.ds4a_sparse_attn_decode_fp8.argtypes = [_vp, _vp, _vp, _i64, _i32, _vp, _vp, _i32, _vp, _i64, _vp, _f32, _vp,
+                                              _vp, _i32, _vp, _sz, _vp]
+    L.ds4a_sparse_attn_decode_fp8.restype = _i32
+    L.ds4a_sparse_attn_prefill_fp8.argtypes = [_vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _vp, _i32, _i32, _f32, _vp,
+                                               _vp, _i32, _vp, _sz, _vp]
+    L.ds4a_sparse_attn_prefill_fp8.restype = _i32
     _lib = L
     return L
 
@@ -356,3 +365,91 @@ def ds4a_compressor_pool(kv, score, out, stream=None):
     U, ratio, width = kv.shape
     st = load().ds4a_compressor_pool(_ptr(kv), _ptr(score), ratio, width, _ptr(out), U, _stream(stream))
     _check(st, "ds4a_compressor_pool")
+
+
+# ----------------------------------------------------------------------------
+# FP8 row store
+# ----------------------------------------------------------------------------
+
+def _req_fp8_rows(rows8, row_scale, n_dims):
+    if rows8.dtype != torch.uint8 or not rows8.is_cuda or rows8.dim() != n_dims or rows8.stride(-1) != 1 \
+            or rows8.shape[-1] != HEAD_DIM or rows8.stride(-2) != HEAD_DIM:
+        raise ValueError("rows8: uint8 CUDA tensor [..., N_cap, 512] of E4M3 codes with contiguous rows")
+    if row_scale.dtype != torch.float32 or not row_scale.is_cuda or row_scale.stride(-1) != 1:
+        raise ValueError("row_scale: float32 CUDA tensor, one scale per row")
+
+
+def ds4a_rows_to_fp8(x, rows8, row_scale, stream=None):
+    """x f32 [n,512] -> rows8 uint8 [n,512] E4M3 codes and row_scale f32 [n]
+    (power-of-two scale per row), both written."""
+    _req(x, "x", torch.float32)
+    _req(rows8, "rows8", torch.uint8)
+    _req(row_scale, "row_scale", torch.float32)
+    n = x.shape[0]
+    if x.shape != (n, HEAD_DIM) or rows8.shape != (n, HEAD_DIM) or row_scale.shape != (n,):
+        raise ValueError("shape mismatch")
+    st = load().ds4a_rows_to_fp8(_ptr(x), n, _ptr(rows8), _ptr(row_scale), _stream(stream))
+    _check(st, "ds4a_rows_to_fp8")
+
+
+def ds4a_sparse_attn_decode_fp8(q, rows8, row_scale, idx, count, raw, n_raw, scale, out, lse=None, ws=None,
+                                stream=None):
+    """ds4a_sparse_attn_decode with the compressed rows as the FP8 store:
+    rows8 uint8 [U,N_cap,512] E4M3 codes, row_scale f32 [U,N_cap] laid out
+    like the rows (unit u's scales start at u * rows8.stride(0) / 512)."""
+    _req(q, "q", torch.bfloat16)
+    _req(idx, "idx", torch.int32)
+    _req(count, "count", torch.int32)
+    _req(n_raw, "n_raw", torch.int32)
+    _req(out, "out", torch.float32)
+    _req_fp8_rows(rows8, row_scale, 3)
+    if raw.dtype != torch.float16 or not raw.is_cuda or raw.dim() != 3 or raw.stride(2) != 1 \
+            or raw.stride(1) != HEAD_DIM or raw.shape[1] != N_SWA:
+        raise ValueError("raw: fp16 CUDA tensor [U, 128, 512] with contiguous rows")
+    U, N_cap = rows8.shape[0], rows8.shape[1]
+    top_k = idx.shape[1]
+    if row_scale.dim() != 2 or row_scale.shape != (U, N_cap) or (U > 1 and
+                                                               row_scale.stride(0) * HEAD_DIM != rows8.stride(0)):
+        raise ValueError("row_scale: [U, N_cap] with unit stride rows8.stride(0) / 512")
+    if q.shape != (U, N_HEAD, HEAD_DIM) or idx.shape[0] != U or count.shape != (U,) or raw.shape[0] != U \
+            or n_raw.shape != (U,) or out.shape != (U, N_HEAD, HEAD_DIM):
+        raise ValueError("shape mismatch")
+    if lse is not None:
+        _req(lse, "lse", torch.float32)
+        if lse.shape != (U, N_HEAD):
+            raise ValueError("lse: [U, 64]")
+    st = load().ds4a_sparse_attn_decode_fp8(_ptr(q), _ptr(rows8), _ptr(row_scale), rows8.stride(0), N_cap, _ptr(idx),
+                                            _ptr(count), top_k, _ptr(raw), raw.stride(0), _ptr(n_raw), float(scale),
+                                            _ptr(out), _ptr(lse), U, _ptr(ws),
+                                            ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream))
+    _check(st, "ds4a_sparse_attn_decode_fp8")
+
+
+def ds4a_sparse_attn_prefill_fp8(q, q_pos, rows8, row_scale, idx, count, raw, raw_pos0, scale, out, lse=None,
+                                 ws=None, stream=None):
+    """ds4a_sparse_attn_prefill with the compressed rows as the FP8 store:
+    rows8 uint8 [N_cap,512], row_scale f32 [N_cap]."""
+    _req(q, "q", torch.bfloat16)
+    _req(q_pos, "q_pos", torch.int32)
+    _req(rows8, "rows8", torch.uint8)
+    _req(row_scale, "row_scale", torch.float32)
+    _req(idx, "idx", torch.int32)
+    _req(count, "count", torch.int32)
+    _req(raw, "raw", torch.float16)
+    _req(out, "out", torch.float32)
+    T = q.shape[0]
+    top_k = idx.shape[1]
+    if q.shape != (T, N_HEAD, HEAD_DIM) or q_pos.shape != (T,) or rows8.dim() != 2 or rows8.shape[1] != HEAD_DIM \
+            or row_scale.shape != (rows8.shape[0],) or idx.shape[0] != T or count.shape != (T,) or raw.dim() != 2 \
+            or raw.shape[1] != HEAD_DIM or out.shape != (T, N_HEAD, HEAD_DIM):
+        raise ValueError("shape mismatch")
+    if lse is not None:
+        _req(lse, "lse", torch.float32)
+        if lse.shape != (T, N_HEAD):
+            raise ValueError("lse: [T, 64]")
+    st = load().ds4a_sparse_attn_prefill_fp8(_ptr(q), _ptr(q_pos), _ptr(rows8), _ptr(row_scale), rows8.shape[0],
+                                             _ptr(idx), _ptr(count), top_k, _ptr(raw), int(raw_pos0), raw.shape[0],
+                                             float(scale), _ptr(out), _ptr(lse), T, _ptr(ws),
+                                             ws.numel() * ws.element_size() if ws is not None else 0,
+                                             _stream(stream))
+    _check(st, "ds4a_sparse_attn_prefill_fp8")

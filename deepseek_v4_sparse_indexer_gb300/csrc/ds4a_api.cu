@@ -245,10 +245,13 @@ ds4a_status check_attn_common(const uint16_t *q, const uint16_t *rows, int N_cap
 namespace {
 // Decode attention over an explicit row list (idx, count, top_k) or, with
 // idx == nullptr, over rows 0 .. count[u]-1 (count = n_rows, top_k = N_cap).
+// rows8 != nullptr: the compressed rows are the FP8 store (rows8, row_scale)
+// and rows is not read.
 ds4a_status attn_decode(int hsplit, const uint16_t *q, const uint16_t *rows, int64_t rows_unit_stride, int N_cap,
                         const int32_t *idx, const int32_t *count, int top_k, const uint16_t *raw,
                         int64_t raw_unit_stride, const int32_t *n_raw, float scale, float *out, float *lse, int U,
-                        void *ws, size_t ws_bytes, void *stream) {
+                        void *ws, size_t ws_bytes, void *stream, const uint8_t *rows8 = nullptr,
+                        const float *row_scale = nullptr) {
     if (!raw || !n_raw || U < 1) return DS4A_EINVAL;
     if (static_cast<long long>(U) * hsplit * kNHead >= (1LL << 31)) return DS4A_EINVAL;
     if (!aligned(raw, 16)) return DS4A_EINVAL;
@@ -287,9 +290,12 @@ ds4a_status attn_decode(int hsplit, const uint16_t *q, const uint16_t *rows, int
     a.status = di->status;
     a.rows_per_unit = rows_per_unit;
     a.raw_per_unit = raw_per_unit;
+    a.rows8 = rows8;
+    a.row_scale = row_scale;
     if (!encode_2d_sw128(&a.tm_q, false, q, kHeadDim, static_cast<unsigned long long>(U) * hsplit * kNHead, 64, 64))
         return DS4A_EINVAL;
-    a.tma_rows = encode_2d_sw128(&a.tm_rows, false, rows, kHeadDim, static_cast<unsigned long long>(total_rows), 64, 64);
+    a.tma_rows = !rows8 &&
+                 encode_2d_sw128(&a.tm_rows, false, rows, kHeadDim, static_cast<unsigned long long>(total_rows), 64, 64);
     a.tma_raw = encode_2d_sw128(&a.tm_raw, true, raw, kHeadDim, static_cast<unsigned long long>(total_raw), 64, 64);
     return launch_sparse_attn(a, di->sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DS4A_OK : DS4A_ECUDA;
 }
@@ -315,6 +321,19 @@ ds4a_status ds4a_sparse_attn_decode(const uint16_t *q, const uint16_t *rows, int
                                          raw_unit_stride, n_raw, scale, out, lse, U, ws, ws_bytes, stream);
 }
 
+ds4a_status ds4a_sparse_attn_decode_fp8(const uint16_t *q, const uint8_t *rows8, const float *row_scale,
+                                        int64_t rows_unit_stride, int N_cap, const int32_t *idx,
+                                        const int32_t *count, int top_k, const uint16_t *raw,
+                                        int64_t raw_unit_stride, const int32_t *n_raw, float scale, float *out,
+                                        float *lse, int U, void *ws, size_t ws_bytes, void *stream) {
+    if (ds4a_status inj = take_injected()) return inj;
+    const uint16_t *as16 = reinterpret_cast<const uint16_t *>(rows8);   // only its pointer checks are used
+    if (ds4a_status st = check_attn_common(q, as16, N_cap, idx, count, top_k, out)) return st;
+    if (!row_scale || !aligned(row_scale, 4)) return DS4A_EINVAL;
+    return attn_decode(1, q, as16, rows_unit_stride, N_cap, idx, count, top_k, raw, raw_unit_stride, n_raw, scale,
+                       out, lse, U, ws, ws_bytes, stream, rows8, row_scale);
+}
+
 ds4a_status ds4a_dense_attn_decode_heads(int n_head, const uint16_t *q, const uint16_t *rows,
                                          int64_t rows_unit_stride, int N_cap, const int32_t *n_rows,
                                          const uint16_t *raw, int64_t raw_unit_stride, const int32_t *n_raw,
@@ -336,15 +355,12 @@ ds4a_status ds4a_dense_attn_decode(const uint16_t *q, const uint16_t *rows, int6
                                         scale, out, lse, U, ws, ws_bytes, stream);
 }
 
-ds4a_status ds4a_sparse_attn_prefill_heads(int n_head, const uint16_t *q, const int32_t *q_pos,
-                                           const uint16_t *rows, int N_cap, const int32_t *idx,
-                                           const int32_t *count, int top_k, const uint16_t *raw, int32_t raw_pos0,
-                                           int n_raw_rows, float scale, float *out, float *lse, int T, void *ws,
-                                           size_t ws_bytes, void *stream) {
-    if (ds4a_status inj = take_injected()) return inj;
-    if (n_head != 64 && n_head != 128) return DS4A_EUNSUPPORTED;
-    const int hsplit = n_head / kNHead;
-    if (ds4a_status st = check_attn_common(q, rows, N_cap, idx, count, top_k, out)) return st;
+namespace {
+ds4a_status attn_prefill(int hsplit, const uint16_t *q, const int32_t *q_pos, const uint16_t *rows, int N_cap,
+                         const int32_t *idx, const int32_t *count, int top_k, const uint16_t *raw, int32_t raw_pos0,
+                         int n_raw_rows, float scale, float *out, float *lse, int T, void *ws, size_t ws_bytes,
+                         void *stream, const uint8_t *rows8, const float *row_scale) {
+    const int n_head = hsplit * kNHead;
     if (!q_pos || T < 1 || n_raw_rows < 0) return DS4A_EINVAL;
     if (n_raw_rows > 0 && (!raw || !aligned(raw, 16))) return DS4A_EINVAL;
     if (!(scale == scale)) return DS4A_EINVAL;
@@ -376,12 +392,41 @@ ds4a_status ds4a_sparse_attn_prefill_heads(int n_head, const uint16_t *q, const 
     a.status = di->status;
     a.rows_per_unit = 0;
     a.raw_per_unit = 0;
+    a.rows8 = rows8;
+    a.row_scale = row_scale;
     if (!encode_2d_sw128(&a.tm_q, false, q, kHeadDim, static_cast<unsigned long long>(T) * n_head, 64, 64))
         return DS4A_EINVAL;
-    a.tma_rows = encode_2d_sw128(&a.tm_rows, false, rows, kHeadDim, static_cast<unsigned long long>(N_cap), 64, 64);
+    a.tma_rows = !rows8 &&
+                 encode_2d_sw128(&a.tm_rows, false, rows, kHeadDim, static_cast<unsigned long long>(N_cap), 64, 64);
     a.tma_raw = n_raw_rows > 0 &&
                 encode_2d_sw128(&a.tm_raw, true, raw, kHeadDim, static_cast<unsigned long long>(n_raw_rows), 64, 64);
     return launch_sparse_attn(a, di->sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DS4A_OK : DS4A_ECUDA;
+}
+}  // namespace
+
+ds4a_status ds4a_sparse_attn_prefill_heads(int n_head, const uint16_t *q, const int32_t *q_pos,
+                                           const uint16_t *rows, int N_cap, const int32_t *idx,
+                                           const int32_t *count, int top_k, const uint16_t *raw, int32_t raw_pos0,
+                                           int n_raw_rows, float scale, float *out, float *lse, int T, void *ws,
+                                           size_t ws_bytes, void *stream) {
+    if (ds4a_status inj = take_injected()) return inj;
+    if (n_head != 64 && n_head != 128) return DS4A_EUNSUPPORTED;
+    if (ds4a_status st = check_attn_common(q, rows, N_cap, idx, count, top_k, out)) return st;
+    return attn_prefill(n_head / kNHead, q, q_pos, rows, N_cap, idx, count, top_k, raw, raw_pos0, n_raw_rows, scale,
+                        out, lse, T, ws, ws_bytes, stream, nullptr, nullptr);
+}
+
+ds4a_status ds4a_sparse_attn_prefill_fp8(const uint16_t *q, const int32_t *q_pos, const uint8_t *rows8,
+                                         const float *row_scale, int N_cap, const int32_t *idx,
+                                         const int32_t *count, int top_k, const uint16_t *raw, int32_t raw_pos0,
+                                         int n_raw_rows, float scale, float *out, float *lse, int T, void *ws,
+                                         size_t ws_bytes, void *stream) {
+    if (ds4a_status inj = take_injected()) return inj;
+    const uint16_t *as16 = reinterpret_cast<const uint16_t *>(rows8);   // only its pointer checks are used
+    if (ds4a_status st = check_attn_common(q, as16, N_cap, idx, count, top_k, out)) return st;
+    if (!row_scale || !aligned(row_scale, 4)) return DS4A_EINVAL;
+    return attn_prefill(1, q, q_pos, as16, N_cap, idx, count, top_k, raw, raw_pos0, n_raw_rows, scale, out, lse, T,
+                        ws, ws_bytes, stream, rows8, row_scale);
 }
 
 ds4a_status ds4a_sparse_attn_prefill(const uint16_t *q, const int32_t *q_pos, const uint16_t *rows, int N_cap,
@@ -390,6 +435,19 @@ ds4a_status ds4a_sparse_attn_prefill(const uint16_t *q, const int32_t *q_pos, co
                                      void *ws, size_t ws_bytes, void *stream) {
     return ds4a_sparse_attn_prefill_heads(64, q, q_pos, rows, N_cap, idx, count, top_k, raw, raw_pos0, n_raw_rows,
                                           scale, out, lse, T, ws, ws_bytes, stream);
+}
+
+ds4a_status ds4a_rows_to_fp8(const float *x, int64_t n_rows, uint8_t *rows8, float *row_scale, void *stream) {
+    if (ds4a_status inj = take_injected()) return inj;
+    if (n_rows < 0 || (n_rows > 0 && (!x || !rows8 || !row_scale))) return DS4A_EINVAL;
+    if (n_rows == 0) return DS4A_OK;
+    if (!aligned(x, 16) || !aligned(rows8, 16) || !aligned(row_scale, 4)) return DS4A_EINVAL;
+    if (n_rows >= (1LL << 40) / kHeadDim) return DS4A_EINVAL;
+    DevInfo *di = nullptr;
+    if (ds4a_status st = current_device(&di)) return st;
+    return launch_rows_to_fp8(x, n_rows, rows8, row_scale, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? DS4A_OK
+               : DS4A_ECUDA;
 }
 
 ds4a_status ds4a_kv_push_raw(const float *kv, uint16_t *raw, int64_t raw_unit_stride, const int32_t *pos,

@@ -61,6 +61,8 @@ struct AttnArgs {
     long long raw_per_unit;      // decode: row offset between units' raw rings
     const uint16_t *q;           // [units][64][512] bf16
     const uint16_t *rows;        // bf16 rows base
+    const uint8_t *rows8;        // FP8 row store (E4M3 codes [row][512]) or null: then rows is unused
+    const float *row_scale;      // FP8 row store: power-of-two scale per row (same row index)
     long long rows_unit_stride;  // elements (0 in prefill: one shared row store)
     int N_cap;
     const int32_t *idx;          // [units][top_k]
@@ -88,6 +90,7 @@ cudaError_t launch_kv_push_raw(const float *kv, uint16_t *raw, long long raw_uni
                                int32_t *n_raw, int U, uint32_t *status, cudaStream_t s);
 cudaError_t launch_compressor_pool(const float *kv, const float *score, int ratio, int width, float *out, int U,
                                    cudaStream_t s);
+cudaError_t launch_rows_to_fp8(const float *x, long long n_rows, uint8_t *codes, float *row_scale, cudaStream_t s);
 
 // ---- shared host helpers of the C ABI -------------------------------------
 // Status word address and SM count of the current device (set up on first use).

@@ -2,9 +2,14 @@
 //   §3-1  the raw window keeps the last 128 tokens' rows rounded through f16;
 //   §3-2  the compressor pools a frontier of `ratio` rows (4 or 128) into one
 //         compressed row with a per-column softmax of learned scores.
+//   §3-2  the new compressed row goes through an FP8 quantisation round trip
+//         before it is stored: here its stored form, E4M3 codes with one
+//         power-of-two scale per row (the pages name no format or scaling;
+//         this is the library's reading), which keeps exactly the values the
+//         round trip produces.
 // The projections that produce kv and scores, the positional bias and the
-// normalisation / RoPE / FP8 steps after pooling need trained weights and are
-// not part of this library; these kernels take the frontier as given.
+// normalisation / RoPE steps after pooling need trained weights and are not
+// part of this library; these kernels take their inputs as given.
 //
 // The raw window here is a ring: the row of position p goes to slot p % 128,
 // so the window holds the same rows as the pages' oldest-first window (which
@@ -110,7 +115,66 @@ __global__ void __launch_bounds__(kPoolThreads) compressor_pool_kernel(const flo
     reinterpret_cast<float4 *>(out + u * width)[c] = o;
 }
 
+// One warp per row of 512 fp32 values; lane l owns elements 16l .. 16l+15.
+//   amax  = max |x| over the row (fmaxf skips NaN);
+//   e     = the smallest integer with amax <= 448 * 2^e, within [-126, 127]
+//           (0 when amax is 0 or infinite): with amax = m * 2^k, m in [0.5, 1),
+//           e = k - 9 if m <= 0.875 (448 = 0.875 * 2^9), else k - 8;
+//   codes = E4M3 of x * 2^-e, rounded to nearest even, saturating at 448
+//           (the scaling by a power of two is exact).
+constexpr int kFp8RowsPerBlock = 4;
+
+DS4A_DEV int fp8_row_exponent(float amax) {
+    const uint32_t b = __float_as_uint(amax);
+    const int field = static_cast<int>(b >> 23);
+    if (amax == 0.f || field >= 255) return 0;            // zero, infinity
+    if (field == 0) return -126;                           // subnormal: below 448 * 2^-127
+    const int k = field - 126;                             // amax = m * 2^k, m in [0.5, 1)
+    int e = (b & 0x7FFFFFu) <= 0x600000u ? k - 9 : k - 8;  // m <= 0.875 <=> fraction <= 0.75 * 2^23
+    return e < -126 ? -126 : (e > 127 ? 127 : e);
+}
+
+DS4A_DEV uint32_t e4m3x4(float a, float b, float c, float d) {
+    uint16_t lo, hi;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));   // a -> low byte
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+__global__ void __launch_bounds__(32 * kFp8RowsPerBlock) rows_to_fp8_kernel(const float *__restrict__ x,
+                                                                          long long n_rows, uint8_t *codes,
+                                                                          float *row_scale) {
+    const long long row = static_cast<long long>(blockIdx.x) * kFp8RowsPerBlock + (threadIdx.x >> 5);
+    if (row >= n_rows) return;
+    const int lane = threadIdx.x & 31;
+    const float4 *src = reinterpret_cast<const float4 *>(x + row * kHeadDim) + lane * 4;
+    float4 v[4];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[i] = src[i];
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const int e = fp8_row_exponent(amax);
+    const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);   // 2^-e (e <= 126 for finite amax)
+    uint4 out;
+    uint32_t *o = reinterpret_cast<uint32_t *>(&out);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = e4m3x4(v[i].x * inv, v[i].y * inv, v[i].z * inv, v[i].w * inv);
+    reinterpret_cast<uint4 *>(codes + row * kHeadDim)[lane] = out;
+    if (lane == 0) row_scale[row] = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+}
+
 }  // namespace
+
+cudaError_t launch_rows_to_fp8(const float *x, long long n_rows, uint8_t *codes, float *row_scale, cudaStream_t s) {
+    const long long blocks = (n_rows + kFp8RowsPerBlock - 1) / kFp8RowsPerBlock;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    rows_to_fp8_kernel<<<static_cast<unsigned>(blocks), 32 * kFp8RowsPerBlock, 0, s>>>(x, n_rows, codes, row_scale);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_kv_push_raw(const float *kv, uint16_t *raw, long long raw_unit_stride, const int32_t *pos,
                                int32_t *n_raw, int U, uint32_t *status, cudaStream_t s) {

@@ -15,7 +15,12 @@
 //            thread fences its copies into the async proxy before its warp
 //            arrives on the buffer's barrier.  A whole tile of contiguous
 //            rows (the raw window, or a dense row list) is instead eight TMA
-//            tile loads (64 columns x 64 rows each) issued by one thread;
+//            tile loads (64 columns x 64 rows each) issued by one thread.
+//            With the FP8 row store, a compressed row is 512 E4M3 codes and a
+//            power-of-two scale: lane l loads codes 16l .. 16l+15 of a row (one
+//            row per warp instruction, into registers), and the warp writes
+//            them out as exact bf16 values (code * scale) into the same
+//            swizzled tile, so the GEMMs below do not change;
 //   logits   warp 4 (one thread): S[64 heads x 64 rows] = q . X^T, 32 UMMAs
 //            (M=64, N=64, K=16, both operands K-major) into one of two TMEM
 //            buffers (head h of the M=64 accumulator sits in TMEM lane
@@ -41,6 +46,8 @@
 //
 // Every wait is bounded (DS4A_DEV_TIMEOUT); on timeout the CTA drains what it
 // issued (bounded), frees TMEM and returns.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -142,6 +149,26 @@ DS4A_DEV void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
         : "memory");
 }
 DS4A_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Eight E4M3 codes (two words) times a power-of-two scale as eight bf16
+// (four words, dims in order).  E4M3 -> f16 is exact, and so are the scaling
+// in fp32 and the rounding to bf16 of a value with at most four significant
+// bits (down to 2^-133, the smallest bf16 subnormal).
+DS4A_DEV void e4m3x8_to_bf16(uint32_t w0, uint32_t w1, float s, uint32_t (&o)[4]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t w = j < 2 ? w0 : w1;
+        const uint16_t pair = static_cast<uint16_t>(w >> (16 * (j & 1)));
+        uint32_t h2;
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+        o[j] = pack2<false>(f.x * s, f.y * s);
+    }
+}
+DS4A_DEV void st_shared_v4(uint32_t addr, const uint32_t (&v)[4]) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
+                 : "memory");
+}
 
 DS4A_DEV bool wait_drain(uint64_t *bar, uint32_t parity) {
     const uint64_t t0 = globaltimer_ns();
@@ -361,8 +388,28 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
             const int first = raw_tile ? (ct_ - cm.ct) * TR : ct_ * TR;
             const bool tma_tile = raw_tile ? (a.tma_raw && first + TR <= cm.nrw)
                                            : (a.tma_rows && !a.idx && first + TR <= cm.cnt);
+            const bool fp8_tile = !raw_tile && a.rows8 != nullptr;
             const uint32_t buf = smem_u32(sX) + xb * kXBuf;
-            if (tma_tile) {
+            uint4 c8[kGroupsPerWarp][4];                 // FP8 tile: codes of the group's four rows
+            float s8[kGroupsPerWarp][4];                 // and their scales
+            if (fp8_tile) {
+#pragma unroll
+                for (int k = 0; k < kGroupsPerWarp; ++k) {
+                    const int g = gw + k * kGatherWarps;
+                    if (g >= kRowGroups) continue;       // warp-uniform
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int sr = __shfl_sync(0xffffffffu, src[k], 8 * i);   // row 4g + i (lanes 8i.. hold it)
+                        if (sr >= 0) {
+                            c8[k][i] = __ldg(reinterpret_cast<const uint4 *>(a.rows8 + static_cast<long long>(sr) * kHeadDim) + lane);
+                            s8[k][i] = __ldg(a.row_scale + sr);
+                        } else {
+                            c8[k][i] = make_uint4(0u, 0u, 0u, 0u);
+                            s8[k][i] = 0.f;
+                        }
+                    }
+                }
+            } else if (tma_tile) {
                 if (gw == 0 && lane == 0) {
                     const int y = static_cast<int>((raw_tile ? cm.raw_row0 : cm.comp_row0) + first);
                     mbar_arrive_expect_tx(&x_full[xb], kXBuf);      // also this warp's arrival
@@ -388,6 +435,34 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
             // While the copies land: the row list of the next tile.
             advance(cit, ct_, cm);
             if (cit < n_items) fetch_rows(cm, ct_, rv);
+            if (fp8_tile) {
+                // dims 16l .. 16l+15 are 16-byte chunks 2(l%4) and 2(l%4)+1 of the
+                // 64-column block l/4.  Lanes of odd blocks write their second
+                // chunk first, so the eight lanes of a store phase hit eight
+                // different 16-byte bank groups.
+                const int blk = lane >> 2, c0 = 2 * (lane & 3), odd = blk & 1;
+#pragma unroll
+                for (int k = 0; k < kGroupsPerWarp; ++k) {
+                    const int g = gw + k * kGatherWarps;
+                    if (g >= kRowGroups) continue;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int r = 4 * g + i;
+                        uint32_t lo[4], hi[4];
+                        e4m3x8_to_bf16(c8[k][i].x, c8[k][i].y, s8[k][i], lo);
+                        e4m3x8_to_bf16(c8[k][i].z, c8[k][i].w, s8[k][i], hi);
+                        const uint32_t rowa = buf + blk * kXBlk + r * 128;
+                        const uint32_t a0 = rowa + ((c0 ^ (r & 7)) << 4), a1 = rowa + (((c0 + 1) ^ (r & 7)) << 4);
+                        if (odd) {
+                            st_shared_v4(a1, hi);
+                            st_shared_v4(a0, lo);
+                        } else {
+                            st_shared_v4(a0, lo);
+                            st_shared_v4(a1, hi);
+                        }
+                    }
+                }
+            }
             cp_async_wait<0>();
             fence_proxy_async();
             __syncwarp();

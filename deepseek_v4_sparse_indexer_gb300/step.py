@@ -5,7 +5,12 @@ PrefillStep: one chunk of T queries of one sequence over a causal row store.
 DenseStep: the ratio-128 layers' attention over all compressed rows (no
 indexer, so no score or select).
 ProducerStep: the cache producer at a ratio boundary: the raw-window push of
-the new token and the compressor pooling of the frontier.
+the new token, the compressor pooling of the frontier and (fp8=True) the FP8
+store of the pooled row.
+
+DecodeStep and PrefillStep with fp8=True read the compressed rows from the FP8
+row store (x["rows8"] E4M3 codes, x["row_scale"] per-row scales) instead of
+the bf16 rows.
 
 Both own their outputs and workspaces (allocated once, reused every call, so a
 call can be captured in a CUDA graph) and run indexer score -> top-k select ->
@@ -25,8 +30,10 @@ def _ws(nbytes, device):
 
 
 class DecodeStep:
-    def __init__(self, U, N_cap, top_k=512, device="cuda", n_head=B.N_HEAD):
-        self.U, self.N_cap, self.top_k, self.n_head = U, N_cap, top_k, n_head
+    def __init__(self, U, N_cap, top_k=512, device="cuda", n_head=B.N_HEAD, fp8=False):
+        if fp8 and n_head != B.N_HEAD:
+            raise ValueError("the FP8 row store is read with 64 query heads")
+        self.U, self.N_cap, self.top_k, self.n_head, self.fp8 = U, N_cap, top_k, n_head, fp8
         dev = torch.device(device)
         flag = B.DS4A_OP_FLAG_128_HEADS if n_head == 128 else 0
         self.scores = torch.empty(U, 1, N_cap, dtype=torch.float32, device=dev)
@@ -46,9 +53,13 @@ class DecodeStep:
         B.ds4a_topk_select(self.scores, x["n_rows"], self.top_k, self.idx, self.count, self.ws_topk, stream=stream)
 
     def attend(self, x, scale=DEFAULT_SCALE, stream=None):
-        B.ds4a_sparse_attn_decode_heads(self.n_head, x["q"], x["rows"], self.idx.view(self.U, self.top_k),
-                                        self.count.view(self.U), x["raw"], x["n_raw"], scale, self.out, self.lse,
-                                        self.ws_attn, stream=stream)
+        idx, count = self.idx.view(self.U, self.top_k), self.count.view(self.U)
+        if self.fp8:
+            B.ds4a_sparse_attn_decode_fp8(x["q"], x["rows8"], x["row_scale"], idx, count, x["raw"], x["n_raw"], scale,
+                                          self.out, self.lse, self.ws_attn, stream=stream)
+            return
+        B.ds4a_sparse_attn_decode_heads(self.n_head, x["q"], x["rows"], idx, count, x["raw"], x["n_raw"], scale,
+                                        self.out, self.lse, self.ws_attn, stream=stream)
 
     def __call__(self, x, scale=DEFAULT_SCALE, stream=None):
         self.score(x, stream)
@@ -58,8 +69,10 @@ class DecodeStep:
 
 
 class PrefillStep:
-    def __init__(self, T, N_cap, top_k=512, device="cuda", n_head=B.N_HEAD):
-        self.T, self.N_cap, self.top_k, self.n_head = T, N_cap, top_k, n_head
+    def __init__(self, T, N_cap, top_k=512, device="cuda", n_head=B.N_HEAD, fp8=False):
+        if fp8 and n_head != B.N_HEAD:
+            raise ValueError("the FP8 row store is read with 64 query heads")
+        self.T, self.N_cap, self.top_k, self.n_head, self.fp8 = T, N_cap, top_k, n_head, fp8
         dev = torch.device(device)
         flag = B.DS4A_OP_FLAG_128_HEADS if n_head == 128 else 0
         self.scores = torch.empty(1, T, N_cap, dtype=torch.float32, device=dev)
@@ -80,9 +93,13 @@ class PrefillStep:
         B.ds4a_topk_select(self.scores, x["n_rows"], self.top_k, self.idx, self.count, self.ws_topk, stream=stream)
 
     def attend(self, x, scale=DEFAULT_SCALE, stream=None):
-        B.ds4a_sparse_attn_prefill_heads(self.n_head, x["q"], x["q_pos"], x["rows"], self.idx.view(self.T, self.top_k),
-                                         self.count.view(self.T), x["raw"], x["raw_pos0"], scale, self.out,
-                                         self.lse, self.ws_attn, stream=stream)
+        idx, count = self.idx.view(self.T, self.top_k), self.count.view(self.T)
+        if self.fp8:
+            B.ds4a_sparse_attn_prefill_fp8(x["q"], x["q_pos"], x["rows8"], x["row_scale"], idx, count, x["raw"],
+                                           x["raw_pos0"], scale, self.out, self.lse, self.ws_attn, stream=stream)
+            return
+        B.ds4a_sparse_attn_prefill_heads(self.n_head, x["q"], x["q_pos"], x["rows"], idx, count, x["raw"],
+                                         x["raw_pos0"], scale, self.out, self.lse, self.ws_attn, stream=stream)
 
     def __call__(self, x, scale=DEFAULT_SCALE, stream=None):
         self.score(x, stream)
@@ -110,9 +127,14 @@ class DenseStep:
 
 
 class ProducerStep:
-    def __init__(self, U, width=B.HEAD_DIM, device="cuda"):
-        self.U, self.width = U, width
-        self.out = torch.empty(U, width, dtype=torch.float32, device=torch.device(device))
+    def __init__(self, U, width=B.HEAD_DIM, device="cuda", fp8=False):
+        if fp8 and width != B.HEAD_DIM:
+            raise ValueError("the FP8 row store holds 512-wide rows")
+        self.U, self.width, self.fp8 = U, width, fp8
+        dev = torch.device(device)
+        self.out = torch.empty(U, width, dtype=torch.float32, device=dev)
+        self.rows8 = torch.empty(U, width, dtype=torch.uint8, device=dev) if fp8 else None
+        self.row_scale = torch.empty(U, dtype=torch.float32, device=dev) if fp8 else None
 
     def push(self, x, stream=None):
         B.ds4a_kv_push_raw(x["row"], x["raw"], x["pos"], x["n_raw"], stream=stream)
@@ -120,7 +142,12 @@ class ProducerStep:
     def pool(self, x, stream=None):
         B.ds4a_compressor_pool(x["kv"], x["score"], self.out, stream=stream)
 
+    def store_fp8(self, stream=None):
+        B.ds4a_rows_to_fp8(self.out, self.rows8, self.row_scale, stream=stream)
+
     def __call__(self, x, stream=None):
         self.push(x, stream)
         self.pool(x, stream)
+        if self.fp8:
+            self.store_fp8(stream)
         return self.out

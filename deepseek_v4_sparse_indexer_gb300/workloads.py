@@ -49,6 +49,7 @@ class Workload:
     heavy_scale: float = 4.0
     seed: int = 0
     heads: int = 64        # query heads (64 Flash, 128 Pro)
+    fp8: bool = False      # compressed rows kept in the FP8 row store (E4M3 codes + row scales)
     extra: dict = field(default_factory=dict)
 
     @property
@@ -78,6 +79,12 @@ WORKLOADS = {
     # sequences x 20 ratio-128 layers, push the new token's raw row and pool
     # the 128-row (kv, score) frontier of width 512 into one compressed row.
     "pool_32x20x128": Workload("pool_32x20x128", "pool", 32 * 20, 128, top_k=0),
+    # The decode and prefill workloads with the compressed rows in the FP8 row
+    # store (§3-2: the compressed row's FP8 round trip): the same fp32 values,
+    # stored as E4M3 codes with one power-of-two scale per row.
+    "decode_fp8_32x43x65536": Workload("decode_fp8_32x43x65536", "decode", 32 * 43, 65536, fp8=True),
+    "prefill_fp8_2048x65536": Workload("prefill_fp8_2048x65536", "prefill", 1, 65536 + 512,
+                                       queries=2048, extra=dict(prior_rows=65536), fp8=True),
 }
 
 
@@ -104,6 +111,33 @@ def normal_fill_(dst: torch.Tensor, d: int, seed: int, stream: int, chunk_elems:
     return dst
 
 
+def normal_fp32_chunks(n_rows: int, d: int, seed: int, stream: int, device="cpu", chunk_elems: int = 1 << 28):
+    """The fp32 values normal_fill_ draws for a [n_rows, d] tensor with the same
+    (seed, stream), before its rounding, chunk by chunk: yields (first_row,
+    fp32 [rows, d]).  The FP8 row store is built from these values by the
+    caller's own quantiser (this module does none of that arithmetic)."""
+    assert chunk_elems % d == 0
+    g = _gen(seed, stream, device)
+    inv = 1.0 / math.sqrt(d)
+    total = n_rows * d
+    for s in range(0, total, chunk_elems):
+        n = min(chunk_elems, total - s)
+        t = torch.randn(n, generator=g, device=device, dtype=torch.float32)
+        t.mul_(inv)
+        yield s // d, t.view(-1, d)
+
+
+def decode_rows_fp32_chunks(units, n_cap, device="cpu", seed=0):
+    """The decode workload's compressed rows (make_decode_inputs' x["rows"]) as
+    fp32 values before their bf16 rounding, in chunks of whole rows."""
+    return normal_fp32_chunks(units * n_cap, HEAD_DIM, seed, 6, device)
+
+
+def prefill_rows_fp32_chunks(n_cap, device="cpu", seed=0):
+    """make_prefill_inputs' x["rows"] as fp32 values before rounding, in chunks."""
+    return normal_fp32_chunks(n_cap, HEAD_DIM, seed, 16, device)
+
+
 def uniform_fill_(dst: torch.Tensor, seed: int, stream: int):
     g = _gen(seed, stream, dst.device)
     dst.copy_(torch.rand(dst.shape, generator=g, device=dst.device, dtype=torch.float32))
@@ -126,13 +160,15 @@ def apply_heavy_tail_(ik: torch.Tensor, frac: float, scale: float, seed: int, st
 
 
 def make_decode_inputs(units, n_cap, device="cpu", seed=0, n_rows=None, n_raw=None,
-                       heavy_frac=0.0, heavy_scale=4.0, q_scale=1.0, with_indexer=True, n_head=N_HEAD):
+                       heavy_frac=0.0, heavy_scale=4.0, q_scale=1.0, with_indexer=True, n_head=N_HEAD,
+                       with_rows=True):
     """Decode-step inputs for `units` independent (sequence x layer) caches.
 
     n_rows / n_raw: per-unit valid compressed rows / raw-window slots (int or
     list); default full.  q_scale multiplies the attention query (x32 gives a
     peaked softmax for stress cases).  with_indexer=False leaves out iq, w and
-    ik (the ratio-128 layers have no indexer).
+    ik (the ratio-128 layers have no indexer).  with_rows=False leaves out the
+    bf16 rows (an FP8 row store is built from decode_rows_fp32_chunks instead).
     """
     dev = torch.device(device)
     bf, hf = torch.bfloat16, torch.float16
@@ -146,7 +182,8 @@ def make_decode_inputs(units, n_cap, device="cpu", seed=0, n_rows=None, n_raw=No
         x["ik"] = normal_fill_(torch.empty(units, n_cap, IDX_DIM, dtype=bf, device=dev), IDX_DIM, seed, 4)
         if heavy_frac > 0:
             apply_heavy_tail_(x["ik"], heavy_frac, heavy_scale, seed, 5)
-    x["rows"] = normal_fill_(torch.empty(units, n_cap, HEAD_DIM, dtype=bf, device=dev), HEAD_DIM, seed, 6)
+    if with_rows:
+        x["rows"] = normal_fill_(torch.empty(units, n_cap, HEAD_DIM, dtype=bf, device=dev), HEAD_DIM, seed, 6)
     x["raw"] = normal_fill_(torch.empty(units, N_SWA, HEAD_DIM, dtype=hf, device=dev), HEAD_DIM, seed, 7)
     nr = n_rows if n_rows is not None else n_cap
     nw = n_raw if n_raw is not None else N_SWA
@@ -171,7 +208,7 @@ def prefill_positions(T, prior_rows, ratio=COMPRESS_RATIO):
     return q_pos, row_pos, P0
 
 
-def make_prefill_inputs(T, prior_rows, device="cpu", seed=0, q_scale=1.0, n_head=N_HEAD):
+def make_prefill_inputs(T, prior_rows, device="cpu", seed=0, q_scale=1.0, n_head=N_HEAD, with_rows=True):
     """Prefill-chunk inputs: T queries over prior_rows + T/4 compressed rows, and
     a contiguous fp16 raw buffer holding positions P0-128 .. P0+T-1."""
     dev = torch.device(device)
@@ -185,7 +222,8 @@ def make_prefill_inputs(T, prior_rows, device="cpu", seed=0, q_scale=1.0, n_head
     x["iq"] = normal_fill_(torch.empty(T, N_IDX_HEAD, IDX_DIM, dtype=bf, device=dev), IDX_DIM, seed, 12)
     x["w"] = uniform_fill_(torch.empty(T, N_IDX_HEAD, dtype=torch.float32, device=dev), seed, 13)
     x["ik"] = normal_fill_(torch.empty(n_cap, IDX_DIM, dtype=bf, device=dev), IDX_DIM, seed, 14)
-    x["rows"] = normal_fill_(torch.empty(n_cap, HEAD_DIM, dtype=bf, device=dev), HEAD_DIM, seed, 16)
+    if with_rows:
+        x["rows"] = normal_fill_(torch.empty(n_cap, HEAD_DIM, dtype=bf, device=dev), HEAD_DIM, seed, 16)
     raw_pos0 = max(P0 - N_SWA, 0)
     n_raw_rows = P0 + T - raw_pos0
     x["raw"] = normal_fill_(torch.empty(n_raw_rows, HEAD_DIM, dtype=hf, device=dev), HEAD_DIM, seed, 17)

@@ -337,14 +337,71 @@ ds4a_status ds4a_kv_push_raw(const float *kv, uint16_t *raw, int64_t raw_unit_st
  *
  *    and out[u,j] = 0 when no score of the column is finite.  fp32 throughout.
  *    The projections that produce kv and score, the positional bias added to
- *    the scores and the steps after pooling (normalisation, RoPE, FP8 round
- *    trip) need trained weights and are not part of this library.
+ *    the scores and the normalisation and RoPE after pooling need trained
+ *    weights and are not part of this library; the FP8 round trip is 4c.
  *
  *    kv, score  fp32 [U][ratio][width] (device).    out  fp32 [U][width] (device).
  *    ratio >= 1; width a positive multiple of 4; pointers 16-byte aligned.
  */
 ds4a_status ds4a_compressor_pool(const float *kv, const float *score, int ratio, int width,
                                  float *out, int U, void *stream);
+
+/*
+ * 4c. FP8 row store (§3-2: after pooling, the new compressed row is
+ *    normalised, its tail rotated, and put through an FP8 quantisation round
+ *    trip before it is stored).  The pages name neither the FP8 format nor
+ *    its scaling; this library reads the round trip as E4M3 codes (1 sign, 4
+ *    exponent bits with bias 7, 3 fraction bits; no infinities; largest
+ *    finite 448) with one power-of-two scale per row, and stores exactly that
+ *    pair, so the stored values are the round trip's values.  Per row r of
+ *    512 fp32 values x:
+ *
+ *      amax        = max_d |x[r,d]|            (NaN elements do not count)
+ *      e           = the smallest integer with amax <= 448 * 2^e, kept in
+ *                    [-126, 127]; e = 0 when amax is 0 or infinite
+ *      row_scale[r]= 2^e
+ *      rows8[r,d]  = E4M3 of x[r,d] / 2^e, rounded to nearest (ties to
+ *                    even), saturating at +-448; NaN stays NaN (code 0x7F)
+ *
+ *    The stored value of element (r,d) is e4m3(rows8[r,d]) * row_scale[r].
+ *    The normalisation and RoPE before it need trained weights and are not
+ *    part of this library.
+ *
+ *    x          fp32 [n_rows][512] (device), 16-byte aligned.
+ *    rows8      uint8 [n_rows][512] (device, written), 16-byte aligned.
+ *    row_scale  fp32 [n_rows] (device, written), 4-byte aligned.
+ *    n_rows >= 0 (0: nothing is launched).
+ */
+ds4a_status ds4a_rows_to_fp8(const float *x, int64_t n_rows, uint8_t *rows8, float *row_scale,
+                             void *stream);
+
+/*
+ * 3e. Sparse attention over the FP8 row store (4c): 3a and 3b with the
+ *    compressed rows given as E4M3 codes and per-row scales instead of bf16.
+ *    Element d of compressed row i is e4m3(rows8[i][d]) * row_scale[i]; the
+ *    kernel expands each gathered row to exactly these values in bf16 (exact
+ *    down to 2^-133) and multiplies as 3a does.  Half the gather bytes of the
+ *    bf16 store.  64 query heads.
+ *
+ *    rows8      uint8 [U][N_cap][512] E4M3 codes; unit u at rows8 +
+ *               u*rows_unit_stride (elements = bytes), 16-byte aligned (device).
+ *    row_scale  fp32 powers of two, one per row, indexed like the rows: unit
+ *               u's row r at row_scale[u*rows_unit_stride/512 + r] (device).
+ *    Everything else, including the workspace (DS4A_OP_SPARSE_ATTN_DECODE /
+ *    _PREFILL) and the bounds reporting, is as in 3a / 3b.
+ */
+ds4a_status ds4a_sparse_attn_decode_fp8(const uint16_t *q, const uint8_t *rows8,
+                                        const float *row_scale, int64_t rows_unit_stride,
+                                        int N_cap, const int32_t *idx, const int32_t *count,
+                                        int top_k, const uint16_t *raw, int64_t raw_unit_stride,
+                                        const int32_t *n_raw, float scale, float *out, float *lse,
+                                        int U, void *ws, size_t ws_bytes, void *stream);
+ds4a_status ds4a_sparse_attn_prefill_fp8(const uint16_t *q, const int32_t *q_pos,
+                                         const uint8_t *rows8, const float *row_scale, int N_cap,
+                                         const int32_t *idx, const int32_t *count, int top_k,
+                                         const uint16_t *raw, int32_t raw_pos0, int n_raw_rows,
+                                         float scale, float *out, float *lse, int T,
+                                         void *ws, size_t ws_bytes, void *stream);
 
 #ifdef __cplusplus
 }
