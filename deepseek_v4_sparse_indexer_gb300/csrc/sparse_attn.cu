@@ -370,27 +370,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                 if (g < kRowGroups && ct_ < cm.ct && ct_ * TR + 4 * g + rsub < cm.cnt && src[k] < 0) bad_idx = true;
             }
             if (__any_sync(0xffffffffu, bad_idx) && lane == 0) report(a.status, DS4A_DEV_BOUNDS);
-            const int xb = jt & 1;
-            ok = __all_sync(0xffffffffu, mbar_wait(&x_empty[xb], xeph[xb] ^ 1, abort_flag));
-            if (!ok) break;
-            xeph[xb] ^= 1;
-            // validity bits first: a warp's barrier arrival publishes them
-#pragma unroll
-            for (int k = 0; k < kGroupsPerWarp; ++k) {
-                const int g = gw + k * kGatherWarps;
-                const uint32_t bal = __ballot_sync(0xffffffffu, src[k] >= 0);
-                if (lane == 0 && g < kRowGroups) sValid[xb * kRowGroups + g] = static_cast<uint8_t>(nibble(bal));
-            }
-            // A whole tile of contiguous rows comes by TMA: raw-window tiles and
-            // the tiles of a dense row list (rows past the valid count must be
-            // zeros, so a partial tile takes the cp.async path).
-            const bool raw_tile = ct_ >= cm.ct;
-            const int first = raw_tile ? (ct_ - cm.ct) * TR : ct_ * TR;
-            const bool tma_tile = raw_tile ? (a.tma_raw && first + TR <= cm.nrw)
-                                           : (a.tma_rows && !a.idx && first + TR <= cm.cnt);
-            const bool fp8_tile = !raw_tile && a.rows8 != nullptr;
-            const uint32_t buf = smem_u32(sX) + xb * kXBuf;
-            uint4 c8[kGroupsPerWarp][4];                 // FP8 tile: codes of the group's four rows
+            // FP8 tile: its codes go to registers before the buffer is free, so
+            // the loads overlap the wait for the values GEMM two tiles back.
+            const bool fp8_tile = ct_ < cm.ct && a.rows8 != nullptr;
+            uint4 c8[kGroupsPerWarp][4];                 // codes of the group's four rows
             float s8[kGroupsPerWarp][4];                 // and their scales
             if (fp8_tile) {
 #pragma unroll
@@ -409,6 +392,28 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                         }
                     }
                 }
+            }
+            const int xb = jt & 1;
+            ok = __all_sync(0xffffffffu, mbar_wait(&x_empty[xb], xeph[xb] ^ 1, abort_flag));
+            if (!ok) break;
+            xeph[xb] ^= 1;
+            // validity bits first: a warp's barrier arrival publishes them
+#pragma unroll
+            for (int k = 0; k < kGroupsPerWarp; ++k) {
+                const int g = gw + k * kGatherWarps;
+                const uint32_t bal = __ballot_sync(0xffffffffu, src[k] >= 0);
+                if (lane == 0 && g < kRowGroups) sValid[xb * kRowGroups + g] = static_cast<uint8_t>(nibble(bal));
+            }
+            // A whole tile of contiguous rows comes by TMA: raw-window tiles and
+            // the tiles of a dense row list (rows past the valid count must be
+            // zeros, so a partial tile takes the cp.async path).
+            const bool raw_tile = ct_ >= cm.ct;
+            const int first = raw_tile ? (ct_ - cm.ct) * TR : ct_ * TR;
+            const bool tma_tile = raw_tile ? (a.tma_raw && first + TR <= cm.nrw)
+                                           : (a.tma_rows && !a.idx && first + TR <= cm.cnt);
+            const uint32_t buf = smem_u32(sX) + xb * kXBuf;
+            if (fp8_tile) {
+                // written below from the codes in registers
             } else if (tma_tile) {
                 if (gw == 0 && lane == 0) {
                     const int y = static_cast<int>((raw_tile ? cm.raw_row0 : cm.comp_row0) + first);
