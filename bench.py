@@ -57,6 +57,9 @@ def parse():
                    help="decode workloads: run only this many units (small cases for profiling)")
     p.add_argument("--prior-rows", type=int, default=None,
                    help="prefill workload: compressed rows before the chunk (small cases for profiling)")
+    p.add_argument("--select", default="auto", choices=["auto", "fused", "two-call"],
+                   help="score + top-k: fused (ds4a_indexer_topk) or two calls; auto = fused for decode "
+                        "batches of at least one row per SM, two calls otherwise (the faster on each)")
     return p.parse_args()
 
 
@@ -143,7 +146,8 @@ def decode_bytes(wl):
     """Algorithmic HBM bytes per unit: every indexer key, the selected rows, the
     raw window, q, iq, w, the fp32 output and the selected indices."""
     H = wl.heads
-    per_unit_fixed = wl.top_k * 1024 + 128 * 1024 + H * 512 * 2 + 64 * 128 * 2 + 64 * 4 + H * 512 * 4 + wl.top_k * 4
+    row_bytes = 512 + 4 if wl.fp8 else 1024           # FP8 store: codes + the row's scale
+    per_unit_fixed = wl.top_k * row_bytes + 128 * 1024 + H * 512 * 2 + 64 * 128 * 2 + 64 * 4 + H * 512 * 4 + wl.top_k * 4
     ik = wl.n_rows * 128 * 2
     idx_kernel = wl.n_rows * 256 + 64 * 128 * 2 + 64 * 4
     return wl.units * (ik + per_unit_fixed), wl.units * idx_kernel
@@ -165,6 +169,18 @@ def dram_traffic(kernel, units, rows):
         return rec["dram_bytes"] * (units * rows) / (rec["units"] * rec["rows"])
     except Exception:
         return None
+
+
+def build_fp8_store(pkg, chunks, shape, dev):
+    """The FP8 row store (E4M3 codes, power-of-two row scales) of a workload's
+    fp32 rows, built chunk by chunk by the library's quantiser (untimed setup)."""
+    import torch
+    codes = torch.empty(*shape, 512, dtype=torch.uint8, device=dev)
+    scale = torch.empty(*shape, dtype=torch.float32, device=dev)
+    c2, s2 = codes.view(-1, 512), scale.view(-1)
+    for r0, c in chunks:
+        pkg.ds4a_rows_to_fp8(c, c2[r0:r0 + c.shape[0]], s2[r0:r0 + c.shape[0]])
+    return codes, scale
 
 
 def pool_bytes(wl, width=512):
@@ -236,8 +252,14 @@ class OracleSample:
                     return unit_source(i)
                 x = make_decode_inputs(1, wl.n_rows, device="cpu", seed=wl.seed + 1000 + i,
                                        heavy_frac=wl.heavy_frac, heavy_scale=wl.heavy_scale, with_indexer=not dense,
-                                       n_head=wl.heads)
-                d = dict(q=u16(x["q"][0]), rows=u16(x["rows"][0]), raw=u16(x["raw"][0]), n=wl.n_rows, nraw=128)
+                                       n_head=wl.heads, with_rows=not wl.fp8)
+                if wl.fp8:
+                    from deepseek_v4_sparse_indexer_gb300.workloads import decode_rows_fp32_chunks
+                    f32 = torch.cat([c for _, c in decode_rows_fp32_chunks(1, wl.n_rows, seed=wl.seed + 1000 + i)])
+                    codes, rs = oracle.quantize_rows_fp8(f32.numpy())
+                    d = dict(q=u16(x["q"][0]), codes=codes, row_scale=rs, raw=u16(x["raw"][0]), n=wl.n_rows, nraw=128)
+                else:
+                    d = dict(q=u16(x["q"][0]), rows=u16(x["rows"][0]), raw=u16(x["raw"][0]), n=wl.n_rows, nraw=128)
                 if not dense:
                     d.update(iq=u16(x["iq"][0]), w=x["w"][0].numpy(), ik=u16(x["ik"][0]))
                 return d
@@ -256,8 +278,15 @@ class OracleSample:
                 (f"{n} of {wl.query_units} units (each whole: {wl.n_rows} rows scored, top-{wl.top_k}, "
                  f"attention over the selected rows + 128-row window)")
         else:
-            x = make_prefill_inputs(wl.queries, wl.extra["prior_rows"], device="cpu", seed=wl.seed)
-            self.np_in = (u16(x["q"]), u16(x["iq"]), x["w"].numpy(), u16(x["ik"]), u16(x["rows"]),
+            x = make_prefill_inputs(wl.queries, wl.extra["prior_rows"], device="cpu", seed=wl.seed,
+                                    with_rows=not wl.fp8)
+            if wl.fp8:
+                from deepseek_v4_sparse_indexer_gb300.workloads import prefill_rows_fp32_chunks
+                f32 = torch.cat([c for _, c in prefill_rows_fp32_chunks(x["ik"].shape[0], seed=wl.seed)])
+                rows = oracle.quantize_rows_fp8(f32.numpy())
+            else:
+                rows = u16(x["rows"])
+            self.np_in = (u16(x["q"]), u16(x["iq"]), x["w"].numpy(), u16(x["ik"]), rows,
                           x["row_pos"].numpy(), x["q_pos"].numpy(), u16(x["raw"]))
             self.nr = int(x["n_rows"][0])
             self.raw_pos0 = x["raw_pos0"]
@@ -275,7 +304,12 @@ class OracleSample:
     def _run(self, item):
         import numpy as np
         wl, o = self.wl, self.oracle
-        if wl.kind == "decode":
+        if wl.kind == "decode" and wl.fp8:
+            d = item
+            s = o.indexer_score(d["iq"][None], d["w"][None], d["ik"], d["n"])[0]
+            idx, _ = o.topk_select(s, wl.top_k)
+            o.sparse_attention_fp8(d["q"], d["codes"], d["row_scale"], idx, d["raw"], np.arange(d["nraw"]), SCALE)
+        elif wl.kind == "decode":
             d = item
             o.decode_unit(d["q"], d["iq"], d["w"], d["ik"], d["rows"], d["n"], d["raw"], d["nraw"], wl.top_k, SCALE)
         elif wl.kind == "dense":
@@ -285,6 +319,13 @@ class OracleSample:
             d = item
             o.push_raw(np.zeros((128, 512), np.uint16), 128, d["row"])
             o.compressor_pool(d["kv"], d["score"])
+        elif wl.fp8:
+            q, iq, w, ik, (codes, rs), row_pos, q_pos, raw = self.np_in
+            p = int(q_pos[item])
+            s = o.indexer_score(iq[item:item + 1], w[item:item + 1], ik, self.nr, q_pos=np.array([p], np.int32),
+                                row_pos=row_pos)[0]
+            idx, _ = o.topk_select(s, wl.top_k)
+            o.sparse_attention_fp8(q[item], codes, rs, idx, raw, o.prefill_window(p, self.raw_pos0, raw.shape[0]), SCALE)
         else:
             q, iq, w, ik, rows, row_pos, q_pos, raw = self.np_in
             o.prefill_query(item, q, iq, w, ik, rows, self.nr, row_pos, q_pos, raw, self.raw_pos0, wl.top_k, SCALE)
@@ -362,7 +403,9 @@ def main():
     import torch.distributed as dist
 
     import deepseek_v4_sparse_indexer_gb300 as pkg
-    from deepseek_v4_sparse_indexer_gb300.workloads import make_decode_inputs, make_pool_inputs, make_prefill_inputs
+    from deepseek_v4_sparse_indexer_gb300.workloads import (decode_rows_fp32_chunks, make_decode_inputs,
+                                                            make_pool_inputs, make_prefill_inputs,
+                                                            prefill_rows_fp32_chunks)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -379,10 +422,18 @@ def main():
             dist.barrier()
 
     seed = wl.seed + rank
+    # auto: the fused select where its candidate kernel (one CTA per row) fills
+    # the GPU (decode with as many rows as SMs); the two kernels otherwise.
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    fused = args.select == "fused" or (args.select == "auto" and wl.kind == "decode" and
+                                       wl.units * wl.queries >= n_sms)
     if wl.kind == "decode":
         x = make_decode_inputs(wl.units, wl.n_rows, device=dev, seed=seed, heavy_frac=wl.heavy_frac,
-                               heavy_scale=wl.heavy_scale, n_head=wl.heads)
-        step = pkg.DecodeStep(wl.units, wl.n_rows, wl.top_k, device=dev, n_head=wl.heads)
+                               heavy_scale=wl.heavy_scale, n_head=wl.heads, with_rows=not wl.fp8)
+        if wl.fp8:
+            x["rows8"], x["row_scale"] = build_fp8_store(pkg, decode_rows_fp32_chunks(wl.units, wl.n_rows, dev, seed),
+                                                         (wl.units, wl.n_rows), dev)
+        step = pkg.DecodeStep(wl.units, wl.n_rows, wl.top_k, device=dev, n_head=wl.heads, fp8=wl.fp8, fused=fused)
     elif wl.kind == "dense":
         x = make_decode_inputs(wl.units, wl.n_rows, device=dev, seed=seed, with_indexer=False)
         step = pkg.DenseStep(wl.units, wl.n_rows, device=dev)
@@ -390,8 +441,11 @@ def main():
         x = make_pool_inputs(wl.units, wl.n_rows, device=dev, seed=seed)
         step = pkg.ProducerStep(wl.units, device=dev)
     else:
-        x = make_prefill_inputs(wl.queries, wl.extra["prior_rows"], device=dev, seed=seed)
-        step = pkg.PrefillStep(wl.queries, x["ik"].shape[0], wl.top_k, device=dev)
+        x = make_prefill_inputs(wl.queries, wl.extra["prior_rows"], device=dev, seed=seed, with_rows=not wl.fp8)
+        if wl.fp8:
+            n_cap = x["ik"].shape[0]
+            x["rows8"], x["row_scale"] = build_fp8_store(pkg, prefill_rows_fp32_chunks(n_cap, dev, seed), (n_cap,), dev)
+        step = pkg.PrefillStep(wl.queries, x["ik"].shape[0], wl.top_k, device=dev, fp8=wl.fp8, fused=fused)
     torch.cuda.synchronize()
 
     for _ in range(args.warmup):
@@ -480,13 +534,16 @@ def main():
         launches_per_step = 1 + 1 + 1 + (1 if pkg.ds4a_workspace_bytes(
             (2 if wl.kind == "decode" else 3) | (0x100 if wl.heads == 128 else 0), wl.units if wl.kind == "decode" else 1,
             1 if wl.kind == "decode" else wl.queries, wl.n_rows, wl.top_k) else 0)
-        if wl.units * wl.queries < 152:
+        if wl.units * wl.queries < 152 and not fused:
             launches_per_step += 2            # top-k: histogram and filter passes before the final one
     cfg = {"workload": wl.name, "units": wl.units, "queries_per_unit": wl.queries, "rows_per_unit": wl.n_rows,
            "top_k": wl.top_k if wl.kind != "dense" else "all rows", "raw_window": 128, "heads": wl.heads,
            "head_dim": 512, "indexer": "64x128" if wl.kind != "dense" else "none (ratio-128 layer)",
            "l2": "inputs exceed the L2 many times over; no flush", "parallelism": f"replicas x{world}",
-           "peak_source": pk["src"]}
+           "peak_source": pk["src"], "rows_store": "fp8 (E4M3 codes + power-of-two row scale)" if wl.fp8 else "bf16",
+           "select": ("fused: ds4a_indexer_topk (no scores array)" if fused else
+                      "two calls: ds4a_indexer_score then ds4a_topk_select") if wl.kind in ("decode", "prefill")
+           else None}
     if wl.kind == "pool":
         pb = pool_bytes(wl)
         achieved = pb / (idx_ms / 1e3) / 1e9
@@ -512,8 +569,9 @@ def main():
         step_bytes, idx_bytes = decode_bytes(wl)
         achieved = idx_bytes / (idx_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
-                "frac": achieved / pk["hbm"], "traffic": dram_traffic("indexer_score_kernel<1>", wl.units, wl.n_rows),
-                "kernel": "indexer_score_kernel<1>",
+                "frac": achieved / pk["hbm"],
+                "traffic": dram_traffic("indexer_score_kernel<1>" + ("+fused" if fused else ""), wl.units, wl.n_rows),
+                "kernel": "indexer_score_kernel<1>" + (" (fused select) + topk_cand_kernel" if fused else ""),
                 "algorithmic_bytes_per_launch": idx_bytes, "launch_ms": idx_ms}
         cfg["step_algorithmic_bytes"] = step_bytes
         cfg["step_hbm_GBps"] = step_bytes / (ms / 1e3) / 1e9
@@ -523,8 +581,8 @@ def main():
         achieved = idx_flops / (idx_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16"], "unit": "TFLOP/s",
                 "frac": achieved / pk["bf16"],
-                "traffic": dram_traffic("indexer_score_kernel<4>", wl.queries, wl.n_rows),
-                "kernel": "indexer_score_kernel<4>",
+                "traffic": dram_traffic("indexer_score_kernel<4>" + ("+fused" if fused else ""), wl.queries, wl.n_rows),
+                "kernel": "indexer_score_kernel<4>" + (" (fused select) + topk_cand_kernel" if fused else ""),
                 "algorithmic_flops_per_launch": idx_flops, "launch_ms": idx_ms}
         cfg["step_algorithmic_flops"] = idx_flops + attn_flops
         cfg["step_TFLOPs"] = (idx_flops + attn_flops) / (ms / 1e3) / 1e12
@@ -554,7 +612,7 @@ def main():
             return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
         unit_source = None
-        if wl.kind == "decode":
+        if wl.kind == "decode" and not wl.fp8:
             def unit_source(i):
                 u = (i * 7919) % wl.units
                 return dict(q=u16(x["q"][u]), iq=u16(x["iq"][u]), w=x["w"][u].cpu().numpy(), ik=u16(x["ik"][u]),

@@ -27,6 +27,7 @@ DS4A_OP_TOPK_SELECT = 1
 DS4A_OP_SPARSE_ATTN_DECODE = 2
 DS4A_OP_SPARSE_ATTN_PREFILL = 3
 DS4A_OP_DENSE_ATTN_DECODE = 4
+DS4A_OP_INDEXER_TOPK = 5
 DS4A_OP_FLAG_128_HEADS = 0x100
 
 N_HEAD, HEAD_DIM, N_IDX_HEAD, IDX_DIM, N_SWA = 64, 512, 64, 128, 128
@@ -37,7 +38,7 @@ EXPORTS = ("ds4a_strerror", "ds4a_version", "ds4a_workspace_bytes", "ds4a_get_de
            "ds4a_topk_select_noalloc", "ds4a_sparse_attn_decode", "ds4a_sparse_attn_prefill",
            "ds4a_dense_attn_decode", "ds4a_kv_push_raw", "ds4a_compressor_pool",
            "ds4a_sparse_attn_decode_heads", "ds4a_sparse_attn_prefill_heads", "ds4a_dense_attn_decode_heads",
-           "ds4a_rows_to_fp8", "ds4a_sparse_attn_decode_fp8", "ds4a_sparse_attn_prefill_fp8")
+           "ds4a_rows_to_fp8", "ds4a_sparse_attn_decode_fp8", "ds4a_sparse_attn_prefill_fp8", "ds4a_indexer_topk")
 DS4A_TOPK_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -100,6 +101,9 @@ def load(build_if_missing: bool = True):
     L.ds4a_sparse_attn_prefill_heads.restype = _i32
     L.ds4a_dense_attn_decode_heads.argtypes = [_i32] + L.ds4a_dense_attn_decode.argtypes
     L.ds4a_dense_attn_decode_heads.restype = _i32
+    L.ds4a_indexer_topk.argtypes = [_vp, _vp, _vp, _i64, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _sz,
+                                    _vp]
+    L.ds4a_indexer_topk.restype = _i32
     L.ds4a_rows_to_fp8.argtypes = [_vp, _i64, _vp, _vp, _vp]
     L.ds4a_rows_to_fp8.restype = _i32
     L.ds4a_sparse_attn_decode_fp8.argtypes = [_vp, _vp, _vp, _i64, _i32, _vp, _vp, _i32, _vp, _i64, _vp, _f32, _vp,
@@ -210,6 +214,37 @@ def ds4a_topk_select(scores, n_rows, top_k, idx, count, ws, stream=None):
     st = load().ds4a_topk_select(_ptr(scores), _ptr(n_rows), U, Q, N_cap, top_k, _ptr(idx), _ptr(count), _ptr(ws),
                                  ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream))
     _check(st, "ds4a_topk_select")
+
+
+def ds4a_indexer_topk(iq, w, ik, n_rows, top_k, idx, count, ws, q_pos=None, row_pos=None, stream=None):
+    """Indexer score and top-k select fused (no scores array): iq bf16
+    [U,Q,64,128]; w f32 [U,Q,64]; ik bf16 [U,N_cap,128]; n_rows i32 [U]; idx
+    i32 [U,Q,top_k] and count i32 [U,Q] (written); ws uint8 CUDA tensor of
+    ds4a_workspace_bytes(DS4A_OP_INDEXER_TOPK, ...) bytes."""
+    _req(iq, "iq", torch.bfloat16)
+    _req(w, "w", torch.float32)
+    _req(n_rows, "n_rows", torch.int32)
+    _req(idx, "idx", torch.int32)
+    _req(count, "count", torch.int32)
+    if ik.dtype != torch.bfloat16 or not ik.is_cuda or ik.dim() != 3 or ik.stride(2) != 1 or ik.stride(1) != IDX_DIM:
+        raise ValueError("ik: bf16 CUDA tensor [U, N_cap, 128] with contiguous rows")
+    U, N_cap = ik.shape[0], ik.shape[1]
+    Q = iq.shape[1]
+    if iq.shape != (U, Q, N_IDX_HEAD, IDX_DIM) or w.shape != (U, Q, N_IDX_HEAD) or n_rows.shape != (U,):
+        raise ValueError("iq / w / n_rows shape")
+    if idx.shape != (U, Q, top_k) or count.shape != (U, Q):
+        raise ValueError("idx / count shape")
+    if (q_pos is None) != (row_pos is None):
+        raise ValueError("q_pos and row_pos go together")
+    if q_pos is not None:
+        _req(q_pos, "q_pos", torch.int32)
+        _req(row_pos, "row_pos", torch.int32)
+        if q_pos.shape != (U, Q) or row_pos.shape != (U, N_cap):
+            raise ValueError("q_pos / row_pos shape")
+    st = load().ds4a_indexer_topk(_ptr(iq), _ptr(w), _ptr(ik), ik.stride(0), _ptr(n_rows), _ptr(q_pos), _ptr(row_pos),
+                                  U, Q, N_cap, top_k, _ptr(idx), _ptr(count), _ptr(ws),
+                                  ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream))
+    _check(st, "ds4a_indexer_topk")
 
 
 def ds4a_topk_select_noalloc(scores, n_rows, top_k, idx, count, stream=None):

@@ -285,4 +285,14 @@ DS4A_DEV uint32_t float_key(float f) {
 // Visible = a real score: not -inf, not NaN.
 DS4A_DEV bool score_visible(float f) { return f == f && f != -__int_as_float(0x7f800000); }
 
+// Adds 1 to h[bin] for every lane with pred, one shared atomic per distinct
+// bin in the warp (scores of one row often share a few bins).  All 32 lanes
+// must call it.
+DS4A_DEV void hist_add_warp(uint32_t *h, uint32_t bin, bool pred) {
+    const uint32_t active = __ballot_sync(0xffffffffu, pred);
+    if (!pred) return;
+    const uint32_t peers = __match_any_sync(active, bin);
+    if (static_cast<int>(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&h[bin], static_cast<uint32_t>(__popc(peers)));
+}
+
 }  // namespace ds4a

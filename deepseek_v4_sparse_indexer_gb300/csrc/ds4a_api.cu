@@ -148,6 +148,9 @@ size_t ds4a_workspace_bytes(int op, int U, int Q, int N_cap, int top_k) {
         if (top_k < 1 || top_k > DS4A_MAX_TOP_K) return static_cast<size_t>(-1);
         return attn_ws_bytes(U, top_k);
     case DS4A_OP_DENSE_ATTN_DECODE: return attn_ws_bytes(U, N_cap);
+    case DS4A_OP_INDEXER_TOPK:
+        if (top_k < 1 || top_k > DS4A_MAX_TOP_K) return static_cast<size_t>(-1);
+        return indexer_topk_ws_bytes(static_cast<long long>(U) * Q, N_cap);
     case DS4A_OP_SPARSE_ATTN_PREFILL: {
         if (top_k < 1 || top_k > DS4A_MAX_TOP_K) return static_cast<size_t>(-1);
         const long long units = static_cast<long long>(U) * Q;
@@ -172,27 +175,28 @@ ds4a_status ds4a_get_device_status(void *stream, unsigned *flags) {
 
 void ds4a_debug_inject_error(ds4a_status code) { g_inject.store(code); }
 
-ds4a_status ds4a_indexer_score(const uint16_t *iq, const float *w, const uint16_t *ik, int64_t ik_unit_stride,
-                               const int32_t *n_rows, const int32_t *q_pos, const int32_t *row_pos, float *scores,
-                               int U, int Q, int N_cap, void *stream) {
-    if (ds4a_status inj = take_injected()) return inj;
-    if (!iq || !w || !ik || !n_rows || !scores) return DS4A_EINVAL;
+}  // extern "C"
+
+namespace {
+// Checks and fills everything of an indexer launch but the outputs.
+ds4a_status indexer_setup(IndexerArgs &a, DevInfo **dio, const uint16_t *iq, const float *w, const uint16_t *ik,
+                          int64_t ik_unit_stride, const int32_t *n_rows, const int32_t *q_pos,
+                          const int32_t *row_pos, int U, int Q, int N_cap) {
+    if (!iq || !w || !ik || !n_rows) return DS4A_EINVAL;
     if ((q_pos == nullptr) != (row_pos == nullptr)) return DS4A_EINVAL;
     if (U < 1 || Q < 1 || N_cap < 1) return DS4A_EINVAL;
     if (static_cast<long long>(U) * Q > (1LL << 24)) return DS4A_EINVAL;           // TMA row coordinate
     if (static_cast<long long>(U) * Q * N_cap >= (1LL << 40)) return DS4A_EINVAL;
-    if (!aligned(iq, 16) || !aligned(ik, 16) || !aligned(w, 4) || !aligned(scores, 4)) return DS4A_EINVAL;
+    if (!aligned(iq, 16) || !aligned(ik, 16) || !aligned(w, 4)) return DS4A_EINVAL;
     if (U > 1 && (ik_unit_stride < static_cast<int64_t>(N_cap) * kIdxDim || (ik_unit_stride & 7) != 0))
         return DS4A_EINVAL;
     DevInfo *di = nullptr;
     if (ds4a_status st = current_device(&di)) return st;
-
-    IndexerArgs a{};
+    *dio = di;
     a.w = w;
     a.n_rows = n_rows;
     a.q_pos = q_pos;
     a.row_pos = row_pos;
-    a.scores = scores;
     a.status = di->status;
     a.U = U;
     a.Q = Q;
@@ -213,8 +217,53 @@ ds4a_status ds4a_indexer_score(const uint16_t *iq, const float *w, const uint16_
         cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kNIdxHead * a.G)};
         if (!encode_bf16(&a.tm_iq, iq, 2, dims, strides, box)) return DS4A_EINVAL;
     }
+    return DS4A_OK;
+}
+}  // namespace
+
+extern "C" {
+
+ds4a_status ds4a_indexer_score(const uint16_t *iq, const float *w, const uint16_t *ik, int64_t ik_unit_stride,
+                               const int32_t *n_rows, const int32_t *q_pos, const int32_t *row_pos, float *scores,
+                               int U, int Q, int N_cap, void *stream) {
+    if (ds4a_status inj = take_injected()) return inj;
+    if (!scores || !aligned(scores, 4)) return DS4A_EINVAL;
+    IndexerArgs a{};
+    DevInfo *di = nullptr;
+    if (ds4a_status st = indexer_setup(a, &di, iq, w, ik, ik_unit_stride, n_rows, q_pos, row_pos, U, Q, N_cap))
+        return st;
+    a.scores = scores;
     if (a.total_tiles == 0) return DS4A_OK;
     return launch_indexer_score(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DS4A_OK : DS4A_ECUDA;
+}
+
+ds4a_status ds4a_indexer_topk(const uint16_t *iq, const float *w, const uint16_t *ik, int64_t ik_unit_stride,
+                              const int32_t *n_rows, const int32_t *q_pos, const int32_t *row_pos, int U, int Q,
+                              int N_cap, int top_k, int32_t *idx, int32_t *count, void *ws, size_t ws_bytes,
+                              void *stream) {
+    if (ds4a_status inj = take_injected()) return inj;
+    if (!idx || !count || top_k < 1 || top_k > DS4A_MAX_TOP_K) return DS4A_EINVAL;
+    if (N_cap > kTopkCandMaxRows) return DS4A_EUNSUPPORTED;
+    IndexerArgs a{};
+    DevInfo *di = nullptr;
+    if (ds4a_status st = indexer_setup(a, &di, iq, w, ik, ik_unit_stride, n_rows, q_pos, row_pos, U, Q, N_cap))
+        return st;
+    const long long R = static_cast<long long>(U) * Q;
+    const size_t need = indexer_topk_ws_bytes(R, N_cap);
+    if (!ws || ws_bytes < need || !aligned(ws, 256)) return DS4A_EWORKSPACE;
+    uint8_t *p = static_cast<uint8_t *>(ws);
+    a.fused = 1;
+    a.top_k = top_k;
+    a.cand = reinterpret_cast<uint2 *>(p);
+    uint32_t *counters = reinterpret_cast<uint32_t *>(p + static_cast<size_t>(R) * N_cap * 8);
+    a.cand_n = counters;
+    a.vis_n = counters + R;
+    a.tau = counters + 2 * R;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(counters, 0, static_cast<size_t>(R) * 12, s) != cudaSuccess) return DS4A_ECUDA;
+    if (a.total_tiles > 0 && launch_indexer_score(a, s) != cudaSuccess) return DS4A_ECUDA;
+    TopkCandArgs t{a.cand, a.cand_n, a.vis_n, static_cast<int>(R), N_cap, top_k, idx, count};
+    return launch_topk_cand(t, s) == cudaSuccess ? DS4A_OK : DS4A_ECUDA;
 }
 
 ds4a_status ds4a_topk_select(const float *scores, const int32_t *n_rows, int U, int Q, int N_cap, int top_k,

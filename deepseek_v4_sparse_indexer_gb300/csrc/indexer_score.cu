@@ -38,6 +38,7 @@ namespace {
 
 constexpr int kTileRows = 128;   // UMMA M
 
+
 template <int G>
 struct IdxCfg {
     static constexpr int N = 64 * G;                      // UMMA N
@@ -64,8 +65,17 @@ struct IdxCfg {
     static constexpr int kOffB = kOffA + kStages * kABytes;
     static constexpr int kWFloatsPerWarp = kQPerEpiWarp * 64;
     static constexpr int kOffW = kOffB + kBBufs * kBBytes;
-    static constexpr int kOffBar = kOffW + kEpiWarps * kWFloatsPerWarp * 4;
-    static constexpr int kNumBars = 2 * kStages + 2 * kBBufs + 2 * kAccBufs + 1;
+    // Fused selection: one histogram of score keys per query of the group
+    // (key bits 31..20 for G = 1, 31..22 for G = 4) and its threshold key.
+    static constexpr int kHistShift = (G == 1) ? 20 : 22;
+    static constexpr int kTauEvery = (G == 1) ? 16 : 8;    // tiles between threshold updates (a power of two)
+    static constexpr int kCandQueue = (G == 1) ? 256 : 64; // candidates staged per epilogue warp and query
+    static constexpr int kHistBins = 1 << (32 - kHistShift);
+    static constexpr int kOffHist = kOffW + kEpiWarps * kWFloatsPerWarp * 4;
+    static constexpr int kOffTau = kOffHist + G * kHistBins * 4;
+    static constexpr int kOffQueue = ((kOffTau + G * 4 + 15) / 16) * 16;   // [kEpiWarps][kQPerEpiWarp][kCandQueue] uint2
+    static constexpr int kOffBar = kOffQueue + kEpiWarps * kQPerEpiWarp * kCandQueue * 8;
+    static constexpr int kNumBars = 2 * kStages + 2 * kBBufs + 2 * kAccBufs + 2;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + slack to 1024-align the base
     static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation must be a power of two");
@@ -164,6 +174,44 @@ DS4A_DEV void relu_weighted_acc(unsigned long long (&acc)[4], const unsigned lon
         asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc[p & 3]) : "l"(w2[half * 16 + p]), "l"(x));
     }
 }
+// The bin b where the number of keys in bins >= b first reaches k; -1 when
+// the histogram of NB bins (a multiple of 1024) holds fewer than k keys.  All
+// lanes call it.  Lane l sums the NB/32 bins of segment 31 - l (lane 0: the
+// top segment), reading them in a rotated order so that the lanes hit
+// distinct banks; a prefix sum over the lanes finds the segment where the
+// count from the top reaches k, and the warp walks that segment from its top.
+template <int NB>
+DS4A_DEV int hist_kth_bin(const uint32_t *h, uint32_t k, int lane) {
+    constexpr int per = NB / 32;
+    const uint32_t *hs = h + (31 - lane) * per;
+    uint32_t sum = 0;
+#pragma unroll 8
+    for (int i = 0; i < per; ++i) sum += hs[(i + lane) & (per - 1)];
+    uint32_t cum = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, cum, o);
+        if (lane >= o) cum += v;
+    }
+    const uint32_t hit = __ballot_sync(0xffffffffu, cum >= k);
+    if (!hit) return -1;
+    const int L = __ffs(hit) - 1;
+    uint32_t above = __shfl_sync(0xffffffffu, cum - sum, L);
+    const int seg0 = (31 - L) * per;
+    for (int top = per - 1; top >= 31; top -= 32) {
+        uint32_t c = h[seg0 + top - lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xffffffffu, c, o);
+            if (lane >= o) c += v;
+        }
+        const uint32_t tot = __shfl_sync(0xffffffffu, c, 31);
+        if (above + tot >= k) return seg0 + top - (__ffs(__ballot_sync(0xffffffffu, above + c >= k)) - 1);
+        above += tot;
+    }
+    return -1;
+}
+
 DS4A_DEV float sum_pairs(const unsigned long long (&acc)[4]) {
     const float2 s0 = unpack_f2(acc[0]), s1 = unpack_f2(acc[1]), s2 = unpack_f2(acc[2]), s3 = unpack_f2(acc[3]);
     return ((s0.x + s0.y) + (s1.x + s1.y)) + ((s2.x + s2.y) + (s3.x + s3.y));
@@ -185,6 +233,10 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
     uint64_t *acc_full = b_empty + C::kBBufs;
     uint64_t *acc_empty = acc_full + C::kAccBufs;
     uint64_t *drain_bar = acc_empty + C::kAccBufs;
+    uint64_t *epi_bar = drain_bar + 1;                 // epilogue-warp group sync (fused selection)
+    uint32_t *hist = reinterpret_cast<uint32_t *>(smem + C::kOffHist);
+    volatile uint32_t *tau_sh = reinterpret_cast<volatile uint32_t *>(smem + C::kOffTau);
+    uint2 *cqueue = reinterpret_cast<uint2 *>(smem + C::kOffQueue);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
 
@@ -205,6 +257,7 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
             mbar_init(&acc_empty[c], C::kEpiWarps);
         }
         mbar_init(drain_bar, 1);
+        mbar_init(epi_bar, C::kEpiWarps);
         *abort_flag = 0;
         mbar_fence_init();
         tma_prefetch_desc(&a.tm_ik);
@@ -317,8 +370,17 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
         float *wsm = sW + e * C::kWFloatsPerWarp;
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         int ab = 0;
-        uint32_t aph = 0;
+        uint32_t aph = 0, eph = 0;
         bool ok = true;
+        // Barrier of the epilogue warps on an mbarrier (a wait that gives up
+        // cannot leave the others stuck).
+        auto epi_sync = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(epi_bar);
+            const bool r = __all_sync(0xffffffffu, mbar_wait_hint(epi_bar, eph, abort_flag));
+            eph ^= 1;
+            return r;
+        };
         for (long long lin = share_lo; ok && lin < share_hi;) {
             const Item m = next_item(a, lin, share_hi);
             const int nr_raw = a.n_rows[m.u];
@@ -328,6 +390,31 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
             if (m.t0 >= m.t1) continue;
             const int nr = nr_raw < 0 ? 0 : (nr_raw > a.N_cap ? a.N_cap : nr_raw);
             const int q0 = m.g * G + half * C::kQPerEpiWarp;
+            if (a.fused) {
+                // Fused selection: a fresh histogram per query of the group once
+                // every epilogue warp is done with the previous item, and the
+                // threshold other CTAs may already have raised for these rows.
+                if (!(ok = epi_sync())) break;
+                for (int i = e * 32 + lane; i < G * C::kHistBins; i += C::kEpiWarps * 32) hist[i] = 0u;
+                const int gq = e * 32 + lane;
+                if (gq < G) tau_sh[gq] = (m.g * G + gq < a.Q) ? a.tau[static_cast<long long>(m.u) * a.Q + m.g * G + gq] : 0u;
+                if (!(ok = epi_sync())) break;
+            }
+            uint32_t my_vis[C::kQPerEpiWarp], qn[C::kQPerEpiWarp];
+#pragma unroll
+            for (int j = 0; j < C::kQPerEpiWarp; ++j) my_vis[j] = qn[j] = 0u;
+            // Staged candidates of query j go out with one global atomic per batch.
+            auto flush = [&](int j) {
+                __syncwarp();
+                const long long R = static_cast<long long>(m.u) * a.Q + q0 + j;
+                uint32_t base = 0;
+                if (lane == 0) base = atomicAdd(a.cand_n + R, qn[j]);
+                base = __shfl_sync(0xffffffffu, base, 0);
+                const uint2 *qq = cqueue + (e * C::kQPerEpiWarp + j) * C::kCandQueue;
+                for (uint32_t i = lane; i < qn[j]; i += 32) a.cand[R * a.N_cap + base + i] = qq[i];
+                qn[j] = 0;
+                __syncwarp();
+            };
             __syncwarp();
             for (int i = lane; i < C::kWFloatsPerWarp; i += 32) {
                 const int qq = q0 + i / kNIdxHead;
@@ -382,7 +469,40 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acc_empty[ab]);
-                if (row < nr) {
+                if (a.fused) {
+                    // Keep the row as a candidate when its key reaches the query's
+                    // threshold, and count it in the query's histogram.  The
+                    // threshold is a bin edge with at least top_k counted keys at
+                    // or above it, so it never passes the final k-th key: every
+                    // row of the top k (ties included) is kept.  Rows below it
+                    // need no count: the bin where the count from the top reaches
+                    // top_k never lies below the threshold, and the bins at or
+                    // above it hold only candidates.
+#pragma unroll
+                    for (int j = 0; j < C::kQPerEpiWarp; ++j) {
+                        const int qq = q0 + j, slot = half * C::kQPerEpiWarp + j;
+                        const bool vis = row < nr && qq < a.Q && !(a.q_pos && rpos > qpos[j]) && score_visible(sc[j]);
+                        const uint32_t key = float_key(sc[j]);
+                        my_vis[j] += vis ? 1u : 0u;
+                        const bool emit = vis && key >= tau_sh[slot];
+                        hist_add_warp(hist + slot * C::kHistBins, key >> C::kHistShift, emit);
+                        const uint32_t bal = __ballot_sync(0xffffffffu, emit);
+                        if (emit)
+                            cqueue[(e * C::kQPerEpiWarp + j) * C::kCandQueue + qn[j] + __popc(bal & ((1u << lane) - 1u))] =
+                                make_uint2(key, static_cast<uint32_t>(row));
+                        qn[j] += __popc(bal);
+                        if (qn[j] > C::kCandQueue - 32) flush(j);
+                    }
+                    // Every few tiles, warp e raises the threshold of query slot e.
+                    if (e < G && ((t - m.t0) & (C::kTauEvery - 1)) == C::kTauEvery - 1 && m.g * G + e < a.Q) {
+                        const int b = hist_kth_bin<C::kHistBins>(hist + e * C::kHistBins, static_cast<uint32_t>(a.top_k), lane);
+                        if (b >= 0 && lane == 0) {
+                            const uint32_t tk = static_cast<uint32_t>(b) << C::kHistShift;
+                            const uint32_t old = atomicMax(a.tau + static_cast<long long>(m.u) * a.Q + m.g * G + e, tk);
+                            tau_sh[e] = tk > old ? tk : old;
+                        }
+                    }
+                } else if (row < nr) {
 #pragma unroll
                     for (int j = 0; j < C::kQPerEpiWarp; ++j) {
                         const int qq = q0 + j;
@@ -394,6 +514,16 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
                     }
                 }
                 if (++ab == C::kAccBufs) { ab = 0; aph ^= 1; }
+            }
+            if (a.fused && ok) {
+#pragma unroll
+                for (int j = 0; j < C::kQPerEpiWarp; ++j) {
+                    if (qn[j]) flush(j);
+                    uint32_t v = my_vis[j];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                    if (lane == 0 && v && q0 + j < a.Q) atomicAdd(a.vis_n + static_cast<long long>(m.u) * a.Q + q0 + j, v);
+                }
             }
         }
         if (!ok) {

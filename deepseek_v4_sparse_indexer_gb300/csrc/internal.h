@@ -23,9 +23,17 @@ struct IndexerArgs {
     const int32_t *n_rows;      // [U]
     const int32_t *q_pos;       // [U*Q] or null
     const int32_t *row_pos;     // [U*N_cap] or null
-    float *scores;              // [U*Q][N_cap]
+    float *scores;              // [U*Q][N_cap] (not written when fused)
+    // Fused selection (scores not materialised): per (u,q) row R = u*Q + q,
+    // candidates (order-preserving key, row) whose key reached the row's
+    // running threshold, their count, the visible-row count and the threshold
+    // key (all zeroed before the launch).
+    int fused;
+    uint2 *cand;                // [U*Q][N_cap]
+    uint32_t *cand_n, *vis_n, *tau;   // [U*Q] each
     uint32_t *status;
     int U, Q, N_cap;
+    int top_k;                  // fused: the k the threshold is kept for
     int G;                      // queries per UMMA (1 or 4)
     int n_groups;               // ceil(Q / G)
     int nt_cap;                 // 128-row tiles per (unit, group): ceil(N_cap / 128)
@@ -37,6 +45,20 @@ int indexer_group_size(int Q);                       // G for a given Q
 void indexer_plan(IndexerArgs &a, int num_sms);      // fills n_groups .. grid
 
 // ---- top-k ---------------------------------------------------------------
+// Exact top-k over the fused indexer's candidate lists (see IndexerArgs).
+struct TopkCandArgs {
+    const uint2 *cand;
+    const uint32_t *cand_n, *vis_n;
+    int R, N_cap, top_k;
+    int32_t *idx, *count;
+};
+cudaError_t launch_topk_cand(const TopkCandArgs &a, cudaStream_t s);
+// Workspace of the fused score + select for R rows: candidates [R][N_cap]
+// (key, row), then cand_n, vis_n and tau [R] u32 each.
+inline size_t indexer_topk_ws_bytes(long long R, int N_cap) {
+    return static_cast<size_t>(R) * N_cap * 8 + static_cast<size_t>(R) * 12;
+}
+constexpr int kTopkCandMaxRows = 1 << 20;   // N_cap limit of the candidate path (its row bitmap)
 constexpr int kTopkBins = 4096;        // first radix digit: key bits 31..20
 constexpr int kTopkCandCap = 8192;     // candidate list capacity per (u,q)
 struct TopkArgs {

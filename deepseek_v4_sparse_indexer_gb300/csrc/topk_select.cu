@@ -497,15 +497,6 @@ __global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float *
 //   4. Output: the chosen candidates in ascending row order (a bitmap of the
 //      row and a prefix sum of its popcounts; a bitonic sort for rows longer
 //      than 131,072), -1 padded; the fallback compacts the row in order.
-// Adds 1 to h[bin] for every lane with pred, one shared atomic per distinct
-// bin in the warp (scores of one row often share a few bins).  All 32 lanes
-// must call it.
-DS4A_DEV void hist_add_warp(uint32_t *h, uint32_t bin, bool pred) {
-    const uint32_t active = __ballot_sync(0xffffffffu, pred);
-    if (!pred) return;
-    const uint32_t peers = __match_any_sync(active, bin);
-    if (static_cast<int>(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&h[bin], static_cast<uint32_t>(__popc(peers)));
-}
 
 constexpr int kRowThreads = 512;
 constexpr int kSample = 2048;
@@ -835,6 +826,139 @@ __global__ void __launch_bounds__(kRowThreads, 2) topk_row_kernel(const float *_
 }
 
 
+// ---------------------------------------------------------------- candidates
+// Exact top-k of one (u,q) row from the fused indexer's candidate list
+// (order-preserving key, row): every row whose key is at or above the row's
+// k-th key is in the list (the indexer's threshold never passed it), so the
+// selection over the list is the selection over the row.  One CTA per row:
+//   1. the k-th key T by radix select over the list (digits 31..20, 19..8,
+//      7..0), and need_eq = how many keys equal to T the selection takes;
+//   2. a row bitmap: the need_eq lowest rows with key T (a prefix count over
+//      the bitmap of tied rows), then every row with key > T;
+//   3. the set rows in ascending order (prefix count again), -1 padding.
+// The list is cached in shared memory when it fits, else read from global.
+constexpr int kCandThreads = 512;
+constexpr int kCandCache = 8192;
+
+// Block-wide exclusive prefix count of set bits over words [0, nw) of bm,
+// thread t owning the contiguous words [t*wpt, (t+1)*wpt).  Returns the
+// number of set bits before this thread's words; *total gets the block total.
+DS4A_DEV uint32_t bitmap_prefix(const uint32_t *bm, int nw, int wpt, uint32_t *warp_sums, uint32_t *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t cnt = 0;
+    for (int j = 0; j < wpt; ++j) {
+        const int w = threadIdx.x * wpt + j;
+        if (w < nw) cnt += __popc(bm[w]);
+    }
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    uint32_t before = 0, tot = 0;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) {
+        const uint32_t v = warp_sums[w];
+        if (w < warp) before += v;
+        tot += v;
+    }
+    __syncthreads();
+    *total = tot;
+    return before + incl - cnt;
+}
+
+__global__ void __launch_bounds__(kCandThreads) topk_cand_kernel(const __grid_constant__ TopkCandArgs a) {
+    extern __shared__ __align__(16) uint8_t cand_smem[];
+    uint2 *cache = reinterpret_cast<uint2 *>(cand_smem);                          // [kCandCache]
+    uint32_t *h = reinterpret_cast<uint32_t *>(cand_smem + kCandCache * 8);       // [kBins]
+    uint32_t *bm = h + kBins;                                                      // [ceil(N_cap / 32)]
+    __shared__ uint32_t scratch[kCandThreads + 4];
+    __shared__ uint32_t warp_sums[32];
+    const long long row = blockIdx.x;
+    const uint32_t k = static_cast<uint32_t>(a.top_k);
+    uint32_t nc = a.cand_n[row];
+    if (nc > static_cast<uint32_t>(a.N_cap)) nc = static_cast<uint32_t>(a.N_cap);
+    const uint32_t total = a.vis_n[row];
+    const uint2 *gc = a.cand + row * a.N_cap;
+    const bool cached = nc <= static_cast<uint32_t>(kCandCache);
+    if (cached)
+        for (uint32_t i = threadIdx.x; i < nc; i += blockDim.x) cache[i] = gc[i];
+    const uint2 *c = cached ? cache : gc;
+    const int nw = (a.N_cap + 31) / 32;
+    const int wpt = (nw + kCandThreads - 1) / kCandThreads;
+    for (int i = threadIdx.x; i < nw; i += blockDim.x) bm[i] = 0u;
+    __syncthreads();
+    if (total <= k) {
+        // every visible row is listed (the threshold never rose): take all
+        for (uint32_t i = threadIdx.x; i < nc; i += blockDim.x) atomicOr(&bm[c[i].y >> 5], 1u << (c[i].y & 31));
+    } else {
+        // ---- 1. the k-th key
+        uint32_t need = k, prefix = 0;
+        const int shifts[3] = {20, 8, 0};
+        const uint32_t masks[3] = {0xFFFu, 0xFFFu, 0xFFu};
+        for (int d = 0; d < 3; ++d) {
+            for (int i = threadIdx.x; i < kBins; i += blockDim.x) h[i] = 0u;
+            __syncthreads();
+            const int sh = shifts[d];
+            const int hs = d == 0 ? 32 : shifts[d - 1];
+            for (uint32_t i0 = 0; i0 < nc; i0 += blockDim.x) {        // block-uniform trip count
+                const uint32_t i = i0 + threadIdx.x;
+                const uint32_t key = i < nc ? c[i].x : 0u;
+                hist_add_warp(h, (key >> sh) & masks[d], i < nc && (hs == 32 || (key >> hs) == prefix));
+            }
+            __syncthreads();
+            uint32_t gt, tot;
+            int b = find_threshold_bin<kCandThreads>(h, kBins, need, &gt, &tot, scratch);
+            if (b < 0) { b = 0; gt = 0; }      // cannot happen: need <= listed keys with this prefix
+            prefix = (d == 0 ? 0u : prefix << (d == 1 ? 12 : 8)) | static_cast<uint32_t>(b);
+            need -= gt;
+        }
+        const uint32_t T = prefix;
+        // ---- 2. ties at T: the need lowest rows
+        for (uint32_t i = threadIdx.x; i < nc; i += blockDim.x)
+            if (c[i].x == T) atomicOr(&bm[c[i].y >> 5], 1u << (c[i].y & 31));
+        __syncthreads();
+        uint32_t ttot;
+        uint32_t pos = bitmap_prefix(bm, nw, wpt, warp_sums, &ttot);
+        for (int j = 0; j < wpt; ++j) {
+            const int w = threadIdx.x * wpt + j;
+            if (w >= nw) break;
+            uint32_t bits = bm[w], keep = 0;
+            while (bits) {
+                const uint32_t low = bits & (0u - bits);
+                if (pos < need) keep |= low;
+                ++pos;
+                bits ^= low;
+            }
+            bm[w] = keep;
+        }
+        __syncthreads();
+        for (uint32_t i = threadIdx.x; i < nc; i += blockDim.x)
+            if (c[i].x > T) atomicOr(&bm[c[i].y >> 5], 1u << (c[i].y & 31));
+    }
+    __syncthreads();
+    // ---- 3. ascending output
+    uint32_t ns;
+    uint32_t pos = bitmap_prefix(bm, nw, wpt, warp_sums, &ns);
+    int32_t *out = a.idx + row * a.top_k;
+    for (int j = 0; j < wpt; ++j) {
+        const int w = threadIdx.x * wpt + j;
+        if (w >= nw) break;
+        uint32_t bits = bm[w];
+        while (bits) {
+            const int b = __ffs(bits) - 1;
+            bits &= bits - 1;
+            if (pos < k) out[pos] = w * 32 + b;
+            ++pos;
+        }
+    }
+    ns = ns < k ? ns : k;
+    for (uint32_t i = ns + threadIdx.x; i < k; i += blockDim.x) out[i] = -1;
+    if (threadIdx.x == 0) a.count[row] = static_cast<int32_t>(ns);
+}
+
 }  // namespace
 
 size_t topk_ws_bytes(long long R, int top_k) {
@@ -881,4 +1005,16 @@ cudaError_t launch_topk(const TopkArgs &a, int num_sms, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+}  // namespace ds4a
+
+namespace ds4a {
+cudaError_t launch_topk_cand(const TopkCandArgs &a, cudaStream_t s) {
+    if (a.R <= 0) return cudaSuccess;
+    const size_t smem = static_cast<size_t>(kCandCache) * 8 + kBins * 4 + static_cast<size_t>((a.N_cap + 31) / 32) * 4;
+    cudaError_t e = cudaFuncSetAttribute(topk_cand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    topk_cand_kernel<<<a.R, kCandThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
 }  // namespace ds4a

@@ -10,7 +10,8 @@ store of the pooled row.
 
 DecodeStep and PrefillStep with fp8=True read the compressed rows from the FP8
 row store (x["rows8"] E4M3 codes, x["row_scale"] per-row scales) instead of
-the bf16 rows.
+the bf16 rows; with fused=True they score and select in one call
+(ds4a_indexer_topk: no scores array, the same selection).
 
 Both own their outputs and workspaces (allocated once, reused every call, so a
 call can be captured in a CUDA graph) and run indexer score -> top-k select ->
@@ -30,26 +31,32 @@ def _ws(nbytes, device):
 
 
 class DecodeStep:
-    def __init__(self, U, N_cap, top_k=512, device="cuda", n_head=B.N_HEAD, fp8=False):
+    def __init__(self, U, N_cap, top_k=512, device="cuda", n_head=B.N_HEAD, fp8=False, fused=False):
         if fp8 and n_head != B.N_HEAD:
             raise ValueError("the FP8 row store is read with 64 query heads")
-        self.U, self.N_cap, self.top_k, self.n_head, self.fp8 = U, N_cap, top_k, n_head, fp8
+        self.U, self.N_cap, self.top_k, self.n_head, self.fp8, self.fused = U, N_cap, top_k, n_head, fp8, fused
         dev = torch.device(device)
         flag = B.DS4A_OP_FLAG_128_HEADS if n_head == 128 else 0
-        self.scores = torch.empty(U, 1, N_cap, dtype=torch.float32, device=dev)
+        self.scores = None if fused else torch.empty(U, 1, N_cap, dtype=torch.float32, device=dev)
+        self.ws_fused = _ws(B.ds4a_workspace_bytes(B.DS4A_OP_INDEXER_TOPK, U, 1, N_cap, top_k), dev) if fused else None
         self.idx = torch.empty(U, 1, top_k, dtype=torch.int32, device=dev)
         self.count = torch.empty(U, 1, dtype=torch.int32, device=dev)
         self.out = torch.empty(U, n_head, B.HEAD_DIM, dtype=torch.float32, device=dev)
         self.lse = torch.empty(U, n_head, dtype=torch.float32, device=dev)
-        self.ws_topk = _ws(B.ds4a_workspace_bytes(B.DS4A_OP_TOPK_SELECT, U, 1, N_cap, top_k), dev)
+        self.ws_topk = None if fused else _ws(B.ds4a_workspace_bytes(B.DS4A_OP_TOPK_SELECT, U, 1, N_cap, top_k), dev)
         self.ws_attn = _ws(B.ds4a_workspace_bytes(B.DS4A_OP_SPARSE_ATTN_DECODE | flag, U, 1, N_cap, top_k), dev)
 
     def score(self, x, stream=None):
-        B.ds4a_indexer_score(x["iq"].view(self.U, 1, B.N_IDX_HEAD, B.IDX_DIM),
-                             x["w"].view(self.U, 1, B.N_IDX_HEAD), x["ik"], x["n_rows"], self.scores,
-                             stream=stream)
+        iq, w = x["iq"].view(self.U, 1, B.N_IDX_HEAD, B.IDX_DIM), x["w"].view(self.U, 1, B.N_IDX_HEAD)
+        if self.fused:
+            B.ds4a_indexer_topk(iq, w, x["ik"], x["n_rows"], self.top_k, self.idx, self.count, self.ws_fused,
+                                stream=stream)
+            return
+        B.ds4a_indexer_score(iq, w, x["ik"], x["n_rows"], self.scores, stream=stream)
 
     def select(self, x, stream=None):
+        if self.fused:
+            return                                   # done by score()
         B.ds4a_topk_select(self.scores, x["n_rows"], self.top_k, self.idx, self.count, self.ws_topk, stream=stream)
 
     def attend(self, x, scale=DEFAULT_SCALE, stream=None):
@@ -69,27 +76,34 @@ class DecodeStep:
 
 
 class PrefillStep:
-    def __init__(self, T, N_cap, top_k=512, device="cuda", n_head=B.N_HEAD, fp8=False):
+    def __init__(self, T, N_cap, top_k=512, device="cuda", n_head=B.N_HEAD, fp8=False, fused=False):
         if fp8 and n_head != B.N_HEAD:
             raise ValueError("the FP8 row store is read with 64 query heads")
-        self.T, self.N_cap, self.top_k, self.n_head, self.fp8 = T, N_cap, top_k, n_head, fp8
+        self.T, self.N_cap, self.top_k, self.n_head, self.fp8, self.fused = T, N_cap, top_k, n_head, fp8, fused
         dev = torch.device(device)
         flag = B.DS4A_OP_FLAG_128_HEADS if n_head == 128 else 0
-        self.scores = torch.empty(1, T, N_cap, dtype=torch.float32, device=dev)
+        self.scores = None if fused else torch.empty(1, T, N_cap, dtype=torch.float32, device=dev)
+        self.ws_fused = _ws(B.ds4a_workspace_bytes(B.DS4A_OP_INDEXER_TOPK, 1, T, N_cap, top_k), dev) if fused else None
         self.idx = torch.empty(1, T, top_k, dtype=torch.int32, device=dev)
         self.count = torch.empty(1, T, dtype=torch.int32, device=dev)
         self.out = torch.empty(T, n_head, B.HEAD_DIM, dtype=torch.float32, device=dev)
         self.lse = torch.empty(T, n_head, dtype=torch.float32, device=dev)
-        self.ws_topk = _ws(B.ds4a_workspace_bytes(B.DS4A_OP_TOPK_SELECT, 1, T, N_cap, top_k), dev)
+        self.ws_topk = None if fused else _ws(B.ds4a_workspace_bytes(B.DS4A_OP_TOPK_SELECT, 1, T, N_cap, top_k), dev)
         self.ws_attn = _ws(B.ds4a_workspace_bytes(B.DS4A_OP_SPARSE_ATTN_PREFILL | flag, 1, T, N_cap, top_k), dev)
 
     def score(self, x, stream=None):
         T, N = self.T, self.N_cap
-        B.ds4a_indexer_score(x["iq"].view(1, T, B.N_IDX_HEAD, B.IDX_DIM), x["w"].view(1, T, B.N_IDX_HEAD),
-                             x["ik"].view(1, N, B.IDX_DIM), x["n_rows"], self.scores,
-                             q_pos=x["q_pos"].view(1, T), row_pos=x["row_pos"].view(1, N), stream=stream)
+        iq, w = x["iq"].view(1, T, B.N_IDX_HEAD, B.IDX_DIM), x["w"].view(1, T, B.N_IDX_HEAD)
+        ik, qp, rp = x["ik"].view(1, N, B.IDX_DIM), x["q_pos"].view(1, T), x["row_pos"].view(1, N)
+        if self.fused:
+            B.ds4a_indexer_topk(iq, w, ik, x["n_rows"], self.top_k, self.idx, self.count, self.ws_fused,
+                                q_pos=qp, row_pos=rp, stream=stream)
+            return
+        B.ds4a_indexer_score(iq, w, ik, x["n_rows"], self.scores, q_pos=qp, row_pos=rp, stream=stream)
 
     def select(self, x, stream=None):
+        if self.fused:
+            return                                   # done by score()
         B.ds4a_topk_select(self.scores, x["n_rows"], self.top_k, self.idx, self.count, self.ws_topk, stream=stream)
 
     def attend(self, x, scale=DEFAULT_SCALE, stream=None):

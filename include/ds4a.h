@@ -76,6 +76,7 @@ typedef int ds4a_status;
 #define DS4A_OP_SPARSE_ATTN_DECODE 2
 #define DS4A_OP_SPARSE_ATTN_PREFILL 3
 #define DS4A_OP_DENSE_ATTN_DECODE 4
+#define DS4A_OP_INDEXER_TOPK 5
 /* OR-ed into an attention op: the workspace of the 128-head (Pro shape) call. */
 #define DS4A_OP_FLAG_128_HEADS 0x100
 
@@ -154,6 +155,31 @@ ds4a_status ds4a_indexer_score(const uint16_t *iq, const float *w, const uint16_
 ds4a_status ds4a_topk_select(const float *scores, const int32_t *n_rows, int U, int Q,
                              int N_cap, int top_k, int32_t *idx, int32_t *count,
                              void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * 1+2. Indexer score and top-k select fused: the result of ds4a_indexer_score
+ *    followed by ds4a_topk_select (the same idx and count, bit for bit),
+ *    without materialising the scores.  While the indexer scans, each query
+ *    keeps a histogram of its score keys and a threshold: a histogram bin edge
+ *    with at least top_k keys at or above it among the rows counted so far
+ *    (shared across the CTAs that scan one query's rows).  Only rows whose
+ *    key reaches the threshold are written out, as (key, row) candidates;
+ *    the threshold never passes the final k-th key, so every row of the
+ *    top k, ties included, is among them, and an exact select over the
+ *    candidates finishes the job.  Scores of random rows leave a few percent
+ *    of the rows as candidates: instead of 8 bytes per row of score traffic,
+ *    8 bytes per candidate.
+ *
+ *    Arguments as in 1 and 2 (no scores array).  N_cap <= 2^20 (else
+ *    DS4A_EUNSUPPORTED: use 1 then 2).  ws: ds4a_workspace_bytes(
+ *    DS4A_OP_INDEXER_TOPK, U, Q, N_cap, top_k) bytes (8 per row per query:
+ *    the candidate lists), 256-byte aligned (device).
+ */
+ds4a_status ds4a_indexer_topk(const uint16_t *iq, const float *w, const uint16_t *ik,
+                              int64_t ik_unit_stride, const int32_t *n_rows,
+                              const int32_t *q_pos, const int32_t *row_pos, int U, int Q,
+                              int N_cap, int top_k, int32_t *idx, int32_t *count,
+                              void *ws, size_t ws_bytes, void *stream);
 
 /* Capacity of the scratch array behind ds4a_topk_select_noalloc (bytes). */
 #define DS4A_TOPK_NOALLOC_SCRATCH_BYTES (8u << 20)
