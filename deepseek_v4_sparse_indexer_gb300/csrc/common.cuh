@@ -16,6 +16,33 @@ namespace ds4a {
 // A device-side wait gives up after this long and reports DS4A_DEV_TIMEOUT.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialisation (launch_k below): it lets the next kernel
+// on the stream start launching at once (pdl_launch_dependents, the first
+// thing each kernel does) and waits for the previous kernel to complete, with
+// its memory visible, before touching global memory (pdl_wait).  Between
+// dependent kernels the launch latency and the block scheduling then overlap
+// the previous kernel's tail; the data order is the stream order, as without
+// it.
+DS4A_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+DS4A_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... Params, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                            Args &&...args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
+
 DS4A_DEV uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

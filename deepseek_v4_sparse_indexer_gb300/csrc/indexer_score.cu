@@ -220,6 +220,8 @@ DS4A_DEV float sum_pairs(const unsigned long long (&acc)[4]) {
 template <int G>
 __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
     indexer_score_kernel(const __grid_constant__ IndexerArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();
     using C = IdxCfg<G>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -554,8 +556,7 @@ cudaError_t launch_g(const IndexerArgs &a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         if (fa.numRegs * C::kThreads < C::kRegsNeeded) return cudaErrorInvalidConfiguration;
     }
-    indexer_score_kernel<G><<<a.grid, C::kThreads, C::kSmemBytes, s>>>(a);
-    return cudaGetLastError();
+    return launch_k(indexer_score_kernel<G>, dim3(a.grid), dim3(C::kThreads), C::kSmemBytes, s, a);
 }
 
 }  // namespace

@@ -29,6 +29,8 @@ __global__ void __launch_bounds__(kPushThreads) kv_push_raw_kernel(const float *
                                                                    long long raw_unit_stride,
                                                                    const int32_t *__restrict__ pos, int32_t *n_raw,
                                                                    uint32_t *status) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int u = blockIdx.x;
     const int p = pos[u];
     if (p < 0) {                                  // no position: nothing is written
@@ -57,6 +59,8 @@ constexpr int kPoolGroup = 8;
 __global__ void __launch_bounds__(kPoolThreads) compressor_pool_kernel(const float *__restrict__ kv,
                                                                        const float *__restrict__ score, int ratio,
                                                                        int width, float *__restrict__ out, int U) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int w4 = width >> 2;
     const long long t = static_cast<long long>(blockIdx.x) * kPoolThreads + threadIdx.x;
     if (t >= static_cast<long long>(U) * w4) return;
@@ -144,6 +148,8 @@ DS4A_DEV uint32_t e4m3x4(float a, float b, float c, float d) {
 __global__ void __launch_bounds__(32 * kFp8RowsPerBlock) rows_to_fp8_kernel(const float *__restrict__ x,
                                                                           long long n_rows, uint8_t *codes,
                                                                           float *row_scale) {
+    pdl_launch_dependents();
+    pdl_wait();
     const long long row = static_cast<long long>(blockIdx.x) * kFp8RowsPerBlock + (threadIdx.x >> 5);
     if (row >= n_rows) return;
     const int lane = threadIdx.x & 31;
@@ -172,14 +178,13 @@ __global__ void __launch_bounds__(32 * kFp8RowsPerBlock) rows_to_fp8_kernel(cons
 cudaError_t launch_rows_to_fp8(const float *x, long long n_rows, uint8_t *codes, float *row_scale, cudaStream_t s) {
     const long long blocks = (n_rows + kFp8RowsPerBlock - 1) / kFp8RowsPerBlock;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-    rows_to_fp8_kernel<<<static_cast<unsigned>(blocks), 32 * kFp8RowsPerBlock, 0, s>>>(x, n_rows, codes, row_scale);
-    return cudaGetLastError();
+    return launch_k(rows_to_fp8_kernel, dim3(static_cast<unsigned>(blocks)), dim3(32 * kFp8RowsPerBlock), 0, s, x, n_rows,
+                    codes, row_scale);
 }
 
 cudaError_t launch_kv_push_raw(const float *kv, uint16_t *raw, long long raw_unit_stride, const int32_t *pos,
                                int32_t *n_raw, int U, uint32_t *status, cudaStream_t s) {
-    kv_push_raw_kernel<<<U, kPushThreads, 0, s>>>(kv, raw, raw_unit_stride, pos, n_raw, status);
-    return cudaGetLastError();
+    return launch_k(kv_push_raw_kernel, dim3(U), dim3(kPushThreads), 0, s, kv, raw, raw_unit_stride, pos, n_raw, status);
 }
 
 cudaError_t launch_compressor_pool(const float *kv, const float *score, int ratio, int width, float *out, int U,
@@ -187,8 +192,8 @@ cudaError_t launch_compressor_pool(const float *kv, const float *score, int rati
     const long long threads = static_cast<long long>(U) * (width >> 2);
     const long long blocks = (threads + kPoolThreads - 1) / kPoolThreads;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-    compressor_pool_kernel<<<static_cast<unsigned>(blocks), kPoolThreads, 0, s>>>(kv, score, ratio, width, out, U);
-    return cudaGetLastError();
+    return launch_k(compressor_pool_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kPoolThreads), 0, s, kv, score, ratio,
+                    width, out, U);
 }
 
 }  // namespace ds4a

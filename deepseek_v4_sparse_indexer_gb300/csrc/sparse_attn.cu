@@ -234,6 +234,8 @@ DS4A_DEV void tmem_ld16x256_x8(uint32_t taddr, uint32_t (&r)[32]) {
 
 __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_constant__ AttnArgs a, int n_split,
                                                                   int n_items) {
+    pdl_launch_dependents();
+    pdl_wait();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sQ = smem + kOffQ;
@@ -825,6 +827,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
 // Combines the split partials of one (unit, head): O = sum_s 2^(m_s - M) O_s /
 // sum_s 2^(m_s - M) l_s, lse = (M + log2 L) ln 2.
 __global__ void __launch_bounds__(128) attn_merge_kernel(const __grid_constant__ AttnArgs a, int n_split) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int unit = blockIdx.x / kNHead;
     const int h = blockIdx.x - unit * kNHead;
     const float *wo = static_cast<const float *>(a.ws);
@@ -891,11 +895,10 @@ cudaError_t launch_sparse_attn(const AttnArgs &a, int num_sms, cudaStream_t s) {
     const long long items = static_cast<long long>(a.units) * n_split;
     if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
     const int grid = static_cast<int>(items < num_sms ? items : num_sms);
-    sparse_attn_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, n_split, static_cast<int>(items));
-    e = cudaGetLastError();
+    e = launch_k(sparse_attn_kernel, dim3(grid), dim3(kThreads), kSmemBytes, s, a, n_split, static_cast<int>(items));
     if (e != cudaSuccess || n_split == 1) return e;
-    attn_merge_kernel<<<static_cast<unsigned>(static_cast<long long>(a.units) * kNHead), 128, 0, s>>>(a, n_split);
-    return cudaGetLastError();
+    return launch_k(attn_merge_kernel, dim3(static_cast<unsigned>(static_cast<long long>(a.units) * kNHead)), dim3(128), 0,
+                    s, a, n_split);
 }
 
 }  // namespace ds4a

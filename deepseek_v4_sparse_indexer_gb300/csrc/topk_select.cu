@@ -63,6 +63,8 @@ __global__ void __launch_bounds__(kHistThreads) topk_hist_kernel(const float *__
                                                                  const int32_t *__restrict__ n_rows, int Q,
                                                                  int N_cap, int chunk, int n_chunks, TopkWs ws,
                                                                  uint32_t *status) {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ uint32_t h[kBins];
     const long long row = blockIdx.x / n_chunks;
     const int cidx = static_cast<int>(blockIdx.x - row * n_chunks);
@@ -199,6 +201,8 @@ __global__ void __launch_bounds__(kHistThreads) topk_filter_kernel(const float *
                                                                    const int32_t *__restrict__ n_rows, int Q,
                                                                    int N_cap, int top_k, int chunk, int n_chunks,
                                                                    TopkWs ws) {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ uint32_t h[kBins];
     __shared__ uint32_t scratch[kHistThreads + 4];
     __shared__ int32_t q_sure[kMaxTopK];
@@ -332,6 +336,8 @@ __global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float *
                                                                    int N_cap, int top_k, TopkWs ws,
                                                                    int32_t *__restrict__ idx_out,
                                                                    int32_t *__restrict__ count_out) {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ uint32_t h[kBins];
     __shared__ uint32_t scratch[kFinalThreads + 4];
     __shared__ int32_t sel[kMaxTopK];
@@ -509,6 +515,8 @@ __global__ void __launch_bounds__(kRowThreads, 2) topk_row_kernel(const float *_
                                                                   int N_cap, int top_k,
                                                                   int32_t *__restrict__ idx_out,
                                                                   int32_t *__restrict__ count_out, uint32_t *status) {
+    pdl_launch_dependents();
+    pdl_wait();
     extern __shared__ __align__(16) uint8_t row_smem[];
     uint2 *cand = reinterpret_cast<uint2 *>(row_smem);                               // [kRowCandCap]
     uint32_t *h = reinterpret_cast<uint32_t *>(row_smem + kRowCandCap * 8);           // [kBins]
@@ -870,6 +878,8 @@ DS4A_DEV uint32_t bitmap_prefix(const uint32_t *bm, int nw, int wpt, uint32_t *w
 }
 
 __global__ void __launch_bounds__(kCandThreads) topk_cand_kernel(const __grid_constant__ TopkCandArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();
     extern __shared__ __align__(16) uint8_t cand_smem[];
     uint2 *cache = reinterpret_cast<uint2 *>(cand_smem);                          // [kCandCache]
     uint32_t *h = reinterpret_cast<uint32_t *>(cand_smem + kCandCache * 8);       // [kBins]
@@ -968,16 +978,19 @@ size_t topk_ws_bytes(long long R, int top_k) {
     return b;
 }
 
+constexpr int kRowKernelMaxShortRow = 32768;   // rows up to this length take the one-CTA-per-row kernel
+
 cudaError_t launch_topk(const TopkArgs &a, int num_sms, cudaStream_t s) {
     const long long R = static_cast<long long>(a.U) * a.Q;
-    if (R >= num_sms) {
-        // Enough rows to fill the GPU: one CTA per row, no workspace.
+    if (R >= num_sms || a.N_cap <= kRowKernelMaxShortRow) {
+        // Enough rows to fill the GPU, or rows short enough for one CTA each
+        // (a single launch beats three on small batches): one CTA per row, no
+        // workspace.
         if (R > 0x7fffffffLL) return cudaErrorInvalidValue;
         cudaError_t e = cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowSmemBytes);
         if (e != cudaSuccess) return e;
-        topk_row_kernel<<<static_cast<unsigned>(R), kRowThreads, kRowSmemBytes, s>>>(a.scores, a.n_rows, a.Q, a.N_cap,
-                                                                                     a.top_k, a.idx, a.count, a.status);
-        return cudaGetLastError();
+        return launch_k(topk_row_kernel, dim3(static_cast<unsigned>(R)), dim3(kRowThreads), kRowSmemBytes, s, a.scores,
+                        a.n_rows, a.Q, a.N_cap, a.top_k, a.idx, a.count, a.status);
     }
     TopkWs ws = topk_ws(a.ws, R, a.top_k);
     // Zero the histograms and counters (contiguous at the front).
@@ -992,17 +1005,14 @@ cudaError_t launch_topk(const TopkArgs &a, int num_sms, cudaStream_t s) {
     const long long blocks = R * n_chunks;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     const unsigned grid = static_cast<unsigned>(blocks);
-    topk_hist_kernel<<<grid, kHistThreads, 0, s>>>(a.scores, a.n_rows, a.Q, a.N_cap, chunk, n_chunks, ws,
-                                                   a.status);
-    e = cudaGetLastError();
+    e = launch_k(topk_hist_kernel, dim3(grid), dim3(kHistThreads), 0, s, a.scores, a.n_rows, a.Q, a.N_cap, chunk, n_chunks,
+                 ws, a.status);
     if (e != cudaSuccess) return e;
-    topk_filter_kernel<<<grid, kHistThreads, 0, s>>>(a.scores, a.n_rows, a.Q, a.N_cap, a.top_k, chunk, n_chunks,
-                                                     ws);
-    e = cudaGetLastError();
+    e = launch_k(topk_filter_kernel, dim3(grid), dim3(kHistThreads), 0, s, a.scores, a.n_rows, a.Q, a.N_cap, a.top_k, chunk,
+                 n_chunks, ws);
     if (e != cudaSuccess) return e;
-    topk_final_kernel<<<dim3(static_cast<unsigned>(R), 1), kFinalThreads, 0, s>>>(a.scores, a.n_rows, a.Q, a.N_cap,
-                                                                                  a.top_k, ws, a.idx, a.count);
-    return cudaGetLastError();
+    return launch_k(topk_final_kernel, dim3(static_cast<unsigned>(R), 1), dim3(kFinalThreads), 0, s, a.scores, a.n_rows,
+                    a.Q, a.N_cap, a.top_k, ws, a.idx, a.count);
 }
 
 }  // namespace ds4a
@@ -1014,7 +1024,6 @@ cudaError_t launch_topk_cand(const TopkCandArgs &a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(topk_cand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    topk_cand_kernel<<<a.R, kCandThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_k(topk_cand_kernel, dim3(a.R), dim3(kCandThreads), smem, s, a);
 }
 }  // namespace ds4a
