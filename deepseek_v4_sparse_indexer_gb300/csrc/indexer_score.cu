@@ -224,7 +224,9 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
     pdl_wait();
     using C = IdxCfg<G>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // Aligned by pointer arithmetic on the __shared__ array (not through an
+    // integer), so that the compiler keeps shared-space accesses for it.
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sA = smem + C::kOffA;
     uint8_t *sB = smem + C::kOffB;
     float *sW = reinterpret_cast<float *>(smem + C::kOffW);

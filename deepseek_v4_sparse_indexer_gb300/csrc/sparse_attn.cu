@@ -237,7 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
     pdl_launch_dependents();
     pdl_wait();
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // Aligned by pointer arithmetic on the __shared__ array (not through an
+    // integer), so that the compiler keeps shared-space accesses for it.
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sQ = smem + kOffQ;
     uint8_t *sX = smem + kOffX;
     uint8_t *sP = smem + kOffP;
@@ -795,6 +797,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
             tc_fence_after();
             float *obase = n_split == 1 ? a.out + static_cast<long long>(m.unit) * kNHead * kHeadDim
                                         : static_cast<float *>(a.ws) + slot * kNHead * kHeadDim;
+            // 1/l of the 64 heads in registers: no shared load between the
+            // global stores below.
+            float il[kNHead];
+#pragma unroll
+            for (int h = 0; h < kNHead; ++h) il[h] = sInvL[h];
             for (int c = 0; c < 8; ++c) {
                 uint32_t v[32];
                 tmem_ld32(tmem + lane_off + kTmemO + c * 32, v);
@@ -803,7 +810,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
 #pragma unroll
                 for (int k = 0; k < 32; ++k) {
                     const int h = (c & 1) * 32 + k;
-                    obase[static_cast<long long>(h) * kHeadDim + d] = __uint_as_float(v[k]) * sInvL[h];
+                    obase[static_cast<long long>(h) * kHeadDim + d] = __uint_as_float(v[k]) * ((c & 1) ? il[32 + k] : il[k]);
                 }
             }
             tc_fence_before();
