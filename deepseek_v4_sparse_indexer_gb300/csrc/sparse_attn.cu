@@ -506,6 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                 int ns = m.t0, nv = m.t0;                    // next S / next V tile
                 uint32_t js = jt, jv = jt;                   // their tile counters
                 uint64_t idle_since = 0;
+                uint32_t idle_polls = 0;
                 while (nv < m.t1) {
                     bool progressed = false;
                     if (nv < ns) {
@@ -566,13 +567,18 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                             progressed = true;
                         }
                     }
+                    // The timer is read only every 64 idle polls: a %globaltimer read
+                    // is slow enough to delay the reaction to a barrier.
                     if (progressed) {
                         idle_since = 0;
-                    } else if (idle_since == 0) {
-                        idle_since = globaltimer_ns();
-                    } else if (*abort_flag || globaltimer_ns() - idle_since > kWaitLimitNs) {
-                        ok = false;
-                        break;
+                        idle_polls = 0;
+                    } else if ((++idle_polls & 63u) == 0) {
+                        if (idle_since == 0) {
+                            idle_since = globaltimer_ns();
+                        } else if (*abort_flag || globaltimer_ns() - idle_since > kWaitLimitNs) {
+                            ok = false;
+                            break;
+                        }
                     }
                 }
                 if (!ok) break;
