@@ -8,7 +8,7 @@
 // unit is one decode query or one query of a prefill chunk.  The unit's row
 // list [selected compressed rows..., raw-window rows...] is cut into 64-row
 // tiles, double-buffered in shared memory:
-//   gather   warps 5-11: the seven warps share every tile (4-row groups dealt
+//   gather   warps 6-11: the six warps share every tile (4-row groups dealt
 //            round-robin) with 16-byte cp.async into eight 8 KB column
 //            blocks in the 128B-swizzled layout; masked rows are zero-filled
 //            and per-group row-validity bits go to shared memory; each
@@ -21,7 +21,7 @@
 //            row per warp instruction, into registers), and the warp writes
 //            them out as exact bf16 values (code * scale) into the same
 //            swizzled tile, so the GEMMs below do not change;
-//   logits   warp 4 (one thread): S[64 heads x 64 rows] = q . X^T, 32 UMMAs
+//   logits   warp 4: S[64 heads x 64 rows] = q . X^T, 32 UMMAs
 //            (M=64, N=64, K=16, both operands K-major) into one of two TMEM
 //            buffers (head h of the M=64 accumulator sits in TMEM lane
 //            32*(h/16) + h%16);
@@ -31,7 +31,7 @@
 //            The per-head tile max is a register max plus two shuffles;
 //            p = exp2(l - m) goes to P[head][row] (the K-major operand of the
 //            values GEMM), row sums stay in registers;
-//   values   warp 4: O^T[512 dims x 64 heads] += X^T . P^T as four M=128
+//   values   warp 5: O^T[512 dims x 64 heads] += X^T . P^T as four M=128
 //            chunks (K = 64 rows; X read as the MN-major operand, P as the
 //            K-major one), accumulating in TMEM; its commit frees the row
 //            buffer and the P buffer.
@@ -43,6 +43,14 @@
 // tiles in fp16 with q converted in place to fp16 (exact for |q| in
 // [2^-14, 65504]).  Split items write unnormalised partials (O, m, l) that
 // attn_merge_kernel combines by log-sum-exp.
+//
+// The two GEMM streams have their own issuing warps, so that the values GEMM
+// of a tile (which frees its row buffer) never queues behind the logits GEMMs
+// of the next one.  A whole converged warp runs each issue loop and one
+// elected lane issues: a lone lane inside a divergent branch issues a UMMA
+// only every ~45 cycles, a converged warp as fast as the tensor core takes them
+// (32 cycles for M=64, N=64, K=16).  Descriptors are advanced by adding the
+// byte offset / 16 to a base descriptor.
 //
 // Every wait is bounded (DS4A_DEV_TIMEOUT); on timeout the CTA drains what it
 // issued (bounded), frees TMEM and returns.
@@ -56,9 +64,10 @@ namespace {
 
 constexpr int TR = 64;                        // rows per tile (UMMA N of the logit GEMM)
 constexpr int kSoftmaxWarps = 4;              // warps 0-3: softmax + epilogue (TMEM lane quarters)
-constexpr int kMmaWarp = 4;                   // warp 4: TMEM owner + UMMA issuer
-constexpr int kFirstGatherWarp = 5;           // warps 5-11: row gather (cp.async)
-constexpr int kGatherWarps = 7;
+constexpr int kMmaWarp = 4;                   // warp 4: TMEM owner + logits UMMA issuer
+constexpr int kPvWarp = 5;                    // warp 5: values UMMA issuer
+constexpr int kFirstGatherWarp = 6;           // warps 6-11: row gather (cp.async)
+constexpr int kGatherWarps = 6;
 constexpr int kRowGroups = TR / 4;            // 4-row groups of a tile, dealt round-robin to the gather warps
 constexpr int kGroupsPerWarp = (kRowGroups + kGatherWarps - 1) / kGatherWarps;
 constexpr int kThreads = (kFirstGatherWarp + kGatherWarps) * 32;
@@ -74,7 +83,7 @@ constexpr int kOffAlpha = kOffValid + 2 * kRowGroups;  // [2][16] row-validity n
 constexpr int kOffFlag = kOffAlpha + 2 * kNHead * 4;
 constexpr int kOffInvL = kOffFlag + 2 * kSoftmaxWarps * 4;
 constexpr int kOffBar = kOffInvL + kNHead * 4;
-constexpr int kNumBars = 16;
+constexpr int kNumBars = 18;                  // 17 used
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 32 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -170,6 +179,28 @@ DS4A_DEV void st_shared_v4(uint32_t addr, const uint32_t (&v)[4]) {
                  : "memory");
 }
 
+// UMMA / commit issued by the elected lane of a converged warp.
+DS4A_DEV void umma_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+DS4A_DEV void commit_elect(uint64_t *bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
+}
+// Warp-wide bounded wait (hinted try_wait: a waiting issuer takes no issue slots).
+DS4A_DEV bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    return __all_sync(0xffffffffu, mbar_wait_hint(bar, parity, abort));
+}
+
 DS4A_DEV bool wait_drain(uint64_t *bar, uint32_t parity) {
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity))
@@ -257,7 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
     uint64_t *q16_ready = q_free + 1;
     uint64_t *o_free = q16_ready + 1;
     uint64_t *drain = o_free + 1;
-    uint64_t *grp = drain + 1;                                         // softmax-group barrier
+    uint64_t *drain_v = drain + 1;
+    uint64_t *grp = drain_v + 1;                                       // softmax-group barrier
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
 
@@ -275,6 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
         mbar_init(q16_ready, kSoftmaxWarps);
         mbar_init(o_free, kSoftmaxWarps);
         mbar_init(drain, 1);
+        mbar_init(drain_v, 1);
         mbar_init(grp, kSoftmaxWarps);
         *abort_flag = 0;
         mbar_fence_init();
@@ -291,8 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
 
     if (warp >= kFirstGatherWarp) {
         // ------------------------------------------------------------ row gather
-        // All seven warps walk the CTA's (item, tile) sequence; warp g copies
-        // the 4-row groups g, g + 7, g + 14 (< 16) of every tile.  Lane l
+        // All six warps walk the CTA's (item, tile) sequence; warp g copies
+        // the 4-row groups g, g + 6, g + 12 (< 16) of every tile.  Lane l
         // copies 16-byte chunk (l & 7) of row 4k + (l >> 3) of group k in
         // every 64-column block: a warp instruction moves four full 128-byte
         // row segments.  Destinations follow the 128B swizzle.
@@ -484,114 +517,98 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
             if (lane == 0) report(a.status, DS4A_DEV_TIMEOUT);
         }
     } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ UMMA issuer
-        // Per item, the logits GEMMs S(t) and the values GEMMs V(t) are issued
-        // in tile order, each stream as soon as its inputs are ready, V first:
-        // V(t-1) frees its row buffer for the gather as early as possible, and
-        // S(t) runs while the softmax works on tile t - 1.
-        if (lane == 0) {
-            uint32_t qph = 0, q16ph = 0, ofph = 0;
-            uint32_t xfph[2] = {0, 0}, seph[2] = {0, 0}, pfph[2] = {0, 0};
-            bool ok = true, first_item = true;
-            constexpr uint32_t id_s_bf = idesc_f16(false, false), id_s_f16 = idesc_f16(true, false);
-            constexpr uint32_t id_v_bf = idesc_f16(false, true), id_v_f16 = idesc_f16(true, true);
-            const uint32_t aQ = smem_u32(sQ), aX = smem_u32(sX), aP = smem_u32(sP);
-            uint32_t jt = 0;                                 // tile counter: buffers jt & 1
-            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-                const Item m = make_item(a, it, n_split);
-                if (m.t0 >= m.t1) continue;
-                if (!mbar_wait(q_full, qph, abort_flag)) { ok = false; break; }
-                qph ^= 1;
-                bool q16 = false;
-                int ns = m.t0, nv = m.t0;                    // next S / next V tile
-                uint32_t js = jt, jv = jt;                   // their tile counters
-                uint64_t idle_since = 0;
-                uint32_t idle_polls = 0;
-                while (nv < m.t1) {
-                    bool progressed = false;
-                    if (nv < ns) {
-                        const int b = jv & 1;
-                        if (mbar_test(&p_full[b], pfph[b])) {
-                            pfph[b] ^= 1;
-                            if (nv == m.t0 && !first_item) {
-                                if (!mbar_wait(o_free, ofph, abort_flag)) { ok = false; break; }
-                                ofph ^= 1;
-                            }
-                            tc_fence_after();
-                            const bool raw = nv >= m.ct;
-                            const uint32_t xa = aX + b * kXBuf, pa = aP + b * kPBuf;
-#pragma unroll
-                            for (int c = 0; c < 4; ++c) {
-#pragma unroll
-                                for (int ks = 0; ks < TR / 16; ++ks)
-                                    umma_bf16(tmem + kTmemO + c * kNHead,
-                                              sw128_desc(xa + 2 * c * kXBlk + ks * 2048, kXBlk, 1024),
-                                              sw128_desc(pa + ks * 32, 16, 1024), raw ? id_v_f16 : id_v_bf,
-                                              (nv == m.t0 && ks == 0) ? 0u : 1u);
-                            }
-                            umma_commit(&x_empty[b]);        // row tile and P buffer free
-                            ++nv;
-                            ++jv;
-                            progressed = true;
-                        }
-                    }
-                    if (!progressed && ns < m.t1) {
-                        const bool raw = ns >= m.ct;
-                        const int b = js & 1;
-                        bool ready = true;
-                        if (raw && !q16) {
-                            ready = mbar_test(q16_ready, q16ph);
-                            if (ready) {
-                                q16ph ^= 1;
-                                q16 = true;
-                            }
-                        }
-                        ready = ready && mbar_test(&s_empty[b], seph[b] ^ 1) && mbar_test(&x_full[b], xfph[b]);
-                        if (ready) {
-                            seph[b] ^= 1;
-                            xfph[b] ^= 1;
-                            tc_fence_after();
-                            const uint32_t xa = aX + b * kXBuf;
-                            for (int blk = 0; blk < 8; ++blk) {
-#pragma unroll
-                                for (int kk = 0; kk < 4; ++kk)
-                                    umma_bf16(tmem + kTmemS + b * TR,
-                                              sw128_desc(aQ + blk * kQBlk + kk * 32, 16, 1024),
-                                              sw128_desc(xa + blk * kXBlk + kk * 32, 16, 1024),
-                                              raw ? id_s_f16 : id_s_bf, (blk | kk) ? 1u : 0u);
-                            }
-                            umma_commit(&s_full[b]);
-                            if (ns == m.t1 - 1) umma_commit(q_free);
-                            ++ns;
-                            ++js;
-                            progressed = true;
-                        }
-                    }
-                    // The timer is read only every 64 idle polls: a %globaltimer read
-                    // is slow enough to delay the reaction to a barrier.
-                    if (progressed) {
-                        idle_since = 0;
-                        idle_polls = 0;
-                    } else if ((++idle_polls & 63u) == 0) {
-                        if (idle_since == 0) {
-                            idle_since = globaltimer_ns();
-                        } else if (*abort_flag || globaltimer_ns() - idle_since > kWaitLimitNs) {
-                            ok = false;
-                            break;
-                        }
-                    }
+        // ------------------------------------------------------------ logits issuer
+        // S(t) once the row tile has landed and the softmax has read the
+        // logits two tiles back; the first raw tile also waits for q in fp16.
+        uint32_t qph = 0, q16ph = 0;
+        uint32_t xfph[2] = {0, 0}, seph[2] = {0, 0};
+        bool ok = true;
+        constexpr uint32_t id_s_bf = idesc_f16(false, false), id_s_f16 = idesc_f16(true, false);
+        const uint64_t dq = sw128_desc(smem_u32(sQ), 16, 1024), dx0 = sw128_desc(smem_u32(sX), 16, 1024);
+        uint32_t js = 0;                                     // tile counter: buffers js & 1
+        for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+            const Item m = make_item(a, it, n_split);
+            if (m.t0 >= m.t1) continue;
+            if (!(ok = warp_wait(q_full, qph, abort_flag))) break;
+            qph ^= 1;
+            bool q16 = false;
+            for (int t = m.t0; t < m.t1; ++t, ++js) {
+                const bool raw = t >= m.ct;
+                const int b = js & 1;
+                if (raw && !q16) {
+                    if (!(ok = warp_wait(q16_ready, q16ph, abort_flag))) break;
+                    q16ph ^= 1;
+                    q16 = true;
                 }
-                if (!ok) break;
-                jt = jv;
-                first_item = false;
+                if (!(ok = warp_wait(&s_empty[b], seph[b] ^ 1, abort_flag))) break;
+                seph[b] ^= 1;
+                if (!(ok = warp_wait(&x_full[b], xfph[b], abort_flag))) break;
+                xfph[b] ^= 1;
+                tc_fence_after();
+                const uint64_t dx = dx0 + static_cast<uint64_t>(b * (kXBuf >> 4));
+#pragma unroll
+                for (int blk = 0; blk < 8; ++blk) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_elect(tmem + kTmemS + b * TR, dq + static_cast<uint64_t>(blk * (kQBlk >> 4) + 2 * kk),
+                                   dx + static_cast<uint64_t>(blk * (kXBlk >> 4) + 2 * kk), raw ? id_s_f16 : id_s_bf,
+                                   (blk | kk) ? 1u : 0u);
+                }
+                commit_elect(&s_full[b]);
+                if (t == m.t1 - 1) commit_elect(q_free);
             }
-            if (!ok) {
-                *abort_flag = 1;
-                report(a.status, DS4A_DEV_TIMEOUT);
-            }
-            umma_commit(drain);
-            wait_drain(drain, 0);
         }
+        if (!ok) {
+            *abort_flag = 1;
+            if (lane == 0) report(a.status, DS4A_DEV_TIMEOUT);
+        }
+        commit_elect(drain);
+        wait_drain(drain, 0);
+        __syncwarp();
+    } else if (warp == kPvWarp) {
+        // ------------------------------------------------------------ values issuer
+        // V(t) once the softmax has written P(t) (and rescaled O when a head's
+        // max was raised); the first tile of an item also waits until the
+        // epilogue has read the previous item's O.  Its commit frees the row
+        // tile and the P buffer.
+        uint32_t ofph = 0, pfph[2] = {0, 0};
+        bool ok = true, first_item = true;
+        constexpr uint32_t id_v_bf = idesc_f16(false, true), id_v_f16 = idesc_f16(true, true);
+        const uint64_t dxv = sw128_desc(smem_u32(sX), kXBlk, 1024), dp = sw128_desc(smem_u32(sP), 16, 1024);
+        uint32_t jv = 0;
+        for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+            const Item m = make_item(a, it, n_split);
+            if (m.t0 >= m.t1) continue;
+            for (int t = m.t0; t < m.t1; ++t, ++jv) {
+                const int b = jv & 1;
+                if (!(ok = warp_wait(&p_full[b], pfph[b], abort_flag))) break;
+                pfph[b] ^= 1;
+                if (t == m.t0 && !first_item) {
+                    if (!(ok = warp_wait(o_free, ofph, abort_flag))) break;
+                    ofph ^= 1;
+                }
+                tc_fence_after();
+                const bool raw = t >= m.ct;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                    for (int ks = 0; ks < TR / 16; ++ks)
+                        umma_elect(tmem + kTmemO + c * kNHead,
+                                   dxv + static_cast<uint64_t>((b * kXBuf + 2 * c * kXBlk + ks * 2048) >> 4),
+                                   dp + static_cast<uint64_t>((b * kPBuf + ks * 32) >> 4), raw ? id_v_f16 : id_v_bf,
+                                   (t == m.t0 && ks == 0) ? 0u : 1u);
+                }
+                commit_elect(&x_empty[b]);               // row tile and P buffer free
+            }
+            if (!ok) break;
+            first_item = false;
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            if (lane == 0) report(a.status, DS4A_DEV_TIMEOUT);
+        }
+        commit_elect(drain_v);
+        wait_drain(drain_v, 0);
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax + epilogue
