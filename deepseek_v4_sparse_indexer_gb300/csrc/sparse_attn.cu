@@ -179,6 +179,13 @@ DS4A_DEV void st_shared_v4(uint32_t addr, const uint32_t (&v)[4]) {
                  : "memory");
 }
 
+// 2^x by the MUFU approximation (relative error ~2^-22; -inf -> +0).
+DS4A_DEV float ex2(float x) {
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // UMMA / commit issued by the elected lane of a converged warp.
 DS4A_DEV void umma_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
     asm volatile(
@@ -697,16 +704,27 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                 if (!ok) break;
                 // rows 8j + 2(t%4) + {0,1}: group 2j + (t%4)/2, bits 2(t%4 & 1) + {0,1}
                 const uint4 vw = *reinterpret_cast<const uint4 *>(sValid + b * kRowGroups);
-                const uint32_t vsh = 8 * (t4 >> 1) + 2 * (t4 & 1);
+                // A tile whose rows are all listed, with a positive scale, keeps the
+                // raw logits: the max is taken before scaling and p = 2^(s*c - M)
+                // is one FMA and one ex2.  Otherwise masked rows are -inf and the
+                // logits are scaled first (c = 1 below).
+                const bool full = (vw.x & vw.y & vw.z & vw.w) == 0x0F0F0F0Fu && sl2 > 0.f;
+                const float mul = full ? sl2 : 1.f;
                 float x[32];
+                if (full) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t w = (j < 2 ? vw.x : j < 4 ? vw.y : j < 6 ? vw.z : vw.w) >> (16 * (j & 1) + vsh);
-                    const bool va = w & 1u, vb = (w >> 1) & 1u;
-                    x[4 * j] = va ? __uint_as_float(r[4 * j]) * sl2 : NEG_INF;
-                    x[4 * j + 1] = vb ? __uint_as_float(r[4 * j + 1]) * sl2 : NEG_INF;
-                    x[4 * j + 2] = va ? __uint_as_float(r[4 * j + 2]) * sl2 : NEG_INF;
-                    x[4 * j + 3] = vb ? __uint_as_float(r[4 * j + 3]) * sl2 : NEG_INF;
+                    for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
+                } else {
+                    const uint32_t vsh = 8 * (t4 >> 1) + 2 * (t4 & 1);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t w = (j < 2 ? vw.x : j < 4 ? vw.y : j < 6 ? vw.z : vw.w) >> (16 * (j & 1) + vsh);
+                        const bool va = w & 1u, vb = (w >> 1) & 1u;
+                        x[4 * j] = va ? __uint_as_float(r[4 * j]) * sl2 : NEG_INF;
+                        x[4 * j + 1] = vb ? __uint_as_float(r[4 * j + 1]) * sl2 : NEG_INF;
+                        x[4 * j + 2] = va ? __uint_as_float(r[4 * j + 2]) * sl2 : NEG_INF;
+                        x[4 * j + 3] = vb ? __uint_as_float(r[4 * j + 3]) * sl2 : NEG_INF;
+                    }
                 }
                 float mx0 = NEG_INF, mx1 = NEG_INF;
 #pragma unroll
@@ -718,18 +736,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                 mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                mx0 *= mul;
+                mx1 *= mul;
                 // The running max is raised only when the tile exceeds it by more than 2^8.
                 float al0 = 1.f, al1 = 1.f;
                 if (M0 == NEG_INF) {
                     M0 = mx0;                            // first finite max: O and sums are still 0
                 } else if (mx0 > M0 + kRescaleThreshold) {
-                    al0 = exp2f(M0 - mx0);
+                    al0 = ex2(M0 - mx0);
                     M0 = mx0;
                 }
                 if (M1 == NEG_INF) {
                     M1 = mx1;
                 } else if (mx1 > M1 + kRescaleThreshold) {
-                    al1 = exp2f(M1 - mx1);
+                    al1 = ex2(M1 - mx1);
                     M1 = mx1;
                 }
                 // Any head raised in any warp: every warp rescales its O^T lanes.
@@ -740,16 +760,17 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                     sAlpha[tb * kNHead + h1] = al1;
                 }
                 if (lane == 0) sFlag[tb * kSoftmaxWarps + q4] = wresc ? 1u : 0u;
-                if (!(ok = group_sync())) break;
-                const uint4 fl = *reinterpret_cast<const uint4 *>(sFlag + tb * kSoftmaxWarps);
-                const bool any_resc = (fl.x | fl.y | fl.z | fl.w) != 0u;
-                const float mr0 = M0 == NEG_INF ? 0.f : M0, mr1 = M1 == NEG_INF ? 0.f : M1;
+                // Arrive now, wait after the exponentials: the exchange of the
+                // rescale flags overlaps this warp's own work.
+                __syncwarp();
+                if (lane == 0) mbar_arrive(grp);
+                const float nr0 = M0 == NEG_INF ? 0.f : -M0, nr1 = M1 == NEG_INF ? 0.f : -M1;
                 float s0 = 0.f, s1 = 0.f;
                 uint32_t pk0[8], pk1[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const float pa = exp2f(x[4 * j] - mr0), pb = exp2f(x[4 * j + 1] - mr0);
-                    const float pc = exp2f(x[4 * j + 2] - mr1), pd = exp2f(x[4 * j + 3] - mr1);
+                    const float pa = ex2(fmaf(x[4 * j], mul, nr0)), pb = ex2(fmaf(x[4 * j + 1], mul, nr0));
+                    const float pc = ex2(fmaf(x[4 * j + 2], mul, nr1)), pd = ex2(fmaf(x[4 * j + 3], mul, nr1));
                     s0 += pa + pb;
                     s1 += pc + pd;
                     pk0[j] = raw ? pack2<true>(pa, pb) : pack2<false>(pa, pb);
@@ -767,6 +788,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                     *reinterpret_cast<uint32_t *>(pbuf + h1 * 128 + ((j ^ sw) << 4) + 4 * t4) = pk1[j];
                 }
                 fence_proxy_async();
+                {
+                    const bool r = __all_sync(0xffffffffu, mbar_wait(grp, gph, abort_flag));
+                    gph ^= 1;
+                    if (!(ok = r)) break;
+                }
+                const uint4 fl = *reinterpret_cast<const uint4 *>(sFlag + tb * kSoftmaxWarps);
+                const bool any_resc = (fl.x | fl.y | fl.z | fl.w) != 0u;
                 if (any_resc && t > m.t0) {
                     // O^T holds the sum up to the previous values GEMM (tile jt - 1): wait for it.
                     ok = __all_sync(0xffffffffu, mbar_wait(&x_empty[(jt - 1) & 1], ((jt - 1) >> 1) & 1, abort_flag));
