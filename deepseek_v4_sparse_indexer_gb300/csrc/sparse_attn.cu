@@ -174,6 +174,15 @@ DS4A_DEV void e4m3x8_to_bf16(uint32_t w0, uint32_t w1, float s, uint32_t (&o)[4]
         o[j] = pack2<false>(f.x * s, f.y * s);
     }
 }
+// 16-byte read-only load that bypasses L1 (rows are read once).  Volatile, so
+// that it stays ahead of the buffer wait that follows it.
+DS4A_DEV uint4 ld_nc_v4(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
 DS4A_DEV void st_shared_v4(uint32_t addr, const uint32_t (&v)[4]) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
                  : "memory");
@@ -414,11 +423,21 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                 if (g < kRowGroups && ct_ < cm.ct && ct_ * TR + 4 * g + rsub < cm.cnt && src[k] < 0) bad_idx = true;
             }
             if (__any_sync(0xffffffffu, bad_idx) && lane == 0) report(a.status, DS4A_DEV_BOUNDS);
-            // FP8 tile: its codes go to registers before the buffer is free, so
-            // the loads overlap the wait for the values GEMM two tiles back.
-            const bool fp8_tile = ct_ < cm.ct && a.rows8 != nullptr;
-            uint4 c8[kGroupsPerWarp][4];                 // codes of the group's four rows
-            float s8[kGroupsPerWarp][4];                 // and their scales
+            // FP8 rows go to registers before their buffer is free, so that the
+            // loads overlap the wait for the values GEMM two tiles back; bf16
+            // rows are copied by cp.async once the buffer is free, and a whole
+            // tile of contiguous rows (the raw window, or a dense row list) by
+            // TMA (rows past the valid count must be zeros, so a partial tile is
+            // gathered).
+            const bool raw_tile = ct_ >= cm.ct;
+            const int first = raw_tile ? (ct_ - cm.ct) * TR : ct_ * TR;
+            const bool fp8_tile = !raw_tile && a.rows8 != nullptr;
+            const bool tma_tile = !fp8_tile && (raw_tile ? (a.tma_raw && first + TR <= cm.nrw)
+                                                         : (a.tma_rows && !a.idx && first + TR <= cm.cnt));
+            // Lane l: codes 16l .. 16l+15 of each row of its groups, and the
+            // rows' scales.
+            uint4 rg[kGroupsPerWarp][4];
+            float s8[kGroupsPerWarp][4];
             if (fp8_tile) {
 #pragma unroll
                 for (int k = 0; k < kGroupsPerWarp; ++k) {
@@ -428,14 +447,22 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                     for (int i = 0; i < 4; ++i) {
                         const int sr = __shfl_sync(0xffffffffu, src[k], 8 * i);   // row 4g + i (lanes 8i.. hold it)
                         if (sr >= 0) {
-                            c8[k][i] = __ldg(reinterpret_cast<const uint4 *>(a.rows8 + static_cast<long long>(sr) * kHeadDim) + lane);
+                            rg[k][i] = ld_nc_v4(reinterpret_cast<const uint4 *>(a.rows8 + static_cast<long long>(sr) * kHeadDim) + lane);
                             s8[k][i] = __ldg(a.row_scale + sr);
                         } else {
-                            c8[k][i] = make_uint4(0u, 0u, 0u, 0u);
+                            rg[k][i] = make_uint4(0u, 0u, 0u, 0u);
                             s8[k][i] = 0.f;
                         }
                     }
                 }
+            }
+            // The row list of the next tile: before the wait, except for a
+            // cp.async tile, where it goes out right after the copies.
+            const long long y_tma = (raw_tile ? cm.raw_row0 : cm.comp_row0) + first;
+            const bool early_next = fp8_tile || tma_tile;
+            if (early_next) {
+                advance(cit, ct_, cm);
+                if (cit < n_items) fetch_rows(cm, ct_, rv);
             }
             const int xb = jt & 1;
             ok = __all_sync(0xffffffffu, mbar_wait(&x_empty[xb], xeph[xb] ^ 1, abort_flag));
@@ -448,42 +475,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                 const uint32_t bal = __ballot_sync(0xffffffffu, src[k] >= 0);
                 if (lane == 0 && g < kRowGroups) sValid[xb * kRowGroups + g] = static_cast<uint8_t>(nibble(bal));
             }
-            // A whole tile of contiguous rows comes by TMA: raw-window tiles and
-            // the tiles of a dense row list (rows past the valid count must be
-            // zeros, so a partial tile takes the cp.async path).
-            const bool raw_tile = ct_ >= cm.ct;
-            const int first = raw_tile ? (ct_ - cm.ct) * TR : ct_ * TR;
-            const bool tma_tile = raw_tile ? (a.tma_raw && first + TR <= cm.nrw)
-                                           : (a.tma_rows && !a.idx && first + TR <= cm.cnt);
             const uint32_t buf = smem_u32(sX) + xb * kXBuf;
-            if (fp8_tile) {
-                // written below from the codes in registers
-            } else if (tma_tile) {
-                if (gw == 0 && lane == 0) {
-                    const int y = static_cast<int>((raw_tile ? cm.raw_row0 : cm.comp_row0) + first);
-                    mbar_arrive_expect_tx(&x_full[xb], kXBuf);      // also this warp's arrival
-                    for (int b = 0; b < 8; ++b)
-                        tma_load_2d_nohint(sX + xb * kXBuf + b * kXBlk, raw_tile ? &a.tm_raw : &a.tm_rows,
-                                           &x_full[xb], b * 64, y);
-                }
-            } else {
-#pragma unroll
-                for (int b = 0; b < 8; ++b) {
-#pragma unroll
-                    for (int k = 0; k < kGroupsPerWarp; ++k) {
-                        const int g = gw + k * kGatherWarps;
-                        if (g >= kRowGroups) continue;
-                        const int r = 4 * g + rsub;
-                        cp_async16(buf + b * kXBlk + r * 128 + ((chunk ^ (r & 7)) << 4),
-                                   src[k] >= 0 ? base + static_cast<long long>(src[k]) * kHeadDim + b * 64 : a.q,
-                                   src[k] >= 0 ? 16u : 0u);
-                    }
-                }
+            if (tma_tile && gw == 0 && lane == 0) {
+                const int y = static_cast<int>(y_tma);
+                mbar_arrive_expect_tx(&x_full[xb], kXBuf);      // also this warp's arrival
+                for (int b = 0; b < 8; ++b)
+                    tma_load_2d_nohint(sX + xb * kXBuf + b * kXBlk, raw_tile ? &a.tm_raw : &a.tm_rows, &x_full[xb], b * 64, y);
             }
-            cp_async_commit();
-            // While the copies land: the row list of the next tile.
-            advance(cit, ct_, cm);
-            if (cit < n_items) fetch_rows(cm, ct_, rv);
             if (fp8_tile) {
                 // dims 16l .. 16l+15 are 16-byte chunks 2(l%4) and 2(l%4)+1 of the
                 // 64-column block l/4.  Lanes of odd blocks write their second
@@ -498,8 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                     for (int i = 0; i < 4; ++i) {
                         const int r = 4 * g + i;
                         uint32_t lo[4], hi[4];
-                        e4m3x8_to_bf16(c8[k][i].x, c8[k][i].y, s8[k][i], lo);
-                        e4m3x8_to_bf16(c8[k][i].z, c8[k][i].w, s8[k][i], hi);
+                        e4m3x8_to_bf16(rg[k][i].x, rg[k][i].y, s8[k][i], lo);
+                        e4m3x8_to_bf16(rg[k][i].z, rg[k][i].w, s8[k][i], hi);
                         const uint32_t rowa = buf + blk * kXBlk + r * 128;
                         const uint32_t a0 = rowa + ((c0 ^ (r & 7)) << 4), a1 = rowa + (((c0 + 1) ^ (r & 7)) << 4);
                         if (odd) {
@@ -511,14 +509,33 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                         }
                     }
                 }
+            } else if (!tma_tile) {
+                // 16-byte cp.async into the 128B-swizzled layout: lane l copies
+                // chunk (l & 7) of row 4k' + (l >> 3) of each of its groups in
+                // every 64-column block, so a warp instruction moves four whole
+                // 128-byte row segments.  Masked rows are zero-filled.
+#pragma unroll
+                for (int b = 0; b < 8; ++b) {
+#pragma unroll
+                    for (int k = 0; k < kGroupsPerWarp; ++k) {
+                        const int g = gw + k * kGatherWarps;
+                        if (g >= kRowGroups) continue;
+                        const int r = 4 * g + rsub;
+                        cp_async16(buf + b * kXBlk + r * 128 + ((chunk ^ (r & 7)) << 4),
+                                   src[k] >= 0 ? base + static_cast<long long>(src[k]) * kHeadDim + b * 64 : a.q,
+                                   src[k] >= 0 ? 16u : 0u);
+                    }
+                }
+                cp_async_commit();
+                advance(cit, ct_, cm);
+                if (cit < n_items) fetch_rows(cm, ct_, rv);
+                cp_async_wait<0>();
             }
-            cp_async_wait<0>();
             fence_proxy_async();
             __syncwarp();
             if (lane == 0 && !(tma_tile && gw == 0)) mbar_arrive(&x_full[xb]);
             ++jt;
         }
-        cp_async_wait<0>();
         if (!ok) {
             *abort_flag = 1;
             if (lane == 0) report(a.status, DS4A_DEV_TIMEOUT);
