@@ -91,7 +91,7 @@ static_assert(kOffBar % 8 == 0, "mbarrier alignment");
 constexpr uint32_t kTmemCols = 512;           // S: 2 x 64 columns, O^T: 4 x 64 columns
 constexpr uint32_t kTmemS = 0;
 constexpr uint32_t kTmemO = 128;
-constexpr int kMaxSplit = 16;
+constexpr int kMaxAttnCtas = 160;            // grid cap (one persistent CTA per SM; 152 on GB300)
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
 
 // UMMA instruction descriptors (see idesc_bf16_f32): logits (M = 64 heads,
@@ -224,9 +224,11 @@ DS4A_DEV bool wait_drain(uint64_t *bar, uint32_t parity) {
     return true;
 }
 
-// What one work item covers.
+// What one work item covers: this CTA's piece of one unit.
 struct Item {
-    int unit, split;     // unit: 64-head sub-unit (q, out, lse); ru: its row-side unit
+    int unit;            // 64-head sub-unit (q, out, lse); ru: its row-side unit
+    bool split;          // the unit's tiles are shared with another CTA: the piece is a partial
+    long long slot;      // its partial's workspace slot
     int ru;
     int cnt;             // selected compressed rows (clamped to [0, top_k])
     int nrw;             // raw rows
@@ -236,13 +238,63 @@ struct Item {
     long long comp_row0; // row index of the unit's compressed row 0 in the rows buffer
 };
 
-DS4A_DEV Item make_item(const AttnArgs &a, int it, int n_split) {
+// Work schedule.  With G CTAs, the first R = floor(units / G) rounds of units
+// are dealt whole and strided (CTA c: units c, c + G, ...), so that the CTAs
+// work on neighbouring units at any time.  The remaining units' tiles (nt per
+// unit: the most a unit can have, top_k compressed rows and the 128-row raw
+// window) are cut into g_rem equal shares, one per CTA c < g_rem, so that
+// every CTA ends with the same number of tiles to within one.  A unit cut by a
+// share boundary is computed in pieces whose partials (unnormalised O, m, l)
+// attn_merge_kernel combines.
+struct Sched {
+    int nt, R, n_pieces;
+    int u_rem0;              // first remainder unit (R x G)
+    long long rs, re;        // this CTA's remainder share: remainder tiles [rs, re)
+    int v0;                  // its first remainder unit (relative to u_rem0)
+};
+
+DS4A_DEV Sched make_sched(const AttnArgs &a, int nt, int g_rem) {
+    Sched sc;
+    const int G = gridDim.x, c = blockIdx.x;
+    sc.nt = nt;
+    sc.R = a.units / G;
+    sc.u_rem0 = sc.R * G;
+    const long long t_rem = static_cast<long long>(a.units - sc.u_rem0) * nt;
+    sc.rs = sc.re = 0;
+    sc.v0 = 0;
+    int n_rem = 0;
+    if (c < g_rem) {
+        sc.rs = static_cast<long long>(c) * t_rem / g_rem;
+        sc.re = static_cast<long long>(c + 1) * t_rem / g_rem;
+        if (sc.re > sc.rs) {
+            sc.v0 = static_cast<int>(sc.rs / nt);
+            n_rem = static_cast<int>((sc.re - 1) / nt) + 1 - sc.v0;
+        }
+    }
+    sc.n_pieces = sc.R + n_rem;
+    return sc;
+}
+
+// Piece i of this CTA's schedule.
+DS4A_DEV Item make_piece(const AttnArgs &a, const Sched &sc, int i) {
     Item m;
-    m.unit = it / n_split;
-    m.split = it - m.unit * n_split;
+    int lt0 = 0, lt1 = sc.nt;
+    if (i < sc.R) {
+        m.unit = blockIdx.x + i * gridDim.x;
+        m.split = false;
+        m.slot = 0;
+    } else {
+        const int v = sc.v0 + (i - sc.R);
+        m.unit = sc.u_rem0 + v;
+        const long long vs = static_cast<long long>(v) * sc.nt;
+        lt0 = static_cast<int>(max(sc.rs - vs, 0LL));
+        lt1 = static_cast<int>(min(sc.re - vs, static_cast<long long>(sc.nt)));
+        m.split = lt0 > 0 || lt1 < sc.nt;
+        m.slot = 2LL * blockIdx.x + (vs <= sc.rs ? 0 : 1);   // first piece of the share: slot 0, last: slot 1
+    }
     m.ru = a.hsplit == 2 ? m.unit >> 1 : m.unit;     // 128 heads: two sub-units share the rows
     int cnt = a.count[m.ru];
-    if (m.split == 0 && (cnt < 0 || cnt > a.top_k) && threadIdx.x == 0) report(a.status, DS4A_DEV_BOUNDS);
+    if (lt0 == 0 && (cnt < 0 || cnt > a.top_k) && threadIdx.x == 0) report(a.status, DS4A_DEV_BOUNDS);
     cnt = cnt < 0 ? 0 : (cnt > a.top_k ? a.top_k : cnt);
     m.cnt = cnt;
     m.comp_row0 = static_cast<long long>(m.ru) * a.rows_per_unit;
@@ -259,10 +311,8 @@ DS4A_DEV Item make_item(const AttnArgs &a, int it, int n_split) {
         m.raw_row0 = static_cast<long long>(m.ru) * a.raw_per_unit;
     }
     m.ct = (m.cnt + TR - 1) / TR;
-    const int nt = m.ct + (m.nrw + TR - 1) / TR;
-    const int tps = (nt + n_split - 1) / n_split;
-    m.t0 = m.split * tps;
-    m.t1 = min(nt, m.t0 + tps);
+    m.t0 = lt0;
+    m.t1 = min(m.ct + (m.nrw + TR - 1) / TR, lt1);
     return m;
 }
 
@@ -279,8 +329,8 @@ DS4A_DEV void tmem_ld16x256_x8(uint32_t taddr, uint32_t (&r)[32]) {
         : "r"(taddr));
 }
 
-__global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_constant__ AttnArgs a, int n_split,
-                                                                  int n_items) {
+__global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_constant__ AttnArgs a, int nt,
+                                                                  int g_rem) {
     pdl_launch_dependents();
     pdl_wait();
     extern __shared__ uint8_t smem_raw[];
@@ -337,6 +387,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const float NEG_INF = -__int_as_float(0x7f800000);
+    const Sched sc = make_sched(a, nt, g_rem);
+    const int u_end = sc.n_pieces;               // pieces 0 .. n_pieces-1
+    const long long n_slots = 2LL * gridDim.x;
 
     if (warp >= kFirstGatherWarp) {
         // ------------------------------------------------------------ row gather
@@ -349,18 +402,18 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
         const int chunk = lane & 7, rsub = lane >> 3;
         uint32_t xeph[2] = {0, 0};
         bool ok = true;
-        auto first_tile = [&](int it, Item &m) -> int {
-            for (; it < n_items; it += gridDim.x) {
-                m = make_item(a, it, n_split);
-                if (m.t0 < m.t1) return it;
+        auto first_tile = [&](int u, Item &m) -> int {
+            for (; u < u_end; ++u) {
+                m = make_piece(a, sc, u);
+                if (m.t0 < m.t1) return u;
             }
-            return n_items;
+            return u_end;
         };
         int ordinal = 0;                                   // item ordinal within this CTA's sequence
-        auto advance = [&](int &it, int &t, Item &m) {
+        auto advance = [&](int &u, int &t, Item &m) {
             if (++t >= m.t1) {
-                it = first_tile(it + gridDim.x, m);
-                t = it < n_items ? m.t0 : 0;
+                u = first_tile(u + 1, m);
+                t = u < u_end ? m.t0 : 0;
                 ++ordinal;
             }
         };
@@ -392,12 +445,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
             return (bal & 1u) | ((bal >> 7) & 2u) | ((bal >> 14) & 4u) | ((bal >> 21) & 8u);
         };
         Item cm;
-        int cit = first_tile(blockIdx.x, cm);
-        int ct_ = cit < n_items ? cm.t0 : 0;
+        int cit = first_tile(0, cm);
+        int ct_ = cit < u_end ? cm.t0 : 0;
         uint32_t jt = 0;
         int rv[kGroupsPerWarp];
-        if (cit < n_items) fetch_rows(cm, ct_, rv);
-        while (ok && cit < n_items) {
+        if (cit < u_end) fetch_rows(cm, ct_, rv);
+        while (ok && cit < u_end) {
             if (ct_ == cm.t0 && gw == 0) {
                 // First tile of an item: q (bf16) by TMA once the previous item's
                 // logits are done.  q_free completes once per item, so item k
@@ -462,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
             const bool early_next = fp8_tile || tma_tile;
             if (early_next) {
                 advance(cit, ct_, cm);
-                if (cit < n_items) fetch_rows(cm, ct_, rv);
+                if (cit < u_end) fetch_rows(cm, ct_, rv);
             }
             const int xb = jt & 1;
             ok = __all_sync(0xffffffffu, mbar_wait(&x_empty[xb], xeph[xb] ^ 1, abort_flag));
@@ -528,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                 }
                 cp_async_commit();
                 advance(cit, ct_, cm);
-                if (cit < n_items) fetch_rows(cm, ct_, rv);
+                if (cit < u_end) fetch_rows(cm, ct_, rv);
                 cp_async_wait<0>();
             }
             fence_proxy_async();
@@ -550,8 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
         constexpr uint32_t id_s_bf = idesc_f16(false, false), id_s_f16 = idesc_f16(true, false);
         const uint64_t dq = sw128_desc(smem_u32(sQ), 16, 1024), dx0 = sw128_desc(smem_u32(sX), 16, 1024);
         uint32_t js = 0;                                     // tile counter: buffers js & 1
-        for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-            const Item m = make_item(a, it, n_split);
+        for (int i = 0; ok && i < sc.n_pieces; ++i) {
+            const Item m = make_piece(a, sc, i);
             if (m.t0 >= m.t1) continue;
             if (!(ok = warp_wait(q_full, qph, abort_flag))) break;
             qph ^= 1;
@@ -600,8 +653,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
         constexpr uint32_t id_v_bf = idesc_f16(false, true), id_v_f16 = idesc_f16(true, true);
         const uint64_t dxv = sw128_desc(smem_u32(sX), kXBlk, 1024), dp = sw128_desc(smem_u32(sP), 16, 1024);
         uint32_t jv = 0;
-        for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-            const Item m = make_item(a, it, n_split);
+        for (int i = 0; ok && i < sc.n_pieces; ++i) {
+            const Item m = make_piece(a, sc, i);
             if (m.t0 >= m.t1) continue;
             for (int t = m.t0; t < m.t1; ++t, ++jv) {
                 const int b = jv & 1;
@@ -672,19 +725,18 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
             __syncwarp();
             if (lane == 0) mbar_arrive(q16_ready);
         };
-        for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-            const Item m = make_item(a, it, n_split);
+        for (int i = 0; ok && i < sc.n_pieces; ++i) {
+            const Item m = make_piece(a, sc, i);
             if (m.t0 >= m.t1) {
                 // Empty row set: out = 0, lse = -inf (or an empty partial).
-                if (n_split == 1) {
+                if (!m.split) {
                     float *o = a.out + static_cast<long long>(m.unit) * kNHead * kHeadDim;
                     for (int k = e; k < kNHead * kHeadDim; k += kSoftmaxWarps * 32) o[k] = 0.f;
                     if (a.lse && e < kNHead) a.lse[static_cast<long long>(m.unit) * kNHead + e] = NEG_INF;
                 } else if (e < kNHead) {
-                    float *ml = static_cast<float *>(a.ws) + static_cast<long long>(a.units) * n_split * kNHead * kHeadDim;
-                    const long long slot = static_cast<long long>(m.unit) * n_split + m.split;
-                    ml[(slot * kNHead + e) * 2] = NEG_INF;
-                    ml[(slot * kNHead + e) * 2 + 1] = 0.f;
+                    float *ml = static_cast<float *>(a.ws) + n_slots * kNHead * kHeadDim;
+                    ml[(m.slot * kNHead + e) * 2] = NEG_INF;
+                    ml[(m.slot * kNHead + e) * 2 + 1] = 0.f;
                 }
                 continue;
             }
@@ -839,20 +891,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
             l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
             l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
             l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-            const long long slot = static_cast<long long>(m.unit) * n_split + m.split;
+            const long long slot = m.slot;
             if (t4 == 0) {
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
                     const int h = k ? h1 : h0;
                     const float L = k ? l1 : l0, M = k ? M1 : M0;
-                    if (n_split == 1) {
+                    if (!m.split) {
                         sInvL[h] = L > 0.f ? 1.f / L : 0.f;
                         if (a.lse)
                             a.lse[static_cast<long long>(m.unit) * kNHead + h] =
                                 L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : NEG_INF;
                     } else {
                         sInvL[h] = 1.f;
-                        float *ml = static_cast<float *>(a.ws) + static_cast<long long>(a.units) * n_split * kNHead * kHeadDim;
+                        float *ml = static_cast<float *>(a.ws) + n_slots * kNHead * kHeadDim;
                         ml[(slot * kNHead + h) * 2] = L > 0.f ? M : NEG_INF;
                         ml[(slot * kNHead + h) * 2 + 1] = L;
                     }
@@ -863,7 +915,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
             ok = __all_sync(0xffffffffu, mbar_wait(&x_empty[(jt - 1) & 1], ((jt - 1) >> 1) & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
-            float *obase = n_split == 1 ? a.out + static_cast<long long>(m.unit) * kNHead * kHeadDim
+            float *obase = !m.split ? a.out + static_cast<long long>(m.unit) * kNHead * kHeadDim
                                         : static_cast<float *>(a.ws) + slot * kNHead * kHeadDim;
             // 1/l of the 64 heads in registers: no shared load between the
             // global stores below.
@@ -899,81 +951,91 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
     }
 }
 
-// Combines the split partials of one (unit, head): O = sum_s 2^(m_s - M) O_s /
-// sum_s 2^(m_s - M) l_s, lse = (M + log2 L) ln 2.
-__global__ void __launch_bounds__(128) attn_merge_kernel(const __grid_constant__ AttnArgs a, int n_split) {
+// Combines the pieces of the remainder units that straddle a share boundary.
+// Block (v, h): head h of remainder unit v, whose tiles [v nt, (v+1) nt) of the
+// remainder tile space lie in the shares of CTAs c0 .. c1 (share c: tiles
+// [c T / g, (c+1) T / g)); a unit inside one share was written directly.
+// O = sum_k 2^(m_k - M) O_k / sum_k 2^(m_k - M) l_k, lse = (M + log2 L) ln 2.
+__global__ void __launch_bounds__(128) attn_merge_kernel(const __grid_constant__ AttnArgs a, int nt, int g_rem, int G) {
     pdl_launch_dependents();
     pdl_wait();
-    const int unit = blockIdx.x / kNHead;
-    const int h = blockIdx.x - unit * kNHead;
+    const int v = blockIdx.x / kNHead;
+    const int h = blockIdx.x - v * kNHead;
+    const long long u_rem0 = static_cast<long long>(a.units / G) * G;
+    const long long T = (a.units - u_rem0) * nt;
+    const long long vs = static_cast<long long>(v) * nt, ve = vs + nt;
+    auto share_of = [&](long long x) -> int { return static_cast<int>(((x + 1) * g_rem - 1) / T); };
+    const int c0 = share_of(vs), c1 = share_of(ve - 1);
+    if (c0 == c1) return;                                   // whole inside one share
     const float *wo = static_cast<const float *>(a.ws);
-    const float *ml = wo + static_cast<long long>(a.units) * n_split * kNHead * kHeadDim;
+    const float *ml = wo + 2LL * G * kNHead * kHeadDim;    // (m, l) after the 2 G O slots
+    // Share c0 holds the unit's start: its first piece (slot 0) when the share
+    // starts exactly there, else its last (slot 1); later shares: their first.
+    auto piece_slot = [&](int c) -> long long {
+        return c == c0 ? 2LL * c + (static_cast<long long>(c) * T / g_rem == vs ? 0 : 1) : 2LL * c;
+    };
     const float NEG_INF = -__int_as_float(0x7f800000);
     float M = NEG_INF;
-    for (int s = 0; s < n_split; ++s) {
-        const long long slot = static_cast<long long>(unit) * n_split + s;
-        const float2 v = *reinterpret_cast<const float2 *>(ml + (slot * kNHead + h) * 2);
-        if (v.y > 0.f) M = fmaxf(M, v.x);
+    for (int c = c0; c <= c1; ++c) {
+        const float2 p = *reinterpret_cast<const float2 *>(ml + (piece_slot(c) * kNHead + h) * 2);
+        if (p.y > 0.f) M = fmaxf(M, p.x);
     }
-    float wts[kMaxSplit];
     float L = 0.f;
-    for (int s = 0; s < n_split; ++s) {
-        const long long slot = static_cast<long long>(unit) * n_split + s;
-        const float2 v = *reinterpret_cast<const float2 *>(ml + (slot * kNHead + h) * 2);
-        wts[s] = v.y > 0.f ? exp2f(v.x - M) : 0.f;
-        L += wts[s] * v.y;
-    }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
     const int d = threadIdx.x * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < n_split; ++s) {
-        if (wts[s] == 0.f) continue;
-        const long long slot = static_cast<long long>(unit) * n_split + s;
-        const float4 v = *reinterpret_cast<const float4 *>(wo + (slot * kNHead + h) * kHeadDim + d);
-        acc.x += wts[s] * v.x;
-        acc.y += wts[s] * v.y;
-        acc.z += wts[s] * v.z;
-        acc.w += wts[s] * v.w;
+    for (int c = c0; c <= c1; ++c) {
+        const long long slot = piece_slot(c);
+        const float2 p = *reinterpret_cast<const float2 *>(ml + (slot * kNHead + h) * 2);
+        if (!(p.y > 0.f)) continue;
+        const float wk = exp2f(p.x - M);
+        L += wk * p.y;
+        const float4 o = *reinterpret_cast<const float4 *>(wo + (slot * kNHead + h) * kHeadDim + d);
+        acc.x += wk * o.x;
+        acc.y += wk * o.y;
+        acc.z += wk * o.z;
+        acc.w += wk * o.w;
     }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
     acc.x *= inv;
     acc.y *= inv;
     acc.z *= inv;
     acc.w *= inv;
-    *reinterpret_cast<float4 *>(a.out + (static_cast<long long>(unit) * kNHead + h) * kHeadDim + d) = acc;
+    const long long u = u_rem0 + v;
+    *reinterpret_cast<float4 *>(a.out + (u * kNHead + h) * kHeadDim + d) = acc;
     if (a.lse && threadIdx.x == 0)
-        a.lse[static_cast<long long>(unit) * kNHead + h] =
-            L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : NEG_INF;
+        a.lse[u * kNHead + h] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : NEG_INF;
 }
+
+// Tiles per unit in the tile space: the top_k compressed rows and the raw window.
+int attn_tiles_per_unit(int top_k) { return (top_k + TR - 1) / TR + (kNSwa + TR - 1) / TR; }
 
 }  // namespace
 
-int attn_num_splits(int units, int top_k) {
-    // Enough work items to cover 152 SMs; a split holds at least one 64-row tile.
-    const int max_tiles = (top_k + TR - 1) / TR + (kNSwa + TR - 1) / TR;
-    if (units >= 152) return 1;
-    int s = (152 + units - 1) / units;
-    if (s > max_tiles) s = max_tiles;
-    if (s > kMaxSplit) s = kMaxSplit;
-    return s < 1 ? 1 : s;
-}
-
 size_t attn_ws_bytes(int units, int top_k) {
-    const int s = attn_num_splits(units, top_k);
-    if (s == 1) return 0;
-    return static_cast<size_t>(units) * s * kNHead * (kHeadDim + 2) * sizeof(float);
+    // Two partial slots per CTA; the grid never exceeds kMaxAttnCtas.
+    const long long T = static_cast<long long>(units) * attn_tiles_per_unit(top_k);
+    const long long G = T < kMaxAttnCtas ? T : kMaxAttnCtas;
+    if (G <= 1) return 0;                                   // one CTA: every unit whole
+    return static_cast<size_t>(2 * G) * kNHead * (kHeadDim + 2) * sizeof(float);
 }
 
 cudaError_t launch_sparse_attn(const AttnArgs &a, int num_sms, cudaStream_t s) {
-    const int n_split = attn_num_splits(a.units, a.top_k);
     cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    const long long items = static_cast<long long>(a.units) * n_split;
-    if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
-    const int grid = static_cast<int>(items < num_sms ? items : num_sms);
-    e = launch_k(sparse_attn_kernel, dim3(grid), dim3(kThreads), kSmemBytes, s, a, n_split, static_cast<int>(items));
-    if (e != cudaSuccess || n_split == 1) return e;
-    return launch_k(attn_merge_kernel, dim3(static_cast<unsigned>(static_cast<long long>(a.units) * kNHead)), dim3(128), 0,
-                    s, a, n_split);
+    const int nt = attn_tiles_per_unit(a.top_k);
+    const long long T = static_cast<long long>(a.units) * nt;
+    if (T <= 0) return cudaSuccess;
+    long long G = num_sms < kMaxAttnCtas ? num_sms : kMaxAttnCtas;
+    if (T < G) G = T;
+    // Remainder units (after the whole rounds) in one-tile-or-larger shares
+    // over up to G CTAs.
+    const long long u_rem = a.units - (a.units / G) * G;
+    const long long t_rem = u_rem * nt;
+    const int g_rem = static_cast<int>(t_rem < G ? t_rem : G);
+    e = launch_k(sparse_attn_kernel, dim3(static_cast<unsigned>(G)), dim3(kThreads), kSmemBytes, s, a, nt, g_rem);
+    if (e != cudaSuccess || g_rem <= 1) return e;
+    return launch_k(attn_merge_kernel, dim3(static_cast<unsigned>(u_rem * kNHead)), dim3(128), 0, s, a, nt, g_rem,
+                    static_cast<int>(G));
 }
 
 }  // namespace ds4a

@@ -242,8 +242,10 @@ ds4a_status ds4a_topk_select_noalloc(const float *scores, const int32_t *n_rows,
  *    n_raw   int32 [U], 0..128 (device).
  *    out     fp32 [U][64][512] (device).   lse   fp32 [U][64] or NULL (device).
  *    ws      workspace of ds4a_workspace_bytes(DS4A_OP_SPARSE_ATTN_DECODE, U, 1,
- *            N_cap, top_k) bytes (used when units are few and each unit's row
- *            set is split over several CTAs).
+ *            N_cap, top_k) bytes: the work is cut into equal per-SM shares of
+ *            64-row tiles, and a unit cut by a share boundary is computed in
+ *            pieces whose partials (at most two per SM, 131,584 bytes each)
+ *            are combined afterwards.  0 only when everything fits one share.
  *    q, rows and raw must be 16-byte aligned; with U > 1 the unit strides must
  *    be whole rows (multiples of 512 elements), at least N_cap resp. 128 rows
  *    (each buffer is addressed as one array of 512-element rows).

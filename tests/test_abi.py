@@ -52,10 +52,14 @@ def test_workspace_sizes():
     t1 = B.ds4a_workspace_bytes(B.DS4A_OP_TOPK_SELECT, 8, 1, 16384, 512)
     t2 = B.ds4a_workspace_bytes(B.DS4A_OP_TOPK_SELECT, 16, 1, 16384, 512)
     assert 0 < t1 < t2
-    # Many units: no split, no attention workspace; few units: split partials.
-    assert B.ds4a_workspace_bytes(B.DS4A_OP_SPARSE_ATTN_DECODE, 1376, 1, 65536, 512) == 0
-    assert B.ds4a_workspace_bytes(B.DS4A_OP_SPARSE_ATTN_DECODE, 4, 1, 262144, 512) > 0
-    assert B.ds4a_workspace_bytes(B.DS4A_OP_SPARSE_ATTN_PREFILL, 1, 2048, 66048, 512) == 0
+    # Attention: two partial slots (64 x (512 + 2) fp32) per share, at most
+    # 160 shares, at most one share per 64-row tile (10 tiles per unit at k = 512).
+    slot = 64 * 514 * 4
+    assert B.ds4a_workspace_bytes(B.DS4A_OP_SPARSE_ATTN_DECODE, 1376, 1, 65536, 512) == 2 * 160 * slot
+    assert B.ds4a_workspace_bytes(B.DS4A_OP_SPARSE_ATTN_DECODE, 4, 1, 262144, 512) == 2 * 40 * slot
+    assert B.ds4a_workspace_bytes(B.DS4A_OP_SPARSE_ATTN_PREFILL, 1, 2048, 66048, 512) == 2 * 160 * slot
+    assert B.ds4a_workspace_bytes(B.DS4A_OP_DENSE_ATTN_DECODE, 1, 1, 64, 0) == 2 * 3 * slot    # 1 + 2 tiles
+    assert B.ds4a_workspace_bytes(B.DS4A_OP_DENSE_ATTN_DECODE | B.DS4A_OP_FLAG_128_HEADS, 3, 1, 8192, 0) == 2 * 160 * slot
     with pytest.raises(ValueError):
         B.ds4a_workspace_bytes(B.DS4A_OP_TOPK_SELECT, 1, 1, 10, 4096)
     with pytest.raises(ValueError):

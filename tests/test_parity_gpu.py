@@ -314,6 +314,14 @@ def test_attention_one_cta_per_unit(q_scale):
     attention_case(160, 700, 512, seed=12, q_scale=q_scale)
 
 
+@pytest.mark.parametrize("U,top_k", [(152, 512), (305, 512), (457, 64), (9, 64)])
+def test_attention_work_schedule(U, top_k):
+    # Whole strided rounds of 152 units, then the remainder units' tiles cut
+    # into equal shares: no remainder, one remainder unit over ten CTAs, three-
+    # tile units, and fewer units than CTAs (every unit in one-tile pieces).
+    attention_case(U, 600, top_k, seed=40 + U)
+
+
 def test_attention_raw_window_extremes_and_odd_k():
     attention_case(4, 300, 100, seed=13, n_raw=[0, 1, 127, 128])
 
@@ -342,8 +350,10 @@ def test_attention_out_of_range_index_is_masked_and_flagged():
     bad[1, 0] = -3
     out = torch.empty(U, 64, 512, device="cuda")
     cnt = torch.full((U,), 64, dtype=torch.int32, device="cuda")
+    ws = torch.empty(max(B.ds4a_workspace_bytes(B.DS4A_OP_SPARSE_ATTN_DECODE, U, 1, N_cap, 64), 1),
+                     dtype=torch.uint8, device="cuda")
     B.ds4a_sparse_attn_decode(x["q"], x["rows"], torch.from_numpy(bad).cuda(), cnt, x["raw"], x["n_raw"], SCALE,
-                              out, None, None)
+                              out, None, ws)
     st, flags = B.ds4a_get_device_status()
     assert st == B.DS4A_EDEVICE and flags & B.DS4A_DEV_BOUNDS
     for u, keep in [(0, np.delete(idx[0], 3)), (1, idx[1, 1:]), (2, idx[2])]:
@@ -523,8 +533,10 @@ def test_sparse_count_out_of_range_is_clamped_and_flagged():
     cnt = torch.full((U,), k, dtype=torch.int32, device="cuda")
     cnt[0] = k + 9
     out = torch.empty(U, 64, 512, device="cuda")
+    ws = torch.empty(max(B.ds4a_workspace_bytes(B.DS4A_OP_SPARSE_ATTN_DECODE, U, 1, N_cap, k), 1),
+                     dtype=torch.uint8, device="cuda")
     B.ds4a_sparse_attn_decode(x["q"], x["rows"], torch.from_numpy(idx).cuda(), cnt, x["raw"], x["n_raw"], SCALE,
-                              out, None, None)
+                              out, None, ws)
     st, flags = B.ds4a_get_device_status()
     assert st == B.DS4A_EDEVICE and flags & B.DS4A_DEV_BOUNDS
     ro, _ = oracle.sparse_attention(u16(x["q"][0]), u16(x["rows"][0]), idx[0], u16(x["raw"][0]), np.arange(3), SCALE)
