@@ -246,7 +246,7 @@ ds4a_status ds4a_topk_select_noalloc(const float *scores, const int32_t *n_rows,
  *            64-row tiles, and a unit cut by a share boundary is computed in
  *            pieces whose partials (at most two per SM, 131,584 bytes each)
  *            are combined afterwards.  0 only when everything fits one share.
- *    q, rows and raw must be 16-byte aligned; with U > 1 the unit strides must
+ *    q, rows, raw and out must be 16-byte aligned; with U > 1 the unit strides must
  *    be whole rows (multiples of 512 elements), at least N_cap resp. 128 rows
  *    (each buffer is addressed as one array of 512-element rows).
  */
