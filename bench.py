@@ -587,7 +587,7 @@ def main():
         step_bytes = dense_bytes(wl)
         achieved = step_bytes / (idx_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
-                "frac": achieved / pk["hbm"], "traffic": None, "kernel": "sparse_attn_kernel",
+                "frac": achieved / pk["hbm"], "traffic": dram_traffic("sparse_attn_kernel", wl.units, wl.n_rows), "kernel": "sparse_attn_kernel",
                 "algorithmic_bytes_per_launch": step_bytes, "launch_ms": idx_ms}
         cfg["step_algorithmic_bytes"] = step_bytes
         cfg["step_hbm_GBps"] = step_bytes / (ms / 1e3) / 1e9
