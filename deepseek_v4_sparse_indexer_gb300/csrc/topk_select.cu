@@ -489,7 +489,8 @@ __global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float *
 // For batches with at least as many rows as SMs (decode batches, prefill
 // chunks): each CTA selects one row's top-k alone and reads the row's scores
 // once from HBM in the common case.
-//   1. A systematic sample of kSample scores (row positions i*n/kSample) sets
+//   1. A sample of kSample scores (64 whole 128-byte lines spread evenly over
+//      the row, so that the sample costs whole lines, not scattered sectors) sets
 //      a threshold key T0: the r-th largest visible sample key with
 //      r = 3k*kSample/n, resolved to 24 bits (two 4096-bin digits over the
 //      sample), so that about 3k rows of the row lie at or above it.
@@ -504,13 +505,22 @@ __global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float *
 //      row and a prefix sum of its popcounts; a bitonic sort for rows longer
 //      than 131,072), -1 padded; the fallback compacts the row in order.
 
-constexpr int kRowThreads = 512;
+// Two shapes: 512 threads, 8,192 candidates, two CTAs per SM (any k, any
+// length); and for k <= kRowSmallMaxK and rows up to kRowSmallMaxN, 256
+// threads, 4,096 candidates and a 1,024-entry sort buffer, four CTAs per SM:
+// the phases of a short row are latency-bound, so twice the rows in flight
+// beat twice the threads per row (2,048 x 16,896: 140 vs 169 us).
 constexpr int kSample = 2048;
 constexpr int kSampleOver = 3;     // expected candidates / k
-constexpr int kRowCandCap = 8192;
-constexpr int kRowSmemBytes = kRowCandCap * 8 + kBins * 4 + kMaxTopK * 4;   // candidates, histogram, chosen
+constexpr int kRowSmallMaxK = 640;
+constexpr int kRowSmallMaxN = 32768;   // longer rows: fewer, wider CTAs (the pass dominates)
+template <int NT, int CAP, int SEL>
+struct RowShape {
+    static constexpr int kSmem = CAP * 8 + kBins * 4 + SEL * 4;   // candidates, histogram, chosen
+};
 
-__global__ void __launch_bounds__(kRowThreads, 2) topk_row_kernel(const float *__restrict__ scores,
+template <int NT, int CAP, int SEL>
+__global__ void __launch_bounds__(NT, NT == 512 ? 2 : 4) topk_row_kernel(const float *__restrict__ scores,
                                                                   const int32_t *__restrict__ n_rows, int Q,
                                                                   int N_cap, int top_k,
                                                                   int32_t *__restrict__ idx_out,
@@ -518,10 +528,10 @@ __global__ void __launch_bounds__(kRowThreads, 2) topk_row_kernel(const float *_
     pdl_launch_dependents();
     pdl_wait();
     extern __shared__ __align__(16) uint8_t row_smem[];
-    uint2 *cand = reinterpret_cast<uint2 *>(row_smem);                               // [kRowCandCap]
-    uint32_t *h = reinterpret_cast<uint32_t *>(row_smem + kRowCandCap * 8);           // [kBins]
-    int32_t *sel = reinterpret_cast<int32_t *>(row_smem + kRowCandCap * 8 + kBins * 4);   // [kMaxTopK]
-    __shared__ uint32_t scratch[kRowThreads + 4];
+    uint2 *cand = reinterpret_cast<uint2 *>(row_smem);                               // [CAP]
+    uint32_t *h = reinterpret_cast<uint32_t *>(row_smem + CAP * 8);           // [kBins]
+    int32_t *sel = reinterpret_cast<int32_t *>(row_smem + CAP * 8 + kBins * 4);   // [SEL]
+    __shared__ uint32_t scratch[NT + 4];
     __shared__ uint32_t n_cand, n_sel;
     __shared__ uint32_t warp_sums[32];
     const long long row = blockIdx.x;
@@ -539,13 +549,17 @@ __global__ void __launch_bounds__(kRowThreads, 2) topk_row_kernel(const float *_
     };
     // ---- 1. threshold estimate
     uint32_t T0 = 0;
-    if (n > kRowCandCap) {
-        uint32_t skey[kSample / kRowThreads];
-        bool svis[kSample / kRowThreads];
+    if (n > CAP) {
+        uint32_t skey[kSample / NT];
+        bool svis[kSample / NT];
         clear_hist();
 #pragma unroll
-        for (int j = 0; j < kSample / kRowThreads; ++j) {
-            const int i = static_cast<int>((static_cast<long long>(threadIdx.x + j * kRowThreads) * n) / kSample);
+        for (int j = 0; j < kSample / NT; ++j) {
+            // sample sj: score (sj & 31) of one of 64 whole 128-byte lines spread
+            // evenly over the row (a warp loads one line: no scattered sectors)
+            const int sj = static_cast<int>(threadIdx.x) + j * NT;
+            const int line = static_cast<int>((static_cast<long long>(sj >> 5) * (n / 32 - 1)) / (kSample / 32 - 1));
+            const int i = line * 32 + (sj & 31);
             const float f = __ldg(s + i);
             svis[j] = score_visible(f);
             skey[j] = float_key(f);
@@ -555,15 +569,15 @@ __global__ void __launch_bounds__(kRowThreads, 2) topk_row_kernel(const float *_
         const long long r_want = (static_cast<long long>(kSampleOver) * k * kSample + n - 1) / n;
         const uint32_t rank = static_cast<uint32_t>(r_want < kSample ? r_want : kSample);
         uint32_t above, total;
-        const int sb1 = find_threshold_bin<kRowThreads>(h, kBins, rank, &above, &total, scratch);
+        const int sb1 = find_threshold_bin<NT>(h, kBins, rank, &above, &total, scratch);
         if (sb1 >= 0) {
             clear_hist();
 #pragma unroll
-            for (int j = 0; j < kSample / kRowThreads; ++j)
+            for (int j = 0; j < kSample / NT; ++j)
                 hist_add_warp(h, (skey[j] >> 8) & 0xFFFu, svis[j] && static_cast<int>(skey[j] >> 20) == sb1);
             __syncthreads();
             uint32_t above2, total2;
-            int sb2 = find_threshold_bin<kRowThreads>(h, kBins, rank - above, &above2, &total2, scratch);
+            int sb2 = find_threshold_bin<NT>(h, kBins, rank - above, &above2, &total2, scratch);
             if (sb2 < 0) sb2 = 0;
             T0 = (static_cast<uint32_t>(sb1) << 20) | (static_cast<uint32_t>(sb2) << 8);
         }
@@ -580,7 +594,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) topk_row_kernel(const float *_
             if (lane == 0) base = atomicAdd(&n_cand, static_cast<uint32_t>(__popc(bal)));
             base = __shfl_sync(0xffffffffu, base, 0);
             const uint32_t p = base + __popc(bal & ((1u << lane) - 1u));
-            if (take && p < static_cast<uint32_t>(kRowCandCap)) cand[p] = make_uint2(key, static_cast<uint32_t>(i));
+            if (take && p < static_cast<uint32_t>(CAP)) cand[p] = make_uint2(key, static_cast<uint32_t>(i));
         }
     };
     if ((N_cap & 3) == 0) {
@@ -591,17 +605,17 @@ __global__ void __launch_bounds__(kRowThreads, 2) topk_row_kernel(const float *_
         auto load = [&](float4 (&v)[B], int g0) {
 #pragma unroll
             for (int j = 0; j < B; ++j) {
-                const int g = g0 + j * kRowThreads + static_cast<int>(threadIdx.x);
+                const int g = g0 + j * NT + static_cast<int>(threadIdx.x);
                 v[j] = g < ngroups ? __ldg(reinterpret_cast<const float4 *>(s) + g) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         };
         float4 cur[B], nxt[B];
         load(cur, 0);
-        for (int g0 = 0; g0 < ngroups; g0 += B * kRowThreads) {
-            if (g0 + B * kRowThreads < ngroups) load(nxt, g0 + B * kRowThreads);
+        for (int g0 = 0; g0 < ngroups; g0 += B * NT) {
+            if (g0 + B * NT < ngroups) load(nxt, g0 + B * NT);
 #pragma unroll
             for (int j = 0; j < B; ++j) {
-                const int i = 4 * (g0 + j * kRowThreads + static_cast<int>(threadIdx.x));
+                const int i = 4 * (g0 + j * NT + static_cast<int>(threadIdx.x));
                 const float f[4] = {cur[j].x, cur[j].y, cur[j].z, cur[j].w};
                 uint32_t key[4];
                 bool take[4];
@@ -629,7 +643,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) topk_row_kernel(const float *_
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const uint32_t p = pos + __popc(bal[c] & lt);
-                        if (take[c] && p < static_cast<uint32_t>(kRowCandCap)) cand[p] = make_uint2(key[c], static_cast<uint32_t>(i + c));
+                        if (take[c] && p < static_cast<uint32_t>(CAP)) cand[p] = make_uint2(key[c], static_cast<uint32_t>(i + c));
                         pos += __popc(bal[c]);
                     }
                 }
@@ -638,7 +652,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) topk_row_kernel(const float *_
             for (int j = 0; j < B; ++j) cur[j] = nxt[j];
         }
     } else {
-        for (int b = 0; b < n; b += kRowThreads) {
+        for (int b = 0; b < n; b += NT) {
             const int i = b + static_cast<int>(threadIdx.x);
             const float f = i < n ? s[i] : 0.f;
             const bool vis = i < n && score_visible(f);
@@ -656,7 +670,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) topk_row_kernel(const float *_
         if (lane == 0) warp_sums[threadIdx.x >> 5] = v;
         __syncthreads();
         total = 0;
-        for (int w = 0; w < kRowThreads / 32; ++w) total += warp_sums[w];
+        for (int w = 0; w < NT / 32; ++w) total += warp_sums[w];
         __syncthreads();
     }
     const uint32_t nc = n_cand;
@@ -665,7 +679,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) topk_row_kernel(const float *_
     // ---- 3. the exact k-th key T and how many keys equal to T to take
     uint32_t T = 0, need_eq = 0;
     const bool all_visible = total <= k;
-    const bool from_cand = all_visible ? nc == total : (nc >= k && nc <= static_cast<uint32_t>(kRowCandCap));
+    const bool from_cand = all_visible ? nc == total : (nc >= k && nc <= static_cast<uint32_t>(CAP));
     if (!all_visible) {
         // digit d: bits [lo, lo + w) of keys whose higher bits equal prefix
         uint32_t need = k;
@@ -692,7 +706,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) topk_row_kernel(const float *_
             }
             __syncthreads();
             uint32_t gt, tot;
-            int b = find_threshold_bin<kRowThreads>(h, kBins, need, &gt, &tot, scratch);
+            int b = find_threshold_bin<NT>(h, kBins, need, &gt, &tot, scratch);
             if (b < 0) { b = 0; gt = 0; }     // cannot happen: need <= count of keys with this prefix
             prefix = (d == 0 ? 0u : prefix << (d == 1 ? 12 : 8)) | static_cast<uint32_t>(b);
             need -= gt;
@@ -715,7 +729,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) topk_row_kernel(const float *_
             if (lane == 0) warp_sums[threadIdx.x >> 5] = v;
             __syncthreads();
             n_eq = 0;
-            for (int w = 0; w < kRowThreads / 32; ++w) n_eq += warp_sums[w];
+            for (int w = 0; w < NT / 32; ++w) n_eq += warp_sums[w];
         }
         if (use_bitmap)
             for (int i = threadIdx.x; i < kBins; i += blockDim.x) h[i] = 0;
@@ -754,7 +768,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) topk_row_kernel(const float *_
         __syncthreads();
         if (use_bitmap) {
             // thread t owns words 8t..8t+7 (rows 256t..256t+255)
-            constexpr int kWords = kBins / kRowThreads;
+            constexpr int kWords = kBins / NT;
             uint32_t wv[kWords], cnt = 0;
 #pragma unroll
             for (int j = 0; j < kWords; ++j) {
@@ -771,7 +785,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) topk_row_kernel(const float *_
             if (lane == 31) warp_sums[threadIdx.x >> 5] = incl;
             __syncthreads();
             uint32_t before = 0, ns = 0;
-            for (int w = 0; w < kRowThreads / 32; ++w) {
+            for (int w = 0; w < NT / 32; ++w) {
                 const uint32_t v = warp_sums[w];
                 if (w < static_cast<int>(threadIdx.x >> 5)) before += v;
                 ns += v;
@@ -987,10 +1001,15 @@ cudaError_t launch_topk(const TopkArgs &a, int num_sms, cudaStream_t s) {
         // (a single launch beats three on small batches): one CTA per row, no
         // workspace.
         if (R > 0x7fffffffLL) return cudaErrorInvalidValue;
-        cudaError_t e = cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowSmemBytes);
-        if (e != cudaSuccess) return e;
-        return launch_k(topk_row_kernel, dim3(static_cast<unsigned>(R)), dim3(kRowThreads), kRowSmemBytes, s, a.scores,
-                        a.n_rows, a.Q, a.N_cap, a.top_k, a.idx, a.count, a.status);
+        auto go = [&](auto kern, int nt, int smem) -> cudaError_t {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return e;
+            return launch_k(kern, dim3(static_cast<unsigned>(R)), dim3(nt), smem, s, a.scores, a.n_rows, a.Q, a.N_cap,
+                            a.top_k, a.idx, a.count, a.status);
+        };
+        if (a.top_k <= kRowSmallMaxK && a.N_cap <= kRowSmallMaxN)
+            return go(topk_row_kernel<256, 4096, 1024>, 256, RowShape<256, 4096, 1024>::kSmem);
+        return go(topk_row_kernel<512, 8192, kMaxTopK>, 512, RowShape<512, 8192, kMaxTopK>::kSmem);
     }
     TopkWs ws = topk_ws(a.ws, R, a.top_k);
     // Zero the histograms and counters (contiguous at the front).
