@@ -217,6 +217,11 @@ DS4A_DEV bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
     return __all_sync(0xffffffffu, mbar_wait_hint(bar, parity, abort));
 }
 
+// Bulk prefetch of [p, p + bytes) into L2 (16-byte aligned, multiple of 16 bytes).
+DS4A_DEV void prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 DS4A_DEV bool wait_drain(uint64_t *bar, uint32_t parity) {
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity))
@@ -441,6 +446,17 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
             if (t < m.ct) return (v < 0 || v >= a.N_cap) ? -1 : static_cast<int>(m.comp_row0 + v);
             return v < 0 ? -1 : static_cast<int>(m.raw_row0 + v);
         };
+        // Dense row lists: the next whole tile of compressed rows goes into L2
+        // ahead with one bulk prefetch, so that its TMA copy, issued once its
+        // buffer is free, reads L2 (dense attention 1.10 -> 1.03 ms).  Gathered
+        // tiles are not prefetched: per-row prefetches slow the gathers down,
+        // and so did prefetching the raw-window tiles of a gathered unit.
+        auto prefetch_next = [&](int u, int t, const Item &m) {
+            if (u >= u_end || a.idx || a.rows8 || t >= m.ct) return;
+            const int nfirst = t * TR;
+            if (a.tma_rows && nfirst + TR <= m.cnt && gw == 0 && lane == 0)
+                prefetch_l2(a.rows + (m.comp_row0 + nfirst) * kHeadDim, TR * kHeadDim * 2);
+        };
         auto nibble = [](uint32_t bal) -> uint32_t {   // lanes 0, 8, 16, 24 -> bits 0..3
             return (bal & 1u) | ((bal >> 7) & 2u) | ((bal >> 14) & 4u) | ((bal >> 21) & 8u);
         };
@@ -516,6 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
             if (early_next) {
                 advance(cit, ct_, cm);
                 if (cit < u_end) fetch_rows(cm, ct_, rv);
+                prefetch_next(cit, ct_, cm);
             }
             const int xb = jt & 1;
             ok = __all_sync(0xffffffffu, mbar_wait(&x_empty[xb], xeph[xb] ^ 1, abort_flag));
@@ -582,6 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                 cp_async_commit();
                 advance(cit, ct_, cm);
                 if (cit < u_end) fetch_rows(cm, ct_, rv);
+                prefetch_next(cit, ct_, cm);
                 cp_async_wait<0>();
             }
             fence_proxy_async();
