@@ -48,13 +48,17 @@ __global__ void __launch_bounds__(kPushThreads) kv_push_raw_kernel(const float *
     if (threadIdx.x == 0) n_raw[u] = p + 1 < kNSwa ? p + 1 : kNSwa;
 }
 
-// One thread pools 4 consecutive columns of one unit in a single pass over
-// the frontier, eight rows of loads in flight at a time: the running column
-// max is raised per group of eight rows (the sums so far are rescaled by
-// e^(old max - new max)), then the group's weights e^(s - max) are added.  A
-// column with no finite score gives 0.
+// Four threads pool 4 consecutive columns of one unit: thread q of the four
+// takes the frontier rows r = q (mod 4), eight rows of loads in flight at a
+// time; the running column max is raised per group of eight rows (the sums so
+// far are rescaled by e^(old max - new max)), then the group's weights
+// e^(s - max) are added.  The four partial (max, sum of weights, weighted sum)
+// are combined by two shuffles.  A column with no finite score gives 0.
+// Lane l of a warp: row quarter l / 8, column group 8 * (warp index) + l % 8,
+// so a warp load covers four 128-byte row segments.
 constexpr int kPoolThreads = 64;
 constexpr int kPoolGroup = 8;
+constexpr int kPoolSplit = 4;
 
 __global__ void __launch_bounds__(kPoolThreads) compressor_pool_kernel(const float *__restrict__ kv,
                                                                        const float *__restrict__ score, int ratio,
@@ -62,23 +66,25 @@ __global__ void __launch_bounds__(kPoolThreads) compressor_pool_kernel(const flo
     pdl_launch_dependents();
     pdl_wait();
     const int w4 = width >> 2;
-    const long long t = static_cast<long long>(blockIdx.x) * kPoolThreads + threadIdx.x;
-    if (t >= static_cast<long long>(U) * w4) return;
-    const long long u = t / w4;
-    const int c = static_cast<int>(t - u * w4);
+    const int lane = threadIdx.x & 31, q = lane >> 3;
+    const long long warp_g = (static_cast<long long>(blockIdx.x) * kPoolThreads + threadIdx.x) >> 5;
+    const long long g = warp_g * 8 + (lane & 7);                  // column group over all units
+    const bool live = g < static_cast<long long>(U) * w4;
+    const long long u = live ? g / w4 : 0;
+    const int c = live ? static_cast<int>(g - u * w4) : 0;
     const float4 *s4 = reinterpret_cast<const float4 *>(score + u * ratio * width) + c;
     const float4 *k4 = reinterpret_cast<const float4 *>(kv + u * ratio * width) + c;
     const float NEG_INF = -__int_as_float(0x7f800000);
     float m[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
     float num[4] = {0.f, 0.f, 0.f, 0.f}, den[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int r0 = 0; r0 < ratio; r0 += kPoolGroup) {
-        const int n = ratio - r0 < kPoolGroup ? ratio - r0 : kPoolGroup;
+    for (int r0 = q; live && r0 < ratio; r0 += kPoolSplit * kPoolGroup) {
         float4 s[kPoolGroup], k[kPoolGroup];
 #pragma unroll
         for (int i = 0; i < kPoolGroup; ++i) {
-            if (i < n) {
-                s[i] = __ldg(s4 + static_cast<long long>(r0 + i) * w4);
-                k[i] = __ldg(k4 + static_cast<long long>(r0 + i) * w4);
+            const int r = r0 + kPoolSplit * i;
+            if (r < ratio) {
+                s[i] = __ldg(s4 + static_cast<long long>(r) * w4);
+                k[i] = __ldg(k4 + static_cast<long long>(r) * w4);
             } else {
                 s[i] = make_float4(NEG_INF, NEG_INF, NEG_INF, NEG_INF);
                 k[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -111,6 +117,25 @@ __global__ void __launch_bounds__(kPoolThreads) compressor_pool_kernel(const flo
             }
         }
     }
+    // combine the four row quarters (lanes l, l ^ 8, l ^ 16, l ^ 24)
+#pragma unroll
+    for (int off = 8; off <= 16; off <<= 1) {
+#pragma unroll
+        for (int col = 0; col < 4; ++col) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m[col], off);
+            const float n2 = __shfl_xor_sync(0xffffffffu, num[col], off);
+            const float d2 = __shfl_xor_sync(0xffffffffu, den[col], off);
+            const float M = fmaxf(m[col], m2);
+            if (M > NEG_INF) {
+                const float a = m[col] > NEG_INF ? expf(m[col] - M) : 0.f;
+                const float b = m2 > NEG_INF ? expf(m2 - M) : 0.f;
+                num[col] = num[col] * a + n2 * b;
+                den[col] = den[col] * a + d2 * b;
+                m[col] = M;
+            }
+        }
+    }
+    if (!live || q != 0) return;
     float4 o;
     o.x = den[0] > 0.f ? num[0] / den[0] : 0.f;
     o.y = den[1] > 0.f ? num[1] / den[1] : 0.f;
@@ -189,8 +214,9 @@ cudaError_t launch_kv_push_raw(const float *kv, uint16_t *raw, long long raw_uni
 
 cudaError_t launch_compressor_pool(const float *kv, const float *score, int ratio, int width, float *out, int U,
                                    cudaStream_t s) {
-    const long long threads = static_cast<long long>(U) * (width >> 2);
-    const long long blocks = (threads + kPoolThreads - 1) / kPoolThreads;
+    // a warp covers 8 column groups (4 threads each)
+    const long long warps = (static_cast<long long>(U) * (width >> 2) + 7) / 8;
+    const long long blocks = (warps * 32 + kPoolThreads - 1) / kPoolThreads;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     return launch_k(compressor_pool_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kPoolThreads), 0, s, kv, score, ratio,
                     width, out, U);
