@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
             mbar_init(&p_full[b], kSoftmaxWarps);
         }
         mbar_init(q_full, 1);
-        mbar_init(q_free, 1);
+        mbar_init(q_free, 1 + kSoftmaxWarps);  // the item's last logits GEMM + each softmax warp past its q wait
         mbar_init(q16_ready, kSoftmaxWarps);
         mbar_init(o_free, kSoftmaxWarps);
         mbar_init(drain, 1);
@@ -469,8 +469,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
         while (ok && cit < u_end) {
             if (ct_ == cm.t0 && gw == 0) {
                 // First tile of an item: q (bf16) by TMA once the previous item's
-                // logits are done.  q_free completes once per item, so item k
-                // waits for phase k-1.
+                // logits are done and every softmax warp has passed its q wait.
+                // q_free completes once per item, so item k waits for phase k-1.
                 if (ordinal > 0) {
                     ok = __all_sync(0xffffffffu, mbar_wait(q_free, (ordinal - 1) & 1, abort_flag));
                     if (!ok) break;
@@ -767,6 +767,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                 convert_q();
                 q16 = true;
             }
+            // The next item's q may overwrite this one only after every softmax
+            // warp has seen this one land: q_full must never run two phases
+            // ahead of a warp's wait (its parity could not tell them apart),
+            // which one-tile items allowed when q_free counted only the logits
+            // GEMMs.
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_free);
             for (int t = m.t0; ok && t < m.t1; ++t, ++jt) {
                 const bool raw = t >= m.ct;
                 const int b = jt & 1;
