@@ -350,8 +350,38 @@ def host_cores():
 # ----------------------------------------------------------------------------
 # Reference arm: the oracle on host cores
 # ----------------------------------------------------------------------------
+# ---------------- multi-process plumbing (one process per GPU, replicas)
+
+def rank_env(environ=None):
+    """(rank, world_size, local_rank) as torchrun exports them; one process by default."""
+    env = os.environ if environ is None else environ
+    return int(env.get("RANK", "0")), int(env.get("WORLD_SIZE", "1")), int(env.get("LOCAL_RANK", "0"))
+
+
+def rank_seed(base_seed, rank):
+    """Each rank's replica of the workload draws its own inputs."""
+    return base_seed + rank
+
+
+def max_over_ranks(values, world, device):
+    """Element-wise max over the ranks (all-reduce MAX) of a list of floats:
+    the job takes as long as its slowest rank.  The identity in one process."""
+    if world == 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def job_value(units_per_rank, world, ms):
+    """Whole-job throughput: every rank processes its own units (weak scaling)."""
+    return world * units_per_rank / (ms / 1e3)
+
+
 def run_reference(args, wl):
-    rank = int(os.environ.get("RANK", "0"))
+    rank, _, _ = rank_env()
     if rank != 0:
         return 0
     metric, unit = metric_unit(wl)
@@ -409,9 +439,7 @@ def main():
                                                             make_pool_inputs, make_prefill_inputs,
                                                             prefill_rows_fp32_chunks)
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rank, world, local = rank_env()
     if world > 1:
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
@@ -423,7 +451,7 @@ def main():
         if world > 1:
             dist.barrier()
 
-    seed = wl.seed + rank
+    seed = rank_seed(wl.seed, rank)
     # auto: the fused select where its candidate kernel (one CTA per row) fills
     # the GPU (decode with as many rows as SMs); the two kernels otherwise.
     n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -517,12 +545,9 @@ def main():
     barrier()
     ms = t0.elapsed_time(t1) / K
     idx_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(sc_s, sc_e))
-    if world > 1:
-        t = torch.tensor([ms, idx_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, idx_ms = float(t[0]), float(t[1])
+    ms, idx_ms = max_over_ranks([ms, idx_ms], world, dev)
     units = wl.query_units
-    value = world * units / (ms / 1e3)
+    value = job_value(units, world, ms)
 
     # ---------------- end to end through the public API with host buffers
     # Every step copies its inputs from pinned host memory and its results back.
@@ -580,11 +605,8 @@ def main():
     if not torch.equal(host_out[last].to(dev), steps[last].out):
         raise SystemExit("end-to-end check: the copied-out result differs from the device result")
     e2e_ms = e0.elapsed_time(e1) / K
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t[0])
-    e2e_value = world * units / (e2e_ms / 1e3)
+    e2e_ms, = max_over_ranks([e2e_ms], world, dev)
+    e2e_value = job_value(units, world, e2e_ms)
     st, flags = pkg.ds4a_get_device_status()
     if st != 0:
         raise SystemExit(f"device status flags {flags} after the timed region")
