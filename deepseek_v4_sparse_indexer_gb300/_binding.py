@@ -34,7 +34,7 @@ N_HEAD, HEAD_DIM, N_IDX_HEAD, IDX_DIM, N_SWA = 64, 512, 64, 128, 128
 
 # The C entry points this binding (and include/ds4a.h) exposes.
 EXPORTS = ("ds4a_strerror", "ds4a_version", "ds4a_workspace_bytes", "ds4a_get_device_status",
-           "ds4a_debug_inject_error", "ds4a_indexer_score", "ds4a_topk_select",
+           "ds4a_debug_inject_error", "ds4a_debug_wait_timeout", "ds4a_indexer_score", "ds4a_topk_select",
            "ds4a_topk_select_noalloc", "ds4a_sparse_attn_decode", "ds4a_sparse_attn_prefill",
            "ds4a_dense_attn_decode", "ds4a_kv_push_raw", "ds4a_compressor_pool",
            "ds4a_sparse_attn_decode_heads", "ds4a_sparse_attn_prefill_heads", "ds4a_dense_attn_decode_heads",
@@ -76,6 +76,8 @@ def load(build_if_missing: bool = True):
     L.ds4a_get_device_status.restype = _i32
     L.ds4a_debug_inject_error.argtypes = [_i32]
     L.ds4a_debug_inject_error.restype = None
+    L.ds4a_debug_wait_timeout.argtypes = [ctypes.c_uint, _vp]
+    L.ds4a_debug_wait_timeout.restype = _i32
     L.ds4a_indexer_score.argtypes = [_vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp]
     L.ds4a_indexer_score.restype = _i32
     L.ds4a_topk_select.argtypes = [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _sz, _vp]
@@ -171,6 +173,12 @@ def ds4a_get_device_status(stream=None):
 
 def ds4a_debug_inject_error(code):
     load().ds4a_debug_inject_error(code)
+
+
+def ds4a_debug_wait_timeout(limit_us, stream=None):
+    """Device-side failure-path hook: a bounded wait that nothing completes
+    gives up after limit_us and sets DS4A_DEV_TIMEOUT (no fault)."""
+    _check(load().ds4a_debug_wait_timeout(int(limit_us), _stream(stream)), "ds4a_debug_wait_timeout")
 
 
 def ds4a_indexer_score(iq, w, ik, n_rows, scores, q_pos=None, row_pos=None, stream=None):

@@ -175,6 +175,15 @@ ds4a_status ds4a_get_device_status(void *stream, unsigned *flags) {
 
 void ds4a_debug_inject_error(ds4a_status code) { g_inject.store(code); }
 
+ds4a_status ds4a_debug_wait_timeout(unsigned limit_us, void *stream) {
+    if (limit_us < 1 || limit_us > 100000) return DS4A_EINVAL;
+    DevInfo *di = nullptr;
+    if (ds4a_status st = current_device(&di)) return st;
+    return ds4a::launch_debug_wait(di->status, 1000ull * limit_us, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? DS4A_OK
+               : DS4A_ECUDA;
+}
+
 }  // extern "C"
 
 namespace {

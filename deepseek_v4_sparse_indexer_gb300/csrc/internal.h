@@ -103,8 +103,8 @@ struct AttnArgs {
     void *ws;
     uint32_t *status;
 };
-int attn_num_splits(int units, int top_k);
 size_t attn_ws_bytes(int units, int top_k);
+cudaError_t launch_debug_wait(uint32_t *status, unsigned long long limit_ns, cudaStream_t s);
 cudaError_t launch_sparse_attn(const AttnArgs &a, int num_sms, cudaStream_t s);
 
 // ---- cache producer --------------------------------------------------------

@@ -107,6 +107,16 @@ ds4a_status ds4a_get_device_status(void *stream, unsigned *flags);
 void ds4a_debug_inject_error(ds4a_status code);
 
 /*
+ * Test hook for the device-side failure path: launches one thread that waits
+ * on an mbarrier nothing completes, gives up after limit_us microseconds
+ * (1 .. 100,000, else DS4A_EINVAL) and sets DS4A_DEV_TIMEOUT in the device
+ * status word, as a compute kernel's bounded wait does when a producer never
+ * arrives.  Nothing faults and the context stays usable; the next
+ * ds4a_get_device_status() returns DS4A_EDEVICE with that flag and clears it.
+ */
+ds4a_status ds4a_debug_wait_timeout(unsigned limit_us, void *stream);
+
+/*
  * 1. Indexer score ("DwarfStar(ds4.c) のアーキテクチャを読む" §3-3: the
  *    indexer's light query system scores each compressed row through its
  *    128-d key; the pages print no formula, this library specifies it):
