@@ -453,10 +453,14 @@ def main():
 
     seed = rank_seed(wl.seed, rank)
     # auto: the fused select where its candidate kernel (one CTA per row) fills
-    # the GPU (decode with as many rows as SMs); the two kernels otherwise.
+    # the GPU (decode with as many rows as SMs), or where every row is a
+    # candidate anyway (rows of at most 4,096 entries, which the candidate
+    # kernel caches whole: 1 x 1,024 rows 0.041 vs 0.053 ms per step); the two
+    # kernels otherwise (8 x 16,384: 0.061 vs 0.087 ms; 4 x 262,144: 0.093 vs
+    # 0.366 ms).
     n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     fused = args.select == "fused" or (args.select == "auto" and wl.kind == "decode" and
-                                       wl.units * wl.queries >= n_sms)
+                                       (wl.units * wl.queries >= n_sms or wl.n_rows <= 4096))
     if wl.kind == "decode":
         x = make_decode_inputs(wl.units, wl.n_rows, device=dev, seed=seed, heavy_frac=wl.heavy_frac,
                                heavy_scale=wl.heavy_scale, n_head=wl.heads, with_rows=not wl.fp8)
