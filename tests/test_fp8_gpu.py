@@ -278,3 +278,47 @@ def test_workload_decode_fp8_sampled():
         ro, rl = oracle.sparse_attention_fp8(u16(x["q"][u]), oc, os_, gidx[:cnt], u16(x["raw"][u]), np.arange(128),
                                              SCALE)
         check_output(st.out[u].cpu().numpy(), ro, st.lse[u].cpu().numpy(), rl)
+
+
+@pytest.mark.slow
+def test_workload_prefill_fp8_sampled():
+    """The benchmarked FP8 prefill chunk (2,048 queries over 65,536 + 512 rows),
+    store built by the device quantiser, sampled queries against the oracle
+    (the first and last query and spread ones; the store of the rows they
+    select checked bit-exact against the oracle's quantiser)."""
+    wl = WORKLOADS["prefill_fp8_2048x65536"]
+    x = make_prefill_inputs(wl.queries, wl.extra["prior_rows"], device="cuda", seed=wl.seed, with_rows=False)
+    n_cap = x["ik"].shape[0]
+    rows8 = torch.empty(n_cap, 512, dtype=torch.uint8, device="cuda")
+    rscale = torch.empty(n_cap, dtype=torch.float32, device="cuda")
+    f32 = []
+    for r0, c in prefill_rows_fp32_chunks(n_cap, device="cuda", seed=wl.seed):
+        B.ds4a_rows_to_fp8(c, rows8[r0:r0 + c.shape[0]], rscale[r0:r0 + c.shape[0]])
+        f32.append(c.cpu())
+    x["rows8"], x["row_scale"] = rows8, rscale
+    st = PrefillStep(wl.queries, n_cap, wl.top_k, fp8=True)
+    st(x, SCALE)
+    torch.cuda.synchronize()
+    device_ok()
+    q, iq, w, ik = u16(x["q"]), u16(x["iq"]), x["w"].cpu().numpy(), u16(x["ik"])
+    row_pos, q_pos, raw = x["row_pos"].cpu().numpy(), x["q_pos"].cpu().numpy(), u16(x["raw"])
+    codes_np, scale_np = rows8.cpu().numpy(), rscale.cpu().numpy()
+    f32 = torch.cat(f32).numpy()
+    n = int(x["n_rows"][0])
+    queries = [0, 1, 700, 1023, 1536, wl.queries - 1]
+
+    def one(t):
+        p = int(q_pos[t])
+        s = oracle.indexer_score(iq[t:t + 1], w[t:t + 1], ik, n, q_pos=np.array([p], np.int32), row_pos=row_pos)[0]
+        check_scores(st.scores[0, t, :n].cpu().numpy(), s[:n], score_tolerance(iq[t], w[t], ik, n))
+        cnt = int(st.count[0, t])
+        gidx = st.idx[0, t].cpu().numpy()
+        check_index_set(gidx, cnt, s[:n], wl.top_k)
+        oc, os_ = oracle.quantize_rows_fp8(f32[gidx[:cnt]])
+        assert np.array_equal(codes_np[gidx[:cnt]], oc) and np.array_equal(scale_np[gidx[:cnt]], os_)
+        win = oracle.prefill_window(p, x["raw_pos0"], raw.shape[0])
+        ro, rl = oracle.sparse_attention_fp8(q[t], codes_np, scale_np, gidx[:cnt], raw, win, SCALE)
+        return check_output(st.out[t].cpu().numpy(), ro, st.lse[t].cpu().numpy(), rl)
+
+    with pool() as p:
+        list(p.map(one, queries))

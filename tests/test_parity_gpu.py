@@ -419,7 +419,14 @@ def test_workload_decode_32x43x65536_sampled():
     units = [0, 1, 42, 687, 1000, wl.units - 1]
     with pool() as p:
         list(p.map(lambda u: check_decode_unit(x, st, u, wl.top_k, SCALE), units))
-    del x, st
+    # the configuration the bench times: the fused score + select, bit-identical
+    # to score-then-select over all 1,376 units
+    sf = DecodeStep(wl.units, wl.n_rows, wl.top_k, fused=True)
+    sf(x, SCALE)
+    torch.cuda.synchronize()
+    device_ok()
+    assert torch.equal(sf.count, st.count) and torch.equal(sf.idx, st.idx) and torch.equal(sf.out, st.out)
+    del x, st, sf
     torch.cuda.empty_cache()
 
 

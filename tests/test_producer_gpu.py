@@ -96,3 +96,24 @@ def test_push_raw_batch_with_strided_rings_and_a_bad_position():
         assert int(n_raw[u]) == n
     assert int(n_raw[3]) == 77 and not ring[3].any()        # the bad position wrote nothing
     device_ok()
+
+
+@pytest.mark.slow
+def test_workload_pool_32x20x128_full():
+    """The benchmarked producer step (raw push + ratio-128 pooling of 640 units)
+    in the bench's launch configuration, every unit against the oracle."""
+    from deepseek_v4_sparse_indexer_gb300 import ProducerStep
+    from deepseek_v4_sparse_indexer_gb300.workloads import WORKLOADS, make_pool_inputs
+    wl = WORKLOADS["pool_32x20x128"]
+    x = make_pool_inputs(wl.units, wl.n_rows, device="cuda", seed=wl.seed)
+    st = ProducerStep(wl.units)
+    st(x)
+    torch.cuda.synchronize()
+    device_ok()
+    kv, sc, got = x["kv"].cpu().numpy(), x["score"].cpu().numpy(), st.out.cpu().numpy().astype(np.float64)
+    for u in range(wl.units):
+        ref = oracle.compressor_pool(kv[u], sc[u])
+        assert np.all(np.abs(got[u] - ref) <= pool_tolerance(kv[u])), u
+    # the new rows landed in ring slot pos % 128, rounded to f16
+    slot = int(x["pos"][0]) % 128
+    assert torch.equal(x["raw"][:, slot], x["row"].half())
