@@ -331,6 +331,31 @@ def test_attention_work_schedule(U, top_k):
     attention_case(U, 600, top_k, seed=40 + U)
 
 
+@pytest.mark.parametrize("scale", [-1 / math.sqrt(512), 0.0, 4 / math.sqrt(512)])
+def test_attention_negative_zero_and_large_scale(scale):
+    # A non-positive scale takes the general softmax path (the max is taken
+    # after scaling); scale 0 gives the plain mean of the row set.
+    U, N_cap, k = 5, 900, 256
+    rng = np.random.default_rng(61)
+    x = make_decode_inputs(U, N_cap, device="cuda", seed=61, n_raw=[128, 64, 0, 1, 100])
+    cnt = np.array([256, 200, 64, 0, 129], np.int32)
+    idx = np.full((U, k), -1, np.int32)
+    for u in range(U):
+        idx[u, :cnt[u]] = np.sort(rng.choice(N_cap, size=cnt[u], replace=False))
+    out = torch.empty(U, 64, 512, device="cuda")
+    lse = torch.empty(U, 64, device="cuda")
+    ws = torch.empty(max(B.ds4a_workspace_bytes(B.DS4A_OP_SPARSE_ATTN_DECODE, U, 1, N_cap, k), 1),
+                     dtype=torch.uint8, device="cuda")
+    B.ds4a_sparse_attn_decode(x["q"], x["rows"], torch.from_numpy(idx).cuda(), torch.from_numpy(cnt).cuda(),
+                              x["raw"], x["n_raw"], scale, out, lse, ws)
+    torch.cuda.synchronize()
+    device_ok()
+    for u in range(U):
+        ro, rl = oracle.sparse_attention(u16(x["q"][u]), u16(x["rows"][u]), idx[u, :cnt[u]], u16(x["raw"][u]),
+                                         np.arange(int(x["n_raw"][u])), scale)
+        check_output(out[u].cpu().numpy(), ro, lse[u].cpu().numpy(), rl)
+
+
 def test_attention_raw_window_extremes_and_odd_k():
     attention_case(4, 300, 100, seed=13, n_raw=[0, 1, 127, 128])
 
