@@ -506,14 +506,15 @@ __global__ void __launch_bounds__(kFinalThreads) topk_final_kernel(const float *
 //      than 131,072), -1 padded; the fallback compacts the row in order.
 
 // Two shapes: 512 threads, 8,192 candidates, two CTAs per SM (any k, any
-// length); and for k <= kRowSmallMaxK and rows up to kRowSmallMaxN, 256
-// threads, 4,096 candidates and a 1,024-entry sort buffer, four CTAs per SM:
-// the phases of a short row are latency-bound, so twice the rows in flight
-// beat twice the threads per row (2,048 x 16,896: 140 vs 169 us).
+// length); and for k <= kRowSmallMaxK and rows up to kRowSmallMaxN (the
+// reach of the row bitmap), 256 threads, 4,096 candidates and a 1,024-entry
+// sort buffer, four CTAs per SM: a row's phases are latency-bound, so twice
+// the rows in flight beat twice the threads per row (2,048 x 16,896: 140 vs
+// 169 us; 2,048 x 66,048: 224 vs 250 us; 1,376 x 65,536: 165 vs 177 us).
 constexpr int kSample = 2048;
 constexpr int kSampleOver = 3;     // expected candidates / k
 constexpr int kRowSmallMaxK = 640;
-constexpr int kRowSmallMaxN = 32768;   // longer rows: fewer, wider CTAs (the pass dominates)
+constexpr int kRowSmallMaxN = kBins * 32;   // 131,072
 template <int NT, int CAP, int SEL>
 struct RowShape {
     static constexpr int kSmem = CAP * 8 + kBins * 4 + SEL * 4;   // candidates, histogram, chosen
@@ -547,6 +548,18 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 2 : 4) topk_row_kernel(const f
         for (int i = threadIdx.x; i < kBins; i += blockDim.x) h[i] = 0;
         __syncthreads();
     };
+    constexpr int B = 4;
+    const int ngroups = (n + 3) / 4;
+    const bool vec4 = (N_cap & 3) == 0;
+    auto load = [&](float4 (&v)[B], int g0) {
+#pragma unroll
+        for (int j = 0; j < B; ++j) {
+            const int g = g0 + j * NT + static_cast<int>(threadIdx.x);
+            v[j] = g < ngroups ? __ldg(reinterpret_cast<const float4 *>(s) + g) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+    float4 cur[B], nxt[B];
+    if (vec4) load(cur, 0);                              // in flight during the threshold estimate
     // ---- 1. threshold estimate
     uint32_t T0 = 0;
     if (n > CAP) {
@@ -597,20 +610,9 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 2 : 4) topk_row_kernel(const f
             if (take && p < static_cast<uint32_t>(CAP)) cand[p] = make_uint2(key, static_cast<uint32_t>(i));
         }
     };
-    if ((N_cap & 3) == 0) {
+    if (vec4) {
         // Whole float4 groups, B per thread in flight plus the next B prefetched;
         // every thread runs the same iterations (the ballots are warp-wide).
-        constexpr int B = 4;
-        const int ngroups = (n + 3) / 4;
-        auto load = [&](float4 (&v)[B], int g0) {
-#pragma unroll
-            for (int j = 0; j < B; ++j) {
-                const int g = g0 + j * NT + static_cast<int>(threadIdx.x);
-                v[j] = g < ngroups ? __ldg(reinterpret_cast<const float4 *>(s) + g) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        };
-        float4 cur[B], nxt[B];
-        load(cur, 0);
         for (int g0 = 0; g0 < ngroups; g0 += B * NT) {
             if (g0 + B * NT < ngroups) load(nxt, g0 + B * NT);
 #pragma unroll

@@ -241,13 +241,22 @@ def test_topk_rows_random_and_ragged():
     topk_case(x, _many(rng, 20000, [20000, 19999, 4097, 4096, 3000, 513, 512, 77, 1, 0]), 512)
 
 
-def test_topk_rows_longer_than_the_narrow_shape():
-    # rows over 32,768 entries take the 512-thread shape of the per-row kernel
+def test_topk_rows_between_32768_and_65536():
+    # long rows through the 256-thread shape (candidates cached, bitmap output)
     rng = np.random.default_rng(17)
     x = rng.standard_normal((ROWS_MANY, 40000)).astype(np.float32)
     x[1::5][:, rng.random(40000) < 0.02] *= 6        # heavy tail
     x[2::5, 30000:] += 2.0                           # the top rows crowded at the end of the row
     topk_case(x, _many(rng, 40000, [40000, 39999, 32769, 32768, 20000, 512]), 512)
+
+
+def test_topk_rows_longer_than_the_row_bitmap():
+    # rows over 131,072 entries take the 512-thread shape and sort the chosen rows
+    rng = np.random.default_rng(18)
+    x = rng.standard_normal((ROWS_MANY, 140000)).astype(np.float32)
+    x[1::4, 135000:] += 3.0                          # the top rows crowded at the end of the row
+    x[2::4] = np.round(x[2::4] * 4) / 4              # heavy ties
+    topk_case(x, _many(rng, 140000, [140000, 139999, 131073, 131072, 70000]), 512)
 
 
 def test_topk_rows_ties_neginf_nan_signed_zero():
