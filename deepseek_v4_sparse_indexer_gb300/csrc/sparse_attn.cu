@@ -976,6 +976,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
     }
 }
 
+constexpr int kMergeMaxPieces = 128;   // one per thread of the merge block; a unit has at most kMaxTopK / 64 + 2 tiles
+static_assert((kMaxTopK + TR - 1) / TR + (kNSwa + TR - 1) / TR <= kMergeMaxPieces, "merge: one thread per piece");
+
 // Combines the pieces of the remainder units that straddle a share boundary.
 // Block (v, h): head h of remainder unit v, whose tiles [v nt, (v+1) nt) of the
 // remainder tile space lie in the shares of CTAs c0 .. c1 (share c: tiles
@@ -1000,25 +1003,54 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const __grid_constant__
         return c == c0 ? 2LL * c + (static_cast<long long>(c) * T / g_rem == vs ? 0 : 1) : 2LL * c;
     };
     const float NEG_INF = -__int_as_float(0x7f800000);
-    float M = NEG_INF;
-    for (int c = c0; c <= c1; ++c) {
-        const float2 p = *reinterpret_cast<const float2 *>(ml + (piece_slot(c) * kNHead + h) * 2);
-        if (p.y > 0.f) M = fmaxf(M, p.x);
+    // Thread i < np loads piece i's (m, l): one round trip for all pieces.
+    // The O rows then load eight pieces at a time, all in flight together.
+    // The sums run in piece order, as a sequential loop would.
+    __shared__ float s_w[kMergeMaxPieces], s_l[kMergeMaxPieces];
+    __shared__ float s_max[4];
+    const int np = c1 - c0 + 1;                              // <= tiles per unit <= kMergeMaxPieces
+    float mk = NEG_INF, lk = 0.f;
+    if (threadIdx.x < np) {
+        const float2 p = *reinterpret_cast<const float2 *>(ml + (piece_slot(c0 + threadIdx.x) * kNHead + h) * 2);
+        if (p.y > 0.f) {
+            mk = p.x;
+            lk = p.y;
+        }
     }
+    float M = mk;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = M;
+    __syncthreads();
+    M = fmaxf(fmaxf(s_max[0], s_max[1]), fmaxf(s_max[2], s_max[3]));
+    if (threadIdx.x < np) {
+        s_w[threadIdx.x] = mk == NEG_INF ? 0.f : exp2f(mk - M);
+        s_l[threadIdx.x] = lk;
+    }
+    __syncthreads();
     float L = 0.f;
+    for (int i = 0; i < np; ++i) L += s_w[i] * s_l[i];
     const int d = threadIdx.x * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c = c0; c <= c1; ++c) {
-        const long long slot = piece_slot(c);
-        const float2 p = *reinterpret_cast<const float2 *>(ml + (slot * kNHead + h) * 2);
-        if (!(p.y > 0.f)) continue;
-        const float wk = exp2f(p.x - M);
-        L += wk * p.y;
-        const float4 o = *reinterpret_cast<const float4 *>(wo + (slot * kNHead + h) * kHeadDim + d);
-        acc.x += wk * o.x;
-        acc.y += wk * o.y;
-        acc.z += wk * o.z;
-        acc.w += wk * o.w;
+    for (int i0 = 0; i0 < np; i0 += 8) {
+        float4 o[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int i = i0 + j;
+            o[j] = (i < np && s_w[i] != 0.f)
+                       ? *reinterpret_cast<const float4 *>(wo + (piece_slot(c0 + i) * kNHead + h) * kHeadDim + d)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int i = i0 + j;
+            if (i >= np || s_w[i] == 0.f) continue;
+            const float wk = s_w[i];
+            acc.x += wk * o[j].x;
+            acc.y += wk * o[j].y;
+            acc.z += wk * o[j].z;
+            acc.w += wk * o[j].w;
+        }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     acc.x *= inv;
