@@ -340,6 +340,12 @@ def test_attention_work_schedule(U, top_k):
     attention_case(U, 600, top_k, seed=40 + U)
 
 
+def test_attention_largest_top_k_in_one_tile_pieces():
+    # top_k = 2,048 on two units: 68 one-tile pieces, 34 per unit, all merged
+    # (the most pieces a unit can have)
+    attention_case(2, 2500, 2048, seed=47)
+
+
 @pytest.mark.parametrize("scale", [-1 / math.sqrt(512), 0.0, 4 / math.sqrt(512)])
 def test_attention_negative_zero_and_large_scale(scale):
     # A non-positive scale takes the general softmax path (the max is taken
