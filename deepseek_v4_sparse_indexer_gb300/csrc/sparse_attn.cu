@@ -8,7 +8,8 @@
 // unit is one decode query or one query of a prefill chunk.  The unit's row
 // list [selected compressed rows..., raw-window rows...] is cut into 64-row
 // tiles, double-buffered in shared memory:
-//   gather   warps 6-11: the six warps share every tile (4-row groups dealt
+//   gather   warps 6-13 (row lists; 6-11 for dense row lists, whose whole
+//            tiles come by TMA): the warps share every tile (4-row groups dealt
 //            round-robin) with 16-byte cp.async into eight 8 KB column
 //            blocks in the 128B-swizzled layout; masked rows are zero-filled
 //            and per-group row-validity bits go to shared memory; each
@@ -67,10 +68,15 @@ constexpr int kSoftmaxWarps = 4;              // warps 0-3: softmax + epilogue (
 constexpr int kMmaWarp = 4;                   // warp 4: TMEM owner + logits UMMA issuer
 constexpr int kPvWarp = 5;                    // warp 5: values UMMA issuer
 constexpr int kFirstGatherWarp = 6;           // warps 6-11: row gather (cp.async)
-constexpr int kGatherWarps = 6;
 constexpr int kRowGroups = TR / 4;            // 4-row groups of a tile, dealt round-robin to the gather warps
-constexpr int kGroupsPerWarp = (kRowGroups + kGatherWarps - 1) / kGatherWarps;
-constexpr int kThreads = (kFirstGatherWarp + kGatherWarps) * 32;
+// Gather warps per CTA: eight for gathered row lists (two 4-row groups each:
+// the copies and the FP8 expansion are the tile's critical path); six for
+// dense row lists, whose tiles arrive by TMA and whose gather warps only
+// arrive on the buffer barrier (fewer threads leave the softmax 168
+// registers instead of 144).
+constexpr int kGatherWarpsList = 8;
+constexpr int kGatherWarpsDense = 6;
+constexpr int attn_threads(int gw) { return (kFirstGatherWarp + gw) * 32; }
 constexpr int kQBlk = kNHead * 128;           // 64 heads x 64 dims x 2 B = 8 KB
 constexpr int kXBlk = TR * 128;               // 64 rows x 64 dims x 2 B = 8 KB
 constexpr int kXBuf = 8 * kXBlk;              // one row tile: 64 KB
@@ -334,8 +340,11 @@ DS4A_DEV void tmem_ld16x256_x8(uint32_t taddr, uint32_t (&r)[32]) {
         : "r"(taddr));
 }
 
-__global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_constant__ AttnArgs a, int nt,
-                                                                  int g_rem) {
+template <int GW>
+__global__ void __launch_bounds__(attn_threads(GW), 1) sparse_attn_kernel(const __grid_constant__ AttnArgs a, int nt,
+                                                                          int g_rem) {
+    constexpr int kGatherWarps = GW;
+    constexpr int kGroupsPerWarp = (kRowGroups + kGatherWarps - 1) / kGatherWarps;
     pdl_launch_dependents();
     pdl_wait();
     extern __shared__ uint8_t smem_raw[];
@@ -398,8 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
 
     if (warp >= kFirstGatherWarp) {
         // ------------------------------------------------------------ row gather
-        // All six warps walk the CTA's (item, tile) sequence; warp g copies
-        // the 4-row groups g, g + 6, g + 12 (< 16) of every tile.  Lane l
+        // All gather warps walk the CTA's (item, tile) sequence; warp g of GW
+        // copies the 4-row groups g, g + GW, ... (< 16) of every tile.  Lane l
         // copies 16-byte chunk (l & 7) of row 4k + (l >> 3) of group k in
         // every 64-column block: a warp instruction moves four full 128-byte
         // row segments.  Destinations follow the 128B swizzle.
@@ -885,7 +894,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                 {
                     const bool r = __all_sync(0xffffffffu, mbar_wait(grp, gph, abort_flag));
                     gph ^= 1;
-                    if (!(ok = r)) break;
+                    ok = r;
+                    if (!ok) break;
                 }
                 const uint4 fl = *reinterpret_cast<const uint4 *>(sFlag + tb * kSoftmaxWarps);
                 const bool any_resc = (fl.x | fl.y | fl.z | fl.w) != 0u;
@@ -1077,7 +1087,10 @@ size_t attn_ws_bytes(int units, int top_k) {
 }
 
 cudaError_t launch_sparse_attn(const AttnArgs &a, int num_sms, cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    const int gw = (a.idx == nullptr && a.rows8 == nullptr) ? kGatherWarpsDense : kGatherWarpsList;
+    void (*kern)(AttnArgs, int, int) =
+        gw == kGatherWarpsDense ? sparse_attn_kernel<kGatherWarpsDense> : sparse_attn_kernel<kGatherWarpsList>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     const int nt = attn_tiles_per_unit(a.top_k);
     const long long T = static_cast<long long>(a.units) * nt;
@@ -1089,7 +1102,7 @@ cudaError_t launch_sparse_attn(const AttnArgs &a, int num_sms, cudaStream_t s) {
     const long long u_rem = a.units - (a.units / G) * G;
     const long long t_rem = u_rem * nt;
     const int g_rem = static_cast<int>(t_rem < G ? t_rem : G);
-    e = launch_k(sparse_attn_kernel, dim3(static_cast<unsigned>(G)), dim3(kThreads), kSmemBytes, s, a, nt, g_rem);
+    e = launch_k(kern, dim3(static_cast<unsigned>(G)), dim3(attn_threads(gw)), kSmemBytes, s, a, nt, g_rem);
     if (e != cudaSuccess || g_rem <= 1) return e;
     return launch_k(attn_merge_kernel, dim3(static_cast<unsigned>(u_rem * kNHead)), dim3(128), 0, s, a, nt, g_rem,
                     static_cast<int>(G));
