@@ -8,7 +8,7 @@
 // unit is one decode query or one query of a prefill chunk.  The unit's row
 // list [selected compressed rows..., raw-window rows...] is cut into 64-row
 // tiles, double-buffered in shared memory:
-//   gather   warps 6-13 (row lists; 6-11 for dense row lists, whose whole
+//   gather   warps 6-13 (row lists; 6-9 for dense row lists, whose whole
 //            tiles come by TMA): the warps share every tile (4-row groups dealt
 //            round-robin) with 16-byte cp.async into eight 8 KB column
 //            blocks in the 128B-swizzled layout; masked rows are zero-filled
@@ -70,12 +70,12 @@ constexpr int kPvWarp = 5;                    // warp 5: values UMMA issuer
 constexpr int kFirstGatherWarp = 6;           // warps 6-11: row gather (cp.async)
 constexpr int kRowGroups = TR / 4;            // 4-row groups of a tile, dealt round-robin to the gather warps
 // Gather warps per CTA: eight for gathered row lists (two 4-row groups each:
-// the copies and the FP8 expansion are the tile's critical path); six for
+// the copies and the FP8 expansion are the tile's critical path); four for
 // dense row lists, whose tiles arrive by TMA and whose gather warps only
-// arrive on the buffer barrier (fewer threads leave the softmax 168
-// registers instead of 144).
+// arrive on the buffer barrier (640 x 8,192: 1.015 ms with four, 1.036 ms
+// with six, 1.09 ms with eight).
 constexpr int kGatherWarpsList = 8;
-constexpr int kGatherWarpsDense = 6;
+constexpr int kGatherWarpsDense = 4;
 constexpr int attn_threads(int gw) { return (kFirstGatherWarp + gw) * 32; }
 constexpr int kQBlk = kNHead * 128;           // 64 heads x 64 dims x 2 B = 8 KB
 constexpr int kXBlk = TR * 128;               // 64 rows x 64 dims x 2 B = 8 KB
