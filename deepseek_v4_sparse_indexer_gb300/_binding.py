@@ -40,6 +40,7 @@ EXPORTS = ("ds4a_strerror", "ds4a_version", "ds4a_workspace_bytes", "ds4a_get_de
            "ds4a_sparse_attn_decode_heads", "ds4a_sparse_attn_prefill_heads", "ds4a_dense_attn_decode_heads",
            "ds4a_rows_to_fp8", "ds4a_sparse_attn_decode_fp8", "ds4a_sparse_attn_prefill_fp8", "ds4a_indexer_topk")
 DS4A_TOPK_NOALLOC_SCRATCH_BYTES = 8 << 20
+DS4A_MAX_TOP_K = 2048
 
 
 class Ds4aError(RuntimeError):

@@ -3,7 +3,11 @@
 // returns a ds4a_status; nothing here synchronises except
 // ds4a_get_device_status().
 #include <atomic>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/ds4a.h"
 #include "internal.h"
@@ -90,6 +94,15 @@ ds4a_status take_injected() {
 }  // namespace
 
 namespace ds4a {
+bool nvtx_enabled() {
+    static const bool on = [] {
+        const char *v = std::getenv("DS4A_NVTX");
+        return v != nullptr && std::strcmp(v, "1") == 0;
+    }();
+    return on;
+}
+void nvtx_push(const char *name) { nvtxRangePushA(name); }
+void nvtx_pop() { nvtxRangePop(); }
 int current_device_info(uint32_t **status, int *sms) {
     DevInfo *di = nullptr;
     const ds4a_status st = current_device(&di);
@@ -143,7 +156,7 @@ size_t ds4a_workspace_bytes(int op, int U, int Q, int N_cap, int top_k) {
     case DS4A_OP_INDEXER_SCORE: return 0;
     case DS4A_OP_TOPK_SELECT:
         if (top_k < 1 || top_k > DS4A_MAX_TOP_K) return static_cast<size_t>(-1);
-        return topk_ws_bytes(static_cast<long long>(U) * Q, top_k);
+        return topk_ws_bytes(static_cast<long long>(U) * Q, N_cap);
     case DS4A_OP_SPARSE_ATTN_DECODE:
         if (top_k < 1 || top_k > DS4A_MAX_TOP_K) return static_cast<size_t>(-1);
         return attn_ws_bytes(U, top_k);
@@ -235,6 +248,7 @@ extern "C" {
 ds4a_status ds4a_indexer_score(const uint16_t *iq, const float *w, const uint16_t *ik, int64_t ik_unit_stride,
                                const int32_t *n_rows, const int32_t *q_pos, const int32_t *row_pos, float *scores,
                                int U, int Q, int N_cap, void *stream) {
+    const NvtxRange nvtx_range("ds4a_indexer_score");
     if (ds4a_status inj = take_injected()) return inj;
     if (!scores || !aligned(scores, 4)) return DS4A_EINVAL;
     IndexerArgs a{};
@@ -250,6 +264,7 @@ ds4a_status ds4a_indexer_topk(const uint16_t *iq, const float *w, const uint16_t
                               const int32_t *n_rows, const int32_t *q_pos, const int32_t *row_pos, int U, int Q,
                               int N_cap, int top_k, int32_t *idx, int32_t *count, void *ws, size_t ws_bytes,
                               void *stream) {
+    const NvtxRange nvtx_range("ds4a_indexer_topk");
     if (ds4a_status inj = take_injected()) return inj;
     if (!idx || !count || top_k < 1 || top_k > DS4A_MAX_TOP_K) return DS4A_EINVAL;
     if (N_cap > kTopkCandMaxRows) return DS4A_EUNSUPPORTED;
@@ -277,13 +292,14 @@ ds4a_status ds4a_indexer_topk(const uint16_t *iq, const float *w, const uint16_t
 
 ds4a_status ds4a_topk_select(const float *scores, const int32_t *n_rows, int U, int Q, int N_cap, int top_k,
                              int32_t *idx, int32_t *count, void *ws, size_t ws_bytes, void *stream) {
+    const NvtxRange nvtx_range("ds4a_topk_select");
     if (ds4a_status inj = take_injected()) return inj;
     if (!scores || !n_rows || !idx || !count) return DS4A_EINVAL;
     if (U < 1 || Q < 1 || N_cap < 1 || top_k < 1 || top_k > DS4A_MAX_TOP_K) return DS4A_EINVAL;
     if (static_cast<long long>(U) * Q > (1LL << 24)) return DS4A_EINVAL;
     if (!aligned(scores, 4)) return DS4A_EINVAL;
-    const size_t need = topk_ws_bytes(static_cast<long long>(U) * Q, top_k);
-    if (!ws || ws_bytes < need || !aligned(ws, 256)) return DS4A_EWORKSPACE;
+    const size_t need = topk_ws_bytes(static_cast<long long>(U) * Q, N_cap);
+    if (need && (!ws || ws_bytes < need || !aligned(ws, 256))) return DS4A_EWORKSPACE;
     DevInfo *di = nullptr;
     if (ds4a_status st = current_device(&di)) return st;
     TopkArgs a{scores, n_rows, U, Q, N_cap, top_k, idx, count, ws, di->status};
@@ -364,6 +380,7 @@ ds4a_status ds4a_sparse_attn_decode_heads(int n_head, const uint16_t *q, const u
                                           const int32_t *count, int top_k, const uint16_t *raw,
                                           int64_t raw_unit_stride, const int32_t *n_raw, float scale, float *out,
                                           float *lse, int U, void *ws, size_t ws_bytes, void *stream) {
+    const NvtxRange nvtx_range("ds4a_sparse_attn_decode_heads");
     if (ds4a_status inj = take_injected()) return inj;
     if (n_head != 64 && n_head != 128) return DS4A_EUNSUPPORTED;
     if (ds4a_status st = check_attn_common(q, rows, N_cap, idx, count, top_k, out)) return st;
@@ -384,6 +401,7 @@ ds4a_status ds4a_sparse_attn_decode_fp8(const uint16_t *q, const uint8_t *rows8,
                                         const int32_t *count, int top_k, const uint16_t *raw,
                                         int64_t raw_unit_stride, const int32_t *n_raw, float scale, float *out,
                                         float *lse, int U, void *ws, size_t ws_bytes, void *stream) {
+    const NvtxRange nvtx_range("ds4a_sparse_attn_decode_fp8");
     if (ds4a_status inj = take_injected()) return inj;
     const uint16_t *as16 = reinterpret_cast<const uint16_t *>(rows8);   // only its pointer checks are used
     if (ds4a_status st = check_attn_common(q, as16, N_cap, idx, count, top_k, out)) return st;
@@ -397,6 +415,7 @@ ds4a_status ds4a_dense_attn_decode_heads(int n_head, const uint16_t *q, const ui
                                          const uint16_t *raw, int64_t raw_unit_stride, const int32_t *n_raw,
                                          float scale, float *out, float *lse, int U, void *ws, size_t ws_bytes,
                                          void *stream) {
+    const NvtxRange nvtx_range("ds4a_dense_attn_decode_heads");
     if (ds4a_status inj = take_injected()) return inj;
     if (n_head != 64 && n_head != 128) return DS4A_EUNSUPPORTED;
     if (!q || !rows || !n_rows || !out || N_cap < 1) return DS4A_EINVAL;
@@ -467,6 +486,7 @@ ds4a_status ds4a_sparse_attn_prefill_heads(int n_head, const uint16_t *q, const 
                                            const int32_t *count, int top_k, const uint16_t *raw, int32_t raw_pos0,
                                            int n_raw_rows, float scale, float *out, float *lse, int T, void *ws,
                                            size_t ws_bytes, void *stream) {
+    const NvtxRange nvtx_range("ds4a_sparse_attn_prefill_heads");
     if (ds4a_status inj = take_injected()) return inj;
     if (n_head != 64 && n_head != 128) return DS4A_EUNSUPPORTED;
     if (ds4a_status st = check_attn_common(q, rows, N_cap, idx, count, top_k, out)) return st;
@@ -479,6 +499,7 @@ ds4a_status ds4a_sparse_attn_prefill_fp8(const uint16_t *q, const int32_t *q_pos
                                          const int32_t *count, int top_k, const uint16_t *raw, int32_t raw_pos0,
                                          int n_raw_rows, float scale, float *out, float *lse, int T, void *ws,
                                          size_t ws_bytes, void *stream) {
+    const NvtxRange nvtx_range("ds4a_sparse_attn_prefill_fp8");
     if (ds4a_status inj = take_injected()) return inj;
     const uint16_t *as16 = reinterpret_cast<const uint16_t *>(rows8);   // only its pointer checks are used
     if (ds4a_status st = check_attn_common(q, as16, N_cap, idx, count, top_k, out)) return st;
@@ -496,6 +517,7 @@ ds4a_status ds4a_sparse_attn_prefill(const uint16_t *q, const int32_t *q_pos, co
 }
 
 ds4a_status ds4a_rows_to_fp8(const float *x, int64_t n_rows, uint8_t *rows8, float *row_scale, void *stream) {
+    const NvtxRange nvtx_range("ds4a_rows_to_fp8");
     if (ds4a_status inj = take_injected()) return inj;
     if (n_rows < 0 || (n_rows > 0 && (!x || !rows8 || !row_scale))) return DS4A_EINVAL;
     if (n_rows == 0) return DS4A_OK;
@@ -510,6 +532,7 @@ ds4a_status ds4a_rows_to_fp8(const float *x, int64_t n_rows, uint8_t *rows8, flo
 
 ds4a_status ds4a_kv_push_raw(const float *kv, uint16_t *raw, int64_t raw_unit_stride, const int32_t *pos,
                              int32_t *n_raw, int U, void *stream) {
+    const NvtxRange nvtx_range("ds4a_kv_push_raw");
     if (ds4a_status inj = take_injected()) return inj;
     if (!kv || !raw || !pos || !n_raw || U < 1) return DS4A_EINVAL;
     if (!aligned(kv, 16) || !aligned(raw, 16)) return DS4A_EINVAL;
@@ -525,6 +548,7 @@ ds4a_status ds4a_kv_push_raw(const float *kv, uint16_t *raw, int64_t raw_unit_st
 
 ds4a_status ds4a_compressor_pool(const float *kv, const float *score, int ratio, int width, float *out, int U,
                                  void *stream) {
+    const NvtxRange nvtx_range("ds4a_compressor_pool");
     if (ds4a_status inj = take_injected()) return inj;
     if (!kv || !score || !out || U < 1 || ratio < 1 || width < 4 || width % 4) return DS4A_EINVAL;
     if (!aligned(kv, 16) || !aligned(score, 16) || !aligned(out, 16)) return DS4A_EINVAL;

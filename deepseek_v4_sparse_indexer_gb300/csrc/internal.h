@@ -47,7 +47,7 @@ void indexer_plan(IndexerArgs &a, int num_sms);      // fills n_groups .. grid
 // ---- top-k ---------------------------------------------------------------
 // Exact top-k over the fused indexer's candidate lists (see IndexerArgs).
 struct TopkCandArgs {
-    const uint2 *cand;
+    uint2 *cand;                // read; rows of tied keys may be compacted in place
     const uint32_t *cand_n, *vis_n;
     int R, N_cap, top_k;
     int32_t *idx, *count;
@@ -59,8 +59,14 @@ inline size_t indexer_topk_ws_bytes(long long R, int N_cap) {
     return static_cast<size_t>(R) * N_cap * 8 + static_cast<size_t>(R) * 12;
 }
 constexpr int kTopkCandMaxRows = 1 << 20;   // N_cap limit of the candidate path (its row bitmap)
-constexpr int kTopkBins = 4096;        // first radix digit: key bits 31..20
-constexpr int kTopkCandCap = 8192;     // candidate list capacity per (u,q)
+// Few long rows: each row is cut over at least two CTAs (at most
+// kTopkSplitMaxCtas in all, one wave on GB300's 152 SMs), each with a
+// candidate slot of at most kTopkSplitSlot entries; rows of at most
+// kTopkRowMaxShortRow scores, and batches of more than kTopkSplitMaxCtas / 2
+// rows, take one CTA per row.
+constexpr int kTopkSplitMaxCtas = 152;
+constexpr int kTopkSplitSlot = 4096;
+constexpr int kTopkRowMaxShortRow = 32768;
 struct TopkArgs {
     const float *scores;
     const int32_t *n_rows;
@@ -70,7 +76,7 @@ struct TopkArgs {
     void *ws;
     uint32_t *status;
 };
-size_t topk_ws_bytes(long long R, int top_k);
+size_t topk_ws_bytes(long long R, int N_cap);   // 0: no workspace
 cudaError_t launch_topk(const TopkArgs &a, int num_sms, cudaStream_t s);
 
 // ---- sparse attention ----------------------------------------------------
@@ -100,6 +106,7 @@ struct AttnArgs {
     float *lse;                  // [units][64] or null
     int units;                   // 64-head sub-units: row-side units x hsplit
     int hsplit;                  // 1 (64 heads) or 2 (128 heads: two sub-units per row-side unit)
+    int cluster;                 // 0: persistent CTAs; C > 0: one cluster of C CTAs per sub-unit
     void *ws;
     uint32_t *status;
 };
@@ -115,6 +122,24 @@ cudaError_t launch_compressor_pool(const float *kv, const float *score, int rati
 cudaError_t launch_rows_to_fp8(const float *x, long long n_rows, uint8_t *codes, float *row_scale, cudaStream_t s);
 
 // ---- shared host helpers of the C ABI -------------------------------------
+// Optional NVTX range around each C-ABI op (one range per call, named after
+// the entry point), for timelines in Nsight Systems.  On only when the
+// environment variable DS4A_NVTX is "1" when the process first calls an op;
+// otherwise each call costs one test of a cached flag.
+bool nvtx_enabled();
+void nvtx_push(const char *name);
+void nvtx_pop();
+struct NvtxRange {
+    bool on;
+    explicit NvtxRange(const char *name) : on(nvtx_enabled()) {
+        if (on) nvtx_push(name);
+    }
+    ~NvtxRange() {
+        if (on) nvtx_pop();
+    }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
 // Status word address and SM count of the current device (set up on first use).
 int current_device_info(uint32_t **status, int *sms);
 // Returns (and disarms) the error code armed by ds4a_debug_inject_error, or 0.

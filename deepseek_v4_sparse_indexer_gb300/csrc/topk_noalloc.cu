@@ -40,19 +40,22 @@ ds4a_status scratch_address(void **out) {
 
 extern "C" ds4a_status ds4a_topk_select_noalloc(const float *scores, const int32_t *n_rows, int U, int Q, int N_cap,
                                                 int top_k, int32_t *idx, int32_t *count, void *stream) {
+    const NvtxRange nvtx_range("ds4a_topk_select_noalloc");
     if (const int inj = take_injected_error()) return inj;
     if (!scores || !n_rows || !idx || !count) return DS4A_EINVAL;
     if (U < 1 || Q < 1 || N_cap < 1 || top_k < 1 || top_k > DS4A_MAX_TOP_K) return DS4A_EINVAL;
     if (static_cast<long long>(U) * Q > (1LL << 24)) return DS4A_EINVAL;
     if ((reinterpret_cast<uintptr_t>(scores) & 3) != 0) return DS4A_EINVAL;
-    if (topk_ws_bytes(static_cast<long long>(U) * Q, top_k) > DS4A_TOPK_NOALLOC_SCRATCH_BYTES)
-        return DS4A_EWORKSPACE;   // beyond the fixed scratch: nothing launched
+    // Only few long rows use scratch (at most about 5 MB, whatever the
+    // sizes); the check guards the fixed array should that ever change.
+    const size_t need = topk_ws_bytes(static_cast<long long>(U) * Q, N_cap);
+    if (need > DS4A_TOPK_NOALLOC_SCRATCH_BYTES) return DS4A_EWORKSPACE;   // nothing launched
     uint32_t *status = nullptr;
     int sms = 0;
     if (const int st = current_device_info(&status, &sms)) return st;
     void *ws = nullptr;
     if (const ds4a_status st = scratch_address(&ws)) return st;
-    // launch_topk clears the histogram and counter region before its kernels.
+    // The kernels write every scratch word they later read: nothing needs clearing.
     TopkArgs a{scores, n_rows, U, Q, N_cap, top_k, idx, count, ws, status};
     return launch_topk(a, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DS4A_OK : DS4A_ECUDA;
 }

@@ -34,9 +34,15 @@
  *    error returns DS4A_ECUDA.  Conditions only the device can see (a row
  *    index out of range, an internal wait that gave up) set bits in a
  *    per-process device status word, read by ds4a_get_device_status().
- *  - Thread-safety: entry points keep no host state between calls (the only
- *    host global is the test hook ds4a_debug_inject_error) and may be called
- *    concurrently on different streams.
+ *  - Thread-safety: entry points keep no per-call host state (host globals:
+ *    the test hook ds4a_debug_inject_error and the per-device set-up below)
+ *    and may be called concurrently on different streams.
+ *  - Per-device set-up: the first call on a device looks up, with that device
+ *    current, its SM count and the device addresses of the library's own
+ *    device globals (the status word; the scratch of 2'), and keeps them for
+ *    the life of the process.  Make that first call before any stream
+ *    capture, and do not use the library on a device after cudaDeviceReset()
+ *    on it in the same process (the kept addresses would be stale).
  */
 #ifndef DS4A_H
 #define DS4A_H
@@ -97,6 +103,12 @@ size_t ds4a_workspace_bytes(int op, int U, int Q, int N_cap, int top_k);
  * Synchronises `stream`, then reads and clears the current device's status
  * word.  *flags (if not NULL) receives the DS4A_DEV_* bits.  Returns DS4A_OK
  * when no bit was set, DS4A_EDEVICE when some were, DS4A_ECUDA on a CUDA error.
+ *
+ * There is one status word per device and process: the kernels of every
+ * stream, thread and caller on the device set bits in the same word, and a
+ * read returns and clears all of them, including bits raised by another
+ * caller's ops (or by ops still running on other streams).  Callers sharing
+ * a device should agree on one reader.
  */
 ds4a_status ds4a_get_device_status(void *stream, unsigned *flags);
 
@@ -160,7 +172,10 @@ ds4a_status ds4a_indexer_score(const uint16_t *iq, const float *w, const uint16_
  *            ascending order, then -1 padding.
  *    count   int32 [U][Q] (device): number selected = min(top_k, visible).
  *    ws      workspace of ds4a_workspace_bytes(DS4A_OP_TOPK_SELECT, U, Q,
- *            N_cap, top_k) bytes, 256-byte aligned (device).
+ *            N_cap, top_k) bytes, 256-byte aligned (device); NULL when that
+ *            is 0.  Only batches of up to 76 (u,q) rows longer than 32,768
+ *            scores use one (each row is then cut over several CTAs);
+ *            it is at most about 5 MB whatever the sizes.
  */
 ds4a_status ds4a_topk_select(const float *scores, const int32_t *n_rows, int U, int Q,
                              int N_cap, int top_k, int32_t *idx, int32_t *count,
@@ -209,14 +224,15 @@ ds4a_status ds4a_indexer_topk(const uint16_t *iq, const float *w, const uint16_t
  *
  *    Limits and rules:
  *    - the request must fit: ds4a_workspace_bytes(DS4A_OP_TOPK_SELECT, U, Q,
- *      N_cap, top_k) <= DS4A_TOPK_NOALLOC_SCRATCH_BYTES (up to 99 (u, q)
- *      rows at top_k 512, 93 at top_k 2048, whatever N_cap); a larger request returns
- *      DS4A_EWORKSPACE and launches nothing;
+ *      N_cap, top_k) <= DS4A_TOPK_NOALLOC_SCRATCH_BYTES, else DS4A_EWORKSPACE
+ *      and nothing is launched.  Every request fits today: only up to 76
+ *      rows of more than 32,768 scores use scratch, at most about 5 MB;
  *    - the first call on a device looks up the array's device address (one
- *      cudaGetSymbolAddress with that device current); make that first call
- *      before any stream capture;
+ *      cudaGetSymbolAddress with that device current) and keeps it for the
+ *      process: make that first call before any stream capture, and do not
+ *      call it after cudaDeviceReset() on that device;
  *    - all calls on a device share the one array, and it keeps what the last
- *      call left (each call clears what must start at zero): calls whose
+ *      call left (each call writes every scratch word it reads): calls whose
  *      kernels overlap on the GPU (other streams, other threads) race and give
  *      wrong results; serialise them on one stream;
  *    - it calls no cudaMalloc, cudaFree or allocating routine.

@@ -223,6 +223,41 @@ def test_topk_one_long_row_split_over_many_ctas():
     topk_case(x, [262144], 512)
 
 
+# Fewer rows than SMs, each longer than 32,768 scores: every row is cut over
+# several CTAs that filter their chunk against one sampled threshold into
+# slots of their own, and one CTA per row selects from the joined slots (or
+# from the whole row when the slots cannot decide).
+
+def test_topk_split_rows_ties_neginf_nan_locality_and_short_rows():
+    rng = np.random.default_rng(20)
+    N = 100000
+    x = rng.standard_normal((8, N)).astype(np.float32)
+    x[1] = np.round(x[1] * 2) / 2                             # heavy ties at the k-th score
+    x[2, rng.random(N) < 0.3] = -np.inf
+    x[2, rng.random(N) < 0.1] = np.nan
+    x[3] = 0.25                                               # all equal: slots overflow, exact pass
+    x[4, N - 5000:] += 3.0                                    # the top rows crowded in the last chunk
+    x[5, ::2] = -0.0
+    x[5, 1::2] = 0.0
+    x[5, 777] = 1.0
+    topk_case(x, [N, N, N, N, N - 3, 9000, 8000, 513], 512)   # 8,000 and 513 rows: every row a candidate
+
+
+@pytest.mark.parametrize("k", [1, 2048])
+def test_topk_split_rows_k_extremes_and_odd_stride(k):
+    rng = np.random.default_rng(21 + k)
+    x = rng.standard_normal((3, 70001)).astype(np.float32)   # N_cap not a multiple of 4: scalar loads
+    x[1, rng.random(70001) < 0.05] *= 4
+    topk_case(x, [70001, 70000, 2047], k)
+
+
+def test_topk_split_many_rows_few_ctas_each():
+    rng = np.random.default_rng(22)
+    x = rng.standard_normal((60, 40000)).astype(np.float32)  # two CTAs per row
+    x[::3, 20000:] += 1.0
+    topk_case(x, [40000 - (i % 7) * 3000 for i in range(60)], 512)
+
+
 # Batches with at least as many rows as SMs take the one-CTA-per-row kernel
 # (sampled threshold, candidate list, exact fallback over the row).
 
@@ -332,18 +367,22 @@ def test_attention_one_cta_per_unit(q_scale):
     attention_case(160, 700, 512, seed=12, q_scale=q_scale)
 
 
-@pytest.mark.parametrize("U,top_k", [(152, 512), (305, 512), (457, 64), (9, 64)])
+@pytest.mark.parametrize("U,top_k", [(152, 512), (305, 512), (457, 64), (40, 512), (17, 64), (9, 64), (16, 512),
+                                     (1, 512)])
 def test_attention_work_schedule(U, top_k):
     # Whole strided rounds of 152 units, then the remainder units' tiles cut
     # into equal shares: no remainder, one remainder unit over ten CTAs, three-
-    # tile units, and fewer units than CTAs (every unit in one-tile pieces).
+    # tile units, fewer units than CTAs (pieces merged by a second kernel);
+    # up to 16 units: one cluster of eight CTAs per unit, merged in shared
+    # memory (one and two tiles per CTA, three-tile units on eight CTAs).
     attention_case(U, 600, top_k, seed=40 + U)
 
 
-def test_attention_largest_top_k_in_one_tile_pieces():
-    # top_k = 2,048 on two units: 68 one-tile pieces, 34 per unit, all merged
-    # (the most pieces a unit can have)
-    attention_case(2, 2500, 2048, seed=47)
+@pytest.mark.parametrize("U", [2, 20])
+def test_attention_largest_top_k_in_many_pieces(U):
+    # top_k = 2,048: 34 tiles per unit.  Two units: clusters of eight CTAs,
+    # four or five tiles each; twenty units: 680 tiles in 152 shares, merged.
+    attention_case(U, 2500, 2048, seed=47 + U)
 
 
 @pytest.mark.parametrize("scale", [-1 / math.sqrt(512), 0.0, 4 / math.sqrt(512)])
@@ -557,11 +596,16 @@ def test_dense_attention_small_ragged(q_scale):
         check_dense_unit(x, out, lse, u)
 
 
-def test_dense_attention_few_units_split_rows():
-    # fewer units than SMs: each unit's rows are split over several CTAs and merged
-    x, out, lse = dense_case(3, 6000, [6000, 4500, 129], [128, 0, 5], seed=32)
+@pytest.mark.parametrize("U", [3, 24])
+def test_dense_attention_few_units_split_rows(U):
+    # fewer units than SMs: each unit's rows are split over several CTAs and
+    # merged (3 units: one cluster each, merged in shared memory; 24 units:
+    # shares of the persistent CTAs, merged by a second kernel)
+    n_rows = ([6000, 4500, 129] * 8)[:U]
+    n_raw = ([128, 0, 5] * 8)[:U]
+    x, out, lse = dense_case(U, 6000, n_rows, n_raw, seed=32)
     device_ok()
-    for u in range(3):
+    for u in range(min(U, 6)):
         check_dense_unit(x, out, lse, u)
 
 
