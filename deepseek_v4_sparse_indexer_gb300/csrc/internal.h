@@ -106,7 +106,6 @@ struct AttnArgs {
     float *lse;                  // [units][64] or null
     int units;                   // 64-head sub-units: row-side units x hsplit
     int hsplit;                  // 1 (64 heads) or 2 (128 heads: two sub-units per row-side unit)
-    int cluster;                 // 0: persistent CTAs; C > 0: one cluster of C CTAs per sub-unit
     void *ws;
     uint32_t *status;
 };

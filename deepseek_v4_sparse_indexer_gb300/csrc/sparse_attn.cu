@@ -88,8 +88,7 @@ constexpr int kOffValid = kOffP + 2 * kPBuf;  // two P buffers: 16 KB
 constexpr int kOffAlpha = kOffValid + 2 * kRowGroups;  // [2][16] row-validity nibbles
 constexpr int kOffFlag = kOffAlpha + 2 * kNHead * 4;
 constexpr int kOffInvL = kOffFlag + 2 * kSoftmaxWarps * 4;
-constexpr int kOffML = kOffInvL + kNHead * 4;      // cluster mode: (m, l) per head of this CTA's piece
-constexpr int kOffBar = kOffML + kNHead * 8;
+constexpr int kOffBar = kOffInvL + kNHead * 4;
 constexpr int kNumBars = 18;                  // 17 used
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 32 + 1024;
@@ -99,13 +98,6 @@ constexpr uint32_t kTmemCols = 512;           // S: 2 x 64 columns, O^T: 4 x 64 
 constexpr uint32_t kTmemS = 0;
 constexpr uint32_t kTmemO = 128;
 constexpr int kMaxAttnCtas = 160;            // grid cap (one persistent CTA per SM; 152 on GB300)
-// Few sub-units: one thread-block cluster of kClusterCtas CTAs per sub-unit
-// instead of the persistent schedule; the unit's tiles are cut into
-// kClusterCtas contiguous shares and the partials are merged through
-// distributed shared memory (no workspace, no merge kernel).
-constexpr int kClusterCtas = 8;
-constexpr int kClusterMaxUnits = 16;
-constexpr int kClusterDims = kHeadDim / kClusterCtas;   // output dims each CTA of a cluster finalises
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
 
 // UMMA instruction descriptors (see idesc_bf16_f32): logits (M = 64 heads,
@@ -243,31 +235,6 @@ DS4A_DEV bool wait_drain(uint64_t *bar, uint32_t parity) {
     return true;
 }
 
-// ---- thread-block cluster helpers
-DS4A_DEV uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-// Every thread of every CTA of the cluster arrives; release/acquire at
-// cluster scope orders the distributed shared-memory stores around it.
-DS4A_DEV void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// The shared::cluster address of local shared address `saddr` in CTA `rank`.
-DS4A_DEV uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-    return r;
-}
-DS4A_DEV void st_cluster_v2(uint32_t addr, float a, float b) {
-    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
-}
-DS4A_DEV void st_cluster_v4(uint32_t addr, float4 v) {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
-                 : "memory");
-}
-
 // What one work item covers: this CTA's piece of one unit.
 struct Item {
     int unit;            // 64-head sub-unit (q, out, lse); ru: its row-side unit
@@ -301,14 +268,6 @@ DS4A_DEV Sched make_sched(const AttnArgs &a, int nt, int g_rem) {
     Sched sc;
     const int G = gridDim.x, c = blockIdx.x;
     sc.nt = nt;
-    if (a.cluster) {                                   // one piece: this CTA's share of its cluster's unit
-        sc.R = 0;
-        sc.u_rem0 = 0;
-        sc.rs = sc.re = 0;
-        sc.v0 = 0;
-        sc.n_pieces = 1;
-        return sc;
-    }
     sc.R = a.units / G;
     sc.u_rem0 = sc.R * G;
     const long long t_rem = static_cast<long long>(a.units - sc.u_rem0) * nt;
@@ -331,12 +290,7 @@ DS4A_DEV Sched make_sched(const AttnArgs &a, int nt, int g_rem) {
 DS4A_DEV Item make_piece(const AttnArgs &a, const Sched &sc, int i) {
     Item m;
     int lt0 = 0, lt1 = sc.nt;
-    const bool cl = a.cluster != 0;
-    if (cl) {
-        m.unit = blockIdx.x / a.cluster;
-        m.split = false;
-        m.slot = 0;
-    } else if (i < sc.R) {
+    if (i < sc.R) {
         m.unit = blockIdx.x + i * gridDim.x;
         m.split = false;
         m.slot = 0;
@@ -368,15 +322,8 @@ DS4A_DEV Item make_piece(const AttnArgs &a, const Sched &sc, int i) {
         m.raw_row0 = static_cast<long long>(m.ru) * a.raw_per_unit;
     }
     m.ct = (m.cnt + TR - 1) / TR;
-    const int tiles = m.ct + (m.nrw + TR - 1) / TR;
-    if (cl) {
-        // share r of the unit's own tiles (contiguous, equal to within one)
-        const int r = static_cast<int>(blockIdx.x % a.cluster);
-        lt0 = r * tiles / a.cluster;
-        lt1 = (r + 1) * tiles / a.cluster;
-    }
     m.t0 = lt0;
-    m.t1 = min(tiles, lt1);
+    m.t1 = min(m.ct + (m.nrw + TR - 1) / TR, lt1);
     return m;
 }
 
@@ -391,101 +338,6 @@ DS4A_DEV void tmem_ld16x256_x8(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
           "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
-}
-
-// ---------------------------------------------------------- cluster merge
-// Called by every thread of every CTA of a cluster once its pipeline is done
-// (kept out of line: its registers do not weigh on the pipeline's).
-__device__ __noinline__ void cluster_merge(const AttnArgs &a, const Item &mi, uint8_t *smem, uint32_t tmem) {
-    uint8_t *sQ = smem + kOffQ;
-    uint8_t *sX = smem + kOffX;
-    uint8_t *sP = smem + kOffP;
-    const float2 *sML = reinterpret_cast<const float2 *>(smem + kOffML);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const float NEG_INF = -__int_as_float(0x7f800000);
-    // Every CTA of the cluster is past its pipeline, so the cluster's row,
-    // P and q buffers are free.  CTA r sends its (m, l) per head to every
-    // CTA and its unnormalised O^T slice [dims of CTA j][64 heads] to CTA
-    // j, which owns output dims [j * kClusterDims, (j + 1) * kClusterDims):
-    //   recvO  (row buffers)  fp32 [C][64 heads][kClusterDims]
-    //   recvML (P buffers)    (m, l) [C][64 heads]
-    // then each CTA merges its dims over the C partials by log-sum-exp.
-    cluster_sync_all();
-    const int C = a.cluster;
-    const uint32_t rank = cluster_rank();
-    const int unit = static_cast<int>(blockIdx.x) / C;
-    const uint32_t recv_o = smem_u32(sX), recv_ml = smem_u32(sP);
-    if (warp < kSoftmaxWarps) {
-        tc_fence_after();
-        const int h = warp * 32 + lane;
-        if (h < kNHead) {
-            const float2 ml = sML[h];
-            for (int j = 0; j < C; ++j)
-                st_cluster_v2(map_to_rank(recv_ml, static_cast<uint32_t>(j)) + (rank * kNHead + h) * 8u, ml.x, ml.y);
-        }
-        if (mi.t0 < mi.t1) {                          // CTA-uniform
-            // Warp w holds dims 128 (c / 2) + 32 w + lane of 32 heads per TMEM load
-            // (lane = dim); a [32 heads][32 dims] block goes through the warp's
-            // staging area (the q buffer is free) so that every remote store
-            // moves 16 bytes: lane l then holds 4 consecutive dims of one head.
-            const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-            float *stg = reinterpret_cast<float *>(sQ) + warp * 32 * 32;
-            for (int c = 0; c < 8; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_off + kTmemO + c * 32, v);
-                tmem_wait_ld(v);
-#pragma unroll
-                for (int k = 0; k < 32; ++k) stg[k * 32 + lane] = __uint_as_float(v[k]);
-                __syncwarp();
-                const int d0 = (c >> 1) * 128 + warp * 32;
-                const int owner = d0 / kClusterDims, dl0 = d0 - owner * kClusterDims;
-                const uint32_t b = map_to_rank(recv_o, static_cast<uint32_t>(owner)) +
-                                   ((rank * kNHead + (c & 1) * 32) * kClusterDims + dl0) * 4u;
-                const int dq = (lane & 7) * 4;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int hr = i * 4 + (lane >> 3);
-                    st_cluster_v4(b + (hr * kClusterDims + dq) * 4u,
-                                  *reinterpret_cast<const float4 *>(stg + hr * 32 + dq));
-                }
-                __syncwarp();
-            }
-        }
-        tc_fence_before();
-    }
-    cluster_sync_all();                                 // every partial delivered
-    const float *ro = reinterpret_cast<const float *>(sX);
-    const float2 *rml = reinterpret_cast<const float2 *>(sP);
-    float *wgt = reinterpret_cast<float *>(sQ) + 4 * 32 * 32;   // past the staging: [C][64] 2^(m_r - M), [64] 1/L
-    if (threadIdx.x < kNHead) {
-        const int h = threadIdx.x;
-        float M = NEG_INF;
-        for (int r = 0; r < C; ++r) {
-            const float2 ml = rml[r * kNHead + h];
-            if (ml.y > 0.f) M = fmaxf(M, ml.x);
-        }
-        float L = 0.f;
-        for (int r = 0; r < C; ++r) {
-            const float2 ml = rml[r * kNHead + h];
-            const float w = ml.y > 0.f ? exp2f(ml.x - M) : 0.f;
-            wgt[r * kNHead + h] = w;
-            L += w * ml.y;
-        }
-        wgt[C * kNHead + h] = L > 0.f ? 1.f / L : 0.f;
-        if (rank == 0 && a.lse)
-            a.lse[static_cast<long long>(unit) * kNHead + h] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : NEG_INF;
-    }
-    __syncthreads();
-    float *o = a.out + static_cast<long long>(unit) * kNHead * kHeadDim + rank * kClusterDims;
-    for (int i = threadIdx.x; i < kNHead * kClusterDims; i += blockDim.x) {
-        const int h = i / kClusterDims, dl = i - h * kClusterDims;
-        float acc = 0.f;
-        for (int r = 0; r < C; ++r) {
-            const float w = wgt[r * kNHead + h];
-            if (w != 0.f) acc += w * ro[(r * kNHead + h) * kClusterDims + dl];
-        }
-        o[static_cast<long long>(h) * kHeadDim + dl] = acc * wgt[C * kNHead + h];
-    }
 }
 
 template <int GW>
@@ -544,8 +396,6 @@ __global__ void __launch_bounds__(attn_threads(GW), 1) sparse_attn_kernel(const 
         if (a.tma_raw) tma_prefetch_desc(&a.tm_raw);
     }
     if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
-    if (a.cluster && threadIdx.x < kNHead)
-        reinterpret_cast<float2 *>(smem + kOffML)[threadIdx.x] = make_float2(-__int_as_float(0x7f800000), 0.f);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -554,9 +404,6 @@ __global__ void __launch_bounds__(attn_threads(GW), 1) sparse_attn_kernel(const 
     const Sched sc = make_sched(a, nt, g_rem);
     const int u_end = sc.n_pieces;               // pieces 0 .. n_pieces-1
     const long long n_slots = 2LL * gridDim.x;
-    // Cluster mode: per head, the piece's running max (log2 units; -inf when
-    // the head saw no row) and row sum, kept for the merge at the end.
-    float2 *sML = reinterpret_cast<float2 *>(smem + kOffML);
 
     if (warp >= kFirstGatherWarp) {
         // ------------------------------------------------------------ row gather
@@ -908,9 +755,7 @@ __global__ void __launch_bounds__(attn_threads(GW), 1) sparse_attn_kernel(const 
         for (int i = 0; ok && i < sc.n_pieces; ++i) {
             const Item m = make_piece(a, sc, i);
             if (m.t0 >= m.t1) {
-                // Empty row set: out = 0, lse = -inf (or an empty partial; in a
-                // cluster, nothing to send).
-                if (a.cluster) continue;
+                // Empty row set: out = 0, lse = -inf (or an empty partial).
                 if (!m.split) {
                     float *o = a.out + static_cast<long long>(m.unit) * kNHead * kHeadDim;
                     for (int k = e; k < kNHead * kHeadDim; k += kSoftmaxWarps * 32) o[k] = 0.f;
@@ -1081,15 +926,6 @@ __global__ void __launch_bounds__(attn_threads(GW), 1) sparse_attn_kernel(const 
             l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
             l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
             l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-            if (a.cluster) {
-                // O^T stays in TMEM for the cluster merge at the end (the values
-                // warp drains its GEMMs before it gets there).
-                if (t4 == 0) {
-                    sML[h0] = make_float2(l0 > 0.f ? M0 : NEG_INF, l0);
-                    sML[h1] = make_float2(l1 > 0.f ? M1 : NEG_INF, l1);
-                }
-                continue;
-            }
             const long long slot = m.slot;
             if (t4 == 0) {
 #pragma unroll
@@ -1144,7 +980,6 @@ __global__ void __launch_bounds__(attn_threads(GW), 1) sparse_attn_kernel(const 
 
     tc_fence_before();
     __syncthreads();
-    if (a.cluster) cluster_merge(a, make_piece(a, sc, 0), smem, tmem);
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -1244,7 +1079,6 @@ int attn_tiles_per_unit(int top_k) { return (top_k + TR - 1) / TR + (kNSwa + TR 
 }  // namespace
 
 size_t attn_ws_bytes(int units, int top_k) {
-    if (units <= kClusterMaxUnits) return 0;                // clusters merge in shared memory
     // Two partial slots per CTA; the grid never exceeds kMaxAttnCtas.
     const long long T = static_cast<long long>(units) * attn_tiles_per_unit(top_k);
     const long long G = T < kMaxAttnCtas ? T : kMaxAttnCtas;
@@ -1261,12 +1095,6 @@ cudaError_t launch_sparse_attn(const AttnArgs &a, int num_sms, cudaStream_t s) {
     const int nt = attn_tiles_per_unit(a.top_k);
     const long long T = static_cast<long long>(a.units) * nt;
     if (T <= 0) return cudaSuccess;
-    if (a.units <= kClusterMaxUnits) {
-        AttnArgs b = a;
-        b.cluster = kClusterCtas;
-        return launch_k_cluster(kern, dim3(static_cast<unsigned>(a.units * kClusterCtas)), dim3(attn_threads(gw)),
-                                kSmemBytes, kClusterCtas, s, b, nt, 0);
-    }
     long long G = num_sms < kMaxAttnCtas ? num_sms : kMaxAttnCtas;
     if (T < G) G = T;
     // Remainder units (after the whole rounds) in one-tile-or-larger shares

@@ -53,13 +53,14 @@ struct __align__(16) SelSmem {
     uint32_t cnt[4];                   // block counters
     uint32_t mm[2];                    // smallest and largest candidate key
     uint32_t warp_sums[32];
+    uint32_t uni[128];                 // the warps' largest sample keys (threshold estimate)
 };
 constexpr int kFastList = 1024;        // keys of the crossing bucket the one-warp search takes
 
-// Clears what select_from_list expects cleared (histogram 0, counters, key
-// range).  Every thread calls it; a __syncthreads must follow before use.
+// Clears what select_from_list expects cleared (counters, key range).  A
+// __syncthreads must follow before any thread uses them (the key-range fold
+// included).
 DS4A_DEV void sel_reset(SelSmem &S) {
-    for (int i = threadIdx.x; i < kDigitBins; i += blockDim.x) S.h[0][i] = 0u;
     if (threadIdx.x == 0) {
         S.cnt[0] = S.cnt[1] = S.cnt[2] = S.cnt[3] = 0u;
         S.mm[0] = 0xffffffffu;
@@ -179,33 +180,62 @@ DS4A_DEV uint32_t block_kth_key(Get get, uint32_t n, uint32_t k, SelSmem &S, uin
 }
 
 // Block-wide k-th largest key among the list keys c[0 .. nc) (nc >= k >= 1),
-// all in [kmin, kmax], by buckets fitted to that range: one block-wide
-// 256-bucket histogram of (key - kmin) >> s, with s the least shift that
-// leaves at most 256 buckets, finds the bucket holding the k-th key; its keys
-// are copied to `list` and one warp narrows the bucket by 8 bits per round
-// (a warp-private histogram) until it is one key wide.  Returns false (the
+// all in [kmin, kmax], by buckets fitted to that range: 32 buckets of
+// (key - kmin) >> s, s the least shift that leaves at most 32, counted by
+// ballots (no atomics), find the bucket holding the k-th key; its keys are
+// copied to `list` and one warp narrows the bucket by 8 bits per round (a
+// warp-private histogram) until it is one key wide.  Returns false (the
 // caller then takes block_kth_key) when the bucket holds more than kFastList
-// keys.  Expects S.h[0] and S.cnt[2] cleared (sel_reset).
+// keys.  Expects S.cnt[2] cleared (sel_reset).
 template <int NT>
 DS4A_DEV bool fast_kth(const uint2 *c, uint32_t nc, uint32_t k, uint32_t kmin, uint32_t kmax, uint32_t *list,
                        SelSmem &S, uint32_t *T_out, uint32_t *need_eq_out) {
+    constexpr int kWarps = NT / 32;
+    static_assert(kWarps <= 16, "warp counts live in the two digit histograms");
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t range = kmax - kmin;
-    const int s = range > 255u ? 24 - __clz(range) : 0;     // (range >> s) < 256
-    for (uint32_t i = threadIdx.x; i < nc; i += NT) atomicAdd(&S.h[0][(c[i].x - kmin) >> s], 1u);
+    const int s = range > 31u ? 27 - __clz(range) : 0;      // (range >> s) < 32
+    // 32 buckets counted without atomics: per 32 keys, five ballots of the
+    // bucket bits; lane b keeps the count of bucket b.
+    uint32_t mine = 0;
+    for (uint32_t i0 = warp * 32; i0 < nc; i0 += NT) {        // warp-uniform trip count
+        const uint32_t i = i0 + lane;
+        const bool v = i < nc;
+        const uint32_t b = v ? (c[i].x - kmin) >> s : 0u;
+        uint32_t match = __ballot_sync(0xffffffffu, v);
+#pragma unroll
+        for (int bit = 0; bit < 5; ++bit) {
+            const uint32_t m = __ballot_sync(0xffffffffu, (b >> bit) & 1u);
+            match &= ((lane >> bit) & 1) ? m : ~m;
+        }
+        mine += __popc(match);
+    }
+    uint32_t *wc = &S.h[0][0];                               // [kWarps][32] per-warp bucket counts
+    wc[warp * 32 + lane] = mine;
     __syncthreads();
-    if (threadIdx.x < 32) {
-        uint32_t above;
-        const int b = warp_find_bin(S.h[0], k, &above);
-        if (threadIdx.x == 0) {
-            S.bc[0] = static_cast<uint32_t>(b < 0 ? 0 : b);   // b < 0 cannot happen: nc >= k
-            S.bc[1] = b < 0 ? 0u : above;
+    if (warp == 0) {
+        uint32_t cnt = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) cnt += wc[w * 32 + lane];
+        uint32_t suf = cnt;                                  // keys in buckets >= lane
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t t = __shfl_down_sync(0xffffffffu, suf, off);
+            if (lane + off < 32) suf += t;
+        }
+        const uint32_t hit = __ballot_sync(0xffffffffu, suf >= k);
+        const int L = hit ? 31 - __clz(hit) : 0;             // hit != 0: nc >= k
+        const uint32_t above = __shfl_sync(0xffffffffu, suf - cnt, L);
+        if (lane == 0) {
+            S.bc[0] = static_cast<uint32_t>(L);
+            S.bc[1] = above;
         }
     }
     __syncthreads();
     const uint32_t b0 = S.bc[0];
     uint32_t need = k - S.bc[1];
     uint32_t lo = kmin + (b0 << s);
-    if (s == 0) {
+    if (s == 0) {                                            // one key per bucket
         *T_out = lo;
         *need_eq_out = need;
         return true;
@@ -218,10 +248,37 @@ DS4A_DEV bool fast_kth(const uint2 *c, uint32_t nc, uint32_t k, uint32_t kmin, u
     __syncthreads();
     const uint32_t L = S.cnt[2];
     if (L > static_cast<uint32_t>(kFastList)) return false;     // block-uniform
+    if (L <= static_cast<uint32_t>(NT)) {
+        // Few keys: thread i ranks key i against the whole bucket (16-byte
+        // loads every lane of a warp shares); the key with fewer than `need`
+        // larger keys and at least `need` at or above it is T.
+        if (threadIdx.x < L) {
+            const uint32_t v = list[threadIdx.x];
+            const uint4 *l4 = reinterpret_cast<const uint4 *>(list);
+            uint32_t gt = 0, ge = 0;
+            for (uint32_t j = 0; j < L / 4; ++j) {
+                const uint4 o = l4[j];
+                gt += (o.x > v) + (o.y > v) + (o.z > v) + (o.w > v);
+                ge += (o.x >= v) + (o.y >= v) + (o.z >= v) + (o.w >= v);
+            }
+            for (uint32_t j = L & ~3u; j < L; ++j) {
+                gt += list[j] > v;
+                ge += list[j] >= v;
+            }
+            if (gt < need && ge >= need) {                       // every such thread holds the same key
+                S.bc[2] = v;
+                S.bc[3] = need - gt;
+            }
+        }
+        __syncthreads();
+        *T_out = S.bc[2];
+        *need_eq_out = S.bc[3];
+        return true;
+    }
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
         uint32_t *h = S.h[1];
-        int cs = s;                                              // list keys of the bucket: key - lo < 2^cs
+        int cs = s;                                              // list keys of the bucket: key - lo < 2^cs (cs <= 27)
         while (cs > 0) {
             const int s2 = cs > 8 ? cs - 8 : 0;
             for (int i = lane; i < kDigitBins; i += 32) h[i] = 0u;
@@ -247,30 +304,6 @@ DS4A_DEV bool fast_kth(const uint2 *c, uint32_t nc, uint32_t k, uint32_t kmin, u
     *T_out = S.bc[2];
     *need_eq_out = S.bc[3];
     return true;
-}
-
-// Ascending bitonic sort of one value per lane across the warp.
-DS4A_DEV int32_t warp_sort32(int32_t x) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int k = 2; k <= 32; k <<= 1) {
-#pragma unroll
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            const int32_t y = __shfl_xor_sync(0xffffffffu, x, j);
-            const bool up = (lane & k) == 0 || k == 32;
-            const bool low = (lane & j) == 0;
-            x = (low == up) ? min(x, y) : max(x, y);
-        }
-    }
-    return x;
-}
-
-// Count of entries below e in a sorted run of 32 (shared memory).
-DS4A_DEV int run_lower_bound(const int32_t *run, int32_t e) {
-    int c = 0;
-#pragma unroll
-    for (int st = 16; st > 0; st >>= 1) c += run[c + st - 1] < e ? st : 0;
-    return c + (c == 31 && run[31] < e ? 1 : 0);
 }
 
 // Block-wide ascending sort of a[0 .. n_pow2) (n_pow2 a power of two).
@@ -312,32 +345,156 @@ DS4A_DEV uint32_t block_rank(bool pred, uint32_t *warp_sums /* 32 u32 smem */, u
     return before + __popc(m & ((1u << lane) - 1u));
 }
 
-// Writes the distinct rows sel[0 .. m) in ascending order to out[0 .. k)
-// with -1 padding, and the count.  sel must have room for the next power of
-// two >= max(m, 32).  Up to 1,024 rows: each warp sorts runs of 32 in
-// registers, then every row goes straight to its rank = its place in its run
-// plus, for every other run, the count of smaller rows (a binary search).
-DS4A_DEV void write_sorted(int32_t *sel, uint32_t m, uint32_t k, int32_t *out, int32_t *count_out) {
-    const int nt = blockDim.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// Writes the rows sel[0 .. m) (distinct, each < n_bound) in ascending order
+// to out[0 .. k) with -1 padding, and the count.  Rows below 65,536 with the
+// bitmap room below: the bitmap.  Otherwise up to 512 rows: each row's rank
+// by counting (sel 16-byte aligned).  Otherwise, when a bitmap of n_bound
+// bits fits bm (bm_words words of shared memory): the rows' bits are set,
+// the popcounts of each 32-word chunk summed and scanned, and every lane then
+// writes the set bits of one word at the place the chunk and lane prefixes
+// give (no sort; a handful of barriers).  Otherwise, up to 1,024 rows: a bitonic sort held in
+// registers (E = p2 / threads elements per thread, each warp owning whole
+// 32-element chunks), whose exchanges with partners less than 32 apart are
+// warp shuffles and the others go through shared memory (sel and tmp
+// alternating, one barrier per such stage).  Larger sets sort in sel in
+// place.  sel must have room for the next power of two >= max(m, 32) when m
+// > 1,024; tmp: shared int32 [1,024].
+DS4A_DEV void write_sorted(int32_t *sel, int32_t *tmp, uint32_t *bm, int bm_words, int n_bound, uint32_t m,
+                           uint32_t k, int32_t *out, int32_t *count_out) {
+    const int nt = blockDim.x;
+    const int words = (n_bound + 31) / 32, chunks = (words + 31) / 32;
+    const bool bitmap = m > 1 && chunks * 32 <= bm_words && chunks <= 1024;
+    if (m > 1 && m <= 512 && !(bitmap && chunks <= 64)) {
+        // Each row goes to its rank: the count of smaller rows, from 16-byte
+        // loads of sel that every lane of a warp shares (no barrier, no sort).
+        const int4 *s4 = reinterpret_cast<const int4 *>(sel);
+        const int m4 = static_cast<int>(m) >> 2;
+        for (uint32_t i = threadIdx.x; i < m; i += nt) {
+            const int32_t e = sel[i];
+            int r = 0;
+            for (int j = 0; j < m4; ++j) {
+                const int4 v = s4[j];
+                r += (v.x < e) + (v.y < e) + (v.z < e) + (v.w < e);
+            }
+            for (int j = 4 * m4; j < static_cast<int>(m); ++j) r += sel[j] < e;
+            out[r] = e;
+        }
+        for (uint32_t i = m + threadIdx.x; i < k; i += nt) out[i] = -1;
+        if (threadIdx.x == 0) *count_out = static_cast<int32_t>(m);
+        return;
+    }
+    if (bitmap) {
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = nt >> 5;
+        for (int i = threadIdx.x; i < chunks * 32; i += nt) bm[i] = 0u;
+        __syncthreads();
+        for (uint32_t i = threadIdx.x; i < m; i += nt) {
+            const int32_t r = sel[i];
+            if (r >= 0 && r < chunks * 1024) atomicOr(&bm[r >> 5], 1u << (r & 31));   // (always in range)
+        }
+        __syncthreads();
+        for (int ch = warp; ch < chunks; ch += nw) {
+            const uint32_t c = __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(__popc(bm[ch * 32 + lane])));
+            if (lane == 0) tmp[ch] = static_cast<int32_t>(c);
+        }
+        __syncthreads();
+        if (warp == 0) {                                     // exclusive scan of the chunk counts
+            const int per = (chunks + 31) / 32;
+            int32_t run = 0;
+            for (int j = 0; j < per; ++j) {
+                const int ch = lane * per + j;
+                run += ch < chunks ? tmp[ch] : 0;
+            }
+            int32_t incl = run;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int32_t t = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += t;
+            }
+            int32_t base = incl - run;
+            for (int j = 0; j < per; ++j) {
+                const int ch = lane * per + j;
+                if (ch < chunks) {
+                    const int32_t v = tmp[ch];
+                    tmp[ch] = base;
+                    base += v;
+                }
+            }
+        }
+        __syncthreads();
+        for (int ch = warp; ch < chunks; ch += nw) {
+            uint32_t w = bm[ch * 32 + lane];
+            const int32_t c = __popc(w);
+            int32_t incl = c;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int32_t t = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += t;
+            }
+            int32_t pos = tmp[ch] + incl - c;
+            const int32_t row0 = (ch * 32 + lane) * 32;
+            while (w) {
+                const int b = __ffs(w) - 1;
+                w &= w - 1;
+                if (pos < static_cast<int32_t>(k)) out[pos] = row0 + b;
+                ++pos;
+            }
+        }
+        for (uint32_t i = m + threadIdx.x; i < k; i += nt) out[i] = -1;
+        if (threadIdx.x == 0) *count_out = static_cast<int32_t>(m);
+        return;
+    }
     int p2 = 32;
     while (p2 < static_cast<int>(m)) p2 <<= 1;
-    for (int i = static_cast<int>(m) + threadIdx.x; i < p2; i += nt) sel[i] = 0x7fffffff;
-    __syncthreads();
     if (p2 > 1024) {
+        for (int i = static_cast<int>(m) + threadIdx.x; i < p2; i += nt) sel[i] = 0x7fffffff;
+        __syncthreads();
         block_bitonic_sort_asc(sel, p2);
         for (uint32_t i = threadIdx.x; i < k; i += nt) out[i] = i < m ? sel[i] : -1;
     } else {
-        const int runs = p2 / 32;
-        for (int r = warp; r < runs; r += nt / 32) sel[r * 32 + lane] = warp_sort32(sel[r * 32 + lane]);
-        __syncthreads();
-        for (int j = threadIdx.x; j < p2; j += nt) {
-            const int32_t e = sel[j];
-            if (e == 0x7fffffff) continue;                     // padding
-            const int r = j >> 5;
-            int pos = j & 31;
-            for (int q = 0; q < runs; ++q)
-                if (q != r) pos += run_lower_bound(sel + q * 32, e);
-            out[pos] = e;
+        constexpr int kMaxE = 4;                                 // 1,024 / 256 threads
+        const int E = p2 > nt ? p2 / nt : 1;
+        const bool active = static_cast<int>(threadIdx.x) < p2;  // warp-uniform (p2 >= 32)
+        int32_t x[kMaxE];
+#pragma unroll
+        for (int e = 0; e < kMaxE; ++e) {
+            const int i = threadIdx.x + e * nt;
+            x[e] = (e < E && active && i < static_cast<int>(m)) ? sel[i] : 0x7fffffff;
+        }
+        int cur = 0;
+        __syncthreads();                                         // every read of sel done
+        for (int k2 = 2; k2 <= p2; k2 <<= 1) {
+            for (int j = k2 >> 1; j > 0; j >>= 1) {
+                if (j >= 32) {
+                    int32_t *d = cur ? tmp : sel;
+                    cur ^= 1;
+#pragma unroll
+                    for (int e = 0; e < kMaxE; ++e)
+                        if (e < E && active) d[threadIdx.x + e * nt] = x[e];
+                    __syncthreads();
+#pragma unroll
+                    for (int e = 0; e < kMaxE; ++e) {
+                        if (e < E && active) {
+                            const int i = threadIdx.x + e * nt;
+                            const int32_t y = d[i ^ j];
+                            x[e] = (((i & j) == 0) == ((i & k2) == 0)) ? min(x[e], y) : max(x[e], y);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < kMaxE; ++e) {
+                        if (e < E) {                             // uniform
+                            const int i = threadIdx.x + e * nt;
+                            const int32_t y = __shfl_xor_sync(0xffffffffu, x[e], j);
+                            x[e] = (((i & j) == 0) == ((i & k2) == 0)) ? min(x[e], y) : max(x[e], y);
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < kMaxE; ++e) {
+            const int i = threadIdx.x + e * nt;
+            if (e < E && active && i < static_cast<int>(m)) out[i] = x[e];
         }
         for (uint32_t i = m + threadIdx.x; i < k; i += nt) out[i] = -1;
     }
@@ -351,13 +508,17 @@ DS4A_DEV void write_sorted(int32_t *sel, uint32_t m, uint32_t k, int32_t *out, i
 // largest key.  sel: shared int32 with room for the next power of two >= k
 // (and >= 32); list: shared u32 [kFastList].  Tied rows beyond kFastList are
 // resolved by an in-place compaction of their rows into c (read-write here).
+// bm / bm_words: shared memory free once the list has been read (the list's
+// own cache, when it is one) for the output bitmap; n_bound: rows are < it.
 template <int NT>
 DS4A_DEV void select_from_list(uint2 *c, uint32_t nc, uint32_t total, uint32_t k, int32_t *sel, uint32_t *list,
-                               SelSmem &S, int32_t *out, int32_t *count_out) {
+                               SelSmem &S, uint32_t *bm, int bm_words, int n_bound, int32_t *out,
+                               int32_t *count_out) {
     if (total <= k) {
         for (uint32_t i = threadIdx.x; i < nc; i += NT) sel[i] = static_cast<int32_t>(c[i].y);
         __syncthreads();
-        write_sorted(sel, nc < k ? nc : k, k, out, count_out);
+        write_sorted(sel, reinterpret_cast<int32_t *>(list), bm, bm_words, n_bound, nc < k ? nc : k, k, out,
+                     count_out);
         return;
     }
     uint32_t T, need_eq;
@@ -407,7 +568,7 @@ DS4A_DEV void select_from_list(uint2 *c, uint32_t nc, uint32_t total, uint32_t k
         for (uint32_t i = threadIdx.x; i < need_eq; i += NT) sel[n_gt + i] = tc[i];
     }
     __syncthreads();
-    write_sorted(sel, k, k, out, count_out);
+    write_sorted(sel, tie, bm, bm_words, n_bound, k, k, out, count_out);
 }
 
 // Exact selection over the whole row s[0 .. n) (global memory), whatever the
@@ -493,16 +654,25 @@ DS4A_DEV uint32_t sample_threshold(const float *__restrict__ s, int n, uint32_t 
     }
     const long long r_want = (static_cast<long long>(kSampleOver) * k * kSample + n - 1) / n;
     const int r = static_cast<int>(r_want < kSample ? r_want : kSample);
-    const int rw = min((r + kWarps - 1) / kWarps + 1, kPer * 32);
+    // rw = the wanted rank's share per warp and two more, so that the union of
+    // the warps' lists most likely holds the sample's r largest keys; when the
+    // union would not fit (short rows, large r), each warp takes its share
+    // and T0 is the smallest of the warps' last keys (a looser threshold).
+    constexpr int kUni = 128 / kWarps;
+    const int share = (r + kWarps - 1) / kWarps;
+    const bool use_union = share + 2 <= kUni;
+    const int rw = min(use_union ? share + 2 : share, kPer * 32);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t t = 0;
     for (int round = 0; round < rw; ++round) {
         uint32_t m = 0;
 #pragma unroll
         for (int j = 0; j < kPer; ++j) m = max(m, key[j]);
         t = __reduce_max_sync(0xffffffffu, m);
+        if (use_union && lane == 0) S.uni[warp * kUni + round] = t;
         if (t == 0u) break;                                   // warp-uniform
         const uint32_t holders = __ballot_sync(0xffffffffu, m == t);
-        if (static_cast<int>(threadIdx.x & 31) == __ffs(holders) - 1) {
+        if (lane == __ffs(holders) - 1) {
             bool done = false;
 #pragma unroll
             for (int j = 0; j < kPer; ++j) {
@@ -512,12 +682,33 @@ DS4A_DEV uint32_t sample_threshold(const float *__restrict__ s, int n, uint32_t 
             }
         }
     }
-    if ((threadIdx.x & 31) == 0) S.warp_sums[threadIdx.x >> 5] = t;
+    if (use_union && lane == 0)
+        for (int round = rw; round < kUni; ++round) S.uni[warp * kUni + round] = 0u;   // past a warp's visible keys
+    if (lane == 0) S.warp_sums[warp] = t;
+    if (threadIdx.x == 0) S.bc[3] = 0u;
     __syncthreads();
-    uint32_t T0 = 0xffffffffu;
+    uint32_t T0;
+    if (use_union) {
+        // the r-th largest of the union: the key with fewer than r larger
+        // keys and at least r at or above it (thread i ranks union entry i)
+        if (threadIdx.x < 128) {
+            const uint32_t v = S.uni[threadIdx.x];
+            uint32_t gt = 0, ge = 0;
+            for (int j = 0; j < 128; ++j) {
+                const uint32_t o = S.uni[j];
+                gt += o > v ? 1u : 0u;
+                ge += o >= v ? 1u : 0u;
+            }
+            if (v != 0u && gt < static_cast<uint32_t>(r) && ge >= static_cast<uint32_t>(r)) S.bc[3] = v;
+        }
+        __syncthreads();
+        T0 = S.bc[3];                                        // 0 when fewer than r visible sample keys
+    } else {
+        T0 = 0xffffffffu;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) T0 = min(T0, S.warp_sums[w]);
-    __syncthreads();                                         // S.warp_sums reusable after this
+        for (int w = 0; w < kWarps; ++w) T0 = min(T0, S.warp_sums[w]);
+    }
+    __syncthreads();                                         // S reusable after this
     return T0;
 }
 
@@ -647,7 +838,8 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 2 : 4) topk_row_kernel(const f
     __syncthreads();
     const bool decides = total <= k ? nc == total : (nc >= k && nc <= static_cast<uint32_t>(CAP));
     if (decides)
-        select_from_list<NT>(cand, nc, total, k, sel, list, S, out, count_out + row);
+        select_from_list<NT>(cand, nc, total, k, sel, list, S, reinterpret_cast<uint32_t *>(cand), 2 * CAP, n, out,
+                             count_out + row);
     else
         select_exact_row<NT>(s, n, k, S, out, count_out + row);
 }
@@ -710,13 +902,29 @@ __global__ void __launch_bounds__(kSplitThreads) topk_split_kernel(const __grid_
             for (int j = 0; j < B; ++j) {
                 const int i = 4 * (g0 + j * kSplitThreads + static_cast<int>(threadIdx.x));
                 const float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+                uint32_t key[4], bal[4], tot = 0;
+                bool take[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const bool vis = i + q < end && score_visible(f[q]);
-                    const uint32_t key = float_key(f[q]);
+                    key[q] = float_key(f[q]);
                     my_vis += vis ? 1u : 0u;
-                    warp_append<uint2>(queue, &S.cnt[3], cap, vis && key >= T0,
-                                       make_uint2(key, static_cast<uint32_t>(i + q)));
+                    take[q] = vis && key[q] >= T0;
+                    bal[q] = __ballot_sync(0xffffffffu, take[q]);
+                    tot += __popc(bal[q]);
+                }
+                if (tot) {                                    // warp-uniform: one shared atomic per float4
+                    const int lane = threadIdx.x & 31;
+                    uint32_t pos = 0;
+                    if (lane == 0) pos = atomicAdd(&S.cnt[3], tot);
+                    pos = __shfl_sync(0xffffffffu, pos, 0);
+                    const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t p = pos + __popc(bal[q] & lt);
+                        if (take[q] && p < cap) queue[p] = make_uint2(key[q], static_cast<uint32_t>(i + q));
+                        pos += __popc(bal[q]);
+                    }
                 }
             }
         }
@@ -803,20 +1011,36 @@ __global__ void __launch_bounds__(kSplitFinalThreads) topk_split_final_kernel(co
         // Join the slots: candidate g sits in the last slot c with base[c] <= g
         // (a binary search), so that all the copies are in flight at once.
         uint32_t kmn = 0xffffffffu, kmx = 0u;
-        for (uint32_t g = threadIdx.x; g < nc; g += kSplitFinalThreads) {
-            int lo = 0, hi = a.C;                         // base[lo] <= g < base[hi]
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (base[mid] <= g) lo = mid; else hi = mid;
+        constexpr int J = 4;                              // candidates per thread in flight
+        for (uint32_t g0 = 0; g0 < nc; g0 += J * kSplitFinalThreads) {
+            uint2 e[J];
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                const uint32_t g = g0 + j * kSplitFinalThreads + threadIdx.x;
+                e[j] = make_uint2(0u, 0u);
+                if (g < nc) {
+                    int lo = 0, hi = a.C;                 // base[lo] <= g < base[hi]
+                    while (hi - lo > 1) {
+                        const int mid = (lo + hi) >> 1;
+                        if (base[mid] <= g) lo = mid; else hi = mid;
+                    }
+                    e[j] = a.cand[(row * a.C + lo) * static_cast<long long>(a.slot) + (g - base[lo])];
+                }
             }
-            const uint2 e = a.cand[(row * a.C + lo) * static_cast<long long>(a.slot) + (g - base[lo])];
-            cache[g] = e;
-            kmn = min(kmn, e.x);
-            kmx = max(kmx, e.x);
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                const uint32_t g = g0 + j * kSplitFinalThreads + threadIdx.x;
+                if (g < nc) {
+                    cache[g] = e[j];
+                    kmn = min(kmn, e[j].x);
+                    kmx = max(kmx, e[j].x);
+                }
+            }
         }
         warp_fold_minmax(kmn, kmx, S);
         __syncthreads();
-        select_from_list<kSplitFinalThreads>(cache, nc, total, k, sel, list, S, out, a.count + row);
+        select_from_list<kSplitFinalThreads>(cache, nc, total, k, sel, list, S, reinterpret_cast<uint32_t *>(cache),
+                                             2 * kSplitCache, n, out, a.count + row);
     } else {
         select_exact_row<kSplitFinalThreads>(a.scores + row * a.N_cap, n, k, S, out, a.count + row);
     }
@@ -854,7 +1078,7 @@ constexpr int kCandThreads = 512;
 // 6,144 cached candidates (48 KB) let three CTAs share an SM.
 constexpr int kCandCache = 6144;
 
-__global__ void __launch_bounds__(kCandThreads) topk_cand_kernel(const __grid_constant__ TopkCandArgs a) {
+__global__ void __launch_bounds__(kCandThreads, 3) topk_cand_kernel(const __grid_constant__ TopkCandArgs a) {
     pdl_launch_dependents();
     pdl_wait();
     extern __shared__ __align__(16) uint8_t cand_smem[];
@@ -863,6 +1087,7 @@ __global__ void __launch_bounds__(kCandThreads) topk_cand_kernel(const __grid_co
     uint32_t *list = reinterpret_cast<uint32_t *>(cand_smem + kCandCache * 8 + kMaxTopK * 4);   // [kFastList]
     SelSmem &S = *reinterpret_cast<SelSmem *>(cand_smem + kCandCache * 8 + kMaxTopK * 4 + kFastList * 4);
     sel_reset(S);
+    __syncthreads();                                  // S.mm set before any warp folds its keys into it
     const long long row = blockIdx.x;
     const uint32_t k = static_cast<uint32_t>(a.top_k);
     uint32_t nc = a.cand_n[row];
@@ -882,8 +1107,8 @@ __global__ void __launch_bounds__(kCandThreads) topk_cand_kernel(const __grid_co
     }
     warp_fold_minmax(kmn, kmx, S);
     __syncthreads();
-    select_from_list<kCandThreads>(cached ? cache : gc, nc, total, k, sel, list, S, a.idx + row * a.top_k,
-                                   a.count + row);
+    select_from_list<kCandThreads>(cached ? cache : gc, nc, total, k, sel, list, S, reinterpret_cast<uint32_t *>(cache),
+                                   cached ? 2 * kCandCache : 0, a.N_cap, a.idx + row * a.top_k, a.count + row);
 }
 
 }  // namespace

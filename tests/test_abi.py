@@ -61,17 +61,13 @@ def test_workspace_sizes():
     assert B.ds4a_workspace_bytes(B.DS4A_OP_TOPK_SELECT, 1, 1, 1 << 24, 2048) <= 152 * slot
     # Attention: two partial slots (64 x (512 + 2) fp32) per share, at most
     # 160 shares, at most one share per 64-row tile (10 tiles per unit at k = 512).
-    # Up to 16 64-head sub-units run as thread-block clusters that merge in
-    # shared memory: no workspace.
     slot = 64 * 514 * 4
     assert B.ds4a_workspace_bytes(B.DS4A_OP_SPARSE_ATTN_DECODE, 1376, 1, 65536, 512) == 2 * 160 * slot
-    assert B.ds4a_workspace_bytes(B.DS4A_OP_SPARSE_ATTN_DECODE, 4, 1, 262144, 512) == 0
-    assert B.ds4a_workspace_bytes(B.DS4A_OP_SPARSE_ATTN_DECODE, 16, 1, 65536, 512) == 0
+    assert B.ds4a_workspace_bytes(B.DS4A_OP_SPARSE_ATTN_DECODE, 4, 1, 262144, 512) == 2 * 40 * slot
     assert B.ds4a_workspace_bytes(B.DS4A_OP_SPARSE_ATTN_DECODE, 17, 1, 65536, 512) == 2 * 160 * slot  # 170 tiles
     assert B.ds4a_workspace_bytes(B.DS4A_OP_SPARSE_ATTN_PREFILL, 1, 2048, 66048, 512) == 2 * 160 * slot
-    assert B.ds4a_workspace_bytes(B.DS4A_OP_DENSE_ATTN_DECODE, 1, 1, 64, 0) == 0
-    assert B.ds4a_workspace_bytes(B.DS4A_OP_DENSE_ATTN_DECODE | B.DS4A_OP_FLAG_128_HEADS, 8, 1, 8192, 0) == 0
-    assert B.ds4a_workspace_bytes(B.DS4A_OP_DENSE_ATTN_DECODE | B.DS4A_OP_FLAG_128_HEADS, 9, 1, 8192, 0) == 2 * 160 * slot
+    assert B.ds4a_workspace_bytes(B.DS4A_OP_DENSE_ATTN_DECODE, 1, 1, 64, 0) == 2 * 3 * slot    # 1 + 2 tiles
+    assert B.ds4a_workspace_bytes(B.DS4A_OP_DENSE_ATTN_DECODE | B.DS4A_OP_FLAG_128_HEADS, 3, 1, 8192, 0) == 2 * 160 * slot
     with pytest.raises(ValueError):
         B.ds4a_workspace_bytes(B.DS4A_OP_TOPK_SELECT, 1, 1, 10, 4096)
     with pytest.raises(ValueError):
@@ -127,7 +123,7 @@ def test_attention_rejects_bad_arguments(lib):
     assert d(*bad) == B.DS4A_EINVAL
     bad = list(args); bad[10] = ctypes.c_float(float("nan"))
     assert d(*bad) == B.DS4A_EINVAL
-    bad = list(args); bad[13] = 20                      # 20 units need split workspace
+    bad = list(args); bad[13] = 4                       # 4 units need split workspace
     bad[2] = 512 * 64
     assert d(*bad) == B.DS4A_EWORKSPACE
     p = lib.ds4a_sparse_attn_prefill

@@ -372,16 +372,16 @@ def test_attention_one_cta_per_unit(q_scale):
 def test_attention_work_schedule(U, top_k):
     # Whole strided rounds of 152 units, then the remainder units' tiles cut
     # into equal shares: no remainder, one remainder unit over ten CTAs, three-
-    # tile units, fewer units than CTAs (pieces merged by a second kernel);
-    # up to 16 units: one cluster of eight CTAs per unit, merged in shared
-    # memory (one and two tiles per CTA, three-tile units on eight CTAs).
+    # tile units, and fewer units than CTAs (pieces merged by a second kernel:
+    # one-tile pieces, shares of several tiles, a single unit over ten CTAs).
     attention_case(U, 600, top_k, seed=40 + U)
 
 
 @pytest.mark.parametrize("U", [2, 20])
 def test_attention_largest_top_k_in_many_pieces(U):
-    # top_k = 2,048: 34 tiles per unit.  Two units: clusters of eight CTAs,
-    # four or five tiles each; twenty units: 680 tiles in 152 shares, merged.
+    # top_k = 2,048: 34 tiles per unit.  Two units: 68 one-tile pieces, 34 per
+    # unit (the most pieces a unit can have); twenty units: 680 tiles in 152
+    # shares, merged.
     attention_case(U, 2500, 2048, seed=47 + U)
 
 
@@ -599,8 +599,7 @@ def test_dense_attention_small_ragged(q_scale):
 @pytest.mark.parametrize("U", [3, 24])
 def test_dense_attention_few_units_split_rows(U):
     # fewer units than SMs: each unit's rows are split over several CTAs and
-    # merged (3 units: one cluster each, merged in shared memory; 24 units:
-    # shares of the persistent CTAs, merged by a second kernel)
+    # merged by a second kernel (3 and 24 units)
     n_rows = ([6000, 4500, 129] * 8)[:U]
     n_raw = ([128, 0, 5] * 8)[:U]
     x, out, lse = dense_case(U, 6000, n_rows, n_raw, seed=32)
