@@ -59,14 +59,15 @@ inline size_t indexer_topk_ws_bytes(long long R, int N_cap) {
     return static_cast<size_t>(R) * N_cap * 8 + static_cast<size_t>(R) * 12;
 }
 constexpr int kTopkCandMaxRows = 1 << 20;   // N_cap limit of the candidate path (its row bitmap)
-// Few long rows: each row is cut over at least two CTAs (at most
+// Very long rows (more than kTopkSplitMinRow scores) in batches of up to
+// kTopkSplitMaxCtas / 2 rows: each row is cut over at least two CTAs (at most
 // kTopkSplitMaxCtas in all, one wave on GB300's 152 SMs), each with a
-// candidate slot of at most kTopkSplitSlot entries; rows of at most
-// kTopkRowMaxShortRow scores, and batches of more than kTopkSplitMaxCtas / 2
-// rows, take one CTA per row.
+// candidate slot of at most kTopkSplitSlot entries in the workspace, then one
+// CTA per row selects.  Shorter rows need no workspace (a cluster of CTAs per
+// row for a few rows, one CTA per row otherwise).
 constexpr int kTopkSplitMaxCtas = 152;
 constexpr int kTopkSplitSlot = 4096;
-constexpr int kTopkRowMaxShortRow = 32768;
+constexpr int kTopkSplitMinRow = 1 << 19;
 struct TopkArgs {
     const float *scores;
     const int32_t *n_rows;

@@ -46,7 +46,7 @@ extern "C" ds4a_status ds4a_topk_select_noalloc(const float *scores, const int32
     if (U < 1 || Q < 1 || N_cap < 1 || top_k < 1 || top_k > DS4A_MAX_TOP_K) return DS4A_EINVAL;
     if (static_cast<long long>(U) * Q > (1LL << 24)) return DS4A_EINVAL;
     if ((reinterpret_cast<uintptr_t>(scores) & 3) != 0) return DS4A_EINVAL;
-    // Only few long rows use scratch (at most about 5 MB, whatever the
+    // Only few very long rows use scratch (at most about 5 MB, whatever the
     // sizes); the check guards the fixed array should that ever change.
     const size_t need = topk_ws_bytes(static_cast<long long>(U) * Q, N_cap);
     if (need > DS4A_TOPK_NOALLOC_SCRATCH_BYTES) return DS4A_EWORKSPACE;   // nothing launched

@@ -18,14 +18,17 @@
 // of them.  Otherwise (a sample that missed, heavy ties) the same digits are
 // taken over the whole row, which is exact whatever the scores.
 //
-// Three launch shapes:
-//   topk_row_kernel         one CTA per row: batches of more than 76 rows
-//                           (decode batches, prefill chunks) and any batch of
-//                           rows of at most 32,768 scores;
-//   topk_split_kernel +     few long rows (long-context decode): C CTAs per row
-//   topk_split_final_kernel each filter a chunk of the row against the same T0
-//                           into a candidate slot of their own; then one CTA
-//                           per row selects from the row's slots;
+// Four launch shapes:
+//   topk_cluster_kernel     up to 16 rows of 4,097 .. 524,288 scores (long-
+//                           context and small decode batches): a cluster of
+//                           eight CTAs per row, the selection agreed through
+//                           distributed shared memory;
+//   topk_split_kernel +     up to 76 rows of more than 524,288 scores: C CTAs
+//   topk_split_final_kernel per row each filter a chunk of the row against the
+//                           same T0 into a candidate slot of their own in the
+//                           workspace; then one CTA per row selects;
+//   topk_row_kernel         one CTA per row: everything else (decode batches,
+//                           prefill chunks, short rows);
 //   topk_cand_kernel        the candidate lists of the fused indexer scan.
 #include "common.cuh"
 #include "internal.h"
@@ -1046,6 +1049,359 @@ __global__ void __launch_bounds__(kSplitFinalThreads) topk_split_final_kernel(co
     }
 }
 
+// ---------------------------------------------------------------- few rows: one cluster per row
+// For up to kClusterMaxRows rows of more than kClusterMinRow scores: a
+// thread-block cluster of kClusterRowCtas CTAs per row.  CTA q filters chunk q
+// of the row against the row's sampled threshold T0 (every CTA derives the
+// same T0 from the same sample) into a candidate list in its own shared
+// memory.  The CTAs then exchange what the exact selection needs through
+// distributed shared memory, each CTA storing its part into every CTA of the
+// cluster, so that every CTA reads only its own shared memory and takes the
+// same decisions:
+//   1. per CTA: candidate count, visible count, smallest and largest key;
+//   2. per CTA: 32-bucket histogram of its candidates over the row's key range;
+//   3. per CTA: the keys of the bucket holding the k-th key, in CTA order.
+// Every CTA then knows the k-th key T, how many keys equal to T the selection
+// takes and, for every CTA, how many rows it contributes: CTA q writes its
+// rows above T and its share of the ties (lowest rows first: the chunks are in
+// row order) in ascending order at its offset.  A row the lists cannot decide
+// (a sample that missed, heavy ties) is selected by CTA 0 alone from the
+// row's scores.  No global scratch; three cluster barriers.
+constexpr int kClusterRowCtas = 8;
+constexpr int kClusterThreads = 512;
+constexpr int kClusterCap = 4096;          // candidates per CTA
+constexpr int kClusterMaxRows = 16;       // more rows: one CTA per row is as fast
+constexpr int kClusterMinRow = 4096;       // rows up to this long: one CTA per row (every row a candidate)
+constexpr int kClusterAllBelow = 8192;     // rows up to this long need no sampled threshold
+
+struct __align__(16) ClusterSmem {
+    uint2 cand[kClusterCap];
+    int32_t sel[kMaxTopK];
+    int32_t tie[kFastList];
+    uint32_t list[kFastList];              // the crossing bucket's keys of every CTA, CTA-ordered
+    uint32_t stat[kClusterRowCtas][4];     // per CTA: candidates, visible rows, smallest key, largest key
+    uint32_t hist[kClusterRowCtas][32];    // per CTA: bucket counts
+    uint32_t seg[kClusterRowCtas][2];      // per CTA: crossing-bucket rows above T, rows equal to T
+    uint32_t warp_cnt[kClusterThreads / 32][32];
+    SelSmem S;
+};
+
+// Each of sel[0 .. m) (distinct rows) to out[base + its rank among them].
+DS4A_DEV void rank_write(const int32_t *sel, uint32_t m, int32_t *out) {
+    const int4 *s4 = reinterpret_cast<const int4 *>(sel);
+    const int m4 = static_cast<int>(m) >> 2;
+    for (uint32_t i = threadIdx.x; i < m; i += blockDim.x) {
+        const int32_t e = sel[i];
+        int r = 0;
+        for (int j = 0; j < m4; ++j) {
+            const int4 v = s4[j];
+            r += (v.x < e) + (v.y < e) + (v.z < e) + (v.w < e);
+        }
+        for (int j = 4 * m4; j < static_cast<int>(m); ++j) r += sel[j] < e;
+        out[r] = e;
+    }
+}
+
+__global__ void __launch_bounds__(kClusterThreads) topk_cluster_kernel(const __grid_constant__ TopkArgs a, int chunk) {
+    pdl_launch_dependents();
+    pdl_wait();
+    extern __shared__ __align__(16) uint8_t cl_smem[];
+    ClusterSmem &M = *reinterpret_cast<ClusterSmem *>(cl_smem);
+    SelSmem &S = M.S;
+    constexpr int C = kClusterRowCtas, NT = kClusterThreads, NW = NT / 32;
+    const uint32_t q = cluster_rank();
+    const long long row = blockIdx.x / C;
+    const int u = static_cast<int>(row / a.Q);
+    const int n = row_len(a.n_rows, u, a.N_cap);
+    if (q == 0 && threadIdx.x == 0 && row % a.Q == 0 && (a.n_rows[u] < 0 || a.n_rows[u] > a.N_cap))
+        report(a.status, DS4A_DEV_BOUNDS);
+    const float *s = a.scores + row * a.N_cap;
+    const uint32_t k = static_cast<uint32_t>(a.top_k);
+    int32_t *out = a.idx + row * a.top_k;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int start = static_cast<int>(q) * chunk;          // chunk is a multiple of 4
+    const int end = min(start + chunk, n);
+    const bool vec4 = (a.N_cap & 3) == 0;
+    constexpr int B = 4;
+    const int g_beg = start / 4, g_end = end > start ? (end + 3) / 4 : g_beg;
+    float4 v[B];
+    auto load = [&](int g0) {
+#pragma unroll
+        for (int j = 0; j < B; ++j) {
+            const int g = g0 + j * NT + static_cast<int>(threadIdx.x);
+            v[j] = g < g_end ? __ldg(reinterpret_cast<const float4 *>(s) + g) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+    if (vec4) load(g_beg);                                    // in flight during the sample
+    const uint32_t T0 = sample_threshold<NT, kSampleSplit>(s, n, k, kClusterAllBelow, S);
+    sel_reset(S);
+    __syncthreads();
+    // ---- the chunk against T0: candidates, visible count, key range
+    uint32_t my_vis = 0, kmn = 0xffffffffu, kmx = 0u;
+    if (vec4) {
+        for (int g0 = g_beg; g0 < g_end; g0 += B * NT) {     // block-uniform
+            if (g0 != g_beg) load(g0);
+#pragma unroll
+            for (int j = 0; j < B; ++j) {
+                const int i = 4 * (g0 + j * NT + static_cast<int>(threadIdx.x));
+                const float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+                uint32_t key[4], bal[4], tot = 0;
+                bool take[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const bool vis = i + c < end && score_visible(f[c]);
+                    key[c] = float_key(f[c]);
+                    my_vis += vis ? 1u : 0u;
+                    take[c] = vis && key[c] >= T0;
+                    kmn = take[c] ? min(kmn, key[c]) : kmn;
+                    kmx = take[c] ? max(kmx, key[c]) : kmx;
+                    bal[c] = __ballot_sync(0xffffffffu, take[c]);
+                    tot += __popc(bal[c]);
+                }
+                if (tot) {                                    // warp-uniform: one shared atomic per float4
+                    uint32_t pos = 0;
+                    if (lane == 0) pos = atomicAdd(&S.cnt[3], tot);
+                    pos = __shfl_sync(0xffffffffu, pos, 0);
+                    const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t p = pos + __popc(bal[c] & lt);
+                        if (take[c] && p < static_cast<uint32_t>(kClusterCap))
+                            M.cand[p] = make_uint2(key[c], static_cast<uint32_t>(i + c));
+                        pos += __popc(bal[c]);
+                    }
+                }
+            }
+        }
+    } else {
+        for (int b = start; b < end; b += NT) {              // block-uniform
+            const int i = b + static_cast<int>(threadIdx.x);
+            const float f = i < end ? s[i] : 0.f;
+            const bool vis = i < end && score_visible(f);
+            const uint32_t key = float_key(f);
+            my_vis += vis ? 1u : 0u;
+            const bool take = vis && key >= T0;
+            kmn = take ? min(kmn, key) : kmn;
+            kmx = take ? max(kmx, key) : kmx;
+            warp_append<uint2>(M.cand, &S.cnt[3], kClusterCap, take, make_uint2(key, static_cast<uint32_t>(i)));
+        }
+    }
+    warp_fold_minmax(kmn, kmx, S);
+    {
+        const uint32_t t = __reduce_add_sync(0xffffffffu, my_vis);
+        if (lane == 0) S.warp_sums[warp] = t;
+    }
+    __syncthreads();
+    const uint32_t nc_q = S.cnt[3];
+    // ---- 1. counts and key range to every CTA
+    if (threadIdx.x < C) {
+        uint32_t vis_q = 0;
+        for (int w = 0; w < NW; ++w) vis_q += S.warp_sums[w];
+        const uint32_t b = smem_u32(&M.stat[q][0]);
+        st_cluster_u32(b, threadIdx.x, nc_q);
+        st_cluster_u32(b + 4, threadIdx.x, vis_q);
+        st_cluster_u32(b + 8, threadIdx.x, S.mm[0]);
+        st_cluster_u32(b + 12, threadIdx.x, S.mm[1]);
+    }
+    cluster_sync_all();                                       // (1 of 3)
+    uint32_t nc = 0, total = 0, kmin = 0xffffffffu, kmax = 0u, below_q = 0;
+    bool overflow = false;
+#pragma unroll
+    for (int j = 0; j < C; ++j) {
+        const uint32_t cj = M.stat[j][0];
+        overflow |= cj > static_cast<uint32_t>(kClusterCap);
+        if (j < static_cast<int>(q)) below_q += cj;
+        nc += cj;
+        total += M.stat[j][1];
+        kmin = min(kmin, M.stat[j][2]);
+        kmax = max(kmax, M.stat[j][3]);
+    }
+    const bool decides = !overflow && (total <= k ? nc == total : nc >= k);
+    if (!decides) {                                           // every CTA of the cluster agrees
+        cluster_sync_all();
+        cluster_sync_all();
+        if (q == 0) select_exact_row<NT>(s, n, k, S, out, a.count + row);
+        return;
+    }
+    if (total <= k) {
+        // every visible row is a candidate: CTA q's rows, ascending, after those of CTAs 0 .. q-1
+        for (uint32_t i = threadIdx.x; i < nc_q; i += NT) M.sel[i] = static_cast<int32_t>(M.cand[i].y);
+        __syncthreads();
+        rank_write(M.sel, nc_q, out + below_q);
+        if (q == 0) {
+            for (uint32_t i = total + threadIdx.x; i < k; i += NT) out[i] = -1;
+            if (threadIdx.x == 0) a.count[row] = static_cast<int32_t>(total);
+        }
+        cluster_sync_all();
+        cluster_sync_all();
+        return;
+    }
+    // ---- 2. 32-bucket histogram of the candidates over [kmin, kmax], to every CTA
+    const uint32_t range = kmax - kmin;
+    const int sh = range > 31u ? 27 - __clz(range) : 0;      // (range >> sh) < 32
+    {
+        uint32_t mine = 0;
+        for (uint32_t i0 = warp * 32; i0 < nc_q; i0 += NT) {  // warp-uniform trip count
+            const uint32_t i = i0 + lane;
+            const bool ok = i < nc_q;
+            const uint32_t bk = ok ? (M.cand[i].x - kmin) >> sh : 0u;
+            uint32_t match = __ballot_sync(0xffffffffu, ok);
+#pragma unroll
+            for (int bit = 0; bit < 5; ++bit) {
+                const uint32_t mb = __ballot_sync(0xffffffffu, (bk >> bit) & 1u);
+                match &= ((lane >> bit) & 1) ? mb : ~mb;
+            }
+            mine += __popc(match);
+        }
+        M.warp_cnt[warp][lane] = mine;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t cb = 0;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) cb += M.warp_cnt[w][lane];
+        const uint32_t b = smem_u32(&M.hist[q][lane]);
+#pragma unroll
+        for (int j = 0; j < C; ++j) st_cluster_u32(b, j, cb);
+    }
+    cluster_sync_all();                                       // (2 of 3)
+    if (warp == 0) {
+        uint32_t tb = 0;
+#pragma unroll
+        for (int j = 0; j < C; ++j) tb += M.hist[j][lane];
+        uint32_t suf = tb;                                    // keys in buckets >= lane
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t t = __shfl_down_sync(0xffffffffu, suf, off);
+            if (lane + off < 32) suf += t;
+        }
+        const uint32_t hit = __ballot_sync(0xffffffffu, suf >= k);
+        const int bb = hit ? 31 - __clz(hit) : 0;             // hit != 0: nc >= k
+        const uint32_t above = __shfl_sync(0xffffffffu, suf - tb, bb);
+        if (lane == 0) {
+            S.bc[0] = static_cast<uint32_t>(bb);
+            S.bc[1] = above;
+        }
+    }
+    __syncthreads();
+    const uint32_t b0 = S.bc[0];
+    const uint32_t need = k - S.bc[1];
+    uint32_t L = 0, off_q = 0;
+#pragma unroll
+    for (int j = 0; j < C; ++j) {
+        if (j < static_cast<int>(q)) off_q += M.hist[j][b0];
+        L += M.hist[j][b0];
+    }
+    if (L > static_cast<uint32_t>(kFastList)) {               // every CTA agrees
+        cluster_sync_all();
+        if (q == 0) select_exact_row<NT>(s, n, k, S, out, a.count + row);
+        return;
+    }
+    // ---- 3. the crossing bucket's keys, CTA q's at [off_q, off_q + hist[q][b0]), to every CTA
+    if (sh > 0) {
+        for (uint32_t i0 = 0; i0 < nc_q; i0 += NT) {          // block-uniform trip count
+            const uint32_t i = i0 + threadIdx.x;
+            const uint32_t key = i < nc_q ? M.cand[i].x : 0u;
+            const bool in = i < nc_q && ((key - kmin) >> sh) == b0;
+            const uint32_t bal = __ballot_sync(0xffffffffu, in);
+            if (bal == 0u) continue;
+            uint32_t p = 0;
+            if (lane == 0) p = atomicAdd(&S.cnt[2], static_cast<uint32_t>(__popc(bal)));
+            p = __shfl_sync(0xffffffffu, p, 0) + __popc(bal & ((1u << lane) - 1u));
+            if (in) {
+                const uint32_t b = smem_u32(&M.list[off_q + p]);
+#pragma unroll
+                for (int j = 0; j < C; ++j) st_cluster_u32(b, j, key);
+            }
+        }
+    }
+    cluster_sync_all();                                       // (3 of 3): no shared memory of another CTA is touched after this
+    // ---- T, how many ties the selection takes, and every CTA's rows
+    uint32_t T, need_eq;
+    if (sh == 0) {                                            // one key per bucket
+        T = kmin + b0;
+        need_eq = need;
+    } else {
+        for (uint32_t i = threadIdx.x; i < L; i += NT) {
+            const uint32_t vi = M.list[i];
+            const uint4 *l4 = reinterpret_cast<const uint4 *>(M.list);
+            uint32_t gt = 0, ge = 0;
+            for (uint32_t j = 0; j < L / 4; ++j) {
+                const uint4 o = l4[j];
+                gt += (o.x > vi) + (o.y > vi) + (o.z > vi) + (o.w > vi);
+                ge += (o.x >= vi) + (o.y >= vi) + (o.z >= vi) + (o.w >= vi);
+            }
+            for (uint32_t j = L & ~3u; j < L; ++j) {
+                gt += M.list[j] > vi;
+                ge += M.list[j] >= vi;
+            }
+            if (gt < need && ge >= need) {                    // every such thread holds the same key
+                S.bc[2] = vi;
+                S.bc[3] = need - gt;
+            }
+        }
+        __syncthreads();
+        T = S.bc[2];
+        need_eq = S.bc[3];
+    }
+    // crossing-bucket rows above T and equal to T of each CTA (warp j: segment j)
+    if (warp < C) {
+        uint32_t o = 0;
+        for (int j = 0; j < warp; ++j) o += M.hist[j][b0];
+        const uint32_t cnt = M.hist[warp][b0];
+        uint32_t g = 0, e = 0;
+        for (uint32_t i = lane; i < cnt; i += 32) {
+            const uint32_t key = sh == 0 ? T : M.list[o + i];
+            g += key > T;
+            e += key == T;
+        }
+        g = __reduce_add_sync(0xffffffffu, g);
+        e = __reduce_add_sync(0xffffffffu, e);
+        if (lane == 0) {
+            M.seg[warp][0] = g;
+            M.seg[warp][1] = e;
+        }
+    }
+    __syncthreads();
+    uint32_t out_q = 0, ties_before = 0, gt_q = 0, eq_q = 0, taken_q = 0;
+#pragma unroll
+    for (int j = 0; j < C; ++j) {
+        uint32_t gj = M.seg[j][0];
+        for (uint32_t b = b0 + 1; b < 32; ++b) gj += M.hist[j][b];
+        const uint32_t ej = M.seg[j][1];
+        const uint32_t left = need_eq > ties_before ? need_eq - ties_before : 0u;
+        const uint32_t tj = min(ej, left);
+        if (j < static_cast<int>(q)) out_q += gj + tj;
+        if (j == static_cast<int>(q)) {
+            gt_q = gj;
+            eq_q = ej;
+            taken_q = tj;
+        }
+        ties_before += ej;
+    }
+    // ---- CTA q's rows: above T, and its share of the ties (its lowest rows)
+    for (uint32_t i0 = 0; i0 < nc_q; i0 += NT) {              // block-uniform trip count
+        const uint32_t i = i0 + threadIdx.x;
+        const uint2 e = i < nc_q ? M.cand[i] : make_uint2(0u, 0u);
+        warp_append<int32_t>(M.sel, &S.cnt[0], k, i < nc_q && e.x > T, static_cast<int32_t>(e.y));
+        warp_append<int32_t>(M.tie, &S.cnt[1], kFastList, i < nc_q && e.x == T, static_cast<int32_t>(e.y));
+    }
+    __syncthreads();
+    if (taken_q == eq_q) {
+        for (uint32_t i = threadIdx.x; i < eq_q; i += NT) M.sel[gt_q + i] = M.tie[i];
+    } else {
+        int p2 = 1;
+        while (p2 < static_cast<int>(eq_q)) p2 <<= 1;
+        for (int i = static_cast<int>(eq_q) + threadIdx.x; i < p2; i += NT) M.tie[i] = 0x7fffffff;
+        __syncthreads();
+        block_bitonic_sort_asc(M.tie, p2);
+        for (uint32_t i = threadIdx.x; i < taken_q; i += NT) M.sel[gt_q + i] = M.tie[i];
+    }
+    __syncthreads();
+    rank_write(M.sel, gt_q + taken_q, out + out_q);
+    if (q == 0 && threadIdx.x == 0) a.count[row] = static_cast<int32_t>(k);
+}
+
 // Split plan for R rows of N_cap scores: at most kTopkSplitMaxCtas CTAs in all
 // (one wave), chunks of at least 1,024 scores (a multiple of 4), a slot of at
 // most kTopkSplitSlot candidates per CTA (about 3k / C are expected; a slot
@@ -1066,7 +1422,7 @@ SplitPlan split_plan(long long R, int N_cap) {
     p.slot = p.chunk < kTopkSplitSlot ? p.chunk : kTopkSplitSlot;
     return p;
 }
-bool split_rows(long long R, int N_cap) { return 2 * R <= kTopkSplitMaxCtas && N_cap > kTopkRowMaxShortRow; }
+bool split_rows(long long R, int N_cap) { return 2 * R <= kTopkSplitMaxCtas && N_cap > kTopkSplitMinRow; }
 
 // ---------------------------------------------------------------- candidates
 // Exact top-k of one (u,q) row from the fused indexer's candidate list
@@ -1123,6 +1479,15 @@ size_t topk_ws_bytes(long long R, int N_cap) {
 cudaError_t launch_topk(const TopkArgs &a, int num_sms, cudaStream_t s) {
     const long long R = static_cast<long long>(a.U) * a.Q;
     if (R <= 0) return cudaSuccess;
+    if (R <= kClusterMaxRows && a.N_cap > kClusterMinRow && a.N_cap <= kTopkSplitMinRow) {
+        const int smem = static_cast<int>(sizeof(ClusterSmem));
+        cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        int chunk = (a.N_cap + kClusterRowCtas - 1) / kClusterRowCtas;
+        chunk = (chunk + 3) & ~3;
+        return launch_k_cluster(topk_cluster_kernel, dim3(static_cast<unsigned>(R * kClusterRowCtas)),
+                                dim3(kClusterThreads), smem, kClusterRowCtas, s, a, chunk);
+    }
     if (!split_rows(R, a.N_cap) || R >= num_sms) {
         // One CTA per row, no workspace.
         if (R > 0x7fffffffLL) return cudaErrorInvalidValue;

@@ -173,7 +173,7 @@ ds4a_status ds4a_indexer_score(const uint16_t *iq, const float *w, const uint16_
  *    count   int32 [U][Q] (device): number selected = min(top_k, visible).
  *    ws      workspace of ds4a_workspace_bytes(DS4A_OP_TOPK_SELECT, U, Q,
  *            N_cap, top_k) bytes, 256-byte aligned (device); NULL when that
- *            is 0.  Only batches of up to 76 (u,q) rows longer than 32,768
+ *            is 0.  Only batches of up to 76 (u,q) rows longer than 524,288
  *            scores use one (each row is then cut over several CTAs);
  *            it is at most about 5 MB whatever the sizes.
  */
@@ -226,7 +226,7 @@ ds4a_status ds4a_indexer_topk(const uint16_t *iq, const float *w, const uint16_t
  *    - the request must fit: ds4a_workspace_bytes(DS4A_OP_TOPK_SELECT, U, Q,
  *      N_cap, top_k) <= DS4A_TOPK_NOALLOC_SCRATCH_BYTES, else DS4A_EWORKSPACE
  *      and nothing is launched.  Every request fits today: only up to 76
- *      rows of more than 32,768 scores use scratch, at most about 5 MB;
+ *      rows of more than 524,288 scores use scratch, at most about 5 MB;
  *    - the first call on a device looks up the array's device address (one
  *      cudaGetSymbolAddress with that device current) and keeps it for the
  *      process: make that first call before any stream capture, and do not

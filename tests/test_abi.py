@@ -49,15 +49,16 @@ def test_version_and_strerror(lib):
 
 def test_workspace_sizes():
     assert B.ds4a_workspace_bytes(B.DS4A_OP_INDEXER_SCORE, 4, 1, 262144, 512) == 0
-    # Top-k: only up to 76 rows, each longer than 32,768 scores, use a
+    # Top-k: only up to 76 rows, each longer than 2^19 scores, use a
     # workspace (candidate slots of the two or more CTAs a row is cut over: at
     # most 152 slots of up to 4,096 (key, row) pairs plus two counters each).
     slot = 4096 * 8 + 8
     assert B.ds4a_workspace_bytes(B.DS4A_OP_TOPK_SELECT, 8, 1, 16384, 512) == 0
     assert B.ds4a_workspace_bytes(B.DS4A_OP_TOPK_SELECT, 1376, 1, 65536, 512) == 0
+    assert B.ds4a_workspace_bytes(B.DS4A_OP_TOPK_SELECT, 4, 1, 262144, 512) == 0
     assert B.ds4a_workspace_bytes(B.DS4A_OP_TOPK_SELECT, 77, 1, 1 << 20, 512) == 0
-    assert B.ds4a_workspace_bytes(B.DS4A_OP_TOPK_SELECT, 4, 1, 262144, 512) == 4 * 38 * slot
-    assert B.ds4a_workspace_bytes(B.DS4A_OP_TOPK_SELECT, 60, 1, 40000, 512) == 60 * 2 * slot
+    assert B.ds4a_workspace_bytes(B.DS4A_OP_TOPK_SELECT, 2, 1, 1 << 20, 512) == 2 * 76 * slot
+    assert B.ds4a_workspace_bytes(B.DS4A_OP_TOPK_SELECT, 60, 1, 600000, 512) == 60 * 2 * slot
     assert B.ds4a_workspace_bytes(B.DS4A_OP_TOPK_SELECT, 1, 1, 1 << 24, 2048) <= 152 * slot
     # Attention: two partial slots (64 x (512 + 2) fp32) per share, at most
     # 160 shares, at most one share per 64-row tile (10 tiles per unit at k = 512).
@@ -101,7 +102,7 @@ def test_topk_rejects_bad_arguments(lib):
     f = lib.ds4a_topk_select
     assert f(_vp(FAKE), _vp(FAKE), 1, 1, 100, 0, _vp(FAKE), _vp(FAKE), _vp(FAKE), 1 << 30, None) == B.DS4A_EINVAL
     assert f(_vp(FAKE), _vp(FAKE), 1, 1, 100, 4096, _vp(FAKE), _vp(FAKE), _vp(FAKE), 1 << 30, None) == B.DS4A_EINVAL
-    N = 65536                                           # one long row: the split path needs a workspace
+    N = 1 << 20                                         # one very long row: the split path needs a workspace
     need = B.ds4a_workspace_bytes(B.DS4A_OP_TOPK_SELECT, 1, 1, N, 8)
     assert need > 0
     assert f(_vp(FAKE), _vp(FAKE), 1, 1, N, 8, _vp(FAKE), _vp(FAKE), None, need, None) == B.DS4A_EWORKSPACE

@@ -223,12 +223,13 @@ def test_topk_one_long_row_split_over_many_ctas():
     topk_case(x, [262144], 512)
 
 
-# Fewer rows than SMs, each longer than 32,768 scores: every row is cut over
-# several CTAs that filter their chunk against one sampled threshold into
-# slots of their own, and one CTA per row selects from the joined slots (or
-# from the whole row when the slots cannot decide).
+# Up to 16 rows of more than 4,096 scores: a cluster of eight CTAs per row
+# filters its chunks against one sampled threshold; the CTAs exchange counts,
+# a bucket histogram and the crossing bucket's keys through distributed shared
+# memory and each writes its own rows (or CTA 0 selects from the whole row when
+# the lists cannot decide).
 
-def test_topk_split_rows_ties_neginf_nan_locality_and_short_rows():
+def test_topk_cluster_rows_ties_neginf_nan_locality_and_short_rows():
     rng = np.random.default_rng(20)
     N = 100000
     x = rng.standard_normal((8, N)).astype(np.float32)
@@ -244,18 +245,43 @@ def test_topk_split_rows_ties_neginf_nan_locality_and_short_rows():
 
 
 @pytest.mark.parametrize("k", [1, 2048])
-def test_topk_split_rows_k_extremes_and_odd_stride(k):
+def test_topk_cluster_rows_k_extremes_and_odd_stride(k):
     rng = np.random.default_rng(21 + k)
     x = rng.standard_normal((3, 70001)).astype(np.float32)   # N_cap not a multiple of 4: scalar loads
     x[1, rng.random(70001) < 0.05] *= 4
     topk_case(x, [70001, 70000, 2047], k)
 
 
-def test_topk_split_many_rows_few_ctas_each():
+def test_topk_cluster_rows_all_candidates_and_sixteen_rows():
     rng = np.random.default_rng(22)
-    x = rng.standard_normal((60, 40000)).astype(np.float32)  # two CTAs per row
-    x[::3, 20000:] += 1.0
-    topk_case(x, [40000 - (i % 7) * 3000 for i in range(60)], 512)
+    x = rng.standard_normal((16, 9000)).astype(np.float32)
+    x[::3, 4500:] += 1.0
+    # rows of at most 8,192 scores take every visible row as a candidate
+    topk_case(x, [9000 - (i % 7) * 700 for i in range(16)], 512)
+
+
+# Rows of more than 2^19 scores in batches of up to 76 rows: every row is cut
+# over several CTAs that filter their chunk against one sampled threshold into
+# slots of their own in the workspace, and one CTA per row selects from the
+# joined slots (or from the whole row when the slots cannot decide).
+
+def test_topk_split_very_long_rows_ties_locality_and_short_rows():
+    rng = np.random.default_rng(23)
+    N = 600000
+    x = rng.standard_normal((4, N)).astype(np.float32)
+    x[1] = np.round(x[1] * 2) / 2                             # heavy ties at the k-th score
+    x[2, N - 40000:] += 3.0                                   # the top rows crowded in the last chunks
+    x[2, rng.random(N) < 0.2] = -np.inf
+    x[3] = 0.5                                                # all equal: slots overflow, exact pass
+    topk_case(x, [N, N - 1, 550000, 7000], 512)
+
+
+@pytest.mark.parametrize("k", [1, 2048])
+def test_topk_split_very_long_rows_k_extremes_and_odd_stride(k):
+    rng = np.random.default_rng(24 + k)
+    x = rng.standard_normal((2, 524289)).astype(np.float32)  # N_cap not a multiple of 4: scalar loads
+    x[1, rng.random(524289) < 0.05] *= 4
+    topk_case(x, [524289, 300000], k)
 
 
 # Batches with at least as many rows as SMs take the one-CTA-per-row kernel

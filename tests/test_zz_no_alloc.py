@@ -6,7 +6,7 @@ ds4a_topk_select gives with a workspace -- call after call, although every
 call reuses the same fixed scratch array.
 
 The cases take the path that uses the scratch (up to 76 (u,q) rows, each
-longer than 32,768 scores: the rows are cut over several CTAs whose candidate
+longer than 2^19 scores: the rows are cut over several CTAs whose candidate
 slots live in the scratch), back to back, so that the second call runs on what
 the first left in the array; a batch that needs no scratch runs in between.
 
@@ -56,9 +56,9 @@ def _no_alloc(lib, scores, n_rows, k):
 def test_no_alloc_topk_matches_the_oracle_on_calls_in_a_row():
     lib = B.load()
     cases = [
-        (64, 65536, 512, 1, None),                                  # scratch: two CTAs per row
+        (3, 600000, 512, 1, None),                                  # scratch: 50 CTAs per row
         (100, 3000, 100, 3, None),                                  # no scratch: one CTA per row
-        (5, 40000, 100, 2, [40000, 39999, 100, 7, 0]),             # scratch again, ragged, ties, -inf
+        (5, 540000, 100, 2, [540000, 539999, 100, 7, 0]),          # scratch again, ragged, ties, -inf
     ]
     for R, N, k, seed, n in cases:
         x = _scores(R, N, seed)
@@ -82,13 +82,13 @@ def test_no_alloc_topk_matches_the_oracle_on_calls_in_a_row():
 
 
 def test_no_alloc_topk_scratch_covers_every_request_and_bad_arguments_launch_nothing():
-    # The scratch is only used by up to 76 long rows, and then by at most
-    # 152 CTA slots: every size fits the fixed array.
+    # The scratch is only used by up to 76 very long rows, and then by at
+    # most 152 CTA slots: every size fits the fixed array.
     cap = B.DS4A_TOPK_NOALLOC_SCRATCH_BYTES
     for R, N, k in [(1, 1 << 24, 2048), (151, 1 << 20, 512), (76, 65536, 512), (4, 262144, 512), (200, 1 << 20, 512)]:
         assert B.ds4a_workspace_bytes(B.DS4A_OP_TOPK_SELECT, R, 1, N, k) <= cap, (R, N, k)
     lib = B.load()
-    R, N = 4, 40000
+    R, N = 4, 600000
     scores = torch.zeros(R, 1, N, device="cuda")
     n_rows = torch.full((R,), N, dtype=torch.int32, device="cuda")
     idx = torch.full((R, 1, 8), 9, dtype=torch.int32, device="cuda")
