@@ -285,6 +285,10 @@ DS4A_DEV uint32_t float_key(float f) {
     if ((b << 1) == 0) b = 0;                  // -0 -> +0
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
+// The float whose key is k (the inverse of float_key; key 0x80000000 gives +0).
+DS4A_DEV float key_float(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
 // Visible = a real score: not -inf, not NaN.
 DS4A_DEV bool score_visible(float f) { return f == f && f != -__int_as_float(0x7f800000); }
 

@@ -182,6 +182,36 @@ DS4A_DEV uint32_t block_kth_key(Get get, uint32_t n, uint32_t k, SelSmem &S, uin
     return prefix;
 }
 
+// One warp (all 32 lanes): the need-th largest key among the keys of list[0 ..
+// L) that lie in [lo, lo + 2^cs) (at least `need` of them do), by narrowing the
+// range 8 bits per round with a warp-private 256-bin histogram (S.h[1]).
+// Lane 0 leaves the key in S.bc[2] and how many keys equal to it the `need`
+// largest take in S.bc[3].
+DS4A_DEV void warp_narrow(const uint32_t *list, uint32_t L, uint32_t lo, int cs, uint32_t need, SelSmem &S) {
+    const int lane = threadIdx.x & 31;
+    uint32_t *h = S.h[1];
+    while (cs > 0) {
+        const int s2 = cs > 8 ? cs - 8 : 0;
+        for (int i = lane; i < kDigitBins; i += 32) h[i] = 0u;
+        __syncwarp();
+        for (uint32_t i = lane; i < L; i += 32) {
+            const uint32_t d = list[i] - lo;
+            if (d < (1u << cs)) atomicAdd(&h[d >> s2], 1u);
+        }
+        __syncwarp();
+        uint32_t above;
+        const int b = warp_find_bin(h, need, &above);           // >= 0: the range holds >= need keys
+        need -= b < 0 ? 0u : above;
+        lo += static_cast<uint32_t>(b < 0 ? 0 : b) << s2;
+        cs = s2;
+        __syncwarp();
+    }
+    if (lane == 0) {
+        S.bc[2] = lo;
+        S.bc[3] = need;
+    }
+}
+
 // Block-wide k-th largest key among the list keys c[0 .. nc) (nc >= k >= 1),
 // all in [kmin, kmax], by buckets fitted to that range: 32 buckets of
 // (key - kmin) >> s, s the least shift that leaves at most 32, counted by
@@ -251,7 +281,7 @@ DS4A_DEV bool fast_kth(const uint2 *c, uint32_t nc, uint32_t k, uint32_t kmin, u
     __syncthreads();
     const uint32_t L = S.cnt[2];
     if (L > static_cast<uint32_t>(kFastList)) return false;     // block-uniform
-    if (L <= static_cast<uint32_t>(NT)) {
+    if (L <= 64u) {
         // Few keys: thread i ranks key i against the whole bucket (16-byte
         // loads every lane of a warp shares); the key with fewer than `need`
         // larger keys and at least `need` at or above it is T.
@@ -278,31 +308,7 @@ DS4A_DEV bool fast_kth(const uint2 *c, uint32_t nc, uint32_t k, uint32_t kmin, u
         *need_eq_out = S.bc[3];
         return true;
     }
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        uint32_t *h = S.h[1];
-        int cs = s;                                              // list keys of the bucket: key - lo < 2^cs (cs <= 27)
-        while (cs > 0) {
-            const int s2 = cs > 8 ? cs - 8 : 0;
-            for (int i = lane; i < kDigitBins; i += 32) h[i] = 0u;
-            __syncwarp();
-            for (uint32_t i = lane; i < L; i += 32) {
-                const uint32_t d = list[i] - lo;
-                if (d < (1u << cs)) atomicAdd(&h[d >> s2], 1u);
-            }
-            __syncwarp();
-            uint32_t above;
-            const int b = warp_find_bin(h, need, &above);           // >= 0: the bucket holds >= need keys
-            need -= b < 0 ? 0u : above;
-            lo += static_cast<uint32_t>(b < 0 ? 0 : b) << s2;
-            cs = s2;
-            __syncwarp();
-        }
-        if (lane == 0) {
-            S.bc[2] = lo;
-            S.bc[3] = need;
-        }
-    }
+    if (threadIdx.x < 32) warp_narrow(list, L, lo, s, need, S);
     __syncthreads();
     *T_out = S.bc[2];
     *need_eq_out = S.bc[3];
@@ -633,8 +639,8 @@ DS4A_DEV void select_exact_row(const float *__restrict__ s, int n, uint32_t k, S
 
 // Threshold estimate for a row of n scores: a key T0 with about (or a little
 // more than) kSampleOver * k of the row's visible keys at or above it, from
-// kSample scores (kSample / 32 whole 128-byte lines spread evenly over the
-// row, so that the sample costs whole lines, not scattered sectors).  Each
+// up to kSample scores (whole 128-byte lines spread evenly over the row, so
+// that the sample costs whole lines, not scattered sectors).  Each
 // warp's share of the sample is spread over the whole row; a warp finds its
 // rw-th largest visible key by rw rounds of a warp-wide max (rw = ceil(r /
 // warps) + 1 for the wanted sample rank r), and T0 is the smallest of the
@@ -645,18 +651,27 @@ template <int NT, int kSample>
 DS4A_DEV uint32_t sample_threshold(const float *__restrict__ s, int n, uint32_t k, int all_below, SelSmem &S) {
     if (n <= all_below) return 0u;
     constexpr int kPer = kSample / NT;
-    constexpr int kLines = kSample / 32;
     constexpr int kWarps = NT / 32;
+    // Shorter rows take a smaller sample (at least NT and 1,024 scores): the
+    // wanted sample rank stays near 64 instead of growing with kSample / n.
+    int samples = kSample;
+    while (samples > NT && samples > 1024 &&
+           static_cast<long long>(kSampleOver) * k * (samples / 2) >= 64LL * n)
+        samples >>= 1;
+    const int per = samples / NT, lines = samples / 32;
     uint32_t key[kPer];
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
-        const int sj = static_cast<int>(threadIdx.x) + j * NT;
-        const int line = static_cast<int>((static_cast<long long>(sj >> 5) * (n / 32 - 1)) / (kLines - 1));
-        const float f = __ldg(s + line * 32 + (sj & 31));
-        key[j] = score_visible(f) ? float_key(f) : 0u;        // visible keys are >= 0x00800000
+        key[j] = 0u;                                          // visible keys are >= 0x00800000
+        if (j < per) {
+            const int sj = static_cast<int>(threadIdx.x) + j * NT;
+            const int line = static_cast<int>((static_cast<long long>(sj >> 5) * (n / 32 - 1)) / (lines - 1));
+            const float f = __ldg(s + line * 32 + (sj & 31));
+            key[j] = score_visible(f) ? float_key(f) : 0u;
+        }
     }
-    const long long r_want = (static_cast<long long>(kSampleOver) * k * kSample + n - 1) / n;
-    const int r = static_cast<int>(r_want < kSample ? r_want : kSample);
+    const long long r_want = (static_cast<long long>(kSampleOver) * k * samples + n - 1) / n;
+    const int r = static_cast<int>(r_want < samples ? r_want : samples);
     // rw = the wanted rank's share per warp and two more, so that the union of
     // the warps' lists most likely holds the sample's r largest keys; when the
     // union would not fit (short rows, large r), each warp takes its share
@@ -692,20 +707,47 @@ DS4A_DEV uint32_t sample_threshold(const float *__restrict__ s, int n, uint32_t 
     __syncthreads();
     uint32_t T0;
     if (use_union) {
-        // the r-th largest of the union: the key with fewer than r larger
-        // keys and at least r at or above it (thread i ranks union entry i)
-        if (threadIdx.x < 128) {
-            const uint32_t v = S.uni[threadIdx.x];
-            uint32_t gt = 0, ge = 0;
-            for (int j = 0; j < 128; ++j) {
-                const uint32_t o = S.uni[j];
-                gt += o > v ? 1u : 0u;
-                ge += o >= v ? 1u : 0u;
+        // the r-th largest of the union: warp 0 sorts its 128 entries (four
+        // per lane, a bitonic sort in registers and shuffles) and reads it off
+        if (warp == 0) {
+            uint32_t x[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) x[j] = S.uni[lane * 4 + j];
+#pragma unroll
+            for (int kk = 2; kk <= 128; kk <<= 1) {
+#pragma unroll
+                for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int e = lane * 4 + j;           // element index, ascending order wanted
+                        uint32_t y;
+                        if (jj < 4) {
+                            y = x[j ^ jj];
+                        } else {
+                            y = __shfl_xor_sync(0xffffffffu, x[j], jj >> 2);
+                        }
+                        const bool up = (e & kk) == 0, low = (e & jj) == 0;
+                        const uint32_t mn = min(x[j], y), mx = max(x[j], y);
+                        // within a lane both partners are updated from the old pair
+                        if (jj < 4) {
+                            if (low) {
+                                x[j] = up ? mn : mx;
+                                x[j ^ jj] = up ? mx : mn;
+                            }
+                        } else {
+                            x[j] = (low == up) ? mn : mx;
+                        }
+                    }
+                }
             }
-            if (v != 0u && gt < static_cast<uint32_t>(r) && ge >= static_cast<uint32_t>(r)) S.bc[3] = v;
+            const int pos = 128 - r;                          // ascending position of the r-th largest
+            const int pj = pos & 3;
+            const uint32_t mine = pj == 0 ? x[0] : pj == 1 ? x[1] : pj == 2 ? x[2] : x[3];
+            const uint32_t t0 = __shfl_sync(0xffffffffu, mine, pos >> 2);
+            if (lane == 0) S.bc[3] = t0;                      // 0 when fewer than r visible sample keys
         }
         __syncthreads();
-        T0 = S.bc[3];                                        // 0 when fewer than r visible sample keys
+        T0 = S.bc[3];
     } else {
         T0 = 0xffffffffu;
 #pragma unroll
@@ -1051,7 +1093,7 @@ __global__ void __launch_bounds__(kSplitFinalThreads) topk_split_final_kernel(co
 
 // ---------------------------------------------------------------- few rows: one cluster per row
 // For up to kClusterMaxRows rows of more than kClusterMinRow scores: a
-// thread-block cluster of kClusterRowCtas CTAs per row.  CTA q filters chunk q
+// thread-block cluster of kClusterRowCtas (8) CTAs per row.  CTA q filters chunk q
 // of the row against the row's sampled threshold T0 (every CTA derives the
 // same T0 from the same sample) into a candidate list in its own shared
 // memory.  The CTAs then exchange what the exact selection needs through
@@ -1067,7 +1109,7 @@ __global__ void __launch_bounds__(kSplitFinalThreads) topk_split_final_kernel(co
 // row order) in ascending order at its offset.  A row the lists cannot decide
 // (a sample that missed, heavy ties) is selected by CTA 0 alone from the
 // row's scores.  No global scratch; three cluster barriers.
-constexpr int kClusterRowCtas = 8;
+constexpr int kClusterRowCtas = 8;        // 16 (non-portable) measured slower: 4 x 262,144 20.3 vs 17.0 us
 constexpr int kClusterThreads = 512;
 constexpr int kClusterCap = 4096;          // candidates per CTA
 constexpr int kClusterMaxRows = 16;       // more rows: one CTA per row is as fast
@@ -1109,6 +1151,7 @@ __global__ void __launch_bounds__(kClusterThreads) topk_cluster_kernel(const __g
     ClusterSmem &M = *reinterpret_cast<ClusterSmem *>(cl_smem);
     SelSmem &S = M.S;
     constexpr int C = kClusterRowCtas, NT = kClusterThreads, NW = NT / 32;
+    static_assert(C <= NW, "a warp per CTA of the cluster counts its crossing-bucket segment");
     const uint32_t q = cluster_rank();
     const long long row = blockIdx.x / C;
     const int u = static_cast<int>(row / a.Q);
@@ -1122,7 +1165,7 @@ __global__ void __launch_bounds__(kClusterThreads) topk_cluster_kernel(const __g
     const int start = static_cast<int>(q) * chunk;          // chunk is a multiple of 4
     const int end = min(start + chunk, n);
     const bool vec4 = (a.N_cap & 3) == 0;
-    constexpr int B = 4;
+    constexpr int B = 8;                                      // float4 loads per thread in flight
     const int g_beg = start / 4, g_end = end > start ? (end + 3) / 4 : g_beg;
     float4 v[B];
     auto load = [&](int g0) {
@@ -1136,8 +1179,13 @@ __global__ void __launch_bounds__(kClusterThreads) topk_cluster_kernel(const __g
     const uint32_t T0 = sample_threshold<NT, kSampleSplit>(s, n, k, kClusterAllBelow, S);
     sel_reset(S);
     __syncthreads();
-    // ---- the chunk against T0: candidates, visible count, key range
+    // ---- the chunk against T0: candidates, visible count, key range.  Plain
+    // float compares (f >= the float of T0 is key(f) >= T0 for a visible f;
+    // NaN and -inf fail both tests); keys only for the rare candidates.
     uint32_t my_vis = 0, kmn = 0xffffffffu, kmx = 0u;
+    const bool take_all = T0 == 0u;
+    const float T0f = key_float(T0);
+    const float kNegInf = -__int_as_float(0x7f800000);
     if (vec4) {
         for (int g0 = g_beg; g0 < g_end; g0 += B * NT) {     // block-uniform
             if (g0 != g_beg) load(g0);
@@ -1145,20 +1193,26 @@ __global__ void __launch_bounds__(kClusterThreads) topk_cluster_kernel(const __g
             for (int j = 0; j < B; ++j) {
                 const int i = 4 * (g0 + j * NT + static_cast<int>(threadIdx.x));
                 const float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-                uint32_t key[4], bal[4], tot = 0;
                 bool take[4];
+                bool any = false;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const bool vis = i + c < end && score_visible(f[c]);
-                    key[c] = float_key(f[c]);
+                    const bool vis = i + c < end && f[c] > kNegInf;
                     my_vis += vis ? 1u : 0u;
-                    take[c] = vis && key[c] >= T0;
+                    take[c] = vis && (take_all || f[c] >= T0f);
+                    any |= take[c];
+                }
+                if (!__any_sync(0xffffffffu, any)) continue;
+                uint32_t key[4], bal[4], tot = 0;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    key[c] = float_key(f[c]);
                     kmn = take[c] ? min(kmn, key[c]) : kmn;
                     kmx = take[c] ? max(kmx, key[c]) : kmx;
                     bal[c] = __ballot_sync(0xffffffffu, take[c]);
                     tot += __popc(bal[c]);
                 }
-                if (tot) {                                    // warp-uniform: one shared atomic per float4
+                {                                             // one shared atomic per warp and float4
                     uint32_t pos = 0;
                     if (lane == 0) pos = atomicAdd(&S.cnt[3], tot);
                     pos = __shfl_sync(0xffffffffu, pos, 0);
@@ -1321,6 +1375,11 @@ __global__ void __launch_bounds__(kClusterThreads) topk_cluster_kernel(const __g
     if (sh == 0) {                                            // one key per bucket
         T = kmin + b0;
         need_eq = need;
+    } else if (L > 256u) {                                    // narrow the bucket 8 bits per round (one warp)
+        if (warp == 0) warp_narrow(M.list, L, kmin + (b0 << sh), sh, need, S);
+        __syncthreads();
+        T = S.bc[2];
+        need_eq = S.bc[3];
     } else {
         for (uint32_t i = threadIdx.x; i < L; i += NT) {
             const uint32_t vi = M.list[i];
