@@ -355,7 +355,7 @@ DS4A_DEV uint32_t block_rank(bool pred, uint32_t *warp_sums /* 32 u32 smem */, u
 }
 
 // Writes the rows sel[0 .. m) (distinct, each < n_bound) in ascending order
-// to out[0 .. k) with -1 padding, and the count.  Rows below 65,536 with the
+// to out[0 .. k) with -1 padding, and the count.  Rows below 131,072 with the
 // bitmap room below: the bitmap.  Otherwise up to 512 rows: each row's rank
 // by counting (sel 16-byte aligned).  Otherwise, when a bitmap of n_bound
 // bits fits bm (bm_words words of shared memory): the rows' bits are set,
@@ -373,7 +373,7 @@ DS4A_DEV void write_sorted(int32_t *sel, int32_t *tmp, uint32_t *bm, int bm_word
     const int nt = blockDim.x;
     const int words = (n_bound + 31) / 32, chunks = (words + 31) / 32;
     const bool bitmap = m > 1 && chunks * 32 <= bm_words && chunks <= 1024;
-    if (m > 1 && m <= 512 && !(bitmap && chunks <= 64)) {
+    if (m > 1 && m <= 512 && !(bitmap && chunks <= 128)) {
         // Each row goes to its rank: the count of smaller rows, from 16-byte
         // loads of sel that every lane of a warp shares (no barrier, no sort).
         const int4 *s4 = reinterpret_cast<const int4 *>(sel);
