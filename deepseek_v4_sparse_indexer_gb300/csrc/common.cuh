@@ -23,7 +23,10 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 // its memory visible, before touching global memory (pdl_wait).  Between
 // dependent kernels the launch latency and the block scheduling then overlap
 // the previous kernel's tail; the data order is the stream order, as without
-// it.
+// it.  The one exception: the top-k kernels read the caller's row counts
+// (n_rows) before the wait.  A kernel starts early only behind a kernel of this
+// library; none of them writes n_rows, and the first kernel of such a chain
+// started only once the stream's earlier work had completed.
 DS4A_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 DS4A_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

@@ -281,7 +281,7 @@ DS4A_DEV bool fast_kth(const uint2 *c, uint32_t nc, uint32_t k, uint32_t kmin, u
     __syncthreads();
     const uint32_t L = S.cnt[2];
     if (L > static_cast<uint32_t>(kFastList)) return false;     // block-uniform
-    if (L <= 64u) {
+    if (L <= static_cast<uint32_t>(NT < 256 ? NT : 256)) {
         // Few keys: thread i ranks key i against the whole bucket (16-byte
         // loads every lane of a warp shares); the key with fewer than `need`
         // larger keys and at least `need` at or above it is T.
@@ -637,9 +637,9 @@ DS4A_DEV void select_exact_row(const float *__restrict__ s, int n, uint32_t k, S
     if (threadIdx.x == 0) *count_out = static_cast<int32_t>(m);
 }
 
-// Threshold estimate for a row of n scores: a key T0 with about (or a little
-// more than) kSampleOver * k of the row's visible keys at or above it, from
-// up to kSample scores (whole 128-byte lines spread evenly over the row, so
+// Threshold estimate for a row of n > all_below >= 4,096 scores: a key T0 with
+// about (or a little more than) kSampleOver * k of the row's visible keys at or
+// above it, from up to kSample scores (whole 128-byte lines spread evenly over the row, so
 // that the sample costs whole lines, not scattered sectors).  Each
 // warp's share of the sample is spread over the whole row; a warp finds its
 // rw-th largest visible key by rw rounds of a warp-wide max (rw = ceil(r /
@@ -659,13 +659,16 @@ DS4A_DEV uint32_t sample_threshold(const float *__restrict__ s, int n, uint32_t 
            static_cast<long long>(kSampleOver) * k * (samples / 2) >= 64LL * n)
         samples >>= 1;
     const int per = samples / NT, lines = samples / 32;
+    const int lsh = 31 - __clz(lines);                        // lines is a power of two
     uint32_t key[kPer];
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
         key[j] = 0u;                                          // visible keys are >= 0x00800000
         if (j < per) {
+            // line li of the sample: row line li * (n / 32) / lines (n / 32 >= lines:
+            // distinct lines, the last one inside the row)
             const int sj = static_cast<int>(threadIdx.x) + j * NT;
-            const int line = static_cast<int>((static_cast<long long>(sj >> 5) * (n / 32 - 1)) / (lines - 1));
+            const int line = static_cast<int>((static_cast<long long>(sj >> 5) * (n >> 5)) >> lsh);
             const float f = __ldg(s + line * 32 + (sj & 31));
             key[j] = score_visible(f) ? float_key(f) : 0u;
         }
@@ -779,15 +782,15 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 2 : 4) topk_row_kernel(const f
                                                                   int32_t *__restrict__ idx_out,
                                                                   int32_t *__restrict__ count_out, uint32_t *status) {
     pdl_launch_dependents();
+    const long long row = blockIdx.x;
+    const int u = static_cast<int>(row / Q);
+    const int n = row_len(n_rows, u, N_cap);             // no kernel of this library writes n_rows
     pdl_wait();
     extern __shared__ __align__(16) uint8_t row_smem[];
     uint2 *cand = reinterpret_cast<uint2 *>(row_smem);                          // [CAP]
     int32_t *sel = reinterpret_cast<int32_t *>(row_smem + CAP * 8);             // [SEL]
     uint32_t *list = reinterpret_cast<uint32_t *>(row_smem + CAP * 8 + SEL * 4);   // [kFastList]
     SelSmem &S = *reinterpret_cast<SelSmem *>(row_smem + CAP * 8 + SEL * 4 + kFastList * 4);
-    const long long row = blockIdx.x;
-    const int u = static_cast<int>(row / Q);
-    const int n = row_len(n_rows, u, N_cap);
     if (threadIdx.x == 0 && row % Q == 0 && (n_rows[u] < 0 || n_rows[u] > N_cap)) report(status, DS4A_DEV_BOUNDS);
     const float *s = scores + row * N_cap;
     const uint32_t k = static_cast<uint32_t>(top_k);
@@ -909,13 +912,13 @@ struct SplitArgs {
 
 __global__ void __launch_bounds__(kSplitThreads) topk_split_kernel(const __grid_constant__ SplitArgs a) {
     pdl_launch_dependents();
-    pdl_wait();
-    __shared__ SelSmem S;
-    __shared__ uint2 queue[kTopkSplitSlot];
     const long long row = blockIdx.x / a.C;
     const int c = static_cast<int>(blockIdx.x - row * a.C);
     const int u = static_cast<int>(row / a.Q);
-    const int n = row_len(a.n_rows, u, a.N_cap);
+    const int n = row_len(a.n_rows, u, a.N_cap);        // no kernel of this library writes n_rows
+    pdl_wait();
+    __shared__ SelSmem S;
+    __shared__ uint2 queue[kTopkSplitSlot];
     if (c == 0 && threadIdx.x == 0 && row % a.Q == 0 && (a.n_rows[u] < 0 || a.n_rows[u] > a.N_cap))
         report(a.status, DS4A_DEV_BOUNDS);
     const float *s = a.scores + row * a.N_cap;
@@ -1146,7 +1149,6 @@ DS4A_DEV void rank_write(const int32_t *sel, uint32_t m, int32_t *out) {
 
 __global__ void __launch_bounds__(kClusterThreads) topk_cluster_kernel(const __grid_constant__ TopkArgs a, int chunk) {
     pdl_launch_dependents();
-    pdl_wait();
     extern __shared__ __align__(16) uint8_t cl_smem[];
     ClusterSmem &M = *reinterpret_cast<ClusterSmem *>(cl_smem);
     SelSmem &S = M.S;
@@ -1155,7 +1157,8 @@ __global__ void __launch_bounds__(kClusterThreads) topk_cluster_kernel(const __g
     const uint32_t q = cluster_rank();
     const long long row = blockIdx.x / C;
     const int u = static_cast<int>(row / a.Q);
-    const int n = row_len(a.n_rows, u, a.N_cap);
+    const int n = row_len(a.n_rows, u, a.N_cap);        // no kernel of this library writes n_rows
+    pdl_wait();
     if (q == 0 && threadIdx.x == 0 && row % a.Q == 0 && (a.n_rows[u] < 0 || a.n_rows[u] > a.N_cap))
         report(a.status, DS4A_DEV_BOUNDS);
     const float *s = a.scores + row * a.N_cap;
@@ -1403,12 +1406,13 @@ __global__ void __launch_bounds__(kClusterThreads) topk_cluster_kernel(const __g
         T = S.bc[2];
         need_eq = S.bc[3];
     }
-    // crossing-bucket rows above T and equal to T of each CTA (warp j: segment j)
+    // each CTA's rows above T (its buckets above the crossing one and its
+    // crossing-bucket keys above T) and equal to T (warp j: CTA j)
     if (warp < C) {
         uint32_t o = 0;
         for (int j = 0; j < warp; ++j) o += M.hist[j][b0];
         const uint32_t cnt = M.hist[warp][b0];
-        uint32_t g = 0, e = 0;
+        uint32_t g = lane > static_cast<int>(b0) ? M.hist[warp][lane] : 0u, e = 0;
         for (uint32_t i = lane; i < cnt; i += 32) {
             const uint32_t key = sh == 0 ? T : M.list[o + i];
             g += key > T;
@@ -1425,8 +1429,7 @@ __global__ void __launch_bounds__(kClusterThreads) topk_cluster_kernel(const __g
     uint32_t out_q = 0, ties_before = 0, gt_q = 0, eq_q = 0, taken_q = 0;
 #pragma unroll
     for (int j = 0; j < C; ++j) {
-        uint32_t gj = M.seg[j][0];
-        for (uint32_t b = b0 + 1; b < 32; ++b) gj += M.hist[j][b];
+        const uint32_t gj = M.seg[j][0];
         const uint32_t ej = M.seg[j][1];
         const uint32_t left = need_eq > ties_before ? need_eq - ties_before : 0u;
         const uint32_t tj = min(ej, left);

@@ -434,8 +434,13 @@ ds4a_status ds4a_rows_to_fp8(const float *x, int64_t n_rows, uint8_t *rows8, flo
  *    compressed rows given as E4M3 codes and per-row scales instead of bf16.
  *    Element d of compressed row i is e4m3(rows8[i][d]) * row_scale[i]; the
  *    kernel expands each gathered row to exactly these values in bf16 (exact
- *    down to 2^-133) and multiplies as 3a does.  Half the gather bytes of the
- *    bf16 store.  64 query heads.
+ *    down to 2^-133) and multiplies as 3a does.  64 query heads.
+ *
+ *    The FP8 store is a storage format, not a speed-up: a row takes 516 bytes
+ *    of HBM instead of 1,024 (twice the context in the same memory) and a
+ *    gather moves half the bytes, but these calls are slower than 3a / 3b over
+ *    bf16 rows, because the expansion of the codes sits on each row tile's
+ *    critical path while the gather is latency-bound.
  *
  *    rows8      uint8 [U][N_cap][512] E4M3 codes; unit u at rows8 +
  *               u*rows_unit_stride (elements = bytes), 16-byte aligned (device).
