@@ -637,6 +637,8 @@ def main():
             1 if wl.kind == "decode" else wl.queries, wl.n_rows, wl.top_k) else 0)
         if wl.units * wl.queries <= 76 and not fused and wl.n_rows > (1 << 19):
             launches_per_step += 1            # top-k over few very long rows: a filter pass before the final one
+        if fused:
+            launches_per_step += 1            # the fused select's counters are zeroed by a kernel of its own
     cfg = {"workload": wl.name, "units": wl.units, "queries_per_unit": wl.queries, "rows_per_unit": wl.n_rows,
            "top_k": wl.top_k if wl.kind != "dense" else "all rows", "raw_window": 128, "heads": wl.heads,
            "head_dim": 512, "indexer": "64x128" if wl.kind != "dense" else "none (ratio-128 layer)",

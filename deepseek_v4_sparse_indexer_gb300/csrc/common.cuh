@@ -21,9 +21,9 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 // on the stream start launching at once (pdl_launch_dependents, the first
 // thing each kernel does) and waits for the previous kernel to complete, with
 // its memory visible, before touching global memory (pdl_wait).  Between
-// dependent kernels the launch latency and the block scheduling then overlap
-// the previous kernel's tail; the data order is the stream order, as without
-// it.  The one exception: the top-k kernels read the caller's row counts
+// dependent kernels the launch latency, the block scheduling and (tcgen05
+// kernels) the barrier and TMEM set-up then overlap the previous kernel's
+// tail; the data order is the stream order, as without it.  The one exception: the top-k kernels read the caller's row counts
 // (n_rows) before the wait.  A kernel starts early only behind a kernel of this
 // library; none of them writes n_rows, and the first kernel of such a chain
 // started only once the stream's earlier work had completed.
@@ -174,6 +174,20 @@ DS4A_DEV bool mbar_wait_hint(uint64_t *bar, uint32_t parity, volatile int *abort
 // ---------------------------------------------------------------------------
 DS4A_DEV void tma_prefetch_desc(const void *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+// L2 prefetch of one box of a tensor map (no shared memory, no barrier).  L2 is
+// the device's point of coherence, so a prefetch issued before the previous
+// kernel has finished writing the tensor cannot leave a stale copy behind.
+DS4A_DEV void tma_prefetch_l2_2d(const void *map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+DS4A_DEV void tma_prefetch_l2_3d(const void *map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
 }
 DS4A_DEV void tma_load_2d(void *dst, const void *map, uint64_t *bar, int x, int y, uint64_t policy) {
     asm volatile(

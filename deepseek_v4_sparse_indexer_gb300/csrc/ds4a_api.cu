@@ -284,7 +284,7 @@ ds4a_status ds4a_indexer_topk(const uint16_t *iq, const float *w, const uint16_t
     a.vis_n = counters + R;
     a.tau = counters + 2 * R;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(counters, 0, static_cast<size_t>(R) * 12, s) != cudaSuccess) return DS4A_ECUDA;
+    if (launch_clear_counters(counters, 3 * R, di->sms, s) != cudaSuccess) return DS4A_ECUDA;
     if (a.total_tiles > 0 && launch_indexer_score(a, s) != cudaSuccess) return DS4A_ECUDA;
     TopkCandArgs t{a.cand, a.cand_n, a.vis_n, static_cast<int>(R), N_cap, top_k, idx, count};
     return launch_topk_cand(t, s) == cudaSuccess ? DS4A_OK : DS4A_ECUDA;

@@ -37,6 +37,7 @@ namespace ds4a {
 namespace {
 
 constexpr int kTileRows = 128;   // UMMA M
+constexpr int kPrefetchTiles = 16;   // key tiles per CTA put into L2 before the dependency wait
 
 
 template <int G>
@@ -220,11 +221,34 @@ DS4A_DEV float sum_pairs(const unsigned long long (&acc)[4]) {
     return ((s0.x + s0.y) + (s1.x + s1.y)) + ((s2.x + s2.y) + (s3.x + s3.y));
 }
 
+// The first key tiles of a CTA's share and their query blocks go into L2
+// before the kernel waits for the previous one: behind a partly idle GPU (a
+// few-unit attention, a short select) the scan's first tiles then come from
+// L2.  Tiles past a unit's n_rows are prefetched too (n_rows is read only
+// after the wait).
+DS4A_DEV void prefetch_share_head(const IndexerArgs &a, long long lo, long long hi, int G) {
+    const long long per_unit = static_cast<long long>(a.n_groups) * a.nt_cap;
+    const long long end = min(hi, lo + kPrefetchTiles);
+    int last_qrow = -1;
+    for (long long lin = lo; lin < end; ++lin) {
+        const int u = static_cast<int>(lin / per_unit);
+        const int rem = static_cast<int>(lin - u * per_unit);
+        const int g = rem / a.nt_cap, t = rem - g * a.nt_cap;
+        const int qrow = (u * a.Q + g * G) * kNIdxHead;
+        if (qrow != last_qrow) {
+            tma_prefetch_l2_2d(&a.tm_iq, 0, qrow);
+            tma_prefetch_l2_2d(&a.tm_iq, 64, qrow);
+            last_qrow = qrow;
+        }
+        tma_prefetch_l2_3d(&a.tm_ik, 0, t * kTileRows, u);
+        tma_prefetch_l2_3d(&a.tm_ik, 64, t * kTileRows, u);
+    }
+}
+
 template <int G>
 __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
     indexer_score_kernel(const __grid_constant__ IndexerArgs a) {
     pdl_launch_dependents();
-    pdl_wait();
     using C = IdxCfg<G>;
     extern __shared__ uint8_t smem_raw[];
     // Aligned by pointer arithmetic on the __shared__ array (not through an
@@ -274,15 +298,18 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
     long long share_lo, share_hi;
     cta_share(a, share_lo, share_hi);
+    if (warp != 0) pdl_wait();                         // the set-up above reads no global memory
+    const uint32_t tmem_base = *tmem_slot;
 
     if (warp < C::kFirstEpiWarp) {
         if constexpr (C::kSplitRegs) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kLowRegs));
     }
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
+        if (lane == 0) prefetch_share_head(a, share_lo, share_hi, G);
+        pdl_wait();
         if (lane == 0) {
             const uint64_t pol_stream = l2_policy_evict_first();
             const uint64_t pol_keep = l2_policy_evict_last();
@@ -564,7 +591,26 @@ cudaError_t launch_g(const IndexerArgs &a, cudaStream_t s) {
     return launch_k(indexer_score_kernel<G>, dim3(a.grid), dim3(C::kThreads), C::kSmemBytes, s, a);
 }
 
+// Zeroes the fused selection's per-row counters.  A kernel rather than a
+// memset, so that the scan launched behind it can start early (and put its
+// first key tiles into L2) while the stream's previous kernels finish.  It
+// waits for them first: the previous select over this workspace reads these
+// counters.
+__global__ void __launch_bounds__(256) clear_counters_kernel(uint32_t *c, long long n) {
+    pdl_launch_dependents();
+    pdl_wait();
+    for (long long i = blockIdx.x * 256LL + threadIdx.x; i < n; i += static_cast<long long>(gridDim.x) * 256)
+        c[i] = 0u;
+}
+
 }  // namespace
+
+cudaError_t launch_clear_counters(uint32_t *c, long long n, int num_sms, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    const long long blocks = (n + 255) / 256;
+    const int grid = static_cast<int>(blocks < 4LL * num_sms ? blocks : 4LL * num_sms);
+    return launch_k(clear_counters_kernel, dim3(grid), dim3(256), 0, s, c, n);
+}
 
 int indexer_group_size(int Q) { return Q >= 4 ? 4 : 1; }
 

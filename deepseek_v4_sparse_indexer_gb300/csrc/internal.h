@@ -41,6 +41,7 @@ struct IndexerArgs {
     int grid;
 };
 cudaError_t launch_indexer_score(const IndexerArgs &a, cudaStream_t s);
+cudaError_t launch_clear_counters(uint32_t *c, long long n, int num_sms, cudaStream_t s);
 int indexer_group_size(int Q);                       // G for a given Q
 void indexer_plan(IndexerArgs &a, int num_sms);      // fills n_groups .. grid
 

@@ -346,7 +346,6 @@ __global__ void __launch_bounds__(attn_threads(GW), 1) sparse_attn_kernel(const 
     constexpr int kGatherWarps = GW;
     constexpr int kGroupsPerWarp = (kRowGroups + kGatherWarps - 1) / kGatherWarps;
     pdl_launch_dependents();
-    pdl_wait();
     extern __shared__ uint8_t smem_raw[];
     // Aligned by pointer arithmetic on the __shared__ array (not through an
     // integer), so that the compiler keeps shared-space accesses for it.
@@ -399,9 +398,16 @@ __global__ void __launch_bounds__(attn_threads(GW), 1) sparse_attn_kernel(const 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    const Sched sc = make_sched(a, nt, g_rem);
+    if (threadIdx.x == 0 && sc.n_pieces > 0) {
+        // q of the first piece into L2 while the previous kernel finishes
+        // (a prefetch cannot go stale: L2 is the point of coherence)
+        const long long u0 = sc.R > 0 ? blockIdx.x : sc.u_rem0 + sc.v0;
+        prefetch_l2(a.q + u0 * kNHead * kHeadDim, kNHead * kHeadDim * 2);
+    }
+    pdl_wait();                                  // the set-up above reads no global memory
     const uint32_t tmem = *tmem_slot;
     const float NEG_INF = -__int_as_float(0x7f800000);
-    const Sched sc = make_sched(a, nt, g_rem);
     const int u_end = sc.n_pieces;               // pieces 0 .. n_pieces-1
     const long long n_slots = 2LL * gridDim.x;
 

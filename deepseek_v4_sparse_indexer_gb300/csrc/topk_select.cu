@@ -44,20 +44,19 @@ constexpr int kSplitThreads = 256;
 constexpr int kSplitFinalThreads = 512;
 constexpr int kSplitCache = 8192;      // candidates a split row's final CTA holds in shared memory
 
-DS4A_DEV int row_len(const int32_t *n_rows, int u, int N_cap) {
-    int n = n_rows[u];
-    return n < 0 ? 0 : (n > N_cap ? N_cap : n);
-}
+DS4A_DEV int clamp_rows(int n, int N_cap) { return n < 0 ? 0 : (n > N_cap ? N_cap : n); }
+DS4A_DEV int row_len(const int32_t *n_rows, int u, int N_cap) { return clamp_rows(n_rows[u], N_cap); }
 
 // Shared scratch of the block-wide selection helpers.
 struct __align__(16) SelSmem {
     uint32_t h[2][kDigitBins];         // digit histograms (alternating)
     uint32_t bc[4];                    // broadcast words
     uint32_t cnt[4];                   // block counters
-    uint32_t mm[2];                    // smallest and largest candidate key
+    uint32_t mm[4];                    // smallest and largest candidate key (2 used: uni 16-byte aligned)
     uint32_t warp_sums[32];
     uint32_t uni[128];                 // the warps' largest sample keys (threshold estimate)
 };
+static_assert(offsetof(SelSmem, uni) % 16 == 0, "uni is read as uint4");
 constexpr int kFastList = 1024;        // keys of the crossing bucket the one-warp search takes
 
 // Clears what select_from_list expects cleared (counters, key range).  A
@@ -641,11 +640,12 @@ DS4A_DEV void select_exact_row(const float *__restrict__ s, int n, uint32_t k, S
 // about (or a little more than) kSampleOver * k of the row's visible keys at or
 // above it, from up to kSample scores (whole 128-byte lines spread evenly over the row, so
 // that the sample costs whole lines, not scattered sectors).  Each
-// warp's share of the sample is spread over the whole row; a warp finds its
-// rw-th largest visible key by rw rounds of a warp-wide max (rw = ceil(r /
-// warps) + 1 for the wanted sample rank r), and T0 is the smallest of the
-// warps' keys, so at least r sample keys lie at or above it.  0 (every
-// visible row) when n <= all_below or a warp's share has fewer than rw
+// warp's share of the sample is spread over the whole row; a warp pulls out
+// its rw largest visible keys by rw rounds of a warp-wide max (rw = ceil(r /
+// warps) + 2 for the wanted sample rank r), and T0 is the r-th largest key of
+// the union of the warps' lists (when the union does not fit, the smallest of
+// the warps' last keys), so at least r sample keys lie at or above it.  0
+// (every visible row) when n <= all_below or the sample has fewer than r
 // visible keys.
 template <int NT, int kSample>
 DS4A_DEV uint32_t sample_threshold(const float *__restrict__ s, int n, uint32_t k, int all_below, SelSmem &S) {
@@ -710,44 +710,22 @@ DS4A_DEV uint32_t sample_threshold(const float *__restrict__ s, int n, uint32_t 
     __syncthreads();
     uint32_t T0;
     if (use_union) {
-        // the r-th largest of the union: warp 0 sorts its 128 entries (four
-        // per lane, a bitonic sort in registers and shuffles) and reads it off
-        if (warp == 0) {
-            uint32_t x[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) x[j] = S.uni[lane * 4 + j];
-#pragma unroll
-            for (int kk = 2; kk <= 128; kk <<= 1) {
-#pragma unroll
-                for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int e = lane * 4 + j;           // element index, ascending order wanted
-                        uint32_t y;
-                        if (jj < 4) {
-                            y = x[j ^ jj];
-                        } else {
-                            y = __shfl_xor_sync(0xffffffffu, x[j], jj >> 2);
-                        }
-                        const bool up = (e & kk) == 0, low = (e & jj) == 0;
-                        const uint32_t mn = min(x[j], y), mx = max(x[j], y);
-                        // within a lane both partners are updated from the old pair
-                        if (jj < 4) {
-                            if (low) {
-                                x[j] = up ? mn : mx;
-                                x[j ^ jj] = up ? mx : mn;
-                            }
-                        } else {
-                            x[j] = (low == up) ? mn : mx;
-                        }
-                    }
-                }
+        // the r-th largest of the union's 128 keys: thread i < 128 counts the
+        // keys above and at key i (16-byte loads that every lane of a warp
+        // shares); the key with fewer than r above it and at least r at or
+        // above it is T0 (0 when the sample has fewer than r visible keys)
+        static_assert(NT >= 128 && sizeof(S.uni) == 512, "one thread per union entry");
+        if (threadIdx.x < 128) {
+            const uint32_t v = S.uni[threadIdx.x];
+            const uint4 *u4 = reinterpret_cast<const uint4 *>(S.uni);
+            uint32_t gt = 0, ge = 0;
+#pragma unroll 8
+            for (int j = 0; j < 32; ++j) {
+                const uint4 o = u4[j];
+                gt += (o.x > v) + (o.y > v) + (o.z > v) + (o.w > v);
+                ge += (o.x >= v) + (o.y >= v) + (o.z >= v) + (o.w >= v);
             }
-            const int pos = 128 - r;                          // ascending position of the r-th largest
-            const int pj = pos & 3;
-            const uint32_t mine = pj == 0 ? x[0] : pj == 1 ? x[1] : pj == 2 ? x[2] : x[3];
-            const uint32_t t0 = __shfl_sync(0xffffffffu, mine, pos >> 2);
-            if (lane == 0) S.bc[3] = t0;                      // 0 when fewer than r visible sample keys
+            if (gt < static_cast<uint32_t>(r) && ge >= static_cast<uint32_t>(r)) S.bc[3] = v;   // all such threads agree
         }
         __syncthreads();
         T0 = S.bc[3];
@@ -784,14 +762,15 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 2 : 4) topk_row_kernel(const f
     pdl_launch_dependents();
     const long long row = blockIdx.x;
     const int u = static_cast<int>(row / Q);
-    const int n = row_len(n_rows, u, N_cap);             // no kernel of this library writes n_rows
+    const int n_given = n_rows[u];                      // no kernel of this library writes n_rows
+    const int n = clamp_rows(n_given, N_cap);
     pdl_wait();
     extern __shared__ __align__(16) uint8_t row_smem[];
     uint2 *cand = reinterpret_cast<uint2 *>(row_smem);                          // [CAP]
     int32_t *sel = reinterpret_cast<int32_t *>(row_smem + CAP * 8);             // [SEL]
     uint32_t *list = reinterpret_cast<uint32_t *>(row_smem + CAP * 8 + SEL * 4);   // [kFastList]
     SelSmem &S = *reinterpret_cast<SelSmem *>(row_smem + CAP * 8 + SEL * 4 + kFastList * 4);
-    if (threadIdx.x == 0 && row % Q == 0 && (n_rows[u] < 0 || n_rows[u] > N_cap)) report(status, DS4A_DEV_BOUNDS);
+    if (threadIdx.x == 0 && row % Q == 0 && n != n_given) report(status, DS4A_DEV_BOUNDS);
     const float *s = scores + row * N_cap;
     const uint32_t k = static_cast<uint32_t>(top_k);
     int32_t *out = idx_out + row * top_k;
@@ -915,11 +894,12 @@ __global__ void __launch_bounds__(kSplitThreads) topk_split_kernel(const __grid_
     const long long row = blockIdx.x / a.C;
     const int c = static_cast<int>(blockIdx.x - row * a.C);
     const int u = static_cast<int>(row / a.Q);
-    const int n = row_len(a.n_rows, u, a.N_cap);        // no kernel of this library writes n_rows
+    const int n_given = a.n_rows[u];                    // no kernel of this library writes n_rows
+    const int n = clamp_rows(n_given, a.N_cap);
     pdl_wait();
     __shared__ SelSmem S;
     __shared__ uint2 queue[kTopkSplitSlot];
-    if (c == 0 && threadIdx.x == 0 && row % a.Q == 0 && (a.n_rows[u] < 0 || a.n_rows[u] > a.N_cap))
+    if (c == 0 && threadIdx.x == 0 && row % a.Q == 0 && n != n_given)
         report(a.status, DS4A_DEV_BOUNDS);
     const float *s = a.scores + row * a.N_cap;
     const uint32_t k = static_cast<uint32_t>(a.top_k);
@@ -1157,9 +1137,10 @@ __global__ void __launch_bounds__(kClusterThreads) topk_cluster_kernel(const __g
     const uint32_t q = cluster_rank();
     const long long row = blockIdx.x / C;
     const int u = static_cast<int>(row / a.Q);
-    const int n = row_len(a.n_rows, u, a.N_cap);        // no kernel of this library writes n_rows
+    const int n_given = a.n_rows[u];                    // no kernel of this library writes n_rows
+    const int n = clamp_rows(n_given, a.N_cap);
     pdl_wait();
-    if (q == 0 && threadIdx.x == 0 && row % a.Q == 0 && (a.n_rows[u] < 0 || a.n_rows[u] > a.N_cap))
+    if (q == 0 && threadIdx.x == 0 && row % a.Q == 0 && n != n_given)
         report(a.status, DS4A_DEV_BOUNDS);
     const float *s = a.scores + row * a.N_cap;
     const uint32_t k = static_cast<uint32_t>(a.top_k);

@@ -167,7 +167,12 @@ ds4a_status ds4a_indexer_score(const uint16_t *iq, const float *w, const uint16_
  *    equal.
  *
  *    scores  fp32 [U][Q][N_cap] (device), as written by ds4a_indexer_score.
- *    n_rows  int32 [U] (device).
+ *    n_rows  int32 [U] (device).  Read as soon as the kernels start, before
+ *            they wait for the previous kernel on the stream: it must not be
+ *            written by a kernel that lets its dependents launch early
+ *            (programmatic dependent launch) right before this call.  Work
+ *            without that feature, copies, and every call of this library
+ *            are fine.
  *    idx     int32 [U][Q][top_k] (device): the selected row indices in
  *            ascending order, then -1 padding.
  *    count   int32 [U][Q] (device): number selected = min(top_k, visible).
