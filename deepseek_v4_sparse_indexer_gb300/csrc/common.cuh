@@ -175,6 +175,16 @@ DS4A_DEV bool mbar_wait_hint(uint64_t *bar, uint32_t parity, volatile int *abort
 DS4A_DEV void tma_prefetch_desc(const void *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from
+// global memory into this CTA's shared memory, completing on `bar`.
+DS4A_DEV void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    uint64_t g;
+    asm("cvta.to.global.u64 %0, %1;" : "=l"(g) : "l"(src));
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(g), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
 // L2 prefetch of one box of a tensor map (no shared memory, no barrier).  L2 is
 // the device's point of coherence, so a prefetch issued before the previous
 // kernel has finished writing the tensor cannot leave a stale copy behind.

@@ -1019,12 +1019,20 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const __grid_constant__
         return c == c0 ? 2LL * c + (static_cast<long long>(c) * T / g_rem == vs ? 0 : 1) : 2LL * c;
     };
     const float NEG_INF = -__int_as_float(0x7f800000);
-    // Thread i < np loads piece i's (m, l): one round trip for all pieces.
-    // The O rows then load eight pieces at a time, all in flight together.
-    // The sums run in piece order, as a sequential loop would.
+    // One round trip for the first kEarly pieces: thread i < np loads piece
+    // i's (m, l) and every thread its four dims of those pieces' O rows, all in
+    // flight together; pieces past kEarly (top_k > 896) then load eight at a
+    // time.  The sums run in piece order, as a sequential loop would.
+    constexpr int kEarly = 16;
     __shared__ float s_w[kMergeMaxPieces], s_l[kMergeMaxPieces];
     __shared__ float s_max[4];
     const int np = c1 - c0 + 1;                              // <= tiles per unit <= kMergeMaxPieces
+    const int d = threadIdx.x * 4;
+    float4 oe[kEarly];
+#pragma unroll
+    for (int j = 0; j < kEarly; ++j)
+        oe[j] = j < np ? *reinterpret_cast<const float4 *>(wo + (piece_slot(c0 + j) * kNHead + h) * kHeadDim + d)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
     float mk = NEG_INF, lk = 0.f;
     if (threadIdx.x < np) {
         const float2 p = *reinterpret_cast<const float2 *>(ml + (piece_slot(c0 + threadIdx.x) * kNHead + h) * 2);
@@ -1046,9 +1054,17 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const __grid_constant__
     __syncthreads();
     float L = 0.f;
     for (int i = 0; i < np; ++i) L += s_w[i] * s_l[i];
-    const int d = threadIdx.x * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i0 = 0; i0 < np; i0 += 8) {
+#pragma unroll
+    for (int j = 0; j < kEarly; ++j) {
+        if (j >= np || s_w[j] == 0.f) continue;             // an empty piece's O was never written
+        const float wk = s_w[j];
+        acc.x += wk * oe[j].x;
+        acc.y += wk * oe[j].y;
+        acc.z += wk * oe[j].z;
+        acc.w += wk * oe[j].w;
+    }
+    for (int i0 = kEarly; i0 < np; i0 += 8) {
         float4 o[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {

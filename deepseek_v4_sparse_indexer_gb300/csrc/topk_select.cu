@@ -22,7 +22,8 @@
 //   topk_cluster_kernel     up to 16 rows of 4,097 .. 524,288 scores (long-
 //                           context and small decode batches): a cluster of
 //                           eight CTAs per row, the selection agreed through
-//                           distributed shared memory;
+//                           distributed shared memory (up to 8 rows: each
+//                           CTA's chunk comes in by bulk copies);
 //   topk_split_kernel +     up to 76 rows of more than 524,288 scores: C CTAs
 //   topk_split_final_kernel per row each filter a chunk of the row against the
 //                           same T0 into a candidate slot of their own in the
@@ -459,7 +460,7 @@ DS4A_DEV void write_sorted(int32_t *sel, int32_t *tmp, uint32_t *bm, int bm_word
         block_bitonic_sort_asc(sel, p2);
         for (uint32_t i = threadIdx.x; i < k; i += nt) out[i] = i < m ? sel[i] : -1;
     } else {
-        constexpr int kMaxE = 4;                                 // 1,024 / 256 threads
+        constexpr int kMaxE = 4;       // p2 / threads: 1,024 / 256, or 512 / 128 (the 128-thread shape has k <= 512)
         const int E = p2 > nt ? p2 / nt : 1;
         const bool active = static_cast<int>(threadIdx.x) < p2;  // warp-uniform (p2 >= 32)
         int32_t x[kMaxE];
@@ -637,7 +638,7 @@ DS4A_DEV void select_exact_row(const float *__restrict__ s, int n, uint32_t k, S
 }
 
 // Threshold estimate for a row of n > all_below >= 4,096 scores: a key T0 with
-// about (or a little more than) kSampleOver * k of the row's visible keys at or
+// about (or a little more than) kOver * k of the row's visible keys at or
 // above it, from up to kSample scores (whole 128-byte lines spread evenly over the row, so
 // that the sample costs whole lines, not scattered sectors).  Each
 // warp's share of the sample is spread over the whole row; a warp pulls out
@@ -647,7 +648,7 @@ DS4A_DEV void select_exact_row(const float *__restrict__ s, int n, uint32_t k, S
 // the warps' last keys), so at least r sample keys lie at or above it.  0
 // (every visible row) when n <= all_below or the sample has fewer than r
 // visible keys.
-template <int NT, int kSample>
+template <int NT, int kSample, int kOver = kSampleOver>
 DS4A_DEV uint32_t sample_threshold(const float *__restrict__ s, int n, uint32_t k, int all_below, SelSmem &S) {
     if (n <= all_below) return 0u;
     constexpr int kPer = kSample / NT;
@@ -656,7 +657,7 @@ DS4A_DEV uint32_t sample_threshold(const float *__restrict__ s, int n, uint32_t 
     // wanted sample rank stays near 64 instead of growing with kSample / n.
     int samples = kSample;
     while (samples > NT && samples > 1024 &&
-           static_cast<long long>(kSampleOver) * k * (samples / 2) >= 64LL * n)
+           static_cast<long long>(kOver) * k * (samples / 2) >= 64LL * n)
         samples >>= 1;
     const int per = samples / NT, lines = samples / 32;
     const int lsh = 31 - __clz(lines);                        // lines is a power of two
@@ -673,7 +674,7 @@ DS4A_DEV uint32_t sample_threshold(const float *__restrict__ s, int n, uint32_t 
             key[j] = score_visible(f) ? float_key(f) : 0u;
         }
     }
-    const long long r_want = (static_cast<long long>(kSampleOver) * k * samples + n - 1) / n;
+    const long long r_want = (static_cast<long long>(kOver) * k * samples + n - 1) / n;
     const int r = static_cast<int>(r_want < samples ? r_want : samples);
     // rw = the wanted rank's share per warp and two more, so that the union of
     // the warps' lists most likely holds the sample's r largest keys; when the
@@ -744,17 +745,20 @@ DS4A_DEV uint32_t sample_threshold(const float *__restrict__ s, int n, uint32_t 
 //    per float4, one shared atomic per warp and float4) counts the visible
 //    scores and appends every row with key >= T0 to the shared candidate list;
 // 3. the selection from the list when it decides it, else from the row.
-// Two shapes: 512 threads and 8,192 candidates (any k), two CTAs per SM; for
-// k <= kRowSmallMaxK 256 threads, 4,096 candidates, four CTAs per SM (a row's
-// phases are latency-bound: more rows in flight beat more threads per row).
+// Three shapes: 512 threads and 8,192 candidates (any k), two CTAs per SM; for
+// k <= kRowSmallMaxK 256 threads, 4,096 candidates, four CTAs per SM; and for
+// k <= kRowTinyMaxK in batches of at least four rows per SM, 128 threads, 2,048
+// candidates (the threshold aimed at 2k), eight CTAs per SM.  A row's phases
+// are latency-bound: more rows in flight beat more threads per row.
 constexpr int kRowSmallMaxK = 640;
+constexpr int kRowTinyMaxK = 512;
 template <int NT, int CAP, int SEL>
 struct RowShape {
     static constexpr int kSmem = CAP * 8 + SEL * 4 + kFastList * 4 + static_cast<int>(sizeof(SelSmem));
 };
 
 template <int NT, int CAP, int SEL>
-__global__ void __launch_bounds__(NT, NT == 512 ? 2 : 4) topk_row_kernel(const float *__restrict__ scores,
+__global__ void __launch_bounds__(NT, 1024 / NT) topk_row_kernel(const float *__restrict__ scores,
                                                                   const int32_t *__restrict__ n_rows, int Q,
                                                                   int N_cap, int top_k,
                                                                   int32_t *__restrict__ idx_out,
@@ -778,7 +782,7 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 2 : 4) topk_row_kernel(const f
 
     constexpr int B = 4;
     const int ngroups = (n + 3) / 4;
-    const bool vec4 = (N_cap & 3) == 0;
+    const bool vec4 = (N_cap & 3) == 0 && (reinterpret_cast<uintptr_t>(scores) & 15) == 0;
     auto load = [&](float4 (&v)[B], int g0) {
 #pragma unroll
         for (int j = 0; j < B; ++j) {
@@ -788,7 +792,8 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 2 : 4) topk_row_kernel(const f
     };
     float4 cur[B], nxt[B];
     if (vec4) load(cur, 0);                              // in flight during the threshold estimate
-    const uint32_t T0 = sample_threshold<NT, kSampleRow>(s, n, k, CAP, S);
+    // 2,048 candidates (128 threads) aim at 2k, the larger lists at 3k
+    const uint32_t T0 = sample_threshold<NT, kSampleRow, CAP <= 2048 ? 2 : kSampleOver>(s, n, k, CAP, S);
     sel_reset(S);
     __syncthreads();
     uint32_t my_vis = 0, kmn = 0xffffffffu, kmx = 0u;      // visible count, candidates' key range
@@ -905,7 +910,8 @@ __global__ void __launch_bounds__(kSplitThreads) topk_split_kernel(const __grid_
     const uint32_t k = static_cast<uint32_t>(a.top_k);
     const int start = c * a.chunk;
     const int end = min(start + a.chunk, n);
-    const bool vec4 = (a.N_cap & 3) == 0;               // chunk is a multiple of 4: float4 groups stay inside
+    // chunk is a multiple of 4: float4 groups stay inside
+    const bool vec4 = (a.N_cap & 3) == 0 && (reinterpret_cast<uintptr_t>(a.scores) & 15) == 0;
     // The first batch of the chunk's loads goes out before the sample's.
     constexpr int B = 8;
     const int g_beg = start / 4, g_end = (end + 3) / 4;
@@ -1099,17 +1105,34 @@ constexpr int kClusterMaxRows = 16;       // more rows: one CTA per row is as fa
 constexpr int kClusterMinRow = 4096;       // rows up to this long: one CTA per row (every row a candidate)
 constexpr int kClusterAllBelow = 8192;     // rows up to this long need no sampled threshold
 
+constexpr int kRingPiece = 8192;           // scores per bulk copy (32 KB)
+constexpr int kRingStages = 4;             // copies in flight: the whole chunk of a row of up to 262,144 scores
+// Up to this many rows the chunks go through the bulk-copy ring; more rows
+// (more clusters of 182 KB CTAs to place at once) load through registers:
+// 16 x 65,536 scores, step 78.9 vs 88.5 us; 8 x 16,384 35.7 vs 38.4 us and
+// 4 x 262,144 75.0 vs 76.8 us the other way.
+constexpr int kClusterRingRows = 8;
+
+template <bool RING>
 struct __align__(16) ClusterSmem {
+    float ring[RING ? kRingStages : 1][RING ? kRingPiece : 4];   // the CTA's chunk of scores, 32 KB at a time
     uint2 cand[kClusterCap];
-    int32_t sel[kMaxTopK];
+    int32_t sel[kMaxTopK];                 // read as int4
     int32_t tie[kFastList];
-    uint32_t list[kFastList];              // the crossing bucket's keys of every CTA, CTA-ordered
+    uint32_t list[kFastList];              // the crossing bucket's keys of every CTA, CTA-ordered; read as uint4
     uint32_t stat[kClusterRowCtas][4];     // per CTA: candidates, visible rows, smallest key, largest key
     uint32_t hist[kClusterRowCtas][32];    // per CTA: bucket counts
     uint32_t seg[kClusterRowCtas][2];      // per CTA: crossing-bucket rows above T, rows equal to T
     uint32_t warp_cnt[kClusterThreads / 32][32];
     SelSmem S;
+    uint64_t full[kRingStages];            // ring stage landed
+    int abort;
 };
+static_assert(offsetof(ClusterSmem<true>, ring) % 16 == 0 && offsetof(ClusterSmem<true>, sel) % 16 == 0 &&
+                  offsetof(ClusterSmem<true>, list) % 16 == 0 && offsetof(ClusterSmem<true>, S) % 16 == 0 &&
+                  offsetof(ClusterSmem<true>, full) % 8 == 0 && offsetof(ClusterSmem<false>, sel) % 16 == 0 &&
+                  offsetof(ClusterSmem<false>, list) % 16 == 0 && offsetof(ClusterSmem<false>, S) % 16 == 0,
+              "bulk copies, vector loads and mbarriers need their alignment");
 
 // Each of sel[0 .. m) (distinct rows) to out[base + its rank among them].
 DS4A_DEV void rank_write(const int32_t *sel, uint32_t m, int32_t *out) {
@@ -1127,10 +1150,11 @@ DS4A_DEV void rank_write(const int32_t *sel, uint32_t m, int32_t *out) {
     }
 }
 
+template <bool RING>
 __global__ void __launch_bounds__(kClusterThreads) topk_cluster_kernel(const __grid_constant__ TopkArgs a, int chunk) {
     pdl_launch_dependents();
     extern __shared__ __align__(16) uint8_t cl_smem[];
-    ClusterSmem &M = *reinterpret_cast<ClusterSmem *>(cl_smem);
+    ClusterSmem<RING> &M = *reinterpret_cast<ClusterSmem<RING> *>(cl_smem);
     SelSmem &S = M.S;
     constexpr int C = kClusterRowCtas, NT = kClusterThreads, NW = NT / 32;
     static_assert(C <= NW, "a warp per CTA of the cluster counts its crossing-bucket segment");
@@ -1148,8 +1172,32 @@ __global__ void __launch_bounds__(kClusterThreads) topk_cluster_kernel(const __g
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int start = static_cast<int>(q) * chunk;          // chunk is a multiple of 4
     const int end = min(start + chunk, n);
-    const bool vec4 = (a.N_cap & 3) == 0;
-    constexpr int B = 8;                                      // float4 loads per thread in flight
+    const bool vec4 = (a.N_cap & 3) == 0 && (reinterpret_cast<uintptr_t>(a.scores) & 15) == 0;
+    // The chunk goes into shared memory by bulk copies, 32 KB each, up to four
+    // in flight from the start (an SM keeps far more bytes in flight this way
+    // than with its threads' loads); the sample's loads run beside them.  The
+    // last copy is rounded up to 16 bytes: still inside the row's N_cap
+    // entries (N_cap is a multiple of 4 here), the excess is never looked at.
+    const int len4 = end > start ? ((end - start + 3) & ~3) : 0;
+    const int n_pieces = (len4 + kRingPiece - 1) / kRingPiece;
+    auto issue = [&](int p) {
+        const int off = p * kRingPiece;
+        const uint32_t bytes = static_cast<uint32_t>(min(kRingPiece, len4 - off)) * 4u;
+        uint64_t *bar = &M.full[p % kRingStages];
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_load(M.ring[p % kRingStages], s + start + off, bytes, bar);
+    };
+    if constexpr (RING) {
+        if (vec4 && threadIdx.x == 0) {
+            for (int i = 0; i < kRingStages; ++i) mbar_init(&M.full[i], 1);
+            M.abort = 0;
+            mbar_fence_init();
+            for (int p = 0; p < min(kRingStages, n_pieces); ++p) issue(p);
+        }
+    }
+    // Without the ring: eight float4 loads per thread in flight, the first
+    // batch during the sample.
+    constexpr int B = 8;
     const int g_beg = start / 4, g_end = end > start ? (end + 3) / 4 : g_beg;
     float4 v[B];
     auto load = [&](int g0) {
@@ -1159,7 +1207,7 @@ __global__ void __launch_bounds__(kClusterThreads) topk_cluster_kernel(const __g
             v[j] = g < g_end ? __ldg(reinterpret_cast<const float4 *>(s) + g) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     };
-    if (vec4) load(g_beg);                                    // in flight during the sample
+    if (!RING && vec4) load(g_beg);
     const uint32_t T0 = sample_threshold<NT, kSampleSplit>(s, n, k, kClusterAllBelow, S);
     sel_reset(S);
     __syncthreads();
@@ -1170,46 +1218,68 @@ __global__ void __launch_bounds__(kClusterThreads) topk_cluster_kernel(const __g
     const bool take_all = T0 == 0u;
     const float T0f = key_float(T0);
     const float kNegInf = -__int_as_float(0x7f800000);
-    if (vec4) {
+    // One float4 of scores (rows i .. i+3); every lane of the warp calls it.
+    auto consume = [&](const float4 v, int i) {
+        const float f[4] = {v.x, v.y, v.z, v.w};
+        bool take[4];
+        bool any = false;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const bool vis = i + c < end && f[c] > kNegInf;
+            my_vis += vis ? 1u : 0u;
+            take[c] = vis && (take_all || f[c] >= T0f);
+            any |= take[c];
+        }
+        if (!__any_sync(0xffffffffu, any)) return;
+        uint32_t key[4], bal[4], tot = 0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            key[c] = float_key(f[c]);
+            kmn = take[c] ? min(kmn, key[c]) : kmn;
+            kmx = take[c] ? max(kmx, key[c]) : kmx;
+            bal[c] = __ballot_sync(0xffffffffu, take[c]);
+            tot += __popc(bal[c]);
+        }
+        uint32_t pos = 0;                                     // one shared atomic per warp and float4
+        if (lane == 0) pos = atomicAdd(&S.cnt[3], tot);
+        pos = __shfl_sync(0xffffffffu, pos, 0);
+        const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t p = pos + __popc(bal[c] & lt);
+            if (take[c] && p < static_cast<uint32_t>(kClusterCap)) M.cand[p] = make_uint2(key[c], static_cast<uint32_t>(i + c));
+            pos += __popc(bal[c]);
+        }
+    };
+    if (RING && vec4) {
+        if constexpr (RING) {
+            bool ring_ok = true;
+            for (int pc = 0; pc < n_pieces; ++pc) {           // block-uniform
+                const int st = pc % kRingStages;
+                // a copy that never lands is reported; the pass goes on (on what
+                // the buffer holds) so that every CTA still meets the cluster barriers
+                if (ring_ok && !mbar_wait(&M.full[st], static_cast<uint32_t>(pc / kRingStages) & 1u, &M.abort)) {
+                    ring_ok = false;
+                    *reinterpret_cast<volatile int *>(&M.abort) = 1;     // the others stop waiting too
+                    if (threadIdx.x == 0) report(a.status, DS4A_DEV_TIMEOUT);
+                }
+                const int off = pc * kRingPiece;
+                const int cnt4 = min(kRingPiece, len4 - off) / 4;
+                const float4 *r4 = reinterpret_cast<const float4 *>(M.ring[st]);
+#pragma unroll 2
+                for (int g0 = 0; g0 < cnt4; g0 += NT) {      // block-uniform
+                    const int g = g0 + static_cast<int>(threadIdx.x);
+                    consume(g < cnt4 ? r4[g] : make_float4(0.f, 0.f, 0.f, 0.f), start + off + 4 * g);
+                }
+                __syncthreads();                              // stage st read by every thread
+                if (threadIdx.x == 0 && pc + kRingStages < n_pieces) issue(pc + kRingStages);
+            }
+        }
+    } else if (vec4) {
         for (int g0 = g_beg; g0 < g_end; g0 += B * NT) {     // block-uniform
             if (g0 != g_beg) load(g0);
 #pragma unroll
-            for (int j = 0; j < B; ++j) {
-                const int i = 4 * (g0 + j * NT + static_cast<int>(threadIdx.x));
-                const float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-                bool take[4];
-                bool any = false;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const bool vis = i + c < end && f[c] > kNegInf;
-                    my_vis += vis ? 1u : 0u;
-                    take[c] = vis && (take_all || f[c] >= T0f);
-                    any |= take[c];
-                }
-                if (!__any_sync(0xffffffffu, any)) continue;
-                uint32_t key[4], bal[4], tot = 0;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    key[c] = float_key(f[c]);
-                    kmn = take[c] ? min(kmn, key[c]) : kmn;
-                    kmx = take[c] ? max(kmx, key[c]) : kmx;
-                    bal[c] = __ballot_sync(0xffffffffu, take[c]);
-                    tot += __popc(bal[c]);
-                }
-                {                                             // one shared atomic per warp and float4
-                    uint32_t pos = 0;
-                    if (lane == 0) pos = atomicAdd(&S.cnt[3], tot);
-                    pos = __shfl_sync(0xffffffffu, pos, 0);
-                    const uint32_t lt = (1u << lane) - 1u;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint32_t p = pos + __popc(bal[c] & lt);
-                        if (take[c] && p < static_cast<uint32_t>(kClusterCap))
-                            M.cand[p] = make_uint2(key[c], static_cast<uint32_t>(i + c));
-                        pos += __popc(bal[c]);
-                    }
-                }
-            }
+            for (int j = 0; j < B; ++j) consume(v[j], 4 * (g0 + j * NT + static_cast<int>(threadIdx.x)));
         }
     } else {
         for (int b = start; b < end; b += NT) {              // block-uniform
@@ -1523,13 +1593,16 @@ cudaError_t launch_topk(const TopkArgs &a, int num_sms, cudaStream_t s) {
     const long long R = static_cast<long long>(a.U) * a.Q;
     if (R <= 0) return cudaSuccess;
     if (R <= kClusterMaxRows && a.N_cap > kClusterMinRow && a.N_cap <= kTopkSplitMinRow) {
-        const int smem = static_cast<int>(sizeof(ClusterSmem));
-        cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
         int chunk = (a.N_cap + kClusterRowCtas - 1) / kClusterRowCtas;
         chunk = (chunk + 3) & ~3;
-        return launch_k_cluster(topk_cluster_kernel, dim3(static_cast<unsigned>(R * kClusterRowCtas)),
-                                dim3(kClusterThreads), smem, kClusterRowCtas, s, a, chunk);
+        auto go = [&](auto kern, int smem) -> cudaError_t {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return e;
+            return launch_k_cluster(kern, dim3(static_cast<unsigned>(R * kClusterRowCtas)), dim3(kClusterThreads), smem,
+                                    kClusterRowCtas, s, a, chunk);
+        };
+        if (R <= kClusterRingRows) return go(topk_cluster_kernel<true>, static_cast<int>(sizeof(ClusterSmem<true>)));
+        return go(topk_cluster_kernel<false>, static_cast<int>(sizeof(ClusterSmem<false>)));
     }
     if (!split_rows(R, a.N_cap) || R >= num_sms) {
         // One CTA per row, no workspace.
@@ -1540,6 +1613,8 @@ cudaError_t launch_topk(const TopkArgs &a, int num_sms, cudaStream_t s) {
             return launch_k(kern, dim3(static_cast<unsigned>(R)), dim3(nt), smem, s, a.scores, a.n_rows, a.Q, a.N_cap,
                             a.top_k, a.idx, a.count, a.status);
         };
+        if (a.top_k <= kRowTinyMaxK && R >= 4LL * num_sms)
+            return go(topk_row_kernel<128, 2048, kRowTinyMaxK>, 128, RowShape<128, 2048, kRowTinyMaxK>::kSmem);
         if (a.top_k <= kRowSmallMaxK)
             return go(topk_row_kernel<256, 4096, 1024>, 256, RowShape<256, 4096, 1024>::kSmem);
         return go(topk_row_kernel<512, 8192, kMaxTopK>, 512, RowShape<512, 8192, kMaxTopK>::kSmem);

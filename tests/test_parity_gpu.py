@@ -163,10 +163,16 @@ def test_indexer_row_count_out_of_range_is_clamped_and_flagged():
 # A2 top-k on given scores: bit-exact against the oracle
 # ----------------------------------------------------------------------------
 
-def topk_case(rows_f32, n_rows, top_k):
-    """rows_f32: float32 [R, N_cap] (one unit per row); checks every row exactly."""
+def topk_case(rows_f32, n_rows, top_k, shift=0):
+    """rows_f32: float32 [R, N_cap] (one unit per row); checks every row exactly.
+    shift > 0 places the scores `shift` floats past a 16-byte boundary."""
     R, N_cap = rows_f32.shape
-    s = torch.from_numpy(rows_f32).cuda().view(R, 1, N_cap)
+    if shift:
+        buf = torch.zeros(R * N_cap + shift, dtype=torch.float32, device="cuda")
+        buf[shift:] = torch.from_numpy(rows_f32).cuda().view(-1)
+        s = buf[shift:].view(R, 1, N_cap)
+    else:
+        s = torch.from_numpy(rows_f32).cuda().view(R, 1, N_cap)
     nr = torch.tensor(n_rows, dtype=torch.int32).cuda()
     idx = torch.full((R, 1, top_k), 777, dtype=torch.int32, device="cuda")
     cnt = torch.full((R, 1), -5, dtype=torch.int32, device="cuda")
@@ -250,6 +256,27 @@ def test_topk_cluster_rows_k_extremes_and_odd_stride(k):
     x = rng.standard_normal((3, 70001)).astype(np.float32)   # N_cap not a multiple of 4: scalar loads
     x[1, rng.random(70001) < 0.05] *= 4
     topk_case(x, [70001, 70000, 2047], k)
+
+
+def test_topk_cluster_rows_longest_chunks_refill_the_ring():
+    # 524,288 scores: 65,536 per CTA, eight 32 KB bulk copies through a ring of
+    # four; ragged ends exercise the copy rounded up to 16 bytes
+    rng = np.random.default_rng(25)
+    N = 524288
+    x = rng.standard_normal((3, N)).astype(np.float32)
+    x[1, rng.random(N) < 0.05] *= 4
+    x[2, 300000:300100] = 9.0                                 # the top rows inside one copy
+    topk_case(x, [N, 400001, 262147], 512)
+
+
+@pytest.mark.parametrize("shape", [(3, 100000), (160, 9000), (2, 600000)])
+def test_topk_scores_not_16_byte_aligned(shape):
+    # 4-byte aligned scores (the API's requirement) one float past a 16-byte
+    # boundary: every kernel takes its scalar loads
+    R, N = shape
+    rng = np.random.default_rng(26 + R)
+    x = rng.standard_normal((R, N)).astype(np.float32)
+    topk_case(x, [N - (r % 3) * 7 for r in range(R)], 512, shift=1)
 
 
 def test_topk_cluster_rows_all_candidates_and_sixteen_rows():
@@ -342,6 +369,25 @@ def test_topk_rows_all_equal_sorted_and_prefix_visible():
     for r in range(3, ROWS_MANY, 4):                            # visible prefix, -inf after (causal)
         x[r, rng.integers(100, 16384):] = -np.inf
     topk_case(x, _many(rng, 16384, [16384, 16383, 9000]), 512)
+
+
+# Batches of at least four rows per SM with k <= 512 take the 128-thread shape
+# (2,048 candidates, the threshold aimed at 2k, eight CTAs per SM).
+ROWS_LOTS = 640      # >= 4 x 152
+
+@pytest.mark.parametrize("k", [1, 100, 512, 513])
+def test_topk_rows_large_batches_small_shape(k):
+    rng = np.random.default_rng(30 + k)
+    N = 20000
+    x = rng.standard_normal((ROWS_LOTS, N)).astype(np.float32)
+    x[0::8] = np.round(x[0::8] * 2) / 2                          # heavy ties at the k-th score
+    x[1::8][:, rng.random(N) < 0.3] = -np.inf
+    x[2::8][:, rng.random(N) < 0.1] = np.nan
+    x[3::8] = 0.25                                               # all equal: candidate overflow
+    x[4::8, 15000:] += 3.0                                       # the top rows crowded at the end
+    x[5::8][:, rng.random(N) < 0.05] *= 4                        # heavy tail
+    lens = [N, N - 1, 4097, 2049, 2048, 513, 77, 0]
+    topk_case(x, [lens[(r // 8) % len(lens)] for r in range(ROWS_LOTS)], k)
 
 
 @pytest.mark.parametrize("k", [1, 2048])
