@@ -311,7 +311,11 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
         if (lane == 0) prefetch_share_head(a, share_lo, share_hi, G);
         pdl_wait();
         if (lane == 0) {
-            const uint64_t pol_stream = l2_policy_evict_first();
+            // Decode (G = 1) reads every key tile once: stream it through L2.  A
+            // prefill chunk's query groups all read the same key tiles: keep
+            // them in L2 (evict-first keys were re-read from DRAM once the
+            // scores written meanwhile had pushed them out).
+            const uint64_t pol_stream = G == 1 ? l2_policy_evict_first() : l2_policy_evict_last();
             const uint64_t pol_keep = l2_policy_evict_last();
             int s = 0, bb = 0;
             uint32_t sph = 0, bph = 0;
