@@ -1173,9 +1173,10 @@ __global__ void __launch_bounds__(kClusterThreads) topk_cluster_kernel(const __g
     const int start = static_cast<int>(q) * chunk;          // chunk is a multiple of 4
     const int end = min(start + chunk, n);
     const bool vec4 = (a.N_cap & 3) == 0 && (reinterpret_cast<uintptr_t>(a.scores) & 15) == 0;
-    // The chunk goes into shared memory by bulk copies, 32 KB each, up to four
-    // in flight from the start (an SM keeps far more bytes in flight this way
-    // than with its threads' loads); the sample's loads run beside them.  The
+    // With the ring (RING: batches of up to kClusterRingRows rows) the chunk
+    // goes into shared memory by bulk copies, 32 KB each, up to four in flight
+    // from the start (an SM keeps far more bytes in flight this way than with
+    // its threads' loads); the sample's loads run beside them.  The
     // last copy is rounded up to 16 bytes: still inside the row's N_cap
     // entries (N_cap is a multiple of 4 here), the excess is never looked at.
     const int len4 = end > start ? ((end - start + 3) & ~3) : 0;
