@@ -173,6 +173,17 @@ def dram_traffic(kernel, units, rows):
         return None
 
 
+def attn_merge_launches(units, top_k, n_sms):
+    """1 when the attention call launches its merge kernel after the attention
+    kernel (the library's launch rule: the units left after whole rounds over
+    the CTAs are cut into pieces, which the merge kernel combines)."""
+    nt = -(-top_k // 64) + 2
+    T = units * nt
+    G = min(n_sms, 160, T)
+    u_rem = units - (units // G) * G
+    return 1 if min(u_rem * nt, G) > 1 else 0
+
+
 def build_fp8_store(pkg, chunks, shape, dev):
     """The FP8 row store (E4M3 codes, power-of-two row scales) of a workload's
     fp32 rows, built chunk by chunk by the library's quantiser (untimed setup)."""
@@ -630,11 +641,10 @@ def main():
     if wl.kind == "pool":
         launches_per_step = 2
     elif wl.kind == "dense":
-        launches_per_step = 1 + (1 if pkg.ds4a_workspace_bytes(4, wl.units, 1, wl.n_rows, 0) else 0)
+        launches_per_step = 1 + attn_merge_launches(wl.units, wl.n_rows, n_sms)
     else:
-        launches_per_step = 1 + 1 + 1 + (1 if pkg.ds4a_workspace_bytes(
-            (2 if wl.kind == "decode" else 3) | (0x100 if wl.heads == 128 else 0), wl.units if wl.kind == "decode" else 1,
-            1 if wl.kind == "decode" else wl.queries, wl.n_rows, wl.top_k) else 0)
+        sub_units = (wl.units if wl.kind == "decode" else wl.queries) * (2 if wl.heads == 128 else 1)
+        launches_per_step = 1 + 1 + 1 + attn_merge_launches(sub_units, wl.top_k, n_sms)
         if wl.units * wl.queries <= 76 and not fused and wl.n_rows > (1 << 19):
             launches_per_step += 1            # top-k over few very long rows: a filter pass before the final one
         if fused:

@@ -440,12 +440,13 @@ def test_attention_one_cta_per_unit(q_scale):
 
 
 @pytest.mark.parametrize("U,top_k", [(152, 512), (305, 512), (457, 64), (40, 512), (17, 64), (9, 64), (16, 512),
-                                     (1, 512)])
+                                     (1, 512), (19, 512), (20, 512), (19, 384), (3, 320)])
 def test_attention_work_schedule(U, top_k):
     # Whole strided rounds of 152 units, then the remainder units' tiles cut
     # into equal shares: no remainder, one remainder unit over ten CTAs, three-
     # tile units, and fewer units than CTAs (pieces merged by a second kernel:
-    # one-tile pieces, shares of several tiles, a single unit over ten CTAs).
+    # one-tile pieces, shares of several tiles, a single unit over ten CTAs,
+    # 19 and 20 units of ten tiles, 19 units of eight, 3 units of seven).
     attention_case(U, 600, top_k, seed=40 + U)
 
 
