@@ -1566,13 +1566,24 @@ __global__ void __launch_bounds__(kCandThreads, 3) topk_cand_kernel(const __grid
     uint2 *gc = a.cand + row * a.N_cap;
     const bool cached = nc <= static_cast<uint32_t>(kCandCache);
     uint32_t kmn = 0xffffffffu, kmx = 0u;
-    for (uint32_t i0 = 0; i0 < nc; i0 += kCandThreads) {             // block-uniform trip count
-        const uint32_t i = i0 + threadIdx.x;
-        if (i < nc) {
-            const uint2 e = gc[i];
-            if (cached) cache[i] = e;
-            kmn = min(kmn, e.x);
-            kmx = max(kmx, e.x);
+    // Four loads per thread in flight per round trip (the list was just written
+    // by the scan: L2 latency, not bandwidth, sets the pace).
+    constexpr int kBatch = 4;
+    for (uint32_t i0 = 0; i0 < nc; i0 += kBatch * kCandThreads) {    // block-uniform trip count
+        uint2 e[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const uint32_t i = i0 + j * kCandThreads + threadIdx.x;
+            e[j] = i < nc ? gc[i] : make_uint2(0u, 0u);
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const uint32_t i = i0 + j * kCandThreads + threadIdx.x;
+            if (i < nc) {
+                if (cached) cache[i] = e[j];
+                kmn = min(kmn, e[j].x);
+                kmx = max(kmx, e[j].x);
+            }
         }
     }
     warp_fold_minmax(kmn, kmx, S);
