@@ -1545,10 +1545,13 @@ bool split_rows(long long R, int N_cap) { return 2 * R <= kTopkSplitMaxCtas && N
 // selection over the list is the selection over the row.  One CTA per row;
 // the list is cached in shared memory when it fits, else used in place.
 constexpr int kCandThreads = 512;
-// 6,144 cached candidates (48 KB) let three CTAs share an SM.
-constexpr int kCandCache = 6144;
+// 6,144 cached candidates (48 KB) let three CTAs share an SM; 12,288 (96 KB), two.
+constexpr int kCandCacheSmall = 6144;
+constexpr int kCandCacheLarge = 12288;
 
-__global__ void __launch_bounds__(kCandThreads, 3) topk_cand_kernel(const __grid_constant__ TopkCandArgs a) {
+template <int kCandCache>
+__global__ void __launch_bounds__(kCandThreads, kCandCache > 6144 ? 2 : 3)
+    topk_cand_kernel(const __grid_constant__ TopkCandArgs a) {
     pdl_launch_dependents();
     pdl_wait();
     extern __shared__ __align__(16) uint8_t cand_smem[];
@@ -1659,10 +1662,16 @@ cudaError_t launch_topk(const TopkArgs &a, int num_sms, cudaStream_t s) {
 
 cudaError_t launch_topk_cand(const TopkCandArgs &a, cudaStream_t s) {
     if (a.R <= 0) return cudaSuccess;
-    const int smem = kCandCache * 8 + kMaxTopK * 4 + kFastList * 4 + static_cast<int>(sizeof(SelSmem));
-    cudaError_t e = cudaFuncSetAttribute(topk_cand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    return launch_k(topk_cand_kernel, dim3(a.R), dim3(kCandThreads), smem, s, a);
+    // top_k above 512 (the Pro shape's 1,024) leaves about twice the
+    // candidates: a list of 12,288 pairs, two CTAs per SM, keeps them cached.
+    auto go = [&](auto kern, int cache) -> cudaError_t {
+        const int smem = cache * 8 + kMaxTopK * 4 + kFastList * 4 + static_cast<int>(sizeof(SelSmem));
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        return launch_k(kern, dim3(a.R), dim3(kCandThreads), smem, s, a);
+    };
+    if (a.top_k > 512) return go(topk_cand_kernel<kCandCacheLarge>, kCandCacheLarge);
+    return go(topk_cand_kernel<kCandCacheSmall>, kCandCacheSmall);
 }
 
 }  // namespace ds4a
