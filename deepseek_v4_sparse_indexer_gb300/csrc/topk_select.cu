@@ -21,9 +21,10 @@
 // Four launch shapes:
 //   topk_cluster_kernel     up to 16 rows of 4,097 .. 524,288 scores (long-
 //                           context and small decode batches): a cluster of
-//                           eight CTAs per row, the selection agreed through
-//                           distributed shared memory (up to 8 rows: each
-//                           CTA's chunk comes in by bulk copies);
+//                           eight CTAs per row (sixteen for up to 4 rows), the
+//                           selection agreed through distributed shared memory
+//                           (up to 8 rows: each CTA's chunk comes in by bulk
+//                           copies);
 //   topk_split_kernel +     up to 76 rows of more than 524,288 scores: C CTAs
 //   topk_split_final_kernel per row each filter a chunk of the row against the
 //                           same T0 into a candidate slot of their own in the
@@ -1098,7 +1099,7 @@ __global__ void __launch_bounds__(kSplitFinalThreads) topk_split_final_kernel(co
 // row order) in ascending order at its offset.  A row the lists cannot decide
 // (a sample that missed, heavy ties) is selected by CTA 0 alone from the
 // row's scores.  No global scratch; three cluster barriers.
-constexpr int kClusterRowCtas = 8;        // 16 (non-portable) measured slower: 4 x 262,144 20.3 vs 17.0 us
+constexpr int kClusterRowCtas = 8;        // CTAs per row (16 for batches of up to kClusterWideRows rows)
 constexpr int kClusterThreads = 512;
 constexpr int kClusterCap = 4096;          // candidates per CTA
 constexpr int kClusterMaxRows = 16;       // more rows: one CTA per row is as fast
@@ -1112,26 +1113,33 @@ constexpr int kRingStages = 4;             // copies in flight: the whole chunk 
 // 16 x 65,536 scores, step 78.9 vs 88.5 us; 8 x 16,384 35.7 vs 38.4 us and
 // 4 x 262,144 75.0 vs 76.8 us the other way.
 constexpr int kClusterRingRows = 8;
+// Up to this many rows, sixteen CTAs per row (a non-portable cluster size):
+// half the chunk per CTA, which the bulk copies bring in twice as fast
+// (4 x 262,144 step 75.3 -> 73.4 us, 2 x 524,288 80.2 -> 74.3 us,
+// 1 x 131,072 39.5 -> 37.8 us; without the ring sixteen were slower).
+constexpr int kClusterWideRows = 4;
 
-template <bool RING>
+template <bool RING, int C = kClusterRowCtas>
 struct __align__(16) ClusterSmem {
     float ring[RING ? kRingStages : 1][RING ? kRingPiece : 4];   // the CTA's chunk of scores, 32 KB at a time
     uint2 cand[kClusterCap];
     int32_t sel[kMaxTopK];                 // read as int4
     int32_t tie[kFastList];
     uint32_t list[kFastList];              // the crossing bucket's keys of every CTA, CTA-ordered; read as uint4
-    uint32_t stat[kClusterRowCtas][4];     // per CTA: candidates, visible rows, smallest key, largest key
-    uint32_t hist[kClusterRowCtas][32];    // per CTA: bucket counts
-    uint32_t seg[kClusterRowCtas][2];      // per CTA: crossing-bucket rows above T, rows equal to T
+    uint32_t stat[C][4];                   // per CTA: candidates, visible rows, smallest key, largest key
+    uint32_t hist[C][32];                  // per CTA: bucket counts
+    uint32_t seg[C][2];                    // per CTA: crossing-bucket rows above T, rows equal to T
     uint32_t warp_cnt[kClusterThreads / 32][32];
     SelSmem S;
     uint64_t full[kRingStages];            // ring stage landed
     int abort;
 };
+using ClusterSmemWide = ClusterSmem<true, 16>;
 static_assert(offsetof(ClusterSmem<true>, ring) % 16 == 0 && offsetof(ClusterSmem<true>, sel) % 16 == 0 &&
                   offsetof(ClusterSmem<true>, list) % 16 == 0 && offsetof(ClusterSmem<true>, S) % 16 == 0 &&
                   offsetof(ClusterSmem<true>, full) % 8 == 0 && offsetof(ClusterSmem<false>, sel) % 16 == 0 &&
-                  offsetof(ClusterSmem<false>, list) % 16 == 0 && offsetof(ClusterSmem<false>, S) % 16 == 0,
+                  offsetof(ClusterSmem<false>, list) % 16 == 0 && offsetof(ClusterSmem<false>, S) % 16 == 0 &&
+                  offsetof(ClusterSmemWide, S) % 16 == 0 && offsetof(ClusterSmemWide, full) % 8 == 0,
               "bulk copies, vector loads and mbarriers need their alignment");
 
 // Each of sel[0 .. m) (distinct rows) to out[base + its rank among them].
@@ -1150,13 +1158,13 @@ DS4A_DEV void rank_write(const int32_t *sel, uint32_t m, int32_t *out) {
     }
 }
 
-template <bool RING>
+template <bool RING, int CL>
 __global__ void __launch_bounds__(kClusterThreads) topk_cluster_kernel(const __grid_constant__ TopkArgs a, int chunk) {
     pdl_launch_dependents();
     extern __shared__ __align__(16) uint8_t cl_smem[];
-    ClusterSmem<RING> &M = *reinterpret_cast<ClusterSmem<RING> *>(cl_smem);
+    ClusterSmem<RING, CL> &M = *reinterpret_cast<ClusterSmem<RING, CL> *>(cl_smem);
     SelSmem &S = M.S;
-    constexpr int C = kClusterRowCtas, NT = kClusterThreads, NW = NT / 32;
+    constexpr int C = CL, NT = kClusterThreads, NW = NT / 32;
     static_assert(C <= NW, "a warp per CTA of the cluster counts its crossing-bucket segment");
     const uint32_t q = cluster_rank();
     const long long row = blockIdx.x / C;
@@ -1608,16 +1616,23 @@ cudaError_t launch_topk(const TopkArgs &a, int num_sms, cudaStream_t s) {
     const long long R = static_cast<long long>(a.U) * a.Q;
     if (R <= 0) return cudaSuccess;
     if (R <= kClusterMaxRows && a.N_cap > kClusterMinRow && a.N_cap <= kTopkSplitMinRow) {
-        int chunk = (a.N_cap + kClusterRowCtas - 1) / kClusterRowCtas;
-        chunk = (chunk + 3) & ~3;
-        auto go = [&](auto kern, int smem) -> cudaError_t {
+        auto go = [&](auto kern, int smem, int cl) -> cudaError_t {
+            int chunk = (a.N_cap + cl - 1) / cl;
+            chunk = (chunk + 3) & ~3;
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
             if (e != cudaSuccess) return e;
-            return launch_k_cluster(kern, dim3(static_cast<unsigned>(R * kClusterRowCtas)), dim3(kClusterThreads), smem,
-                                    kClusterRowCtas, s, a, chunk);
+            if (cl > 8) {
+                e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                if (e != cudaSuccess) return e;
+            }
+            return launch_k_cluster(kern, dim3(static_cast<unsigned>(R * cl)), dim3(kClusterThreads), smem, cl, s, a,
+                                    chunk);
         };
-        if (R <= kClusterRingRows) return go(topk_cluster_kernel<true>, static_cast<int>(sizeof(ClusterSmem<true>)));
-        return go(topk_cluster_kernel<false>, static_cast<int>(sizeof(ClusterSmem<false>)));
+        if (R <= kClusterWideRows)
+            return go(topk_cluster_kernel<true, 16>, static_cast<int>(sizeof(ClusterSmemWide)), 16);
+        if (R <= kClusterRingRows)
+            return go(topk_cluster_kernel<true, 8>, static_cast<int>(sizeof(ClusterSmem<true>)), 8);
+        return go(topk_cluster_kernel<false, 8>, static_cast<int>(sizeof(ClusterSmem<false>)), 8);
     }
     if (!split_rows(R, a.N_cap) || R >= num_sms) {
         // One CTA per row, no workspace.

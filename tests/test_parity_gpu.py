@@ -258,6 +258,21 @@ def test_topk_cluster_rows_k_extremes_and_odd_stride(k):
     topk_case(x, [70001, 70000, 2047], k)
 
 
+def test_topk_cluster_rows_nine_to_sixteen_rows_load_through_registers():
+    # more than eight rows: the cluster CTAs load their chunks eight float4 per
+    # thread (no bulk-copy ring); ties, -inf, NaN, crowding, ragged rows
+    rng = np.random.default_rng(27)
+    N = 100000
+    x = rng.standard_normal((12, N)).astype(np.float32)
+    x[1] = np.round(x[1] * 2) / 2
+    x[2, rng.random(N) < 0.3] = -np.inf
+    x[3, rng.random(N) < 0.1] = np.nan
+    x[4, N - 5000:] += 3.0
+    x[5] = 0.25                                               # all equal: exact pass by CTA 0
+    x[6, rng.random(N) < 0.05] *= 4
+    topk_case(x, [N, N, N, N, N, N, N - 7, 50001, 9000, 8193, 8192, 513], 512)
+
+
 def test_topk_cluster_rows_longest_chunks_refill_the_ring():
     # 524,288 scores: 65,536 per CTA, eight 32 KB bulk copies through a ring of
     # four; ragged ends exercise the copy rounded up to 16 bytes
