@@ -274,14 +274,31 @@ def test_topk_cluster_rows_nine_to_sixteen_rows_load_through_registers():
 
 
 def test_topk_cluster_rows_longest_chunks_refill_the_ring():
-    # 524,288 scores: 65,536 per CTA, eight 32 KB bulk copies through a ring of
-    # four; ragged ends exercise the copy rounded up to 16 bytes
+    # five rows of 524,288 scores: eight CTAs per row, 65,536 scores each, eight
+    # 32 KB bulk copies through a ring of four; ragged ends exercise the copy
+    # rounded up to 16 bytes
     rng = np.random.default_rng(25)
     N = 524288
-    x = rng.standard_normal((3, N)).astype(np.float32)
+    x = rng.standard_normal((5, N)).astype(np.float32)
     x[1, rng.random(N) < 0.05] *= 4
     x[2, 300000:300100] = 9.0                                 # the top rows inside one copy
-    topk_case(x, [N, 400001, 262147], 512)
+    x[3] = np.round(x[3] * 2) / 2
+    topk_case(x, [N, 400001, 262147, N - 3, 100000], 512)
+
+
+def test_topk_cluster_rows_sixteen_ctas_per_row():
+    # up to four rows: sixteen CTAs per row (ties, -inf, NaN, all equal, ragged,
+    # the top rows crowded into one CTA's chunk)
+    rng = np.random.default_rng(28)
+    N = 300000
+    x = rng.standard_normal((4, N)).astype(np.float32)
+    x[0] = np.round(x[0] * 2) / 2
+    x[1, rng.random(N) < 0.3] = -np.inf
+    x[1, rng.random(N) < 0.1] = np.nan
+    x[2] = 0.125                                              # all equal: exact pass by CTA 0
+    x[3, 120000:125000] += 3.0
+    topk_case(x, [N, N - 1, 200003, 150001], 512)
+    topk_case(x[:2].copy(), [N, 77777], 2048)
 
 
 @pytest.mark.parametrize("shape", [(3, 100000), (160, 9000), (2, 600000)])
