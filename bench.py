@@ -470,9 +470,10 @@ def main():
     # auto: the fused select where its candidate kernel (one CTA per row) fills
     # the GPU (decode with as many rows as SMs), or where every row is a
     # candidate anyway (rows of at most 4,096 entries, which the candidate
-    # kernel caches whole: 1 x 1,024 rows 0.041 vs 0.053 ms per step); the two
-    # kernels otherwise (8 x 16,384: 0.061 vs 0.087 ms; 4 x 262,144: 0.093 vs
-    # 0.366 ms).
+    # kernel caches whole: 1 x 1,024 rows 27.8 vs 28.4 us per step, ten steps
+    # to a graph); the two kernels otherwise (8 x 16,384: 36 vs 89 us;
+    # 4 x 262,144: 73 vs 342 us: a few long rows leave the scan's per-CTA
+    # thresholds loose, so most rows become candidates).
     n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     fused = args.select == "fused" or (args.select == "auto" and wl.kind == "decode" and
                                        (wl.units * wl.queries >= n_sms or wl.n_rows <= 4096))
