@@ -3,20 +3,23 @@
 // main attention).
 //
 // Every path compares scores through an order-preserving 32-bit key
-// (float_key: a > b as floats, -0 == +0, implies key(a) > key(b)) and finds
-// the k-th largest key by radix select, MSB first, in four 8-bit digits over
-// 256-bin shared-memory histograms.  A selection is the rows whose key is
-// above that k-th key T, then the lowest-index rows whose key equals T until
-// k rows are taken; they are written in ascending row order (a bitonic sort of
-// the at most k chosen rows), then -1 padding.
+// (float_key: a > b as floats, -0 == +0, implies key(a) > key(b)).  A
+// selection is the rows whose key is above the k-th largest key T, then the
+// lowest-index rows whose key equals T until k rows are taken; they are
+// written in ascending row order, then -1 padding.
 //
 // The row is first cut down to a short candidate list: a sample of the row's
-// scores gives a threshold T0 near the key of rank 3k, and every visible row
-// with key >= T0 becomes a candidate (about 3k of them).  The list decides the
-// selection exactly when it holds at least k rows (then T >= T0, and every row
-// at or above T is listed) or, when the row has at most k visible scores, all
-// of them.  Otherwise (a sample that missed, heavy ties) the same digits are
-// taken over the whole row, which is exact whatever the scores.
+// scores gives a threshold T0 near the key of rank 3k (2k for the smallest
+// row shape), and every visible row with key >= T0 becomes a candidate.  The
+// list decides the selection exactly when it holds at least k rows (then
+// T >= T0, and every row at or above T is listed) or, when the row has at most
+// k visible scores, all of them.  Over the list, T comes from a count of the
+// candidates in 32 buckets of their key range (ballots, no atomics) and a rank
+// (or an 8-bit-per-round narrowing) of the keys in the bucket where the count
+// from the top reaches k; the chosen rows go out through a bitmap of the row,
+// a count of smaller rows, or a bitonic sort.  Otherwise (a sample that missed,
+// heavy ties) T is found over the whole row by 8-bit radix digits in 256-bin
+// shared-memory histograms, which is exact whatever the scores.
 //
 // Four launch shapes:
 //   topk_cluster_kernel     up to 16 rows of 4,097 .. 524,288 scores (long-
@@ -1083,7 +1086,8 @@ __global__ void __launch_bounds__(kSplitFinalThreads) topk_split_final_kernel(co
 
 // ---------------------------------------------------------------- few rows: one cluster per row
 // For up to kClusterMaxRows rows of more than kClusterMinRow scores: a
-// thread-block cluster of kClusterRowCtas (8) CTAs per row.  CTA q filters chunk q
+// thread-block cluster of kClusterRowCtas (8) CTAs per row, 16 for batches of
+// up to kClusterWideRows rows.  CTA q filters chunk q
 // of the row against the row's sampled threshold T0 (every CTA derives the
 // same T0 from the same sample) into a candidate list in its own shared
 // memory.  The CTAs then exchange what the exact selection needs through
