@@ -37,7 +37,14 @@ namespace ds4a {
 namespace {
 
 constexpr int kTileRows = 128;   // UMMA M
-constexpr int kPrefetchTiles = 16;   // key tiles per CTA put into L2 before the dependency wait
+// Key tiles per CTA put into L2 before the dependency wait.  Decode (G = 1):
+// an eighth of the CTA's share, 4 to 24 (a long scan gains a deeper start;
+// behind a partly idle GPU, a short one loses when its prefetch competes with
+// the kernel still running: 4 x 262,144 step 71.8 us with 8 tiles, 73.6 with
+// 16, 77.6 with 24; the 1,376-unit decode step 3,547 / 3,540 / 3,532 us).  A
+// prefill chunk (G = 4), whose key tiles stay in L2 once read: 16 (24 cost
+// 13 us on the 2,048-query step).
+constexpr int kPrefetchMin = 4, kPrefetchMax = 24, kPrefetchGroups = 16;
 
 
 template <int G>
@@ -228,7 +235,9 @@ DS4A_DEV float sum_pairs(const unsigned long long (&acc)[4]) {
 // after the wait).
 DS4A_DEV void prefetch_share_head(const IndexerArgs &a, long long lo, long long hi, int G) {
     const long long per_unit = static_cast<long long>(a.n_groups) * a.nt_cap;
-    const long long end = min(hi, lo + kPrefetchTiles);
+    const long long depth = G > 1 ? kPrefetchGroups
+                                  : min(static_cast<long long>(kPrefetchMax), max(static_cast<long long>(kPrefetchMin), (hi - lo) / 8));
+    const long long end = min(hi, lo + depth);
     int last_qrow = -1;
     for (long long lin = lo; lin < end; ++lin) {
         const int u = static_cast<int>(lin / per_unit);
