@@ -108,18 +108,23 @@ def test_fused_long_rows_split_over_many_ctas():
     oracle_check(iq, w, ik, n_rows, idx, cnt, k, [(u, 0) for u in range(U)])
 
 
-def test_fused_all_equal_scores_take_the_lowest_rows():
-    U, N_cap, k = 3, 20_000, 512
+@pytest.mark.parametrize("k", [512, 1024])
+def test_fused_all_equal_scores_take_the_lowest_rows(k):
+    # every row a candidate: 20,000 pairs, more than either candidate cache
+    # (6,144 at k <= 512, 12,288 above) holds, so the list is read in place
+    U, N_cap = 3, 20_000
     iq, w, ik = rand_case(U, 1, N_cap, seed=74)
     ik = ik[:, :1].expand(U, N_cap, 128).contiguous()            # identical keys: every score equal
-    n_rows = torch.tensor([20_000, 511, 9000], dtype=torch.int32, device="cuda")
+    n_rows = torch.tensor([20_000, k - 1, 9000], dtype=torch.int32, device="cuda")
     idx, cnt, _ = both_paths(iq, w, ik, n_rows, k)
-    assert idx[0, 0].tolist() == list(range(512)) and int(cnt[1, 0]) == 511
+    assert idx[0, 0].tolist() == list(range(k)) and int(cnt[1, 0]) == k - 1
+    assert idx[2, 0].tolist() == list(range(k))
 
 
-def test_fused_rising_scores_keep_every_row_as_candidate():
+@pytest.mark.parametrize("k", [512, 1024])
+def test_fused_rising_scores_keep_every_row_as_candidate(k):
     # key of row r scaled by (1 + r/N): every row beats the threshold of the rows before it
-    U, N_cap, k = 2, 30_000, 512
+    U, N_cap = 2, 30_000
     ramp = (1 + torch.arange(N_cap, dtype=torch.float32) / N_cap)[None, :, None]
     iq, w, ik = rand_case(U, 1, N_cap, seed=75)
     base = ik[:, :1].float().abs()                                  # one positive key per unit
